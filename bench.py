@@ -1,0 +1,461 @@
+"""KDA layer throughput on GB300: tokens/s and fraction of the HBM roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|verify|prefill_varlen|prefill_long] [--no-legs]
+
+One step is one pass of the layer's hot path over one batch of seeded
+synthetic input.  The headline workload is the decode step (64 sequences x
+1 row, 32 heads, dk = dv = 128, bf16 rows, fp32 state, softplus gate, gated
+RMSNorm epilogue): one kda_decode call = conv + SiLU + L2 norms + gates + the
+delta rule + the output norm for every (sequence, head).  The other
+workloads (varlen prefill, long prefill, verify window + commit) are measured
+once more in the same run and reported under "legs".
+
+Timing: W untimed warm-up steps, then exactly K steps timed with CUDA events
+on the launching stream, bracketed by a barrier and a device synchronise on
+both sides; the max over ranks is reported.  Inputs rotate over several
+sets whose total footprint is well above the 129 MB L2, so every step reads
+its state from HBM.  Under torchrun each rank runs its own batch (weak
+scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), float(
+            d.get("bf16_tflops_sustained", d.get("bf16_tflops", FALLBACK_BF16_TFLOPS))), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while it runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kda_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        sm = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "power_w_max": max(r[2] for r in rows), "reasons": reasons}
+
+
+def time_steps(fn, steps, stream):
+    """Per-step CUDA-event durations (ms) of fn() on `stream`."""
+    import torch
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        starts[i].record(stream)
+        fn(i)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+# ------------------------------------------------------- algorithmic bytes
+
+def decode_bytes_per_unit(d=128, K=4, io=2, out=2, out_gate=True):
+    """HBM bytes one (sequence, head) decode row must move: state read and
+    write, the q/k/v/gate rows, beta, the output gate, the output, and the
+    conv state's K-1 rows read and written."""
+    conv = (K - 1) * 3 * d * io
+    return 2 * d * d * 4 + 4 * d * io + io + (d * io if out_gate else 0) + d * out + 2 * conv
+
+
+def prefill_bytes_per_token_head(d=128, io=2, out=4, out_gate=False):
+    """HBM bytes per (row, head) of a fully fused prefill: raw q, k, v, gate
+    rows and beta in, the output out (states amortised over the sequence)."""
+    return 4 * d * io + io + (d * io if out_gate else 0) + d * out
+
+
+def prefill_state_bytes(N, H, d=128, K=4, io=2):
+    return N * H * (2 * d * d * 4 + 2 * (K - 1) * 3 * d * io)
+
+
+# --------------------------------------------------------------- workloads
+
+def make_sets(wl_fn, n_sets, out_dtype):
+    from linear_attention_serving_kda_gb300.runtime import DeviceCase
+
+    sets = []
+    wl = wl_fn()
+    for i in range(n_sets):
+        sets.append(DeviceCase(wl, out_dtype=out_dtype))
+    return wl, sets
+
+
+def bench_decode(kda, steps, warmup, stream):
+    from linear_attention_serving_kda_gb300 import workloads as W
+
+    wl = W.decode_case()
+    per_set = decode_bytes_per_unit() * wl.N * wl.H
+    n_sets = max(3, int(np.ceil(3 * L2_BYTES / per_set)))
+    _, sets = make_sets(W.decode_case, n_sets, W.BF16)
+    for s in sets:
+        s.params_c = s.params()
+
+    def step(i):
+        s = sets[i % n_sets]
+        kda.check(kda.kda_decode(s.params_c, wl.N, s.q, s.k, s.v, s.f, s.b, s.g, None, s.conv_state,
+                                 s.rec_state, s.out, s.dev_status, stream))
+
+    for i in range(warmup):
+        step(i)
+    return wl, sets, step, per_set
+
+
+def run_timed(step, steps, stream, dist):
+    import torch
+
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    durs = time_steps(step, steps, stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall
+    total_ms = sum(durs)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64,
+                         device="cuda" if dist.get_backend() == "nccl" else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, durs, wall
+
+
+def leg_prefill(kda, wl_fn, reps, stream):
+    import torch
+
+    from linear_attention_serving_kda_gb300 import workloads as W
+    from linear_attention_serving_kda_gb300.runtime import DeviceCase
+
+    wl = wl_fn()
+    dc = DeviceCase(wl, out_dtype=W.BF16)
+    kda.check(dc.prefill(stream=stream))  # warm-up
+    durs = []
+    for _ in range(reps):
+        dc.reset_states()
+        torch.cuda.synchronize()
+        durs += time_steps(lambda i: kda.check(dc.prefill(stream=stream)), 1, stream)
+    ms = statistics.median(durs)
+    bpt = prefill_bytes_per_token_head(out=2, out_gate=wl.has_out_gate)
+    alg = wl.T * wl.H * bpt + prefill_state_bytes(wl.N, wl.H)
+    return {"workload": wl.name, "tokens": wl.T, "ms": ms, "tokens_per_s": wl.T / (ms * 1e-3),
+            "alg_bytes": alg, "achieved_gbs": alg / (ms * 1e-3) / 1e9}
+
+
+def leg_verify(kda, reps, stream):
+    import torch
+
+    from linear_attention_serving_kda_gb300 import workloads as W
+    from linear_attention_serving_kda_gb300.runtime import DeviceCase
+
+    wl = W.verify_case()
+    n_sets = 4
+    sets = [DeviceCase(wl, out_dtype=W.BF16) for _ in range(n_sets)]
+    for s in sets:
+        s.alloc_log()
+    tv, tc = [], []
+    for r in range(reps + 1):
+        s = sets[r % n_sets]
+        s.reset_states()
+        torch.cuda.synchronize()
+        dv = time_steps(lambda i: kda.check(s.verify(stream=stream)), 1, stream)
+        dcm = time_steps(lambda i: kda.check(s.commit(stream=stream)), 1, stream)
+        if r:
+            tv += dv
+            tc += dcm
+    mv, mc = statistics.median(tv), statistics.median(tc)
+    acc = int(wl.arrays["accepted"].sum())
+    rows = wl.N * wl.W
+    return {"workload": wl.name, "rows": rows, "accepted_rows": acc, "verify_ms": mv, "commit_ms": mc,
+            "rows_verified_per_s": rows / (mv * 1e-3),
+            "committed_tokens_per_s": acc / ((mv + mc) * 1e-3)}
+
+
+def e2e_decode(kda, steps, warmup, stream):
+    """Same decode step through the public API, host buffers: pinned host
+    rows copied in and the output copied back inside the timed region."""
+    import torch
+
+    from linear_attention_serving_kda_gb300 import workloads as W
+    from linear_attention_serving_kda_gb300.runtime import DeviceCase
+
+    wl = W.decode_case()
+    dc = DeviceCase(wl, out_dtype=W.BF16)
+    p = dc.params()
+    host_in = {nm: wl.to_torch(nm).pin_memory() for nm in ("q", "k", "v", "f", "b", "g")}
+    dev_in = {nm: torch.empty_like(t, device="cuda") for nm, t in host_in.items()}
+    host_out = torch.empty(dc.out.shape, dtype=dc.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def step(i):
+        for nm in host_in:
+            dev_in[nm].copy_(host_in[nm], non_blocking=True)
+        kda.check(kda.kda_decode(p, wl.N, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["f"], dev_in["b"],
+                                 dev_in["g"], None, dc.conv_state, dc.rec_state, dc.out, dc.dev_status, stream))
+        host_out.copy_(dc.out, non_blocking=True)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    durs = time_steps(step, steps, stream)
+    ms = sum(durs) / steps
+    return {"value": wl.N / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+# --------------------------------------------------------- CPU oracle legs
+
+def oracle_decode_rate(seconds=10.0):
+    """The oracle (threads over (sequence, head) units, as it stands) on the
+    decode step, repeated with carried states for about `seconds`."""
+    import oracle
+    from linear_attention_serving_kda_gb300 import workloads as W
+
+    oracle.build()
+    wl = W.decode_case()
+    cores = os.cpu_count() or 1
+    steps = 0
+    t0 = time.perf_counter()
+    arrays = dict(wl.arrays)
+    while True:
+        res = oracle.forward(wl, threads=cores, arrays=arrays)
+        arrays["rec_state"], arrays["conv_state"] = res["rec_state"], res["conv_state"]
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return wl.N * steps / el, cores, steps, el
+
+
+# --------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-legs", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "verify", "prefill_varlen", "prefill_long"])
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, world)
+        return
+
+    import torch
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        dist = tdist
+
+    import linear_attention_serving_kda_gb300 as kda
+    from linear_attention_serving_kda_gb300 import build as kbuild
+
+    if rank == 0 or world == 1:
+        kbuild.build()
+    if dist is not None:
+        dist.barrier()
+    kda.load()
+    stream = torch.cuda.current_stream()  # every launch and every event goes on this stream
+    hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = load_peaks()
+    sampler = ClockSampler(local_rank).start() if rank == 0 else None
+
+    if args.workload != "decode":
+        res = run_single_leg(kda, args, stream)
+        if sampler:
+            res["clocks"] = sampler.stop()
+        if rank == 0:
+            print(json.dumps(res))
+        return
+
+    wl, sets, step, per_set = bench_decode(kda, args.steps, args.warmup, stream)
+    total_ms, durs, wall = run_timed(step, args.steps, stream, dist)
+    ms = total_ms / args.steps
+    tokens = wl.N * world * args.steps
+    value = tokens / (total_ms * 1e-3)
+    kernel_ms = statistics.mean(durs)
+    achieved = per_set / (kernel_ms * 1e-3) / 1e9
+
+    legs = {}
+    if not args.no_legs:
+        from linear_attention_serving_kda_gb300 import workloads as W
+
+        legs["prefill_varlen"] = leg_prefill(kda, W.varlen_prefill_case, 3, stream)
+        legs["prefill_long"] = leg_prefill(kda, W.long_prefill_case, 3, stream)
+        legs["verify_commit"] = leg_verify(kda, 10, stream)
+        for k in ("prefill_varlen", "prefill_long"):
+            legs[k]["hbm_frac"] = legs[k]["achieved_gbs"] / hbm_gbs
+    e2e = e2e_decode(kda, args.steps, args.warmup, stream)
+    e2e["value"] *= world
+    clocks = sampler.stop() if sampler else None
+
+    cpu = None
+    if rank == 0 and world == 1:
+        rate, cores, n, el = oracle_decode_rate(args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"full decode step (64 seq x 32 heads) repeated {n}x with carried state, {el:.1f} s"}
+
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            with open(tpath) as fh:
+                traffic = json.load(fh).get("bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    line = {
+        "metric": "KDA tokens/s (decode step; prefill and verify legs alongside)",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.N, "heads": wl.H, "head_dim": wl.dk,
+                   "conv_kernel": wl.K, "io": "bf16", "state": "fp32", "gate": "softplus",
+                   "epilogue": "sigmoid-gated RMSNorm", "parallelism": f"replica x{world}",
+                   "l2": f"inputs rotate over {len(sets)} sets, {len(sets) * per_set / 1e6:.0f} MB > L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "traffic": traffic, "kernel": "kda_recurrent_kernel<decode>",
+                     "alg_bytes_per_launch": per_set, "peak_source": peak_src},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "legs": legs,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_single_leg(kda, args, stream):
+    from linear_attention_serving_kda_gb300 import workloads as W
+
+    if args.workload == "verify":
+        return leg_verify(kda, args.steps, stream)
+    fn = W.varlen_prefill_case if args.workload == "prefill_varlen" else W.long_prefill_case
+    return leg_prefill(kda, fn, args.steps, stream)
+
+
+def run_reference(args, world):
+    """The fp64 oracle on the host cores, same workload, metric and unit."""
+    from linear_attention_serving_kda_gb300 import workloads as W
+    import oracle
+
+    oracle.build()
+    wl = W.decode_case()
+    cores = os.cpu_count() or 1
+    arrays = dict(wl.arrays)
+    for _ in range(args.warmup):
+        res = oracle.forward(wl, threads=cores, arrays=arrays)
+        arrays["rec_state"], arrays["conv_state"] = res["rec_state"], res["conv_state"]
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        res = oracle.forward(wl, threads=cores, arrays=arrays)
+        arrays["rec_state"], arrays["conv_state"] = res["rec_state"], res["conv_state"]
+    el = time.perf_counter() - t0
+    value = wl.N * args.steps / el
+    line = {
+        "impl": "reference",
+        "metric": "KDA tokens/s (decode step; prefill and verify legs alongside)",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.N, "heads": wl.H, "head_dim": wl.dk,
+                   "conv_kernel": wl.K, "io": "bf16", "state": "fp64 (oracle)", "gate": "softplus"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"full decode step x {args.steps} with carried state"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -32,3 +32,14 @@ def cuda_lib():
 
     kda.load()  # raises if the library is missing: no silent fallback
     return kda
+
+
+def pytest_terminal_summary(terminalreporter):
+    try:
+        from tests.parity import RECORD
+    except Exception:
+        return
+    if RECORD:
+        terminalreporter.write_line("parity record (what, rel L2, max-abs/RMS):")
+        for what, e, m in RECORD:
+            terminalreporter.write_line(f"  {what:40s} {e:.3e} {m:.3e}")

@@ -1,0 +1,111 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_serving_kda_gb300 as kda
+from linear_attention_serving_kda_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+FAKE = 1 << 20  # a 16-byte-aligned non-null address; never dereferenced here
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kda.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return re.findall(r"KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", text)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"kda_prefill_varlen", "kda_decode", "kda_verify_window", "kda_commit"} <= set(names)
+    raw = ctypes.CDLL(kbuild.LIB)
+    for n in names:
+        assert hasattr(raw, n), n
+    assert lib.kda_abi_version() == 100
+
+
+def _params(**kw):
+    base = dict(num_heads=4, head_dim=128, conv_kernel=4, gate_mode=kda.KDA_GATE_SAFE,
+                A_log=FAKE, dt_bias=FAKE, conv_weight=FAKE, gate_lower_bound=-5.0, num_slots=4)
+    base.update(kw)
+    return kda.Params(**base)
+
+
+def _decode(p, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, gate=FAKE, beta=FAKE, out_gate=None, slots=None,
+                conv_state=FAKE, rec_state=FAKE, out=FAKE)
+    args.update(over)
+    return kda.kda_decode(p, 2, args["q"], args["k"], args["v"], args["gate"], args["beta"],
+                          args["out_gate"], args["slots"], args["conv_state"], args["rec_state"],
+                          args["out"], None, 0)
+
+
+@pytest.mark.parametrize("kw,rc", [
+    (dict(head_dim=96), kda.KDA_ERR_UNSUPPORTED_GEOMETRY),
+    (dict(head_dim=256), kda.KDA_ERR_UNSUPPORTED_GEOMETRY),
+    (dict(head_dim_v=64), kda.KDA_ERR_UNSUPPORTED_GEOMETRY),
+    (dict(conv_kernel=5), kda.KDA_ERR_UNSUPPORTED_GEOMETRY),
+    (dict(conv_kernel=1), kda.KDA_ERR_UNSUPPORTED_GEOMETRY),
+    (dict(gate_lower_bound=0.0), kda.KDA_ERR_INVALID_BOUND),
+    (dict(gate_lower_bound=float("nan")), kda.KDA_ERR_INVALID_BOUND),
+    (dict(gate_lower_bound=float("-inf")), kda.KDA_ERR_INVALID_BOUND),
+    (dict(gate_mode=7), kda.KDA_ERR_INVALID_ARGUMENT),
+    (dict(num_heads=0), kda.KDA_ERR_INVALID_ARGUMENT),
+    (dict(num_slots=0), kda.KDA_ERR_INVALID_ARGUMENT),
+    (dict(io_dtype=5), kda.KDA_ERR_INVALID_ARGUMENT),
+    (dict(l2_eps=-1.0), kda.KDA_ERR_INVALID_ARGUMENT),
+    (dict(scale=float("inf")), kda.KDA_ERR_INVALID_ARGUMENT),
+    (dict(A_log=None), kda.KDA_ERR_INVALID_ARGUMENT),
+    (dict(dt_bias=FAKE + 4), kda.KDA_ERR_INVALID_ARGUMENT),
+])
+def test_params_rejected_before_launch(lib, kw, rc):
+    assert _decode(_params(**kw)) == rc
+
+
+def test_bound_checked_only_in_safe_mode(lib):
+    # a positive bound is irrelevant to the softplus gate: validation passes and
+    # the call only fails later at the device check (no GPU here)
+    p = _params(gate_mode=kda.KDA_GATE_SOFTPLUS, gate_lower_bound=3.0)
+    assert _decode(p) in (kda.KDA_ERR_DEVICE, kda.KDA_OK, kda.KDA_ERR_LAUNCH)
+    assert _decode(_params(gate_lower_bound=3.0)) == kda.KDA_ERR_INVALID_BOUND
+
+
+def test_pointer_checks(lib):
+    p = _params()
+    assert _decode(p, q=None) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert _decode(p, out=FAKE + 2) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert _decode(p, out_gate=FAKE + 8) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert kda.kda_decode(p, -1, *([FAKE] * 5), None, None, FAKE, FAKE, FAKE, None, 0) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert kda.kda_decode(p, 0, *([None] * 10), None, 0) == kda.KDA_OK  # empty batch: no-op
+    # prefill: zero sequences is a no-op; negative sizes are rejected
+    assert kda.kda_prefill_varlen(p, None, 0, 0, *([None] * 10), None, 0, None, 0) == kda.KDA_OK
+    assert kda.kda_prefill_varlen(p, FAKE, -1, 0, *([None] * 10), None, 0, None, 0) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert kda.kda_verify_window(p, 2, 4, *([FAKE] * 5), None, None, FAKE, FAKE, None, FAKE, None, 0) \
+        == kda.KDA_ERR_INVALID_ARGUMENT  # missing log
+    assert kda.kda_commit(p, 2, 4, None, None, FAKE, FAKE, FAKE, None, 0) == kda.KDA_ERR_INVALID_ARGUMENT
+
+
+def test_sizes(lib):
+    p = _params(io_dtype=kda.KDA_DTYPE_BF16)
+    n = kda.kda_verify_log_bytes(p, 32, 8)
+    floats = 32 * 8 * 4 * 3 * 128 * 4
+    raw = 32 * 8 * 4 * 3 * 128 * 2
+    assert n >= floats + raw and n % 256 == 0
+    assert kda.kda_verify_log_bytes(_params(head_dim=96), 32, 8) == 0
+    assert kda.kda_prefill_workspace_bytes(p, 8, 1000) % 256 == 0
+
+
+def test_status_strings(lib):
+    for rc in range(7):
+        assert kda.status_string(rc).startswith("KDA_")
+    assert kda.status_string(99) == "KDA_ERR_UNKNOWN"

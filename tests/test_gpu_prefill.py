@@ -1,0 +1,155 @@
+"""Variable-length prefill on the GPU against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from linear_attention_serving_kda_gb300 import workloads as W
+from linear_attention_serving_kda_gb300.runtime import DeviceCase
+from tests.parity import assert_bf16_within_one_ulp, assert_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _prefill(kda, wl, out_dtype=W.F32, **kw):
+    dc = DeviceCase(wl, out_dtype=out_dtype, **kw)
+    kda.check(dc.prefill())
+    torch.cuda.synchronize()
+    assert int(dc.dev_status.item()) == 0
+    return dc
+
+
+def _check_all(dc, ref):
+    T = dc.wl.T
+    assert_close(to_np(dc.out[:T]), ref["out"], "out")
+    assert_close(to_np(dc.rec_state), ref["rec_state"], "rec_state")
+    assert np.array_equal(to_np(dc.conv_state), ref["conv_state"].astype(np.float32))
+
+
+def test_tiny_case(cuda_lib, oracle_mod):
+    """1 sequence, T=64, H=2, dk=dv=32, conv 4, fp32, safe gate, zero states."""
+    wl = W.tiny_oracle_case()
+    _check_all(_prefill(cuda_lib, wl), oracle_mod.forward(wl))
+
+
+VARLEN = [
+    # lens, d, io, gate, K, out_gate, init
+    ([1, 15, 16, 17], 32, W.F32, W.SAFE, 4, False, "random"),
+    ([63, 64, 65], 64, W.BF16, W.SAFE, 4, True, "random"),
+    ([130, 0, 2, 1], 128, W.BF16, W.SAFE, 3, False, "random"),
+    ([129, 64, 200], 128, W.BF16, W.SOFTPLUS, 4, True, "zero"),
+    ([257, 3], 128, W.F32, W.SAFE, 2, True, "random"),
+    ([0, 0], 64, W.F32, W.SAFE, 4, False, "random"),
+]
+
+
+@pytest.mark.parametrize("lens,d,io,gate,K,og,init", VARLEN)
+def test_varlen_cases(cuda_lib, oracle_mod, lens, d, io, gate, K, og, init):
+    wl = W.make_workload("vl", 300 + sum(lens) + d, lens, H=3, d=d, K=K, io_dtype=io,
+                         gate_mode=gate, lower_bound=-5.0, out_gate=og, init_state=init)
+    _check_all(_prefill(cuda_lib, wl), oracle_mod.forward(wl))
+
+
+def test_bf16_output(cuda_lib, oracle_mod):
+    wl = W.make_workload("vlb", 311, [100, 37], H=2, d=128, K=4, io_dtype=W.BF16,
+                         gate_mode=W.SAFE, lower_bound=-5.0, out_gate=True, init_state="random")
+    ref = oracle_mod.forward(wl)
+    dc = _prefill(cuda_lib, wl, out_dtype=W.BF16)
+    assert_bf16_within_one_ulp(to_np(dc.out[:wl.T]), ref["out"])
+
+
+def test_prompt_cut_bits(cuda_lib):
+    """A prompt cut at a multiple of 64 rows gives the bits of one uncut call."""
+    T, cut = 320, 128
+    wl = W.make_workload("cut", 312, [T], H=2, d=128, K=4, io_dtype=W.BF16,
+                         gate_mode=W.SAFE, lower_bound=-5.0, out_gate=True, init_state="random")
+    full = _prefill(cuda_lib, wl)
+    from tests.parity import gather_rows
+
+    a = gather_rows(wl, [(0, cut)])
+    b = gather_rows(wl, [(cut, T)])
+    da = _prefill(cuda_lib, a)
+    db = DeviceCase(b)
+    db.conv_state.copy_(da.conv_state)
+    db.rec_state.copy_(da.rec_state)
+    cuda_lib.check(db.prefill())
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([da.out[:cut], db.out[:T - cut]]), full.out[:T])
+    assert torch.equal(db.rec_state, full.rec_state)
+    assert torch.equal(db.conv_state, full.conv_state)
+
+
+def test_slots_and_bad_seqlens(cuda_lib, oracle_mod):
+    wl = W.make_workload("pslot", 313, [70, 5, 33], H=2, d=64, K=4, io_dtype=W.F32,
+                         gate_mode=W.SAFE, lower_bound=-5.0, init_state="random")
+    ref = oracle_mod.forward(wl)
+    dc = DeviceCase(wl, num_slots=5, slots=[3, -1, 0])
+    rs0 = dc.rec_state.clone()
+    dc.out.fill_(float("nan"))
+    cuda_lib.check(dc.prefill())
+    torch.cuda.synchronize()
+    out = to_np(dc.out)
+    assert np.all(np.isnan(out[70:75]))
+    assert_close(out[:70], ref["out"][:70], "out s0")
+    assert_close(out[75:], ref["out"][75:], "out s2")
+    assert_close(to_np(dc.rec_state[3]), ref["rec_state"][0], "state s0")
+    assert_close(to_np(dc.rec_state[0]), ref["rec_state"][2], "state s2")
+    for sl in (1, 2, 4):
+        assert torch.equal(dc.rec_state[sl], rs0[sl])
+    # a non-monotone cu_seqlens is flagged, not trapped
+    dc2 = DeviceCase(wl)
+    dc2.cu_seqlens.copy_(torch.tensor([0, 80, 75, 108], dtype=torch.int32))
+    cuda_lib.check(dc2.prefill())
+    torch.cuda.synchronize()
+    assert int(dc2.dev_status.item()) & cuda_lib.KDA_DEV_BAD_SEQLENS
+
+
+def _sampled_units(wl, n, seed):
+    rng = np.random.default_rng(seed)
+    units = {(int(s), int(h)) for s, h in zip(rng.integers(0, wl.N, n), rng.integers(0, wl.H, n))}
+    units.add((int(np.argmax(np.diff(wl.cu_seqlens))), wl.H - 1))  # the longest sequence
+    return sorted(units)
+
+
+def _check_sampled(oracle_mod, wl, dc, units):
+    out = to_np(dc.out)
+    rec = to_np(dc.rec_state)
+    assert np.all(np.isfinite(out[:wl.T])) and np.all(np.isfinite(rec))
+
+    def one(u):
+        s, h = u
+        sub = W.head_slice(wl, s, h)
+        return u, oracle_mod.forward(sub, threads=1)
+
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=8) as ex:
+        results = list(ex.map(one, units))
+    for (s, h), ref in results:
+        t0, t1 = wl.cu_seqlens[s], wl.cu_seqlens[s + 1]
+        assert_close(out[t0:t1, h], ref["out"][:, 0], f"out s{s} h{h}")
+        assert_close(rec[s, h], ref["rec_state"][0, 0], f"state s{s} h{h}")
+
+
+@pytest.mark.slow
+def test_varlen_full_size_sampled(cuda_lib, oracle_mod):
+    """8 sequences, lengths ~U{512..8192}, H=32, dk=dv=128, bf16, safe gate:
+    sampled (sequence, head) units against the oracle, all outputs finite,
+    every conv state exact."""
+    wl = W.varlen_prefill_case()
+    dc = _prefill(cuda_lib, wl)
+    _check_sampled(oracle_mod, wl, dc, _sampled_units(wl, 6, 1))
+    # conv state: the last K-1 raw rows of each sequence, exactly
+    cs = to_np(dc.conv_state)
+    for s in range(wl.N):
+        t1 = wl.cu_seqlens[s + 1]
+        raw = np.concatenate([wl.arrays["q"][t1 - 3:t1].reshape(3, -1), wl.arrays["k"][t1 - 3:t1].reshape(3, -1),
+                              wl.arrays["v"][t1 - 3:t1].reshape(3, -1)], axis=1)
+        assert np.array_equal(cs[s], raw)
+
+
+@pytest.mark.slow
+def test_long_prefill_sampled(cuda_lib, oracle_mod):
+    """1 sequence of 32768 rows, H=32, dk=dv=128, bf16, gated RMSNorm: sampled
+    heads against the oracle."""
+    wl = W.long_prefill_case()
+    dc = _prefill(cuda_lib, wl)
+    _check_sampled(oracle_mod, wl, dc, [(0, 0), (0, 13), (0, 31)])
