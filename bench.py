@@ -105,18 +105,25 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(r[2] for r in rows), "reasons": reasons}
 
 
-def time_steps(fn, steps, stream):
-    """Per-step CUDA-event durations (ms) of fn() on `stream`."""
+def time_steps(fn, steps, stream, queue_ahead=True):
+    """Per-step CUDA-event durations (ms) of fn(i) on `stream`, and the
+    elapsed time of the whole sequence.  With queue_ahead the stream first
+    sleeps on the GPU so the host can enqueue every step before the GPU
+    reaches the first one: the events then time GPU execution, not host
+    launch overhead (which the end-to-end figure measures)."""
     import torch
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if queue_ahead:
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(2e6) + 200000 * steps)
     for i in range(steps):
         starts[i].record(stream)
         fn(i)
         ends[i].record(stream)
     torch.cuda.synchronize()
-    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], starts[0].elapsed_time(ends[-1])
 
 
 # ------------------------------------------------------- algorithmic bytes
@@ -158,13 +165,12 @@ def bench_decode(kda, steps, warmup, stream):
     per_set = decode_bytes_per_unit() * wl.N * wl.H
     n_sets = max(3, int(np.ceil(3 * L2_BYTES / per_set)))
     _, sets = make_sets(W.decode_case, n_sets, W.BF16)
-    for s in sets:
-        s.params_c = s.params()
+    calls = [kda.Prepared("kda_decode", s.params(), wl.N, s.q, s.k, s.v, s.f, s.b, s.g, None,
+                          s.conv_state, s.rec_state, s.out, s.dev_status, stream=stream) for s in sets]
 
     def step(i):
-        s = sets[i % n_sets]
-        kda.check(kda.kda_decode(s.params_c, wl.N, s.q, s.k, s.v, s.f, s.b, s.g, None, s.conv_state,
-                                 s.rec_state, s.out, s.dev_status, stream))
+        if calls[i % n_sets]() != 0:
+            raise RuntimeError("kda_decode failed")
 
     for i in range(warmup):
         step(i)
@@ -179,12 +185,11 @@ def run_timed(step, steps, stream, dist):
         dist.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    durs = time_steps(step, steps, stream)
+    durs, total_ms = time_steps(step, steps, stream)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     wall = time.perf_counter() - t_wall
-    total_ms = sum(durs)
     if dist is not None:
         t = torch.tensor([total_ms], dtype=torch.float64,
                          device="cuda" if dist.get_backend() == "nccl" else "cpu")
@@ -206,7 +211,7 @@ def leg_prefill(kda, wl_fn, reps, stream):
     for _ in range(reps):
         dc.reset_states()
         torch.cuda.synchronize()
-        durs += time_steps(lambda i: kda.check(dc.prefill(stream=stream)), 1, stream)
+        durs += time_steps(lambda i: kda.check(dc.prefill(stream=stream)), 1, stream)[0]
     ms = statistics.median(durs)
     bpt = prefill_bytes_per_token_head(out=2, out_gate=wl.has_out_gate)
     alg = wl.T * wl.H * bpt + prefill_state_bytes(wl.N, wl.H)
@@ -230,8 +235,8 @@ def leg_verify(kda, reps, stream):
         s = sets[r % n_sets]
         s.reset_states()
         torch.cuda.synchronize()
-        dv = time_steps(lambda i: kda.check(s.verify(stream=stream)), 1, stream)
-        dcm = time_steps(lambda i: kda.check(s.commit(stream=stream)), 1, stream)
+        dv = time_steps(lambda i: kda.check(s.verify(stream=stream)), 1, stream)[0]
+        dcm = time_steps(lambda i: kda.check(s.commit(stream=stream)), 1, stream)[0]
         if r:
             tv += dv
             tc += dcm
@@ -270,8 +275,8 @@ def e2e_decode(kda, steps, warmup, stream):
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
-    durs = time_steps(step, steps, stream)
-    ms = sum(durs) / steps
+    _, total = time_steps(step, steps, stream, queue_ahead=False)
+    ms = total / steps
     return {"value": wl.N / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 

@@ -72,6 +72,7 @@ extern "C" {
 #define KDA_DEV_BAD_SEQLENS 1  /* cu_seqlens not monotone or outside [0, T] */
 #define KDA_DEV_BAD_SLOT 2     /* slots[b] >= num_slots */
 #define KDA_DEV_BAD_ACCEPTED 4 /* accepted[b] outside [0, W] */
+#define KDA_DEV_TIMEOUT 8      /* a bounded on-chip wait gave up; the unit was skipped */
 
 #define KDA_DTYPE_F32 0
 #define KDA_DTYPE_BF16 1

@@ -1,23 +1,30 @@
 // kda_recurrent.cu -- row-recurrent KDA kernels for sm_103a: decode rows,
 // verify windows, the serial prefill, and the verify commit.
 //
-// One CTA of 256 threads owns one (sequence, head) unit.  The fp32 dk x dv
-// state lives in registers for the whole call: warp w holds rows
+// A (sequence, head) unit is processed by 256 threads.  The fp32 dk x dv
+// state lives in registers while the unit's rows run: warp w holds rows
 // [w*D/8, (w+1)*D/8) and lane l holds columns [l*D/32, (l+1)*D/32), so each
-// warp streams whole 128-float rows (coalesced, 16-byte vector loads) and
-// the two key-dim reductions per row (S'^T k and S^T q) are an in-register
-// partial over the warp's rows followed by a fixed-order sum over the 8
-// warps in shared memory.
+// warp touches whole D-float rows (coalesced, vector accesses) and the two
+// key-dim reductions per row (S'^T k and S^T q) are an in-register partial
+// over the warp's rows followed by a fixed-order sum over the 8 warps.
 //
-// Decode, verify and commit run the same per-element expressions in the same
-// order -- S' = alpha * S (rounded), then S = fma(k, u, S') -- with the same
-// thread-to-element map and the same reduction trees, so a verified row has
-// the bits of a decoded row and a committed state the bits of serial decode
+// Every kernel here runs one row through row_step(): the same expressions in
+// the same order -- S' = alpha * S (rounded), then S = fma(k, u, S') -- with
+// the same thread-to-element map and reduction trees.  So a verified row has
+// the bits of a decoded row, and a committed state the bits of serial decode
 // (TensorFold issue #850, Oct 15 comment: a window logs each row's decay,
-// normalized key and update, and the replay gives the bits of rows decoded
+// normalized key and update, and replaying them gives the bits of rows decoded
 // one at a time; Oct 19 comment: preserve rounding, reduction order, replay).
+//
+// Decode at dk = dv = 128 -- the memory-bound serving step -- uses a
+// persistent kernel: one CTA per SM, a producer warp that streams each unit's
+// 64 KiB state, rows, conv history and parameters into a double-buffered
+// shared-memory stage with bulk async copies, and 8 consumer warps that run
+// row_step on the previous stage meanwhile and write the state back with
+// streaming stores.
 #include "kda_common.cuh"
 #include "kda_internal.h"
+#include "kda_ptx.cuh"
 
 namespace kda {
 
@@ -29,7 +36,7 @@ template <int D> struct RecShape {
     static constexpr int RPW = D / REC_WARPS; // state rows per warp
 };
 
-template <int D> struct RecSmem {
+template <int D> struct RowSmem {
     float win[4][3 * D];      // ring of the last 4 raw conv rows (this head's q|k|v channels)
     float cw[3 * D][4];       // conv taps
     float dtb[D];             // dt_bias of this head
@@ -39,7 +46,16 @@ template <int D> struct RecSmem {
     float scal[8];
 };
 
+struct RowConst {
+    int gate_mode;
+    float lb, ea, l2_eps, norm_eps, scale;
+    const float* norm_w;
+};
+
 __device__ __forceinline__ int ring(int x) { return x & 3; }
+
+// Barrier over the 256 row threads only (a streaming CTA also has a producer warp).
+__device__ __forceinline__ void row_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // Global channel of local channel c (q | k | v of head h) in the conv layout.
 template <int D> __device__ __forceinline__ int conv_channel(int c, int h, int H)
@@ -49,8 +65,9 @@ template <int D> __device__ __forceinline__ int conv_channel(int c, int h, int H
     return 2 * H * D + h * D + (c - 2 * D);
 }
 
-template <int D> __device__ __forceinline__ void load_tile(const float* Sg, int r0, int c0,
-                                                           float (&s)[RecShape<D>::RPW][RecShape<D>::CPT])
+template <int D, typename Src>
+__device__ __forceinline__ void load_tile(const Src* Sg, int r0, int c0,
+                                          float (&s)[RecShape<D>::RPW][RecShape<D>::CPT])
 {
     constexpr int RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT;
 #pragma unroll
@@ -65,6 +82,19 @@ template <int D> __device__ __forceinline__ void load_tile(const float* Sg, int 
         } else {
             s[rr][0] = __ldcs(p);
         }
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void load_tile_smem(const float* Ss, int r0, int c0,
+                                               float (&s)[RecShape<D>::RPW][RecShape<D>::CPT])
+{
+    constexpr int RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT;
+    static_assert(CPT == 4, "shared-memory tile path is for D = 128");
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) {
+        float4 x = *reinterpret_cast<const float4*>(Ss + (r0 + rr) * D + c0);
+        s[rr][0] = x.x; s[rr][1] = x.y; s[rr][2] = x.z; s[rr][3] = x.w;
     }
 }
 
@@ -85,11 +115,120 @@ template <int D> __device__ __forceinline__ void store_tile(float* Sg, int r0, i
     }
 }
 
+// One row of the layer for one (sequence, head); called by all 256 threads.
+// On entry sm.win[ring(t)] holds the raw q|k|v row, the K-1 ring slots before
+// it the previous raw rows, sm.fr the gate row, sm.cw / sm.dtb the head's
+// parameters; bval is the beta logit and gval the output gate of column tid
+// (used when has_g).  On return S is updated in registers, sm.alpha / sm.kn /
+// sm.u hold the row's decay, normalised key and update, and the result is the
+// output of column tid (tid < D).  The caller syncs before the next row.
+template <int D>
+__device__ __forceinline__ float row_step(RowSmem<D>& sm, float (&s)[RecShape<D>::RPW][RecShape<D>::CPT],
+                                          int t, int K, const RowConst& rc, float bval, float gval, bool has_g)
+{
+    constexpr int RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r0 = warp * RPW, c0 = lane * CPT;
+
+    // conv window + SiLU, and the decay of each key dim
+    for (int c = tid; c < 3 * D; c += REC_THREADS) {
+        float acc = 0.0f;
+        for (int j = 0; j < K; ++j) acc = __fmaf_rn(sm.cw[c][j], sm.win[ring(t - K + 1 + j)][c], acc);
+        sm.act[c] = siluf_(acc);
+    }
+    for (int i = tid; i < D; i += REC_THREADS)
+        sm.alpha[i] = __expf(log_alpha(rc.gate_mode, rc.lb, rc.ea, sm.fr[i], sm.dtb[i]));
+    row_sync();
+
+    // q / k L2 norms and beta
+    if (warp < 2) {
+        float ss = 0.0f;
+        for (int c = lane; c < D; c += 32) ss = __fmaf_rn(sm.act[warp * D + c], sm.act[warp * D + c], ss);
+        ss = warp_sum(ss);
+        if (lane == 0) sm.scal[warp] = rsqrtf(ss + rc.l2_eps);
+    } else if (warp == 2 && lane == 0) {
+        sm.scal[2] = sigmoidf_(bval);
+    }
+    row_sync();
+    for (int c = tid; c < D; c += REC_THREADS) {
+        sm.qn[c] = sm.act[c] * sm.scal[0];
+        sm.kn[c] = sm.act[D + c] * sm.scal[1];
+    }
+    row_sync();
+
+    // S' = Diag(alpha) S ; kv = S'^T k (partial over this warp's rows)
+    const float beta = sm.scal[2];
+    float part[CPT];
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) part[cc] = 0.0f;
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) {
+        const float ai = sm.alpha[r0 + rr], ki = sm.kn[r0 + rr];
+#pragma unroll
+        for (int cc = 0; cc < CPT; ++cc) {
+            s[rr][cc] = __fmul_rn(ai, s[rr][cc]);
+            part[cc] = __fmaf_rn(s[rr][cc], ki, part[cc]);
+        }
+    }
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) sm.red[warp][c0 + cc] = part[cc];
+    row_sync();
+    if (tid < D) {
+        float kv = 0.0f;
+#pragma unroll
+        for (int w = 0; w < REC_WARPS; ++w) kv += sm.red[w][tid];
+        sm.u[tid] = beta * (sm.act[2 * D + tid] - kv);
+    }
+    row_sync();
+
+    // S = S' + k u^T ; o = S^T q (partial)
+    float uc[CPT];
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) { uc[cc] = sm.u[c0 + cc]; part[cc] = 0.0f; }
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) {
+        const float ki = sm.kn[r0 + rr], qi = sm.qn[r0 + rr];
+#pragma unroll
+        for (int cc = 0; cc < CPT; ++cc) {
+            s[rr][cc] = __fmaf_rn(ki, uc[cc], s[rr][cc]);
+            part[cc] = __fmaf_rn(s[rr][cc], qi, part[cc]);
+        }
+    }
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) sm.red[warp][c0 + cc] = part[cc];
+    row_sync();
+
+    float o = 0.0f;
+    if (tid < D) {
+#pragma unroll
+        for (int w = 0; w < REC_WARPS; ++w) o += sm.red[w][tid];
+        o *= rc.scale;
+    }
+    if (has_g) {
+        // sigmoid-gated RMSNorm over the head's D outputs
+        float sq = tid < D ? o * o : 0.0f;
+        sq = warp_sum(sq);
+        if (lane == 0 && warp < D / 32) sm.scal[4 + warp] = sq;
+        row_sync();
+        if (tid < D) {
+            float tot = 0.0f;
+            for (int w = 0; w < D / 32; ++w) tot += sm.scal[4 + w];
+            const float r = rsqrtf(tot * (1.0f / D) + rc.norm_eps);
+            const float w = rc.norm_w ? rc.norm_w[tid] : 1.0f;
+            o = o * r * w * sigmoidf_(gval);
+        }
+    }
+    return o;
+}
+
+// ------------------------------------------------------------------------
+// Register kernel: one CTA per unit, all of the unit's rows.
+
 template <int D, typename IO, int MODE>
 __global__ void __launch_bounds__(REC_THREADS, 2) kda_recurrent_kernel(const RecArgs a)
 {
     constexpr int RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT;
-    __shared__ RecSmem<D> sm;
+    __shared__ RowSmem<D> sm;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, K = a.K;
     const int seq = blockIdx.x / H, h = blockIdx.x % H;
@@ -140,7 +279,7 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_recurrent_kernel(const Rec
             sm.win[ring(r - (K - 1))][c] = ldv(cs + ((size_t)slot * (K - 1) + r) * conv_dim + ch);
     }
     for (int i = tid; i < D; i += REC_THREADS) sm.dtb[i] = a.dt_bias[(size_t)h * D + i];
-    const float ea = expf(a.A_log[h]);
+    RowConst rc{a.gate_mode, a.lb, expf(a.A_log[h]), a.l2_eps, a.norm_eps, a.scale, a.norm_w};
     __syncthreads();
 
     for (int t = 0; t < L; ++t) {
@@ -155,96 +294,11 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_recurrent_kernel(const Rec
             sm.win[cur][c] = x;
         }
         for (int i = tid; i < D; i += REC_THREADS) sm.fr[i] = ldv(f + rh * D + i);
+        const float bval = ldv(b + rh);
+        const float gval = (g != nullptr && tid < D) ? ldv(g + rh * D + tid) : 0.0f;
         __syncthreads();
 
-        // conv window + SiLU, and the decay of each key dim
-        for (int c = tid; c < 3 * D; c += REC_THREADS) {
-            float acc = 0.0f;
-            for (int j = 0; j < K; ++j) acc = __fmaf_rn(sm.cw[c][j], sm.win[ring(t - K + 1 + j)][c], acc);
-            sm.act[c] = siluf_(acc);
-        }
-        for (int i = tid; i < D; i += REC_THREADS)
-            sm.alpha[i] = __expf(log_alpha(a.gate_mode, a.lb, ea, sm.fr[i], sm.dtb[i]));
-        __syncthreads();
-
-        // q / k L2 norms and beta
-        if (warp < 2) {
-            float ss = 0.0f;
-            for (int c = lane; c < D; c += 32) ss = __fmaf_rn(sm.act[warp * D + c], sm.act[warp * D + c], ss);
-            ss = warp_sum(ss);
-            if (lane == 0) sm.scal[warp] = rsqrtf(ss + a.l2_eps);
-        } else if (warp == 2 && lane == 0) {
-            sm.scal[2] = sigmoidf_(ldv(b + rh));
-        }
-        __syncthreads();
-        for (int c = tid; c < D; c += REC_THREADS) {
-            sm.qn[c] = sm.act[c] * sm.scal[0];
-            sm.kn[c] = sm.act[D + c] * sm.scal[1];
-        }
-        __syncthreads();
-
-        // S' = Diag(alpha) S ; kv = S'^T k (partial over this warp's rows)
-        const float beta = sm.scal[2];
-        float part[CPT];
-#pragma unroll
-        for (int cc = 0; cc < CPT; ++cc) part[cc] = 0.0f;
-#pragma unroll
-        for (int rr = 0; rr < RPW; ++rr) {
-            const float ai = sm.alpha[r0 + rr], ki = sm.kn[r0 + rr];
-#pragma unroll
-            for (int cc = 0; cc < CPT; ++cc) {
-                s[rr][cc] = __fmul_rn(ai, s[rr][cc]);
-                part[cc] = __fmaf_rn(s[rr][cc], ki, part[cc]);
-            }
-        }
-#pragma unroll
-        for (int cc = 0; cc < CPT; ++cc) sm.red[warp][c0 + cc] = part[cc];
-        __syncthreads();
-        if (tid < D) {
-            float kv = 0.0f;
-#pragma unroll
-            for (int w = 0; w < REC_WARPS; ++w) kv += sm.red[w][tid];
-            sm.u[tid] = beta * (sm.act[2 * D + tid] - kv);
-        }
-        __syncthreads();
-
-        // S = S' + k u^T ; o = S^T q (partial)
-        float uc[CPT];
-#pragma unroll
-        for (int cc = 0; cc < CPT; ++cc) { uc[cc] = sm.u[c0 + cc]; part[cc] = 0.0f; }
-#pragma unroll
-        for (int rr = 0; rr < RPW; ++rr) {
-            const float ki = sm.kn[r0 + rr], qi = sm.qn[r0 + rr];
-#pragma unroll
-            for (int cc = 0; cc < CPT; ++cc) {
-                s[rr][cc] = __fmaf_rn(ki, uc[cc], s[rr][cc]);
-                part[cc] = __fmaf_rn(s[rr][cc], qi, part[cc]);
-            }
-        }
-#pragma unroll
-        for (int cc = 0; cc < CPT; ++cc) sm.red[warp][c0 + cc] = part[cc];
-        __syncthreads();
-
-        float o = 0.0f;
-        if (tid < D) {
-#pragma unroll
-            for (int w = 0; w < REC_WARPS; ++w) o += sm.red[w][tid];
-            o *= a.scale;
-        }
-        if (g != nullptr) {
-            // sigmoid-gated RMSNorm over the head's D outputs
-            float sq = tid < D ? o * o : 0.0f;
-            sq = warp_sum(sq);
-            if (lane == 0 && warp < D / 32) sm.scal[4 + warp] = sq;
-            __syncthreads();
-            if (tid < D) {
-                float tot = 0.0f;
-                for (int w = 0; w < D / 32; ++w) tot += sm.scal[4 + w];
-                const float r = rsqrtf(tot * (1.0f / D) + a.norm_eps);
-                const float w = a.norm_w ? a.norm_w[tid] : 1.0f;
-                o = o * r * w * sigmoidf_(ldv(g + rh * D + tid));
-            }
-        }
+        const float o = row_step<D>(sm, s, t, K, rc, bval, gval, g != nullptr);
         if (tid < D) store_out(a.out, rh * D + tid, o, a.out_bf16);
 
         if (MODE == REC_VERIFY) {
@@ -270,6 +324,167 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_recurrent_kernel(const Rec
         }
     }
 }
+
+// ------------------------------------------------------------------------
+// Streaming decode (D = 128): persistent CTAs, producer warp + 8 consumer warps.
+//
+// CTA c owns a contiguous, head-major range of units (u = head * N + seq), so
+// a CTA meets at most a couple of heads and loads each head's conv taps and
+// dt_bias once.  The producer keeps DEC_STAGES units in flight.
+
+constexpr int DEC_D = 128;
+constexpr int DEC_THREADS = REC_THREADS + 32;
+// three stages fit in shared memory with bf16 rows, two with fp32 rows
+template <typename IO> constexpr int dec_stages() { return sizeof(IO) == 2 ? 3 : 2; }
+
+template <typename IO> struct DecStage {
+    float S[DEC_D * DEC_D];        // the unit's state, row-major (64 KiB)
+    IO rows[5][DEC_D];             // raw q, k, v, gate, output-gate rows
+    IO hist[3][3][DEC_D];          // conv history [row][q|k|v][channel]
+    float bval;                    // beta logit
+    int slot;                      // state slot, or -1: skip the unit
+    int pad[2];
+};
+
+template <typename IO> struct DecSmem {
+    static constexpr int STAGES = dec_stages<IO>();
+    DecStage<IO> stage[STAGES];
+    RowSmem<DEC_D> row;
+    float normw[DEC_D];
+    uint64_t full[STAGES], empty[STAGES];
+};
+
+template <typename IO>
+__global__ void __launch_bounds__(DEC_THREADS, 1) kda_decode_stream_kernel(const RecArgs a)
+{
+    extern __shared__ __align__(128) unsigned char dyn_smem[];
+    DecSmem<IO>& sm = *reinterpret_cast<DecSmem<IO>*>(dyn_smem);
+    constexpr int D = DEC_D;
+    constexpr int DEC_STAGES = DecSmem<IO>::STAGES;
+    constexpr int RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.H, K = a.K, N = a.N;
+    const int conv_dim = H * 3 * D;
+    const int units = N * H;
+    const int u_begin = (int)(((long long)units * blockIdx.x) / gridDim.x);
+    const int u_end = (int)(((long long)units * (blockIdx.x + 1)) / gridDim.x);
+
+    if (tid == 0) {
+        for (int s = 0; s < DEC_STAGES; ++s) {
+            ptx::mbar_init(&sm.full[s], 1);
+            ptx::mbar_init(&sm.empty[s], 1);
+        }
+        ptx::fence_mbar_init();
+    }
+    for (int c = tid; c < D; c += DEC_THREADS) sm.normw[c] = a.norm_w ? a.norm_w[c] : 1.0f;
+    __syncthreads();
+
+    const IO* q = static_cast<const IO*>(a.q);
+    const IO* k = static_cast<const IO*>(a.k);
+    const IO* v = static_cast<const IO*>(a.v);
+    const IO* f = static_cast<const IO*>(a.f);
+    const IO* b = static_cast<const IO*>(a.b);
+    const IO* g = static_cast<const IO*>(a.g);
+    IO* cs = static_cast<IO*>(a.conv_state);
+    const bool has_g = g != nullptr;
+
+    if (warp == REC_WARPS) {
+        // ---------------- producer
+        if (lane != 0) return;
+        const uint64_t pol = ptx::policy_evict_first();
+        for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
+            const int s = i % DEC_STAGES, n = i / DEC_STAGES;
+            if (n > 0 && !ptx::mbar_wait(&sm.empty[s], (n - 1) & 1)) {
+                flag_status(a.dev_status, KDA_DEV_TIMEOUT);
+                return;
+            }
+            DecStage<IO>& st = sm.stage[s];
+            const int h = u / N, seq = u % N;
+            int slot = a.slots ? a.slots[seq] : seq;
+            if (slot >= a.num_slots) {
+                flag_status(a.dev_status, KDA_DEV_BAD_SLOT);
+                slot = -1;
+            }
+            if (slot >= 0) {
+                const uint32_t rowb = D * sizeof(IO);
+                const uint32_t bytes = D * D * 4 + (has_g ? 5 : 4) * rowb + 3 * (K - 1) * rowb;
+                asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(ptx::smem_u32(&sm.full[s])),
+                             "r"(bytes) : "memory");
+                ptx::bulk_g2s_stream(st.S, a.rec_state + ((size_t)slot * H + h) * D * D, D * D * 4, &sm.full[s], pol);
+                const size_t rh = (size_t)seq * H + h;
+                ptx::bulk_g2s(st.rows[0], q + rh * D, rowb, &sm.full[s]);
+                ptx::bulk_g2s(st.rows[1], k + rh * D, rowb, &sm.full[s]);
+                ptx::bulk_g2s(st.rows[2], v + rh * D, rowb, &sm.full[s]);
+                ptx::bulk_g2s(st.rows[3], f + rh * D, rowb, &sm.full[s]);
+                if (has_g) ptx::bulk_g2s(st.rows[4], g + rh * D, rowb, &sm.full[s]);
+                for (int r = 0; r < K - 1; ++r)
+                    for (int seg = 0; seg < 3; ++seg)
+                        ptx::bulk_g2s(st.hist[r][seg],
+                                      cs + ((size_t)slot * (K - 1) + r) * conv_dim + (size_t)seg * H * D + h * D,
+                                      rowb, &sm.full[s]);
+                st.bval = ldv(b + rh);
+            }
+            st.slot = slot;
+            ptx::mbar_arrive(&sm.full[s]);
+        }
+        return;
+    }
+
+    // ---------------- consumers (256 threads)
+    const int r0 = warp * RPW, c0 = lane * CPT;
+    float sreg[RPW][CPT];
+    int cur_head = -1;
+    RowConst rc{a.gate_mode, a.lb, 0.0f, a.l2_eps, a.norm_eps, a.scale, sm.normw};
+    for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
+        const int s = i % DEC_STAGES, n = i / DEC_STAGES;
+        const int h = u / N, seq = u % N;
+        if (h != cur_head) {
+            // this head's conv taps, dt_bias and decay scale (L2-resident)
+            for (int c = tid; c < 3 * D; c += REC_THREADS) {
+                const int ch = conv_channel<D>(c, h, H);
+                for (int j = 0; j < K; ++j) sm.row.cw[c][j] = a.conv_w[(size_t)ch * K + j];
+            }
+            for (int c = tid; c < D; c += REC_THREADS) sm.row.dtb[c] = a.dt_bias[(size_t)h * D + c];
+            rc.ea = expf(a.A_log[h]);
+            cur_head = h;
+        }
+        if (!ptx::mbar_wait(&sm.full[s], n & 1)) {
+            if (tid == 0) flag_status(a.dev_status, KDA_DEV_TIMEOUT);
+            return;
+        }
+        DecStage<IO>& st = sm.stage[s];
+        const int slot = st.slot;
+        float bval = 0.0f, gval = 0.0f;
+        if (slot >= 0) {
+            load_tile_smem<D>(st.S, r0, c0, sreg);
+            for (int c = tid; c < 3 * D; c += REC_THREADS) {
+                const int seg = c / D, ch = c % D;
+                for (int r = 0; r < K - 1; ++r) sm.row.win[ring(r - (K - 1))][c] = ldv(&st.hist[r][seg][ch]);
+                sm.row.win[ring(0)][c] = ldv(&st.rows[seg][ch]);
+            }
+            for (int c = tid; c < D; c += REC_THREADS) sm.row.fr[c] = ldv(&st.rows[3][c]);
+            bval = st.bval;
+            if (has_g && tid < D) gval = ldv(&st.rows[4][tid]);
+        }
+        row_sync();  // stage s fully read: hand it back to the producer
+        if (tid == 0) ptx::mbar_arrive(&sm.empty[s]);
+        if (slot < 0) continue;
+
+        const float o = row_step<D>(sm.row, sreg, 0, K, rc, bval, gval, has_g);
+        const size_t rh = (size_t)seq * H + h;
+        if (tid < D) store_out(a.out, rh * D + tid, o, a.out_bf16);
+        store_tile<D>(a.rec_state + ((size_t)slot * H + h) * D * D, r0, c0, sreg);
+        for (int c = tid; c < 3 * D; c += REC_THREADS) {
+            const int ch = conv_channel<D>(c, h, H);
+            for (int r = 0; r < K - 1; ++r)
+                stv(cs + ((size_t)slot * (K - 1) + r) * conv_dim + ch, sm.row.win[ring(1 - (K - 1) + r)][c]);
+        }
+        row_sync();  // row arrays are rewritten by the next unit
+    }
+}
+
+// ------------------------------------------------------------------------
+// Commit: replay the accepted prefix of a verify window from its log.
 
 template <int D, typename IO>
 __global__ void __launch_bounds__(REC_THREADS, 2) kda_commit_kernel(const CommitArgs a)
@@ -324,6 +539,42 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_commit_kernel(const Commit
     }
 }
 
+// ------------------------------------------------------------------------
+// launchers
+
+static int sm_count()
+{
+    static int n[128];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 128) return 148;
+    if (n[dev] == 0) {
+        int c = 0;
+        cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+        n[dev] = c > 0 ? c : 148;
+    }
+    return n[dev];
+}
+
+static_assert(sizeof(DecSmem<__nv_bfloat16>) <= 232448, "decode stage buffers exceed shared memory");
+static_assert(sizeof(DecSmem<float>) <= 232448, "decode stage buffers exceed shared memory");
+
+template <typename IO> static cudaError_t launch_decode_stream(const RecArgs& a, int units, cudaStream_t st)
+{
+    static bool attr_done[128];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int smem = (int)sizeof(DecSmem<IO>);
+    if (dev >= 0 && dev < 128 && !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kda_decode_stream_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    const int grid = units < sm_count() ? units : sm_count();
+    kda_decode_stream_kernel<IO><<<grid, DEC_THREADS, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
 template <int D, typename IO>
 static cudaError_t launch_rec_d(int mode, const RecArgs& a, int units, cudaStream_t st)
 {
@@ -340,7 +591,10 @@ cudaError_t launch_recurrent(int mode, int io_bf16, const RecArgs& a, int units,
     switch (a.D) {
     case 32: return io_bf16 ? launch_rec_d<32, __nv_bfloat16>(mode, a, units, st) : launch_rec_d<32, float>(mode, a, units, st);
     case 64: return io_bf16 ? launch_rec_d<64, __nv_bfloat16>(mode, a, units, st) : launch_rec_d<64, float>(mode, a, units, st);
-    case 128: return io_bf16 ? launch_rec_d<128, __nv_bfloat16>(mode, a, units, st) : launch_rec_d<128, float>(mode, a, units, st);
+    case 128:
+        if (mode == REC_DECODE)
+            return io_bf16 ? launch_decode_stream<__nv_bfloat16>(a, units, st) : launch_decode_stream<float>(a, units, st);
+        return io_bf16 ? launch_rec_d<128, __nv_bfloat16>(mode, a, units, st) : launch_rec_d<128, float>(mode, a, units, st);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -25,6 +25,7 @@ KDA_ERR_DEVICE = 6
 KDA_DEV_BAD_SEQLENS = 1
 KDA_DEV_BAD_SLOT = 2
 KDA_DEV_BAD_ACCEPTED = 4
+KDA_DEV_TIMEOUT = 8
 KDA_DTYPE_F32 = 0
 KDA_DTYPE_BF16 = 1
 KDA_GATE_SOFTPLUS = 0
@@ -185,3 +186,25 @@ def kda_commit(params: Params, B: int, W: int, accepted, slots, log, conv_state,
     return load().kda_commit(
         ctypes.byref(params.c_struct()), B, W, _ptr(accepted), _ptr(slots), _ptr(log),
         _ptr(conv_state), _ptr(rec_state), _ptr(dev_status), _stream(stream))
+
+
+class Prepared:
+    """A call of one entry point with its arguments marshalled once.
+
+    ``Prepared("kda_decode", params, B, q, ...)()`` calls the C function with
+    the same pointers every time (the tensors must stay alive and in place).
+    """
+
+    def __init__(self, name: str, params: Params, *args, stream=None):
+        self.fn = getattr(load(), name)
+        self.pstruct = params.c_struct()
+        conv = []
+        for a in args:
+            if a is None or isinstance(a, int):
+                conv.append(a)
+            else:
+                conv.append(a.data_ptr())
+        self.args = (ctypes.byref(self.pstruct), *conv, _stream(stream))
+
+    def __call__(self) -> int:
+        return self.fn(*self.args)
