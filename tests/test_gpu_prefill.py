@@ -49,6 +49,32 @@ def test_varlen_cases(cuda_lib, oracle_mod, lens, d, io, gate, K, og, init):
     _check_all(_prefill(cuda_lib, wl), oracle_mod.forward(wl))
 
 
+CHUNK = [
+    # lens, K, out_gate, init -- dk = dv = 128, bf16 rows, safe gate: the tensor-core path
+    ([1, 63, 64, 65], 4, True, "random"),
+    ([128, 200, 17], 2, False, "zero"),
+    ([333], 3, True, "random"),
+]
+
+
+@pytest.mark.parametrize("lens,K,og,init", CHUNK)
+def test_chunk_path_cases(cuda_lib, oracle_mod, lens, K, og, init):
+    wl = W.make_workload("ck", 400 + sum(lens) + K, lens, H=2, d=128, K=K, io_dtype=W.BF16,
+                         gate_mode=W.SAFE, lower_bound=-5.0, out_gate=og, init_state=init)
+    _check_all(_prefill(cuda_lib, wl), oracle_mod.forward(wl))
+
+
+@pytest.mark.parametrize("fval", [-30.0, 30.0])
+def test_chunk_gate_extremes(cuda_lib, oracle_mod, fval):
+    """Every row at the gate's ends: alpha ~ 1 (long memory, f -> -inf) and
+    log alpha ~ -5 (the lower bound, the widest factor range in a chunk)."""
+    wl = W.make_workload("gx", 420, [150, 64], H=2, d=128, K=4, io_dtype=W.BF16,
+                         gate_mode=W.SAFE, lower_bound=-5.0, out_gate=False, init_state="random")
+    wl.arrays["f"][:] = fval
+    wl.arrays["A_log"][:] = 0.0
+    _check_all(_prefill(cuda_lib, wl), oracle_mod.forward(wl))
+
+
 def test_bf16_output(cuda_lib, oracle_mod):
     wl = W.make_workload("vlb", 311, [100, 37], H=2, d=128, K=4, io_dtype=W.BF16,
                          gate_mode=W.SAFE, lower_bound=-5.0, out_gate=True, init_state="random")
