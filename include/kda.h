@@ -125,6 +125,32 @@ KDA_API int kda_prefill_varlen(const kda_params* p, const int32_t* cu_seqlens, i
 KDA_API size_t kda_prefill_workspace_bytes(const kda_params* p, int32_t N, int32_t T);
 
 /*
+ * kda_prefill_varlen without a caller-provided workspace, for callers that
+ * cannot allocate device memory (an allocator-free runtime, a plugin barred
+ * from the host's memory pools, a serving loop that must never call
+ * cudaMalloc).  The source pages have no counterpart: this is a service of
+ * this library.  Arguments and results are those of kda_prefill_varlen; the
+ * scratch is a fixed array of kda_prefill_static_workspace_capacity() bytes
+ * (256 KiB: up to 65535 sequences per call) in the library's device memory
+ * on every GPU that uses it, kept until the process exits.
+ *   - Allocates nothing and calls no allocating routine.
+ *   - Returns KDA_ERR_WORKSPACE, before any launch, when N needs more scratch
+ *     than the array holds.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the array.  Calls whose kernels could run at the same
+ *     time on one GPU (unordered streams) race on it: order them.
+ */
+KDA_API int kda_prefill_varlen_static_ws(const kda_params* p, const int32_t* cu_seqlens, int32_t N,
+                                         int32_t T, const void* q, const void* k, const void* v,
+                                         const void* gate, const void* beta, const void* out_gate,
+                                         const int32_t* slots, void* conv_state, float* rec_state,
+                                         void* out, int32_t* dev_status, cudaStream_t stream);
+
+/* Bytes of the built-in scratch behind kda_prefill_varlen_static_ws. */
+KDA_API size_t kda_prefill_static_workspace_capacity(void);
+
+/*
  * Decode: one row per sequence, B sequences (row b belongs to sequence b).
  * Updates the conv and recurrent states in place and writes out [B][H][dv]
  * (TensorFold #850, Oct 15 comment: decode rows).

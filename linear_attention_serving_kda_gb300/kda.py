@@ -51,6 +51,9 @@ _SIG = {
     "kda_prefill_varlen": (ctypes.c_int, [ctypes.POINTER(kda_params), _VP, _I32, _I32, _VP, _VP, _VP, _VP,
                                           _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP, _VP]),
     "kda_prefill_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(kda_params), _I32, _I32]),
+    "kda_prefill_varlen_static_ws": (ctypes.c_int, [ctypes.POINTER(kda_params), _VP, _I32, _I32, _VP, _VP, _VP,
+                                                    _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "kda_prefill_static_workspace_capacity": (ctypes.c_size_t, []),
     "kda_decode": (ctypes.c_int, [ctypes.POINTER(kda_params), _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   _VP, _VP, _VP, _VP, _VP]),
     "kda_verify_window": (ctypes.c_int, [ctypes.POINTER(kda_params), _I32, _I32, _VP, _VP, _VP, _VP, _VP,
@@ -163,6 +166,20 @@ def kda_prefill_varlen(params: Params, cu_seqlens, N: int, T: int, q, k, v, gate
         ctypes.byref(params.c_struct()), _ptr(cu_seqlens), N, T, _ptr(q), _ptr(k), _ptr(v), _ptr(gate),
         _ptr(beta), _ptr(out_gate), _ptr(slots), _ptr(conv_state), _ptr(rec_state), _ptr(out),
         _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
+
+
+def kda_prefill_varlen_static_ws(params: Params, cu_seqlens, N: int, T: int, q, k, v, gate, beta, out_gate,
+                                 slots, conv_state, rec_state, out, dev_status=None, stream=None) -> int:
+    """kda_prefill_varlen with the library's built-in scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    return load().kda_prefill_varlen_static_ws(
+        ctypes.byref(params.c_struct()), _ptr(cu_seqlens), N, T, _ptr(q), _ptr(k), _ptr(v), _ptr(gate),
+        _ptr(beta), _ptr(out_gate), _ptr(slots), _ptr(conv_state), _ptr(rec_state), _ptr(out),
+        _ptr(dev_status), _stream(stream))
+
+
+def kda_prefill_static_workspace_capacity() -> int:
+    return load().kda_prefill_static_workspace_capacity()
 
 
 def kda_decode(params: Params, B: int, q, k, v, gate, beta, out_gate, slots, conv_state, rec_state,
