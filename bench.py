@@ -177,6 +177,22 @@ def bench_decode(kda, steps, warmup, stream):
     return wl, sets, step, per_set
 
 
+def max_over_ranks(x: float, dist) -> float:
+    """The largest of every rank's x (the job is as slow as its slowest rank)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(tokens_per_rank_step: int, world: int, steps: int, total_ms: float) -> float:
+    """Whole-job tokens/s: every rank processes its own batch each step."""
+    return tokens_per_rank_step * world * steps / (total_ms * 1e-3)
+
+
 def run_timed(step, steps, stream, dist):
     import torch
 
@@ -190,12 +206,7 @@ def run_timed(step, steps, stream, dist):
     if dist is not None:
         dist.barrier()
     wall = time.perf_counter() - t_wall
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64,
-                         device="cuda" if dist.get_backend() == "nccl" else "cpu")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    return total_ms, durs, wall
+    return max_over_ranks(total_ms, dist), durs, wall
 
 
 def leg_prefill(kda, wl_fn, reps, stream):
@@ -305,6 +316,23 @@ def oracle_decode_rate(seconds=10.0):
     return wl.N * steps / el, cores, steps, el
 
 
+def measured_traffic():
+    """DRAM bytes per decode launch from the committed ncu record, or None
+    when the kernel source has changed since the counters were taken."""
+    import hashlib
+
+    tpath = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(tpath) as fh:
+            rec = json.load(fh)
+        with open(os.path.join(ROOT, rec["source"]), "rb") as fh:
+            if hashlib.sha256(fh.read()).hexdigest() != rec["source_sha256"]:
+                return None
+        return rec["bytes_per_launch"]
+    except Exception:
+        return None
+
+
 # --------------------------------------------------------------------- main
 
 def main():
@@ -316,7 +344,7 @@ def main():
     ap.add_argument("--no-legs", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "verify", "prefill_varlen", "prefill_long"])
+                    choices=["decode", "verify", "prefill_varlen", "prefill_long", "prefill_small"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -363,8 +391,7 @@ def main():
     wl, sets, step, per_set = bench_decode(kda, args.steps, args.warmup, stream)
     total_ms, durs, wall = run_timed(step, args.steps, stream, dist)
     ms = total_ms / args.steps
-    tokens = wl.N * world * args.steps
-    value = tokens / (total_ms * 1e-3)
+    value = weak_scaling_value(wl.N, world, args.steps, total_ms)
     kernel_ms = statistics.mean(durs)
     achieved = per_set / (kernel_ms * 1e-3) / 1e9
 
@@ -387,14 +414,7 @@ def main():
         cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"full decode step (64 seq x 32 heads) repeated {n}x with carried state, {el:.1f} s"}
 
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "decode_traffic.json")
-    if os.path.exists(tpath):
-        try:
-            with open(tpath) as fh:
-                traffic = json.load(fh).get("bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = measured_traffic()
 
     line = {
         "metric": "KDA tokens/s (decode step; prefill and verify legs alongside)",
@@ -406,7 +426,7 @@ def main():
                    "epilogue": "sigmoid-gated RMSNorm", "parallelism": f"replica x{world}",
                    "l2": f"inputs rotate over {len(sets)} sets, {len(sets) * per_set / 1e6:.0f} MB > L2"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": achieved / hbm_gbs, "traffic": traffic, "kernel": "kda_recurrent_kernel<decode>",
+                     "frac": achieved / hbm_gbs, "traffic": traffic, "kernel": "kda_decode_stream_kernel<bf16>",
                      "alg_bytes_per_launch": per_set, "peak_source": peak_src},
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -425,6 +445,12 @@ def run_single_leg(kda, args, stream):
 
     if args.workload == "verify":
         return leg_verify(kda, args.steps, stream)
+    if args.workload == "prefill_small":
+        # a profiling-sized prefill: 2 sequences x 2048 rows, 32 heads, same dtypes and gate
+        fn = lambda: W.make_workload("prefill_small_n2x2048_h32_d128_bf16", 5, [2048, 2048], H=32, d=128,  # noqa: E731
+                                     K=4, io_dtype=W.BF16, gate_mode=W.SAFE, lower_bound=-5.0,
+                                     init_state="random")
+        return leg_prefill(kda, fn, args.steps, stream)
     fn = W.varlen_prefill_case if args.workload == "prefill_varlen" else W.long_prefill_case
     return leg_prefill(kda, fn, args.steps, stream)
 
