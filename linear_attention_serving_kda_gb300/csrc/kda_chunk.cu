@@ -1,6 +1,6 @@
 // kda_chunk.cu -- chunked (WY/UT) KDA prefill on tcgen05 tensor cores (sm_103a).
 //
-// One CTA (256 threads, one per SM) walks one (sequence, head) chain in chunks
+// One CTA (512 threads, one per SM) walks one (sequence, head) chain in chunks
 // of C = 64 rows, restarting at each segment's first row (TensorFold issue
 // #850, Oct 15 comment: prompt rows in chunks from a segment's first row).
 // With G_r = sum_{t<=r} log alpha_t inside a chunk (per key dim) and S the
@@ -57,7 +57,8 @@ namespace chk {
 
 constexpr int D = 128;
 constexpr int C = 64;
-constexpr int NT = 256;
+constexpr int NT = 512;         // 16 warps: thread (column c, quarter q) owns rows [16q, 16q+16) of column c
+constexpr int RPT = 16;         // rows per thread
 constexpr int HALO = 3;
 constexpr int RAWR = C + HALO;  // staged raw rows per tensor
 
@@ -69,6 +70,7 @@ constexpr uint32_t TM_COLS = 512;
 constexpr int SM_RAW = 0;                      // q, k, v [67][128] bf16 then f [64][128] bf16
 constexpr int RAW_T = RAWR * D * 2;            // 17152 per tensor
 constexpr int SM_RAWF = 3 * RAW_T;             // 51456
+constexpr int RAW_END = SM_RAWF + C * D * 2;   // 67840
 constexpr int SM_AX = 0;                       // [Q~lo | K~ | Q~hi] x 4 K-blocks of 24 KiB
 constexpr int AX_KB = 3 * 64 * 128;            // 24576
 constexpr int SM_B1H = 98304;                  // B1 high, 96 rows x 128 K
@@ -79,21 +81,22 @@ constexpr int SM_AKK = 0;                      // A [64][65] fp32 (after the fir
 constexpr int SM_PTMP = 16896;                 // [Q~lo ; K~] B1hi^T part of P [64][65]
 constexpr int SM_TS = 33792;                   // solve scratch [64][65]
 constexpr int SM_T = 51200;                    // T tile 64 x 64
-constexpr int SM_PH = 67584;                   // P high tile 64 x 64
-constexpr int SM_PL = 83968;                   // P low tile
-constexpr int SM_QE = 100352;                  // Q o e^G tile 64 x 128
-constexpr int SM_KD = 133120;                  // (K o e^{G_C - G})^T tile 128 x 64
-constexpr int SM_KDL = 165888;                 // low part of the KD tile
+constexpr int SM_PH = 68608;                   // P high tile 64 x 64
+constexpr int SM_PL = 84992;                   // P low tile
+constexpr int SM_QE = 101376;                  // Q o e^G tile 64 x 128
+constexpr int SM_KD = 134144;                  // (K o e^{G_C - G})^T tile 128 x 64
+constexpr int SM_KDL = 166912;                 // low part of the KD tile
 constexpr int SM_QEL = 0;                      // low part of the QE tile (after the solve)
 constexpr int SM_NW = 33792;                   // -W tile 64 x 128 (after the second product)
-constexpr int SM_MISC = 198656;
+constexpr int SM_MISC = 199680;
 struct Misc {
     float beta[C];
-    float gx[3][D];           // G at rows 31, 48, 63 (per key dim)
-    float npart[2][2][4][32]; // q/k row-norm partials [qk][half][warp][row]
+    float gq[4][D];           // per-quarter totals of log alpha (per key dim)
+    float gx[3][D];           // G at rows 16, 48, 63
+    float npart[2][4][4][16]; // q/k row-norm partials [qk][quarter][lane quarter][row]
     float nrm[2][C];          // q/k inverse norms
     float gamma[D];           // e^{G_C}
-    float epart[2][4][32];    // output-norm partials
+    float epart[4][4][16];    // output-norm partials [quarter][lane quarter][row]
     float rms[C];
     float M[3][16][16];       // solve scratch
     uint64_t bar;
@@ -101,7 +104,7 @@ struct Misc {
     int err;
 };
 constexpr int SMEM_BYTES = SM_MISC + (int)sizeof(Misc);
-static_assert(SM_RAWF + C * D * 2 <= SM_B1H, "raw staging overlaps B1");
+static_assert(RAW_END <= SM_B1H && RAW_END <= SM_PH, "raw staging overlaps B1 or the P tiles");
 static_assert(SM_AX + 4 * AX_KB <= SM_B1H && SM_B1H + 4 * B1_KB <= SM_B1L && SM_B1L + 4 * B1_KB <= SM_MISC,
               "first-product operands overlap");
 static_assert(SM_PTMP >= SM_AKK + 64 * 65 * 4 && SM_TS >= SM_PTMP + 64 * 65 * 4 && SM_T >= SM_TS + 64 * 65 * 4,
@@ -143,12 +146,12 @@ __device__ __forceinline__ void st_hilo(unsigned char* sm, uint32_t off_hi, uint
     st_raw(sm, off_lo, tf32r(x - hi));
 }
 
-// Warp transpose-reduction: v[k] (k = 0..31) per lane -> lane l returns the
-// sum over the warp's lanes of v[l].  31 shuffles.
-__device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane)
+// Warp transpose-reduction of 16 values per lane: lane l returns the sum over
+// all 32 lanes of v[l & 15].  16 shuffles.
+__device__ __forceinline__ float transpose_reduce16(float (&v)[16], int lane)
 {
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
+    for (int off = 8; off >= 1; off >>= 1) {
         const bool up = (lane & off) != 0;
 #pragma unroll
         for (int k = 0; k < off; ++k) {
@@ -157,7 +160,7 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane)
             v[k] = keep + __shfl_xor_sync(0xffffffffu, give, off);
         }
     }
-    return v[0];
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
 __device__ __forceinline__ uint64_t dsc(unsigned char* sm, int off)
@@ -192,13 +195,50 @@ __global__ void kda_chunk_schedule_kernel(const int32_t* cu, int N, int32_t* ord
     }
 }
 
+// Issue the cp.async copies of one chunk's raw rows (q, k, v with 3 halo rows,
+// the first chunk's halo from the conv state; gate rows); zero beyond the segment.
+__device__ __forceinline__ void stage_chunk(unsigned char* sm, const ChunkArgs& a, int c0, int seg0, int seg1,
+                                            int slot, int h)
+{
+    const int H = a.H, K = a.K, conv_dim = 3 * H * D;
+    const __nv_bfloat16* cs = static_cast<const __nv_bfloat16*>(a.conv_state);
+    const __nv_bfloat16* fg = static_cast<const __nv_bfloat16*>(a.f);
+    for (int idx = threadIdx.x; idx < 3 * RAWR * 16; idx += NT) {
+        const int tsel = idx / (RAWR * 16), rem = idx % (RAWR * 16), sr = rem >> 4, c16 = rem & 15;
+        const int gr = c0 - HALO + sr;
+        const __nv_bfloat16* base = static_cast<const __nv_bfloat16*>(tsel == 0 ? a.q : (tsel == 1 ? a.k : a.v));
+        const void* src = base;
+        uint32_t bytes = 0;
+        if (gr >= seg0 && gr < seg1) {
+            src = base + ((size_t)gr * H + h) * D + c16 * 8;
+            bytes = 16;
+        } else if (gr < seg0) {
+            const int cr = (K - 1) + (gr - seg0);  // conv-state row
+            if (cr >= 0) {
+                src = cs + ((size_t)slot * (K - 1) + cr) * conv_dim + (size_t)tsel * H * D + h * D + c16 * 8;
+                bytes = 16;
+            }
+        }
+        ptx::cp_async16(sm + SM_RAW + tsel * RAW_T + sr * (D * 2) + c16 * 16, src, bytes);
+    }
+    for (int idx = threadIdx.x; idx < C * 16; idx += NT) {
+        const int sr = idx >> 4, c16 = idx & 15, gr = c0 + sr;
+        const bool ok = gr < seg1;
+        ptx::cp_async16(sm + SM_RAWF + sr * (D * 2) + c16 * 16,
+                        ok ? (const void*)(fg + ((size_t)gr * H + h) * D + c16 * 8) : (const void*)fg, ok ? 16 : 0);
+    }
+    ptx::cp_async_commit();
+}
+
 __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
 {
     extern __shared__ __align__(1024) unsigned char sm[];
     Misc& ms = *reinterpret_cast<Misc*>(sm + SM_MISC);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int col = tid & (D - 1);  // channel / key dim / value dim / TMEM lane of this thread
-    const int half = tid >> 7;      // chunk rows [32*half, 32*half + 32)
+    const int qq = tid >> 7;        // quarter: chunk rows [16 qq, 16 qq + 16); also the TMEM column group
+    const int half = qq >> 1;       // 32-row half holding those rows
+    const int lq = warp & 3;        // TMEM lane quarter of this warp (lanes 32 lq ..)
     const int H = a.H, K = a.K;
     const int conv_dim = 3 * H * D;
     const int seq = a.schedule ? a.schedule[blockIdx.x / H] : blockIdx.x / H;
@@ -222,14 +262,11 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
         return;
     }
 
-    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
-    const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
-    const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(a.v);
-    const __nv_bfloat16* fg = static_cast<const __nv_bfloat16*>(a.f);
     const __nv_bfloat16* bg = static_cast<const __nv_bfloat16*>(a.b);
     const __nv_bfloat16* gg = static_cast<const __nv_bfloat16*>(a.g);
     __nv_bfloat16* cs = static_cast<__nv_bfloat16*>(a.conv_state);
 
+    stage_chunk(sm, a, seg0, seg0, seg1, slot, h);  // first chunk's rows, in flight during set-up
     if (warp == 0) ptx::tmem_alloc(&ms.tmem, TM_COLS);
     if (tid == 0) {
         ptx::mbar_init(&ms.bar, 1);
@@ -240,8 +277,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = ms.tmem;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quarter
-    const int lrow = (warp & 3) * 32 + lane;                        // TMEM lane of this thread (== col)
+    const uint32_t lane_base = (uint32_t)(lq * 32) << 16;  // this warp's TMEM lane quarter
     uint32_t ph = 0;
 
     // ---- per-CTA constants: this thread's conv taps (4-tap form) and gate params
@@ -257,51 +293,24 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
     const float ea = expf(a.A_log[h]);
     const float nw = a.norm_w ? a.norm_w[col] : 1.0f;
 
-    // ---- initial state -> TMEM S^T (lane j = col, key dims [64*half, +64))
+    // ---- initial state -> TMEM S^T (lane j = col, key dims [32 qq, +32))
     {
         const float* Sg = a.rec_state + ((size_t)slot * H + h) * D * D;
         float v[32];
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-#pragma unroll
-            for (int x = 0; x < 32; ++x) v[x] = Sg[(size_t)(64 * half + 32 * part + x) * D + col];
-            ptx::tmem_st32(tmem + lane_base + TM_ST + 64 * half + 32 * part, v);
-        }
+        for (int x = 0; x < 32; ++x) v[x] = Sg[(size_t)(32 * qq + x) * D + col];
+        ptx::tmem_st32(tmem + lane_base + TM_ST + 32 * qq, v);
     }
 
     const int nchunks = (seg1 - seg0 + C - 1) / C;
+    float bnext = 0.0f;  // beta logit of row `tid` of the next chunk
+    if (tid < C && seg0 + tid < seg1) bnext = __bfloat162float(bg[(size_t)(seg0 + tid) * H + h]);
     for (int ch = 0; ch < nchunks && !ms.err; ++ch) {
         const int c0 = seg0 + ch * C;
         const int nvalid = min(C, seg1 - c0);
-        const int r0 = 32 * half;
+        const int r0 = RPT * qq;
 
-        // ---- stage the raw rows (q, k, v with 3 halo rows; gate f) in shared memory
-        for (int idx = tid; idx < 3 * RAWR * 16; idx += NT) {
-            const int tsel = idx / (RAWR * 16), rem = idx % (RAWR * 16), sr = rem >> 4, c16 = rem & 15;
-            const int gr = c0 - HALO + sr;
-            const __nv_bfloat16* base = tsel == 0 ? qg : (tsel == 1 ? kg : vg);
-            const void* src = base;
-            uint32_t bytes = 0;
-            if (gr >= seg0 && gr < seg1) {
-                src = base + ((size_t)gr * H + h) * D + c16 * 8;
-                bytes = 16;
-            } else if (gr < seg0) {
-                const int cr = (K - 1) + (gr - seg0);  // conv-state row
-                if (cr >= 0) {
-                    src = cs + ((size_t)slot * (K - 1) + cr) * conv_dim + (size_t)tsel * H * D + h * D + c16 * 8;
-                    bytes = 16;
-                }
-            }
-            ptx::cp_async16(sm + SM_RAW + tsel * RAW_T + sr * (D * 2) + c16 * 16, src, bytes);
-        }
-        for (int idx = tid; idx < C * 16; idx += NT) {
-            const int sr = idx >> 4, c16 = idx & 15, gr = c0 + sr;
-            const bool ok = gr < seg1;
-            ptx::cp_async16(sm + SM_RAWF + sr * (D * 2) + c16 * 16,
-                            ok ? (const void*)(fg + ((size_t)gr * H + h) * D + c16 * 8) : (const void*)fg, ok ? 16 : 0);
-        }
-        ptx::cp_async_commit();
-        if (tid < C) ms.beta[tid] = tid < nvalid ? sigmoidf_(__bfloat162float(bg[(size_t)(c0 + tid) * H + h])) : 0.0f;
+        if (tid < C) ms.beta[tid] = tid < nvalid ? sigmoidf_(bnext) : 0.0f;
         ptx::cp_async_wait_all();
         __syncthreads();
 
@@ -317,8 +326,8 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
             }
         }
 
-        // ---- prep: conv + SiLU, gate, running G for this thread's column and 32 rows
-        float qv[32], kv[32], vv[32], G[32];
+        // ---- prep: conv + SiLU, gate, running log-decay for this thread's column and 16 rows
+        float qv[RPT], kv[RPT], vv[RPT], G[RPT];
         {
             float xq[4], xk[4], xv[4];
 #pragma unroll
@@ -329,7 +338,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
             }
             float run = 0.0f;
 #pragma unroll
-            for (int r = 0; r < 32; ++r) {
+            for (int r = 0; r < RPT; ++r) {
                 const int lr = r0 + r;
                 xq[3] = __bfloat162float(raw[0 * RAWR * D + (lr + 3) * D + col]);
                 xk[3] = __bfloat162float(raw[1 * RAWR * D + (lr + 3) * D + col]);
@@ -352,75 +361,81 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
                 for (int j = 0; j < 3; ++j) { xq[j] = xq[j + 1]; xk[j] = xk[j + 1]; xv[j] = xv[j + 1]; }
             }
         }
-        // row norms of q' and k' (this warp's 32 columns), and the first half's G total
+        // row norms of q' and k' (this warp's 32 columns) and this quarter's log-decay total
         {
-            float t[32];
+            float t[RPT];
 #pragma unroll
-            for (int r = 0; r < 32; ++r) t[r] = qv[r] * qv[r];
-            const float pq = transpose_reduce(t, lane);
+            for (int r = 0; r < RPT; ++r) t[r] = qv[r] * qv[r];
+            const float pq = transpose_reduce16(t, lane);
 #pragma unroll
-            for (int r = 0; r < 32; ++r) t[r] = kv[r] * kv[r];
-            const float pk = transpose_reduce(t, lane);
-            ms.npart[0][half][warp & 3][lane] = pq;
-            ms.npart[1][half][warp & 3][lane] = pk;
-            if (half == 0) ms.gx[0][col] = G[31];
+            for (int r = 0; r < RPT; ++r) t[r] = kv[r] * kv[r];
+            const float pk = transpose_reduce16(t, lane);
+            if (lane < 16) {
+                ms.npart[0][qq][lq][lane] = pq;
+                ms.npart[1][qq][lq][lane] = pk;
+            }
+            ms.gq[qq][col] = G[RPT - 1];
         }
         __syncthreads();
-        if (half == 1) {
-            const float g31 = ms.gx[0][col];
+        {
+            float off = 0.0f;
+            for (int q2 = 0; q2 < qq; ++q2) off += ms.gq[q2][col];
 #pragma unroll
-            for (int r = 0; r < 32; ++r) G[r] += g31;
-            ms.gx[1][col] = G[16];   // row 48
-            ms.gx[2][col] = G[31];   // row 63 (G_C)
-            ms.gamma[col] = __expf(G[31]);
+            for (int r = 0; r < RPT; ++r) G[r] += off;
+            if (qq == 1) ms.gx[0][col] = G[0];          // row 16
+            if (qq == 3) {
+                ms.gx[1][col] = G[0];                   // row 48
+                ms.gx[2][col] = G[RPT - 1];             // row 63 (G_C)
+                ms.gamma[col] = __expf(G[RPT - 1]);
+            }
         }
         if (tid < 2 * C) {
             const int qk = tid / C, r = tid % C;
-            const float tot = ms.npart[qk][r >> 5][0][r & 31] + ms.npart[qk][r >> 5][1][r & 31] +
-                              ms.npart[qk][r >> 5][2][r & 31] + ms.npart[qk][r >> 5][3][r & 31];
+            const float tot = ms.npart[qk][r >> 4][0][r & 15] + ms.npart[qk][r >> 4][1][r & 15] +
+                              ms.npart[qk][r >> 4][2][r & 15] + ms.npart[qk][r >> 4][3][r & 15];
             ms.nrm[qk][r] = rsqrtf(tot + a.l2_eps);
         }
         __syncthreads();
-        // normalise in place: qv, kv now hold q^, k^
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
+        for (int r = 0; r < RPT; ++r) {
             qv[r] *= ms.nrm[0][r0 + r];
             kv[r] *= ms.nrm[1][r0 + r];
         }
 
         // ---- operands of the first and second products
-        const float Gm = G[16];  // reference row 16 (first half) or 48 (second half)
+        const float Gm = ms.gx[half][col];   // reference row 16 (first half) or 48 (second half)
+        const float Gm1 = ms.gx[1][col];
+        const float GC = ms.gx[2][col];
         {
-            const float Gm1 = ms.gx[1][col];
-            const float eGm0 = __expf(Gm);  // first half only: e^{G_16} >= e^{-85}
-            float xt[32], yt[32];
+            // the cross block (keys of the first half seen from the second half's
+            // reference) is written by the first half; the second half writes its
+            // own diagonal value a second time instead, which keeps this loop free
+            // of per-half code paths
+            const float Gx = half == 0 ? Gm1 : Gm;
+            const int xrow = half == 0 ? 64 : 0;
+            const float eGm = __expf(Gm);    // e^{G_16} >= e^{-85} in the first half
+            float xt[RPT], yt[RPT], yl[RPT];
 #pragma unroll
-            for (int r = 0; r < 32; ++r) {
+            for (int r = 0; r < RPT; ++r) {
                 const int rr = r0 + r;
                 const float e = __expf(G[r] - Gm);
                 const float ie = __expf(Gm - G[r]);
-                const float qq = qv[r] * e;
-                // [Q~lo | K~ | Q~hi] slots of 64 rows inside each K-block
                 const uint32_t o = swz(rr, col, AX_KB);
                 st_hi(sm, SM_AX + 8192 + o, kv[r] * e);
-                st_hilo(sm, SM_AX + 16384 + o, SM_AX + o, qq);
+                st_hilo(sm, SM_AX + 16384 + o, SM_AX + o, qv[r] * e);
                 st_hilo(sm, SM_B1H + swz(rr, col, B1_KB), SM_B1L + swz(rr, col, B1_KB), kv[r] * ie);
-                if (half == 0)
-                    st_hilo(sm, SM_B1H + swz(64 + rr, col, B1_KB), SM_B1L + swz(64 + rr, col, B1_KB),
-                            kv[r] * __expf(Gm1 - G[r]));
-                const float eG = half == 0 ? e * eGm0 : __expf(G[r]);
-                xt[r] = tf32r(ms.beta[rr] * kv[r] * eG);
-                yt[r] = ms.beta[rr] * vv[r];
+                st_hilo(sm, SM_B1H + swz(xrow + rr, col, B1_KB), SM_B1L + swz(xrow + rr, col, B1_KB),
+                        kv[r] * __expf(Gx - G[r]));
+                const float eG = half == 0 ? e * eGm : __expf(G[r]);
+                const float be = ms.beta[rr];
+                xt[r] = tf32r(be * kv[r] * eG);
+                const float y = be * vv[r];
+                yt[r] = tf32r(y);
+                yl[r] = tf32r(y - yt[r]);
             }
-            ptx::tmem_st32(tmem + lane_base + TM_XT + 32 * half, xt);
-#pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                const float hi = tf32r(yt[r]);
-                xt[r] = tf32r(yt[r] - hi);
-                yt[r] = hi;
-            }
-            ptx::tmem_st32(tmem + lane_base + TM_YT + 32 * half, yt);
-            ptx::tmem_st32(tmem + lane_base + TM_YL + 32 * half, xt);
+            ptx::tmem_st16(tmem + lane_base + TM_XT + RPT * qq, xt);
+            ptx::tmem_st16(tmem + lane_base + TM_YT + RPT * qq, yt);
+            ptx::tmem_st16(tmem + lane_base + TM_YL + RPT * qq, yl);
         }
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
@@ -433,123 +448,85 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
             for (int ks = 0; ks < 16; ++ks) {
                 const int ka = (ks >> 2) * AX_KB + (ks & 3) * 32, kb = (ks >> 2) * B1_KB + (ks & 3) * 32;
                 ptx::mma_tf32_ss(tmem + TM_D1, dsc(sm, SM_AX + 8192 + ka), dsc(sm, SM_B1H + kb), id, ks > 0);
-            }
-            for (int ks = 0; ks < 16; ++ks) {
-                const int ka = (ks >> 2) * AX_KB + (ks & 3) * 32, kb = (ks >> 2) * B1_KB + (ks & 3) * 32;
                 ptx::mma_tf32_ss(tmem + TM_D1, dsc(sm, SM_AX + 8192 + ka), dsc(sm, SM_B1L + kb), id, 1);
-            }
-            for (int ks = 0; ks < 16; ++ks) {
-                const int ka = (ks >> 2) * AX_KB + (ks & 3) * 32, kb = (ks >> 2) * B1_KB + (ks & 3) * 32;
                 ptx::mma_tf32_ss(tmem + TM_D1C, dsc(sm, SM_AX + ka), dsc(sm, SM_B1H + kb), id, ks > 0);
             }
             ptx::mma_commit(&ms.bar);
         }
         if (!wait_mma(ms, ph, a.dev_status)) break;
 
-        // ---- A from D1 lanes 0..63; the D1c lanes 0..63 part of P into PTMP.
-        // D1 column of (row r, key row s): the first half reads its own block
-        // (column s), the second half its own block (column s >= 32) and, for
-        // s < 32, the cross block (column 64 + s).  Warps whose lanes are
-        // 0..63 (warp & 3 < 2) do this; the branch is warp-uniform.
-        if (lrow < 64) {
+        // ---- A (D1 lanes 0..63) and the D1c part of P.  D1 column of (row r,
+        // key row s): the first half reads its own block (column s), the second
+        // half its own block (column s >= 32) and, for s < 32, the cross block
+        // (column 64 + s).  Warp (lane quarter lq, column group qq) reads columns
+        // [32 qq, +32); the branches are warp-uniform.
+        if (lq < 2 && qq < 3) {
             float* akk = reinterpret_cast<float*>(sm + SM_AKK);
             float* ptmp = reinterpret_cast<float*>(sm + SM_PTMP);
-            const int r = lrow;
+            const int r = col;
             const float br = ms.beta[r];
-            float v[32];
-            if (half == 0) {
+            float v[32], w[32];
+            ptx::tmem_ld32(tmem + lane_base + TM_D1 + 32 * qq, v);
+            ptx::tmem_ld32(tmem + lane_base + TM_D1C + 32 * qq, w);
+            if (qq == 0 && r < 32) {
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    ptx::tmem_ld32(tmem + lane_base + TM_D1 + 32 * part, v);
+                for (int x = 0; x < 32; ++x) { akk[r * 65 + x] = x < r ? br * v[x] : 0.0f; ptmp[r * 65 + x] = w[x]; }
+            } else if (qq == 1) {
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) {
-                        const int s = 32 * part + x;
-                        if (r < 32 && s >= 32) akk[r * 65 + s] = 0.0f;
-                        else if (r < 32 || s >= 32) akk[r * 65 + s] = s < r ? br * v[x] : 0.0f;
-                    }
-                    ptx::tmem_ld32(tmem + lane_base + TM_D1C + 32 * part, v);
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) {
-                        const int s = 32 * part + x;
-                        if (r < 32 && s >= 32) ptmp[r * 65 + s] = 0.0f;
-                        else if (r < 32 || s >= 32) ptmp[r * 65 + s] = v[x];
-                    }
+                for (int x = 0; x < 32; ++x) {
+                    const int s = 32 + x;
+                    akk[r * 65 + s] = (r >= 32 && s < r) ? br * v[x] : 0.0f;
+                    ptmp[r * 65 + s] = r >= 32 ? w[x] : 0.0f;
                 }
-            } else {
-                ptx::tmem_ld32(tmem + lane_base + TM_D1 + 64, v);
-                if (r >= 32) {
+            } else if (qq == 2 && r >= 32) {
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) akk[r * 65 + x] = br * v[x];
-                }
-                ptx::tmem_ld32(tmem + lane_base + TM_D1C + 64, v);
-                if (r >= 32) {
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) ptmp[r * 65 + x] = v[x];
-                }
+                for (int x = 0; x < 32; ++x) { akk[r * 65 + x] = br * v[x]; ptmp[r * 65 + x] = w[x]; }
             }
         }
         __syncthreads();
         // ---- P = D1 lanes 64..127 + PTMP, masked to s <= r, as high and low tiles
-        if (lrow >= 64) {
+        if (lq >= 2 && qq < 3) {
             const float* ptmp = reinterpret_cast<const float*>(sm + SM_PTMP);
-            const int r = lrow - 64;
+            const int r = col - 64;
             float v[32];
-            if (half == 0) {
+            ptx::tmem_ld32(tmem + lane_base + TM_D1 + 32 * qq, v);
+            if (qq == 0 && r < 32) {
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    ptx::tmem_ld32(tmem + lane_base + TM_D1 + 32 * part, v);
+                for (int x = 0; x < 32; ++x)
+                    st_hilo(sm, SM_PH + swz(r, x, T64_KB), SM_PL + swz(r, x, T64_KB), x <= r ? v[x] + ptmp[r * 65 + x] : 0.0f);
+            } else if (qq == 1) {
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) {
-                        const int s = 32 * part + x;
-                        if (r < 32 && s >= 32) {
-                            st_raw(sm, SM_PH + swz(r, s, T64_KB), 0.0f);
-                            st_raw(sm, SM_PL + swz(r, s, T64_KB), 0.0f);
-                        } else if (r < 32 || s >= 32) {
-                            const float p = s <= r ? v[x] + ptmp[r * 65 + s] : 0.0f;
-                            st_hilo(sm, SM_PH + swz(r, s, T64_KB), SM_PL + swz(r, s, T64_KB), p);
-                        }
-                    }
+                for (int x = 0; x < 32; ++x) {
+                    const int s = 32 + x;
+                    const float p = (r >= 32 && s <= r) ? v[x] + ptmp[r * 65 + s] : 0.0f;
+                    st_hilo(sm, SM_PH + swz(r, s, T64_KB), SM_PL + swz(r, s, T64_KB), p);
                 }
-            } else {
-                ptx::tmem_ld32(tmem + lane_base + TM_D1 + 64, v);
-                if (r >= 32) {
+            } else if (qq == 2 && r >= 32) {
 #pragma unroll
-                    for (int x = 0; x < 32; ++x)
-                        st_hilo(sm, SM_PH + swz(r, x, T64_KB), SM_PL + swz(r, x, T64_KB), v[x] + ptmp[r * 65 + x]);
-                }
+                for (int x = 0; x < 32; ++x)
+                    st_hilo(sm, SM_PH + swz(r, x, T64_KB), SM_PL + swz(r, x, T64_KB), v[x] + ptmp[r * 65 + x]);
             }
         }
         // ---- Q o e^G and (K o e^{G_C - G})^T tiles for the later products
-        float qe[32];  // q^ e^G, whose low part is stored after the solve
+        float qe[RPT];  // q^ e^G, whose low part is stored after the solve
         {
-            const float GC = ms.gx[2][col];
-            const float eGm0 = __expf(Gm);
-            const float cGCm1 = __expf(GC - Gm);  // second half: e^{G_63 - G_48} >= e^{-75}
-            float kd[32], kl[32];
+            float kd[RPT], kl[RPT];
 #pragma unroll
-            for (int r = 0; r < 32; ++r) {
+            for (int r = 0; r < RPT; ++r) {
                 const int rr = r0 + r;
-                float eG, edec;
-                if (half == 0) {
-                    eG = __expf(G[r] - Gm) * eGm0;
-                    edec = __expf(GC - G[r]);
-                } else {
-                    eG = __expf(G[r]);
-                    edec = __expf(Gm - G[r]) * cGCm1;
-                }
-                qe[r] = qv[r] * eG;
+                qe[r] = qv[r] * __expf(G[r]);
                 st_hi(sm, SM_QE + swz(rr, col, T64_KB), qe[r]);
-                const float x = kv[r] * edec;
+                const float x = kv[r] * __expf(GC - G[r]);
                 kd[r] = tf32r(x);
                 kl[r] = tf32r(x - kd[r]);
             }
+            // KD^T row col, key rows [16 qq, +16): K-block qq >> 1, 16-byte chunks 4 (qq & 1) + j
 #pragma unroll
-            for (int qd = 0; qd < 8; ++qd) {
-                const uint32_t o = half * 128 * 128 + col * 128 + ((qd ^ (col & 7)) << 4);
-                *reinterpret_cast<float4*>(sm + SM_KD + o) =
-                    make_float4(kd[4 * qd], kd[4 * qd + 1], kd[4 * qd + 2], kd[4 * qd + 3]);
-                *reinterpret_cast<float4*>(sm + SM_KDL + o) =
-                    make_float4(kl[4 * qd], kl[4 * qd + 1], kl[4 * qd + 2], kl[4 * qd + 3]);
+            for (int j = 0; j < 4; ++j) {
+                const int qd = 4 * (qq & 1) + j;
+                const uint32_t o = (qq >> 1) * 128 * 128 + col * 128 + ((qd ^ (col & 7)) << 4);
+                *reinterpret_cast<float4*>(sm + SM_KD + o) = make_float4(kd[4 * j], kd[4 * j + 1], kd[4 * j + 2], kd[4 * j + 3]);
+                *reinterpret_cast<float4*>(sm + SM_KDL + o) = make_float4(kl[4 * j], kl[4 * j + 1], kl[4 * j + 2], kl[4 * j + 3]);
             }
         }
         ptx::tc_fence_before();
@@ -603,7 +580,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
         }
         // the low part of the QE tile (over the dead A and P scratch)
 #pragma unroll
-        for (int r = 0; r < 32; ++r) st_hi(sm, SM_QEL + swz(r0 + r, col, T64_KB), qe[r] - tf32r(qe[r]));
+        for (int r = 0; r < RPT; ++r) st_hi(sm, SM_QEL + swz(r0 + r, col, T64_KB), qe[r] - tf32r(qe[r]));
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncthreads();
@@ -622,19 +599,17 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
         }
         if (!wait_mma(ms, ph, a.dev_status)) break;
 
-        // ---- -W tile from W^T (lane i = col, rows 32*half .. +32); S_lo = S - S_hi
+        // ---- -W tile from W^T (lane i = col, rows [16 qq, +16)); S_lo = S - S_hi (key dims [32 qq, +32))
         {
-            float v[32];
-            ptx::tmem_ld32(tmem + lane_base + TM_WT + 32 * half, v);
+            float v[RPT];
+            ptx::tmem_ld16(tmem + lane_base + TM_WT + RPT * qq, v);
 #pragma unroll
-            for (int x = 0; x < 32; ++x) st_hi(sm, SM_NW + swz(32 * half + x, col, T64_KB), -v[x]);
+            for (int x = 0; x < RPT; ++x) st_hi(sm, SM_NW + swz(RPT * qq + x, col, T64_KB), -v[x]);
+            float s[32];
+            ptx::tmem_ld32(tmem + lane_base + TM_ST + 32 * qq, s);
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                ptx::tmem_ld32(tmem + lane_base + TM_ST + 64 * half + 32 * part, v);
-#pragma unroll
-                for (int x = 0; x < 32; ++x) v[x] -= __uint_as_float(__float_as_uint(v[x]) & 0xFFFFE000u);
-                ptx::tmem_st32(tmem + lane_base + TM_SL + 64 * half + 32 * part, v);
-            }
+            for (int x = 0; x < 32; ++x) s[x] -= __uint_as_float(__float_as_uint(s[x]) & 0xFFFFE000u);
+            ptx::tmem_st32(tmem + lane_base + TM_SL + 32 * qq, s);
         }
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
@@ -655,27 +630,30 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
         }
         if (!wait_mma(ms, ph, a.dev_status)) break;
 
+        // the raw staging region is free from here: prefetch the next chunk's rows
+        if (ch + 1 < nchunks) {
+            stage_chunk(sm, a, c0 + C, seg0, seg1, slot, h);
+            if (tid < C && c0 + C + tid < seg1) bnext = __bfloat162float(bg[(size_t)(c0 + C + tid) * H + h]);
+        }
+
         // ---- S^T <- S^T Diag(e^{G_C}); U^T -> high part in place and low part
         {
             float v[32];
+            const uint32_t ta = tmem + lane_base + TM_ST + 32 * qq;
+            ptx::tmem_ld32(ta, v);
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                const uint32_t ta = tmem + lane_base + TM_ST + 64 * half + 32 * part;
-                ptx::tmem_ld32(ta, v);
+            for (int x = 0; x < 32; ++x) v[x] *= ms.gamma[32 * qq + x];
+            ptx::tmem_st32(ta, v);
+            float u[RPT], lo[RPT];
+            ptx::tmem_ld16(tmem + lane_base + TM_UT + RPT * qq, u);
 #pragma unroll
-                for (int x = 0; x < 32; ++x) v[x] *= ms.gamma[64 * half + 32 * part + x];
-                ptx::tmem_st32(ta, v);
+            for (int x = 0; x < RPT; ++x) {
+                const float hi = tf32r(u[x]);
+                lo[x] = tf32r(u[x] - hi);
+                u[x] = hi;
             }
-            float lo[32];
-            ptx::tmem_ld32(tmem + lane_base + TM_UT + 32 * half, v);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) {
-                const float hi = tf32r(v[x]);
-                lo[x] = tf32r(v[x] - hi);
-                v[x] = hi;
-            }
-            ptx::tmem_st32(tmem + lane_base + TM_UT + 32 * half, v);
-            ptx::tmem_st32(tmem + lane_base + TM_UL + 32 * half, lo);
+            ptx::tmem_st16(tmem + lane_base + TM_UT + RPT * qq, u);
+            ptx::tmem_st16(tmem + lane_base + TM_UL + RPT * qq, lo);
         }
         ptx::tc_fence_before();
         __syncthreads();
@@ -700,27 +678,28 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
         }
         if (!wait_mma(ms, ph, a.dev_status)) break;
 
-        // ---- outputs (lane j = col, rows 32*half .. +32), optional gated RMSNorm
+        // ---- outputs (lane j = col, rows [16 qq, +16)), optional gated RMSNorm
         {
-            float o[32];
-            ptx::tmem_ld32(tmem + lane_base + TM_OT + 32 * half, o);
+            float o[RPT];
+            ptx::tmem_ld16(tmem + lane_base + TM_OT + RPT * qq, o);
 #pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] *= a.scale;
+            for (int x = 0; x < RPT; ++x) o[x] *= a.scale;
             if (gg != nullptr) {
-                float t[32];
+                float t[RPT];
 #pragma unroll
-                for (int x = 0; x < 32; ++x) t[x] = o[x] * o[x];
-                ms.epart[half][warp & 3][lane] = transpose_reduce(t, lane);
+                for (int x = 0; x < RPT; ++x) t[x] = o[x] * o[x];
+                const float pr = transpose_reduce16(t, lane);
+                if (lane < 16) ms.epart[qq][lq][lane] = pr;
                 __syncthreads();
                 if (tid < C) {
                     const int r = tid;
-                    const float tot = ms.epart[r >> 5][0][r & 31] + ms.epart[r >> 5][1][r & 31] +
-                                      ms.epart[r >> 5][2][r & 31] + ms.epart[r >> 5][3][r & 31];
+                    const float tot = ms.epart[r >> 4][0][r & 15] + ms.epart[r >> 4][1][r & 15] +
+                                      ms.epart[r >> 4][2][r & 15] + ms.epart[r >> 4][3][r & 15];
                     ms.rms[r] = rsqrtf(tot * (1.0f / D) + a.norm_eps);
                 }
                 __syncthreads();
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
+                for (int x = 0; x < RPT; ++x) {
                     const int r = r0 + x;
                     if (r < nvalid) {
                         const float gv = __bfloat162float(gg[((size_t)(c0 + r) * H + h) * D + col]);
@@ -729,7 +708,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
                 }
             }
 #pragma unroll
-            for (int x = 0; x < 32; ++x) {
+            for (int x = 0; x < RPT; ++x) {
                 const int r = r0 + x;
                 if (r < nvalid) store_out(a.out, ((size_t)(c0 + r) * H + h) * D + col, o[x], a.out_bf16);
             }
@@ -738,16 +717,14 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
         __syncthreads();
     }
 
-    // ---- final state S^T -> rec_state (S[i][j], lane j = col)
+    // ---- final state S^T -> rec_state (S[i][j], lane j = col, key dims [32 qq, +32))
+    ptx::cp_async_wait_all();  // nothing may land in shared memory after the CTA ends
     if (!ms.err) {
         float* Sg = a.rec_state + ((size_t)slot * H + h) * D * D;
         float v[32];
+        ptx::tmem_ld32(tmem + lane_base + TM_ST + 32 * qq, v);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            ptx::tmem_ld32(tmem + lane_base + TM_ST + 64 * half + 32 * part, v);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) Sg[(size_t)(64 * half + 32 * part + x) * D + col] = v[x];
-        }
+        for (int x = 0; x < 32; ++x) Sg[(size_t)(32 * qq + x) * D + col] = v[x];
     }
     ptx::tc_fence_before();
     __syncthreads();
