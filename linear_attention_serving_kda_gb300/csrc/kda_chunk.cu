@@ -22,19 +22,20 @@
 // Precision.  Outputs are dominated by the most recent rows (o_r ~ P_rr u_r),
 // a chain of products whose TF32 operand roundings (2^-11 each) would leave
 // the largest outputs ~1e-3 off -- too much for a per-element bound of a few
-// thousandths of the output RMS.  So the operands on that chain are split
-// into a TF32 high part and a TF32 low part (x = hi + lo to ~2^-22):
+// thousandths of the output RMS.  So the operands on that chain are split:
+// the high part is x itself as the tensor core reads it (the low 13 mantissa
+// bits dropped) and the low part the exact remainder, itself read truncated
+// (x = hi + lo to within 2^-20 |x|):
 //     P (and A)  = [K~; Q~hi] (B1hi + B1lo)^T + [Q~lo; K~] B1hi^T
 //     U'         = T (Y + Ylo)                    (Y = Diag(beta) V)
 //     P U        = P_hi U_hi + P_hi U_lo + P_lo U_hi
 //     K~^T U     = KD_hi U_hi + KD_hi U_lo + KD_lo U_hi   (the state update)
 //     (Q o e^G) S = QE_hi S_hi + QE_hi S_lo + QE_lo S_hi  (long prompts: the
 //                  carried state dominates the outputs)
-// where S_hi is the state as the tensor core reads it from TMEM (fp32 with
-// the low 13 mantissa bits dropped) and S_lo = S - S_hi, exact in fp32.  The
-// remaining products (W, W S, T) are single TF32 with operands rounded to
-// nearest.  The two A operands of the first product share their K~ rows:
-// within each 24 KiB K-block the layout is [Q~lo | K~ | Q~hi] (64 rows each),
+// (S in TMEM and U in TMEM are split the same way in place).  The remaining
+// products (W, W S, T) are single TF32 with operands rounded to nearest.  The
+// two A operands of the first product share their K~ rows: within each
+// 24 KiB K-block the layout is [Q~lo | K~ | Q~hi] (64 rows each),
 // and the tiles start at the first and the second 64-row slot.
 //
 // Range of the decay factors: e^{G} over 64 rows reaches e^{-320}, so A and P
@@ -48,6 +49,16 @@
 // Ylo^T [256,320), D1 [320,416), D1c [416,512) until the first product is
 // read; then W^T [320,384), U'^T -> U^T (hi) [384,448), O^T [128,192),
 // S^T low part [192,320), U^T low part [448,512).
+//
+// Staging.  A chunk's raw rows (q, k, v with the three rows before it, and
+// the gate rows) arrive as four 2-D tensor copies issued by one thread, the
+// next chunk's while the current one finishes; a segment's first chunk takes
+// its three earlier rows from the conv state instead.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_ptx.cuh"
@@ -98,8 +109,9 @@ struct Misc {
     float gamma[D];           // e^{G_C}
     float epart[4][4][16];    // output-norm partials [quarter][lane quarter][row]
     float rms[C];
-    float M[3][16][16];       // solve scratch
-    uint64_t bar;
+    float X[32][33];          // solve scratch: A[H1,H0] inv(H0)
+    uint64_t bar;             // tensor-core completion
+    uint64_t rbar;            // raw-row copies
     uint32_t tmem;
     int err;
 };
@@ -137,13 +149,23 @@ __device__ __forceinline__ void st_raw(unsigned char* sm, uint32_t off, float x)
     *reinterpret_cast<float*>(sm + off) = x;
 }
 
-// store the TF32 high part of x, or its high and low parts into two tiles
+// store the TF32 value nearest to x (an operand used unsplit)
 __device__ __forceinline__ void st_hi(unsigned char* sm, uint32_t off, float x) { st_raw(sm, off, tf32r(x)); }
-__device__ __forceinline__ void st_hilo(unsigned char* sm, uint32_t off_hi, uint32_t off_lo, float x)
+
+// Low part of a split operand.  The tensor core reads an fp32 operand with its
+// low 13 mantissa bits dropped, so x itself serves as the high part and the
+// remainder x - trunc(x) (exact in fp32) as the low part; the low part is read
+// truncated too, which leaves x = hi + lo to within 2^-20 |x|.
+__device__ __forceinline__ float tf32_lo(float x)
 {
-    const float hi = tf32r(x);
-    st_raw(sm, off_hi, hi);
-    st_raw(sm, off_lo, tf32r(x - hi));
+    return x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
+// store x as a split operand: high part (x) and low part into two tiles
+__device__ __forceinline__ void st_split(unsigned char* sm, uint32_t off_hi, uint32_t off_lo, float x)
+{
+    st_raw(sm, off_hi, x);
+    st_raw(sm, off_lo, tf32_lo(x));
 }
 
 // Warp transpose-reduction of 16 values per lane: lane l returns the sum over
@@ -197,40 +219,27 @@ __global__ void kda_chunk_schedule_kernel(const int32_t* cu, int N, int32_t* ord
 
 // Issue the cp.async copies of one chunk's raw rows (q, k, v with 3 halo rows,
 // the first chunk's halo from the conv state; gate rows); zero beyond the segment.
-__device__ __forceinline__ void stage_chunk(unsigned char* sm, const ChunkArgs& a, int c0, int seg0, int seg1,
-                                            int slot, int h)
+// Tensor maps of the raw rows: q, k, v and the gate f, each viewed as a
+// [T][H * 128] bf16 matrix; boxes of 128 channels x (C + HALO) rows (C for f).
+struct RawMaps {
+    CUtensorMap q, k, v, f;
+};
+
+// Issue the copies of the raw rows of the chunk starting at row c0 of head h
+// (one thread).  Rows past the end of the tensor read as zero; rows past the
+// segment's end are read but never used.
+__device__ __forceinline__ void stage_chunk(unsigned char* sm, const RawMaps& m, Misc& ms, int c0, int h)
 {
-    const int H = a.H, K = a.K, conv_dim = 3 * H * D;
-    const __nv_bfloat16* cs = static_cast<const __nv_bfloat16*>(a.conv_state);
-    const __nv_bfloat16* fg = static_cast<const __nv_bfloat16*>(a.f);
-    for (int idx = threadIdx.x; idx < 3 * RAWR * 16; idx += NT) {
-        const int tsel = idx / (RAWR * 16), rem = idx % (RAWR * 16), sr = rem >> 4, c16 = rem & 15;
-        const int gr = c0 - HALO + sr;
-        const __nv_bfloat16* base = static_cast<const __nv_bfloat16*>(tsel == 0 ? a.q : (tsel == 1 ? a.k : a.v));
-        const void* src = base;
-        uint32_t bytes = 0;
-        if (gr >= seg0 && gr < seg1) {
-            src = base + ((size_t)gr * H + h) * D + c16 * 8;
-            bytes = 16;
-        } else if (gr < seg0) {
-            const int cr = (K - 1) + (gr - seg0);  // conv-state row
-            if (cr >= 0) {
-                src = cs + ((size_t)slot * (K - 1) + cr) * conv_dim + (size_t)tsel * H * D + h * D + c16 * 8;
-                bytes = 16;
-            }
-        }
-        ptx::cp_async16(sm + SM_RAW + tsel * RAW_T + sr * (D * 2) + c16 * 16, src, bytes);
-    }
-    for (int idx = threadIdx.x; idx < C * 16; idx += NT) {
-        const int sr = idx >> 4, c16 = idx & 15, gr = c0 + sr;
-        const bool ok = gr < seg1;
-        ptx::cp_async16(sm + SM_RAWF + sr * (D * 2) + c16 * 16,
-                        ok ? (const void*)(fg + ((size_t)gr * H + h) * D + c16 * 8) : (const void*)fg, ok ? 16 : 0);
-    }
-    ptx::cp_async_commit();
+    const uint64_t pol = ptx::policy_evict_first();  // rows are read once (and the halo twice)
+    ptx::fence_proxy_async_smem();
+    ptx::mbar_arrive_expect_tx(&ms.rbar, 3 * RAW_T + C * D * 2);
+    ptx::tma_load_2d(sm + SM_RAW, &m.q, h * D, c0 - HALO, &ms.rbar, pol);
+    ptx::tma_load_2d(sm + SM_RAW + RAW_T, &m.k, h * D, c0 - HALO, &ms.rbar, pol);
+    ptx::tma_load_2d(sm + SM_RAW + 2 * RAW_T, &m.v, h * D, c0 - HALO, &ms.rbar, pol);
+    ptx::tma_load_2d(sm + SM_RAWF, &m.f, h * D, c0, &ms.rbar, pol);
 }
 
-__global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
+__global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, const __grid_constant__ RawMaps maps)
 {
     extern __shared__ __align__(1024) unsigned char sm[];
     Misc& ms = *reinterpret_cast<Misc*>(sm + SM_MISC);
@@ -266,28 +275,31 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
     const __nv_bfloat16* gg = static_cast<const __nv_bfloat16*>(a.g);
     __nv_bfloat16* cs = static_cast<__nv_bfloat16*>(a.conv_state);
 
-    stage_chunk(sm, a, seg0, seg0, seg1, slot, h);  // first chunk's rows, in flight during set-up
-    if (warp == 0) ptx::tmem_alloc(&ms.tmem, TM_COLS);
     if (tid == 0) {
         ptx::mbar_init(&ms.bar, 1);
+        ptx::mbar_init(&ms.rbar, 1);
         ptx::fence_mbar_init();
         ms.err = 0;
+        stage_chunk(sm, maps, ms, seg0, h);  // first chunk's rows, in flight during set-up
     }
+    if (warp == 0) ptx::tmem_alloc(&ms.tmem, TM_COLS);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = ms.tmem;
     const uint32_t lane_base = (uint32_t)(lq * 32) << 16;  // this warp's TMEM lane quarter
     uint32_t ph = 0;
+    uint32_t rph = 0;        // parity of the raw-row copies being waited for
+    bool rpending = true;    // raw-row copies issued and not yet waited for
 
     // ---- per-CTA constants: this thread's conv taps (4-tap form) and gate params
     float wq[4], wk[4], wv[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) { wq[j] = 0.f; wk[j] = 0.f; wv[j] = 0.f; }
-    for (int j = 0; j < K; ++j) {
-        wq[j + 4 - K] = a.conv_w[((size_t)0 * H * D + h * D + col) * K + j];
-        wk[j + 4 - K] = a.conv_w[((size_t)1 * H * D + h * D + col) * K + j];
-        wv[j + 4 - K] = a.conv_w[((size_t)2 * H * D + h * D + col) * K + j];
+    for (int j = 0; j < 4; ++j) {
+        const int src = j - (4 - K);  // K < 4: the oldest taps are zero
+        wq[j] = src >= 0 ? a.conv_w[((size_t)0 * H * D + h * D + col) * K + src] : 0.f;
+        wk[j] = src >= 0 ? a.conv_w[((size_t)1 * H * D + h * D + col) * K + src] : 0.f;
+        wv[j] = src >= 0 ? a.conv_w[((size_t)2 * H * D + h * D + col) * K + src] : 0.f;
     }
     const float dtc = a.dt_bias[(size_t)h * D + col];
     const float ea = expf(a.A_log[h]);
@@ -311,11 +323,31 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
         const int r0 = RPT * qq;
 
         if (tid < C) ms.beta[tid] = tid < nvalid ? sigmoidf_(bnext) : 0.0f;
-        ptx::cp_async_wait_all();
+        if (tid == 0 && !ptx::mbar_wait(&ms.rbar, rph)) {
+            ms.err = 1;
+            flag_status(a.dev_status, KDA_DEV_TIMEOUT);
+        }
         __syncthreads();
+        if (ms.err) break;
+        (void)ptx::mbar_try_wait(&ms.rbar, rph);  // completed: makes the copied rows visible to this thread
+        rph ^= 1u;
+        rpending = false;
 
         const __nv_bfloat16* raw = reinterpret_cast<const __nv_bfloat16*>(sm + SM_RAW);
         const __nv_bfloat16* rawf = reinterpret_cast<const __nv_bfloat16*>(sm + SM_RAWF);
+        if (ch == 0) {
+            // a segment's first chunk: the rows before it are the carried conv
+            // state (oldest first; zero where K - 1 < HALO)
+            __nv_bfloat16* rw = reinterpret_cast<__nv_bfloat16*>(sm + SM_RAW);
+            for (int idx = tid; idx < 3 * HALO * D; idx += NT) {
+                const int tsel = idx / (HALO * D), sr = (idx / D) % HALO, cc = idx % D;
+                const int cr = (K - 1) - HALO + sr;
+                rw[tsel * RAWR * D + sr * D + cc] =
+                    cr >= 0 ? cs[((size_t)slot * (K - 1) + cr) * conv_dim + (size_t)tsel * H * D + h * D + cc]
+                            : __float2bfloat16_rn(0.0f);
+            }
+            __syncthreads();
+        }
         if (ch == nchunks - 1) {
             // the new conv state: the sequence's last K-1 raw rows
             for (int idx = tid; idx < 3 * D * (K - 1); idx += NT) {
@@ -354,7 +386,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
                 qv[r] = ok ? siluf_(aq) : 0.0f;
                 kv[r] = ok ? siluf_(ak) : 0.0f;
                 vv[r] = ok ? siluf_(av) : 0.0f;
-                const float la = ok ? log_alpha(a.gate_mode, a.lb, ea, __bfloat162float(rawf[lr * D + col]), dtc) : 0.0f;
+                const float la = ok ? a.lb * sigmoidf_(ea * (__bfloat162float(rawf[lr * D + col]) + dtc)) : 0.0f;  // safe gate
                 run += la;
                 G[r] = run;
 #pragma unroll
@@ -402,18 +434,21 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
             kv[r] *= ms.nrm[1][r0 + r];
         }
 
-        // ---- operands of the first and second products
+        // ---- operands of the first and second products; q^ e^G and k^ e^{G_C - G}
+        // are formed here too and kept in registers until their tiles are free
         const float Gm = ms.gx[half][col];   // reference row 16 (first half) or 48 (second half)
-        const float Gm1 = ms.gx[1][col];
-        const float GC = ms.gx[2][col];
+        float qe[RPT], kdx[RPT];
         {
+            const float Gm1 = ms.gx[1][col];
+            const float GC = ms.gx[2][col];
             // the cross block (keys of the first half seen from the second half's
             // reference) is written by the first half; the second half writes its
             // own diagonal value a second time instead, which keeps this loop free
             // of per-half code paths
             const float Gx = half == 0 ? Gm1 : Gm;
             const int xrow = half == 0 ? 64 : 0;
-            const float eGm = __expf(Gm);    // e^{G_16} >= e^{-85} in the first half
+            const float eGm = __expf(Gm);          // first half: e^{G_16} >= e^{-85}
+            const float cGC = __expf(GC - Gm);     // second half: e^{G_63 - G_48} >= e^{-75}
             float xt[RPT], yt[RPT], yl[RPT];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
@@ -422,16 +457,22 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
                 const float ie = __expf(Gm - G[r]);
                 const uint32_t o = swz(rr, col, AX_KB);
                 st_hi(sm, SM_AX + 8192 + o, kv[r] * e);
-                st_hilo(sm, SM_AX + 16384 + o, SM_AX + o, qv[r] * e);
-                st_hilo(sm, SM_B1H + swz(rr, col, B1_KB), SM_B1L + swz(rr, col, B1_KB), kv[r] * ie);
-                st_hilo(sm, SM_B1H + swz(xrow + rr, col, B1_KB), SM_B1L + swz(xrow + rr, col, B1_KB),
+                st_split(sm, SM_AX + 16384 + o, SM_AX + o, qv[r] * e);
+                st_split(sm, SM_B1H + swz(rr, col, B1_KB), SM_B1L + swz(rr, col, B1_KB), kv[r] * ie);
+                st_split(sm, SM_B1H + swz(xrow + rr, col, B1_KB), SM_B1L + swz(xrow + rr, col, B1_KB),
                         kv[r] * __expf(Gx - G[r]));
+                // e^{G_r}: a product of two in-range factors in the first half; direct in the
+                // second (e^{G_48} may underflow).  e^{G_C - G_r}: direct in the first half
+                // (e^{G_C - G_16} may underflow); a product in the second.
                 const float eG = half == 0 ? e * eGm : __expf(G[r]);
+                const float edec = half == 0 ? __expf(GC - G[r]) : ie * cGC;
+                qe[r] = qv[r] * eG;
+                kdx[r] = kv[r] * edec;
                 const float be = ms.beta[rr];
                 xt[r] = tf32r(be * kv[r] * eG);
                 const float y = be * vv[r];
-                yt[r] = tf32r(y);
-                yl[r] = tf32r(y - yt[r]);
+                yt[r] = y;
+                yl[r] = tf32_lo(y);
             }
             ptx::tmem_st16(tmem + lane_base + TM_XT + RPT * qq, xt);
             ptx::tmem_st16(tmem + lane_base + TM_YT + RPT * qq, yt);
@@ -445,6 +486,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
         if (tid == 0) {
             ptx::tc_fence_after();
             const uint32_t id = ptx::idesc_tf32(128, 96);
+#pragma unroll 1
             for (int ks = 0; ks < 16; ++ks) {
                 const int ka = (ks >> 2) * AX_KB + (ks & 3) * 32, kb = (ks >> 2) * B1_KB + (ks & 3) * 32;
                 ptx::mma_tf32_ss(tmem + TM_D1, dsc(sm, SM_AX + 8192 + ka), dsc(sm, SM_B1H + kb), id, ks > 0);
@@ -459,8 +501,11 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
         // key row s): the first half reads its own block (column s), the second
         // half its own block (column s >= 32) and, for s < 32, the cross block
         // (column 64 + s).  Warp (lane quarter lq, column group qq) reads columns
-        // [32 qq, +32); the branches are warp-uniform.
-        if (lq < 2 && qq < 3) {
+        // [32 qq, +32) for key rows [sb, sb + 32): group 0 serves rows r < 32,
+        // group 2 rows r >= 32 and group 1 all rows.
+        const int sb = qq == 1 ? 32 : 0;
+        const bool dact = qq == 1 || (qq == 0) == ((col & 63) < 32);
+        if (lq < 2 && qq < 3 && dact) {
             float* akk = reinterpret_cast<float*>(sm + SM_AKK);
             float* ptmp = reinterpret_cast<float*>(sm + SM_PTMP);
             const int r = col;
@@ -468,57 +513,44 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
             float v[32], w[32];
             ptx::tmem_ld32(tmem + lane_base + TM_D1 + 32 * qq, v);
             ptx::tmem_ld32(tmem + lane_base + TM_D1C + 32 * qq, w);
-            if (qq == 0 && r < 32) {
 #pragma unroll
-                for (int x = 0; x < 32; ++x) { akk[r * 65 + x] = x < r ? br * v[x] : 0.0f; ptmp[r * 65 + x] = w[x]; }
-            } else if (qq == 1) {
-#pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    const int s = 32 + x;
-                    akk[r * 65 + s] = (r >= 32 && s < r) ? br * v[x] : 0.0f;
-                    ptmp[r * 65 + s] = r >= 32 ? w[x] : 0.0f;
-                }
-            } else if (qq == 2 && r >= 32) {
-#pragma unroll
-                for (int x = 0; x < 32; ++x) { akk[r * 65 + x] = br * v[x]; ptmp[r * 65 + x] = w[x]; }
+            for (int x = 0; x < 32; ++x) {
+                akk[r * 65 + sb + x] = sb + x < r ? br * v[x] : 0.0f;
+                ptmp[r * 65 + sb + x] = w[x];
             }
         }
         __syncthreads();
-        // ---- P = D1 lanes 64..127 + PTMP, masked to s <= r, as high and low tiles
-        if (lq >= 2 && qq < 3) {
+        // ---- P = D1 lanes 64..127 + PTMP, masked to s <= r, as high and low
+        // tiles (16-byte stores: four consecutive key rows share a swizzle chunk)
+        if (lq >= 2 && qq < 3 && dact) {
             const float* ptmp = reinterpret_cast<const float*>(sm + SM_PTMP);
             const int r = col - 64;
             float v[32];
             ptx::tmem_ld32(tmem + lane_base + TM_D1 + 32 * qq, v);
-            if (qq == 0 && r < 32) {
+            const uint32_t rowo = (uint32_t)((sb >> 5) * T64_KB + r * 128);
 #pragma unroll
-                for (int x = 0; x < 32; ++x)
-                    st_hilo(sm, SM_PH + swz(r, x, T64_KB), SM_PL + swz(r, x, T64_KB), x <= r ? v[x] + ptmp[r * 65 + x] : 0.0f);
-            } else if (qq == 1) {
+            for (int c4 = 0; c4 < 8; ++c4) {
+                float hi[4], lo[4];
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    const int s = 32 + x;
-                    const float p = (r >= 32 && s <= r) ? v[x] + ptmp[r * 65 + s] : 0.0f;
-                    st_hilo(sm, SM_PH + swz(r, s, T64_KB), SM_PL + swz(r, s, T64_KB), p);
+                for (int u = 0; u < 4; ++u) {
+                    const int s2 = sb + 4 * c4 + u;
+                    const float pv = s2 <= r ? v[4 * c4 + u] + ptmp[r * 65 + s2] : 0.0f;
+                    hi[u] = pv;
+                    lo[u] = tf32_lo(pv);
                 }
-            } else if (qq == 2 && r >= 32) {
-#pragma unroll
-                for (int x = 0; x < 32; ++x)
-                    st_hilo(sm, SM_PH + swz(r, x, T64_KB), SM_PL + swz(r, x, T64_KB), v[x] + ptmp[r * 65 + x]);
+                const uint32_t o = rowo + ((c4 ^ (r & 7)) << 4);
+                *reinterpret_cast<float4*>(sm + SM_PH + o) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<float4*>(sm + SM_PL + o) = make_float4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
         // ---- Q o e^G and (K o e^{G_C - G})^T tiles for the later products
-        float qe[RPT];  // q^ e^G, whose low part is stored after the solve
         {
             float kd[RPT], kl[RPT];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
-                const int rr = r0 + r;
-                qe[r] = qv[r] * __expf(G[r]);
-                st_hi(sm, SM_QE + swz(rr, col, T64_KB), qe[r]);
-                const float x = kv[r] * __expf(GC - G[r]);
-                kd[r] = tf32r(x);
-                kl[r] = tf32r(x - kd[r]);
+                st_raw(sm, SM_QE + swz(r0 + r, col, T64_KB), qe[r]);
+                kd[r] = kdx[r];
+                kl[r] = tf32_lo(kdx[r]);
             }
             // KD^T row col, key rows [16 qq, +16): K-block qq >> 1, 16-byte chunks 4 (qq & 1) + j
 #pragma unroll
@@ -532,55 +564,90 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
         ptx::tc_fence_before();
         __syncthreads();
 
-        // ---- T = (I + A)^{-1}: 16x16 diagonal blocks, then off-diagonal blocks by level
+        // ---- T = (I + A)^{-1} (unit lower triangular) in two levels.  The 32x32
+        // diagonal halves are inverted by column-oriented forward substitution, one
+        // row per lane and four columns per warp; the off-diagonal half follows as
+        // T[H1,H0] = -inv(H1) A[H1,H0] inv(H0).  Each value goes to the fp32 copy
+        // (operand of the later steps) and to the T operand tile as it is formed.
         {
             const float* akk = reinterpret_cast<const float*>(sm + SM_AKK);
             float* ts = reinterpret_cast<float*>(sm + SM_TS);
-            for (int idx = tid; idx < C * 65; idx += NT) ts[idx] = 0.0f;
-            __syncthreads();
-            if (tid < C) {
-                const int bb = tid >> 4, cc = tid & 15;
-                float x[16];
+            {
+                const int hb = warp >> 3, cb = (warp & 7) * 4, rb = 32 * hb;
+                float av[31];  // this lane's row of A inside the half, zero on and above the diagonal
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float accv = (i == cc) ? 1.0f : 0.0f;
+                for (int j = 0; j < 31; ++j) av[j] = lane > j ? akk[(rb + lane) * 65 + rb + j] : 0.0f;
+                float x[4];
 #pragma unroll
-                    for (int j = 0; j < i; ++j) accv = __fmaf_rn(-akk[(16 * bb + i) * 65 + 16 * bb + j], x[j], accv);
-                    x[i] = accv;
+                for (int c = 0; c < 4; ++c) x[c] = lane == cb + c ? 1.0f : 0.0f;
+                // x_j is final once the steps before j are done (steps j < c add
+                // exact zeros to column c)
+#pragma unroll
+                for (int j = 0; j < 31; ++j) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) x[c] = __fmaf_rn(-av[j], __shfl_sync(0xffffffffu, x[c], j), x[c]);
                 }
 #pragma unroll
-                for (int i = 0; i < 16; ++i) ts[(16 * bb + i) * 65 + 16 * bb + cc] = x[i];
+                for (int c = 0; c < 4; ++c) {
+                    ts[(rb + lane) * 65 + rb + cb + c] = x[c];
+                    st_hi(sm, SM_T + swz(rb + lane, rb + cb + c, T64_KB), x[c]);
+                }
+                // the block above the diagonal, rows [0, 32) x columns [32, 64), is zero
+#pragma unroll
+                for (int e2 = 0; e2 < 2; ++e2) {
+                    const int e = tid + e2 * NT;
+                    st_raw(sm, SM_T + swz(e >> 5, 32 + (e & 31), T64_KB), 0.0f);
+                }
             }
             __syncthreads();
-            for (int d = 1; d <= 3; ++d) {
-                const int nb = 4 - d;
-                for (int idx = tid; idx < nb * 256; idx += NT) {
-                    const int bj = idx >> 8, x = (idx >> 4) & 15, y = idx & 15, bi = bj + d;
-                    float accv = 0.0f;
-                    for (int kk = bj; kk < bi; ++kk)
+            {   // X = A[H1,H0] inv(H0).  inv(H0) is stored with its zeros above the
+                // diagonal, so column y may start at any z <= y: at y rounded down to 4.
+                // Warp w takes columns w and 31 - w, lane = row of X.
+                const int y0 = warp, y1 = 31 - warp;
+                const float* arow = akk + (32 + lane) * 65;
+                float s0 = 0.0f, s1 = 0.0f;
+                for (int z4 = y0 & ~3; z4 < (y1 & ~3); z4 += 4) {
 #pragma unroll
-                        for (int z = 0; z < 16; ++z)
-                            accv = __fmaf_rn(akk[(16 * bi + x) * 65 + 16 * kk + z], ts[(16 * kk + z) * 65 + 16 * bj + y], accv);
-                    ms.M[bj][x][y] = accv;
+                    for (int u = 0; u < 4; ++u) s0 = __fmaf_rn(arow[z4 + u], ts[(z4 + u) * 65 + y0], s0);
                 }
-                __syncthreads();
-                for (int idx = tid; idx < nb * 256; idx += NT) {
-                    const int bj = idx >> 8, x = (idx >> 4) & 15, y = idx & 15, bi = bj + d;
-                    float accv = 0.0f;
+                for (int z4 = y1 & ~3; z4 < 32; z4 += 4) {
 #pragma unroll
-                    for (int z = 0; z < 16; ++z) accv = __fmaf_rn(ts[(16 * bi + x) * 65 + 16 * bi + z], ms.M[bj][z][y], accv);
-                    ts[(16 * bi + x) * 65 + 16 * bj + y] = -accv;
+                    for (int u = 0; u < 4; ++u) {
+                        const float az = arow[z4 + u];
+                        s0 = __fmaf_rn(az, ts[(z4 + u) * 65 + y0], s0);
+                        s1 = __fmaf_rn(az, ts[(z4 + u) * 65 + y1], s1);
+                    }
                 }
-                __syncthreads();
+                ms.X[lane][y0] = s0;
+                ms.X[lane][y1] = s1;
             }
-            for (int idx = tid; idx < C * C; idx += NT) {
-                const int r = idx / C, s = idx % C;
-                st_hi(sm, SM_T + swz(r, s, T64_KB), ts[r * 65 + s]);
+            __syncthreads();
+            {   // T[H1,H0] = -inv(H1) X.  inv(H1) is stored with its zeros above the
+                // diagonal, so row x may end at any z >= x: at x rounded up to 4.
+                // Warp w takes rows w and 31 - w, lane = column.
+                const int x0 = warp, x1 = 31 - warp;
+                const float* t0 = ts + (32 + x0) * 65 + 32;
+                const float* t1 = ts + (32 + x1) * 65 + 32;
+                float s0 = 0.0f, s1 = 0.0f;
+                for (int z4 = 0; z4 <= x0; z4 += 4) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float xz = ms.X[z4 + u][lane];
+                        s0 = __fmaf_rn(t0[z4 + u], xz, s0);
+                        s1 = __fmaf_rn(t1[z4 + u], xz, s1);
+                    }
+                }
+                for (int z4 = (x0 | 3) + 1; z4 <= x1; z4 += 4) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) s1 = __fmaf_rn(t1[z4 + u], ms.X[z4 + u][lane], s1);
+                }
+                st_hi(sm, SM_T + swz(32 + x0, lane, T64_KB), -s0);
+                st_hi(sm, SM_T + swz(32 + x1, lane, T64_KB), -s1);
             }
         }
         // the low part of the QE tile (over the dead A and P scratch)
 #pragma unroll
-        for (int r = 0; r < RPT; ++r) st_hi(sm, SM_QEL + swz(r0 + r, col, T64_KB), qe[r] - tf32r(qe[r]));
+        for (int r = 0; r < RPT; ++r) st_raw(sm, SM_QEL + swz(r0 + r, col, T64_KB), tf32_lo(qe[r]));
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncthreads();
@@ -589,6 +656,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
         if (tid == 0) {
             ptx::tc_fence_after();
             const uint32_t id = ptx::idesc_tf32(128, 64);
+#pragma unroll 1
             for (int ks = 0; ks < 8; ++ks) {
                 const uint64_t bd = dsc(sm, SM_T + (ks >> 2) * T64_KB + (ks & 3) * 32);
                 ptx::mma_tf32_ts(tmem + TM_WT, tmem + TM_XT + ks * 8, bd, id, ks > 0);
@@ -619,6 +687,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
         if (tid == 0) {
             ptx::tc_fence_after();
             const uint32_t id = ptx::idesc_tf32(128, 64);
+#pragma unroll 1
             for (int ks = 0; ks < 16; ++ks) {
                 const int kb = (ks >> 2) * T64_KB + (ks & 3) * 32;
                 ptx::mma_tf32_ts(tmem + TM_UT, tmem + TM_ST + ks * 8, dsc(sm, SM_NW + kb), id, 1);
@@ -632,11 +701,12 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
 
         // the raw staging region is free from here: prefetch the next chunk's rows
         if (ch + 1 < nchunks) {
-            stage_chunk(sm, a, c0 + C, seg0, seg1, slot, h);
+            if (tid == 0) stage_chunk(sm, maps, ms, c0 + C, h);
+            rpending = true;
             if (tid < C && c0 + C + tid < seg1) bnext = __bfloat162float(bg[(size_t)(c0 + C + tid) * H + h]);
         }
 
-        // ---- S^T <- S^T Diag(e^{G_C}); U^T -> high part in place and low part
+        // ---- S^T <- S^T Diag(e^{G_C}); U^T stays as the high part of U, its low part beside it
         {
             float v[32];
             const uint32_t ta = tmem + lane_base + TM_ST + 32 * qq;
@@ -644,16 +714,11 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
 #pragma unroll
             for (int x = 0; x < 32; ++x) v[x] *= ms.gamma[32 * qq + x];
             ptx::tmem_st32(ta, v);
-            float u[RPT], lo[RPT];
+            float u[RPT];
             ptx::tmem_ld16(tmem + lane_base + TM_UT + RPT * qq, u);
 #pragma unroll
-            for (int x = 0; x < RPT; ++x) {
-                const float hi = tf32r(u[x]);
-                lo[x] = tf32r(u[x] - hi);
-                u[x] = hi;
-            }
-            ptx::tmem_st16(tmem + lane_base + TM_UT + RPT * qq, u);
-            ptx::tmem_st16(tmem + lane_base + TM_UL + RPT * qq, lo);
+            for (int x = 0; x < RPT; ++x) u[x] = tf32_lo(u[x]);
+            ptx::tmem_st16(tmem + lane_base + TM_UL + RPT * qq, u);
         }
         ptx::tc_fence_before();
         __syncthreads();
@@ -662,12 +727,14 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
         if (tid == 0) {
             ptx::tc_fence_after();
             const uint32_t id64 = ptx::idesc_tf32(128, 64), id128 = ptx::idesc_tf32(128, 128);
+#pragma unroll 1
             for (int ks = 0; ks < 8; ++ks) {
                 const int kb = (ks >> 2) * T64_KB + (ks & 3) * 32;
                 ptx::mma_tf32_ts(tmem + TM_OT, tmem + TM_UT + ks * 8, dsc(sm, SM_PH + kb), id64, 1);
                 ptx::mma_tf32_ts(tmem + TM_OT, tmem + TM_UL + ks * 8, dsc(sm, SM_PH + kb), id64, 1);
                 ptx::mma_tf32_ts(tmem + TM_OT, tmem + TM_UT + ks * 8, dsc(sm, SM_PL + kb), id64, 1);
             }
+#pragma unroll 1
             for (int ks = 0; ks < 8; ++ks) {
                 const int kb = (ks >> 2) * 128 * 128 + (ks & 3) * 32;
                 ptx::mma_tf32_ts(tmem + TM_ST, tmem + TM_UT + ks * 8, dsc(sm, SM_KD + kb), id128, 1);
@@ -675,6 +742,20 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
                 ptx::mma_tf32_ts(tmem + TM_ST, tmem + TM_UT + ks * 8, dsc(sm, SM_KDL + kb), id128, 1);
             }
             ptx::mma_commit(&ms.bar);
+        }
+        // the output gate of this chunk's rows (bf16 bits, two rows per register),
+        // loaded while the product runs
+        uint32_t gp[RPT / 2];
+#pragma unroll
+        for (int x = 0; x < RPT / 2; ++x) gp[x] = 0u;
+        if (gg != nullptr) {
+            const unsigned short* gb = reinterpret_cast<const unsigned short*>(gg);
+#pragma unroll
+            for (int x = 0; x < RPT; ++x) {
+                const int r = r0 + x;
+                const uint32_t bits = r < nvalid ? gb[((size_t)(c0 + r) * H + h) * D + col] : 0u;
+                gp[x >> 1] |= bits << (16 * (x & 1));
+            }
         }
         if (!wait_mma(ms, ph, a.dev_status)) break;
 
@@ -700,17 +781,21 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
                 __syncthreads();
 #pragma unroll
                 for (int x = 0; x < RPT; ++x) {
-                    const int r = r0 + x;
-                    if (r < nvalid) {
-                        const float gv = __bfloat162float(gg[((size_t)(c0 + r) * H + h) * D + col]);
-                        o[x] = o[x] * ms.rms[r] * nw * sigmoidf_(gv);
-                    }
+                    const float gx = __uint_as_float((x & 1) ? (gp[x >> 1] & 0xFFFF0000u) : (gp[x >> 1] << 16));
+                    o[x] = o[x] * ms.rms[r0 + x] * nw * sigmoidf_(gx);
                 }
             }
+            const size_t ob = ((size_t)(c0 + r0) * H + h) * D + col;
+            if (a.out_bf16) {
+                __nv_bfloat16* ou = static_cast<__nv_bfloat16*>(a.out);
 #pragma unroll
-            for (int x = 0; x < RPT; ++x) {
-                const int r = r0 + x;
-                if (r < nvalid) store_out(a.out, ((size_t)(c0 + r) * H + h) * D + col, o[x], a.out_bf16);
+                for (int x = 0; x < RPT; ++x)
+                    if (r0 + x < nvalid) ou[ob + (size_t)x * H * D] = __float2bfloat16_rn(o[x]);
+            } else {
+                float* ou = static_cast<float*>(a.out);
+#pragma unroll
+                for (int x = 0; x < RPT; ++x)
+                    if (r0 + x < nvalid) ou[ob + (size_t)x * H * D] = o[x];
             }
         }
         ptx::tc_fence_before();
@@ -718,7 +803,8 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a)
     }
 
     // ---- final state S^T -> rec_state (S[i][j], lane j = col, key dims [32 qq, +32))
-    ptx::cp_async_wait_all();  // nothing may land in shared memory after the CTA ends
+    // nothing may land in shared memory after the CTA ends
+    if (tid == 0 && rpending) (void)ptx::mbar_wait(&ms.rbar, rph);
     if (!ms.err) {
         float* Sg = a.rec_state + ((size_t)slot * H + h) * D * D;
         float v[32];
@@ -741,6 +827,40 @@ bool chunk_supported(const kda_params* p)
            p->gate_mode == KDA_GATE_SAFE && p->gate_lower_bound >= -5.0f;
 }
 
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// [T][H * 128] bf16 rows (16-byte aligned base, row pitch H * 256 bytes); box of
+// one head's 128 channels x box_rows rows; zero fill outside the tensor.
+bool encode_rows(CUtensorMap* m, const void* base, int H, int T, int box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || base == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)H * chk::D, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)H * chk::D * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)chk::D, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
 {
     if (!io_bf16) return cudaErrorNotSupported;
@@ -753,8 +873,15 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
+    chk::RawMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (a.T > 0) {  // with no rows every unit returns before its first copy
+        if (!encode_rows(&maps.q, a.q, a.H, a.T, chk::RAWR) || !encode_rows(&maps.k, a.k, a.H, a.T, chk::RAWR) ||
+            !encode_rows(&maps.v, a.v, a.H, a.T, chk::RAWR) || !encode_rows(&maps.f, a.f, a.H, a.T, chk::C))
+            return cudaErrorInvalidValue;
+    }
     if (a.schedule) chk::kda_chunk_schedule_kernel<<<1, 256, 0, st>>>(a.cu_seqlens, a.N, a.schedule);
-    chk::kda_chunk_kernel<<<a.N * a.H, chk::NT, chk::SMEM_BYTES, st>>>(a);
+    chk::kda_chunk_kernel<<<a.N * a.H, chk::NT, chk::SMEM_BYTES, st>>>(a, maps);
     return cudaGetLastError();
 }
 

@@ -80,6 +80,20 @@ __device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint
         : "memory");
 }
 
+// 2-D tiled tensor copy global -> shared: the box of the tensor map at
+// element coordinates (x, y), completing its bytes on the mbarrier.  x times
+// the element size must be a multiple of 16 bytes; y may be negative or past
+// the tensor's end (those rows read as zero).
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar,
+                                            uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;
