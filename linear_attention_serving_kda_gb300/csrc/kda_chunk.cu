@@ -32,8 +32,10 @@
 //     K~^T U     = KD_hi U_hi + KD_hi U_lo + KD_lo U_hi   (the state update)
 //     (Q o e^G) S = QE_hi S_hi + QE_hi S_lo + QE_lo S_hi  (long prompts: the
 //                  carried state dominates the outputs)
+//     W S        = W (S_hi + S_lo)        (the state read truncated would bias
+//                  U when the decay is weak and the state grows)
 // (S in TMEM and U in TMEM are split the same way in place).  The remaining
-// products (W, W S, T) are single TF32 with operands rounded to nearest.  The
+// products (W and T) are single TF32 with operands rounded to nearest.  The
 // two A operands of the first product share their K~ rows: within each
 // 24 KiB K-block the layout is [Q~lo | K~ | Q~hi] (64 rows each),
 // and the tiles start at the first and the second 64-row slot.
@@ -683,7 +685,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
         ptx::tc_fence_before();
         __syncthreads();
 
-        // ---- third product: U^T = U'^T - S^T W^T ; O^T = S^T (Q o e^G)^T (split)
+        // ---- third product: U^T = U'^T - (S_hi + S_lo)^T W^T ; O^T = S^T (Q o e^G)^T (split)
         if (tid == 0) {
             ptx::tc_fence_after();
             const uint32_t id = ptx::idesc_tf32(128, 64);
@@ -691,6 +693,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
             for (int ks = 0; ks < 16; ++ks) {
                 const int kb = (ks >> 2) * T64_KB + (ks & 3) * 32;
                 ptx::mma_tf32_ts(tmem + TM_UT, tmem + TM_ST + ks * 8, dsc(sm, SM_NW + kb), id, 1);
+                ptx::mma_tf32_ts(tmem + TM_UT, tmem + TM_SL + ks * 8, dsc(sm, SM_NW + kb), id, 1);
                 ptx::mma_tf32_ts(tmem + TM_OT, tmem + TM_ST + ks * 8, dsc(sm, SM_QE + kb), id, ks > 0);
                 ptx::mma_tf32_ts(tmem + TM_OT, tmem + TM_SL + ks * 8, dsc(sm, SM_QE + kb), id, 1);
                 ptx::mma_tf32_ts(tmem + TM_OT, tmem + TM_ST + ks * 8, dsc(sm, SM_QEL + kb), id, 1);
