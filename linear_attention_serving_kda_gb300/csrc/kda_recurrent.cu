@@ -41,8 +41,9 @@ template <int D> struct RowSmem {
     float cw[3 * D][4];       // conv taps
     float dtb[D];             // dt_bias of this head
     float act[3 * D];         // post-SiLU q', k', v'
-    float qn[D], kn[D], alpha[D], u[D], fr[D];
-    float red[REC_WARPS][D];  // cross-warp partial sums
+    float alpha[D], fr[D];
+    float red[REC_WARPS][D];  // cross-warp partial sums of S'^T k
+    float red2[REC_WARPS][D]; // cross-warp partial sums of S^T q
     float scal[8];
 };
 
@@ -119,9 +120,16 @@ template <int D> __device__ __forceinline__ void store_tile(float* Sg, int r0, i
 // On entry sm.win[ring(t)] holds the raw q|k|v row, the K-1 ring slots before
 // it the previous raw rows, sm.fr the gate row, sm.cw / sm.dtb the head's
 // parameters; bval is the beta logit and gval the output gate of column tid
-// (used when has_g).  On return S is updated in registers, sm.alpha / sm.kn /
-// sm.u hold the row's decay, normalised key and update, and the result is the
+// (used when has_g).  On return S is updated in registers, sm.alpha holds the
+// row's decay, sm.act the post-SiLU q|k|v row, sm.scal[0..2] the q and k
+// inverse norms and beta, sm.red the per-warp partials of S'^T k (so the
+// normalised key is act[D + i] * scal[1] and the update u_j = beta (act[2D + j]
+// - sum_w red[w][j]), the same expressions as here), and the result is the
 // output of column tid (tid < D).  The caller syncs before the next row.
+//
+// Every warp computes the norms, beta and the update of its own columns
+// itself (identical operands in an identical order, so identical bits), which
+// leaves three barriers per row.
 template <int D>
 __device__ __forceinline__ float row_step(RowSmem<D>& sm, float (&s)[RecShape<D>::RPW][RecShape<D>::CPT],
                                           int t, int K, const RowConst& rc, float bval, float gval, bool has_g)
@@ -140,30 +148,29 @@ __device__ __forceinline__ float row_step(RowSmem<D>& sm, float (&s)[RecShape<D>
         sm.alpha[i] = __expf(log_alpha(rc.gate_mode, rc.lb, rc.ea, sm.fr[i], sm.dtb[i]));
     row_sync();
 
-    // q / k L2 norms and beta
-    if (warp < 2) {
-        float ss = 0.0f;
-        for (int c = lane; c < D; c += 32) ss = __fmaf_rn(sm.act[warp * D + c], sm.act[warp * D + c], ss);
-        ss = warp_sum(ss);
-        if (lane == 0) sm.scal[warp] = rsqrtf(ss + rc.l2_eps);
-    } else if (warp == 2 && lane == 0) {
-        sm.scal[2] = sigmoidf_(bval);
+    // q / k inverse L2 norms and beta (every warp; a butterfly sum leaves the
+    // same bits in every lane)
+    float ssq = 0.0f, ssk = 0.0f;
+    for (int c = lane; c < D; c += 32) {
+        ssq = __fmaf_rn(sm.act[c], sm.act[c], ssq);
+        ssk = __fmaf_rn(sm.act[D + c], sm.act[D + c], ssk);
     }
-    row_sync();
-    for (int c = tid; c < D; c += REC_THREADS) {
-        sm.qn[c] = sm.act[c] * sm.scal[0];
-        sm.kn[c] = sm.act[D + c] * sm.scal[1];
+    const float rq = rsqrtf(warp_sum(ssq) + rc.l2_eps);
+    const float rk = rsqrtf(warp_sum(ssk) + rc.l2_eps);
+    const float beta = sigmoidf_(bval);
+    if (tid == 0) {
+        sm.scal[0] = rq;
+        sm.scal[1] = rk;
+        sm.scal[2] = beta;
     }
-    row_sync();
 
     // S' = Diag(alpha) S ; kv = S'^T k (partial over this warp's rows)
-    const float beta = sm.scal[2];
     float part[CPT];
 #pragma unroll
     for (int cc = 0; cc < CPT; ++cc) part[cc] = 0.0f;
 #pragma unroll
     for (int rr = 0; rr < RPW; ++rr) {
-        const float ai = sm.alpha[r0 + rr], ki = sm.kn[r0 + rr];
+        const float ai = sm.alpha[r0 + rr], ki = sm.act[D + r0 + rr] * rk;
 #pragma unroll
         for (int cc = 0; cc < CPT; ++cc) {
             s[rr][cc] = __fmul_rn(ai, s[rr][cc]);
@@ -173,21 +180,22 @@ __device__ __forceinline__ float row_step(RowSmem<D>& sm, float (&s)[RecShape<D>
 #pragma unroll
     for (int cc = 0; cc < CPT; ++cc) sm.red[warp][c0 + cc] = part[cc];
     row_sync();
-    if (tid < D) {
-        float kv = 0.0f;
-#pragma unroll
-        for (int w = 0; w < REC_WARPS; ++w) kv += sm.red[w][tid];
-        sm.u[tid] = beta * (sm.act[2 * D + tid] - kv);
-    }
-    row_sync();
 
-    // S = S' + k u^T ; o = S^T q (partial)
+    // u of this thread's columns: the 8 partials summed in warp order
     float uc[CPT];
 #pragma unroll
-    for (int cc = 0; cc < CPT; ++cc) { uc[cc] = sm.u[c0 + cc]; part[cc] = 0.0f; }
+    for (int cc = 0; cc < CPT; ++cc) {
+        float kv = 0.0f;
+#pragma unroll
+        for (int w = 0; w < REC_WARPS; ++w) kv += sm.red[w][c0 + cc];
+        uc[cc] = beta * (sm.act[2 * D + c0 + cc] - kv);
+        part[cc] = 0.0f;
+    }
+
+    // S = S' + k u^T ; o = S^T q (partial)
 #pragma unroll
     for (int rr = 0; rr < RPW; ++rr) {
-        const float ki = sm.kn[r0 + rr], qi = sm.qn[r0 + rr];
+        const float ki = sm.act[D + r0 + rr] * rk, qi = sm.act[r0 + rr] * rq;
 #pragma unroll
         for (int cc = 0; cc < CPT; ++cc) {
             s[rr][cc] = __fmaf_rn(ki, uc[cc], s[rr][cc]);
@@ -195,13 +203,13 @@ __device__ __forceinline__ float row_step(RowSmem<D>& sm, float (&s)[RecShape<D>
         }
     }
 #pragma unroll
-    for (int cc = 0; cc < CPT; ++cc) sm.red[warp][c0 + cc] = part[cc];
+    for (int cc = 0; cc < CPT; ++cc) sm.red2[warp][c0 + cc] = part[cc];
     row_sync();
 
     float o = 0.0f;
     if (tid < D) {
 #pragma unroll
-        for (int w = 0; w < REC_WARPS; ++w) o += sm.red[w][tid];
+        for (int w = 0; w < REC_WARPS; ++w) o += sm.red2[w][tid];
         o *= rc.scale;
     }
     if (has_g) {
@@ -219,6 +227,15 @@ __device__ __forceinline__ float row_step(RowSmem<D>& sm, float (&s)[RecShape<D>
         }
     }
     return o;
+}
+
+// The update u_j of the last row_step (column j), from what it left in shared memory.
+template <int D> __device__ __forceinline__ float row_update(const RowSmem<D>& sm, int j)
+{
+    float kv = 0.0f;
+#pragma unroll
+    for (int w = 0; w < REC_WARPS; ++w) kv += sm.red[w][j];
+    return sm.scal[2] * (sm.act[2 * D + j] - kv);
 }
 
 // ------------------------------------------------------------------------
@@ -305,8 +322,8 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_recurrent_kernel(const Rec
             float* lg = a.log_f + (((size_t)seq * a.W + t) * H + h) * (3 * D);
             if (tid < D) {
                 lg[tid] = sm.alpha[tid];
-                lg[D + tid] = sm.kn[tid];
-                lg[2 * D + tid] = sm.u[tid];
+                lg[D + tid] = sm.act[D + tid] * sm.scal[1];
+                lg[2 * D + tid] = row_update<D>(sm, tid);
             }
             IO* lr = static_cast<IO*>(a.log_raw) + ((size_t)seq * a.W + t) * conv_dim;
             for (int c = tid; c < 3 * D; c += REC_THREADS) stv(lr + conv_channel<D>(c, h, H), sm.win[cur][c]);
