@@ -23,7 +23,7 @@
  *   - All pointers except `p` (and the host-side params it holds) are DEVICE
  *     pointers, owned by the caller, 16-byte aligned, dense row-major.  The
  *     library allocates nothing, never synchronises the host, and only
- *     enqueues work on `stream`; calls are CUDA-graph capturable.
+ *     enqueues work on `stream`; calls are CUDA-graph capturable (see below).
  *   - Row tensors are token-major: q, k, gate f: [rows][H][dk]; v, out_gate g,
  *     out: [rows][H][dv]; beta logits b: [rows][H].  Row tensors and the conv
  *     state use p->io_dtype; `out` uses p->out_dtype.
@@ -32,7 +32,17 @@
  *   - Recurrent state: fp32 [num_slots][H][dk][dv].
  *   - `slots` (nullable = identity) maps sequence b to its state slot; a
  *     negative slot skips the sequence entirely (no output, no state change).
- *   - States are updated in place; verify never writes them.
+ *   - States are updated in place; verify never writes them.  The conv
+ *     state and the recurrent state are the whole hand-off between calls: a
+ *     prompt prefilled and then decoded (or verified and committed) row by
+ *     row continues one recurrence.  On the chunked prefill path a prompt
+ *     cut into calls at multiples of 64 rows gives the bits of one uncut
+ *     call (TensorFold #850, Oct 15 comment: chunks start at a segment's
+ *     first row).
+ *   - Under CUDA-graph capture a call keeps its pointers, sizes and params;
+ *     the buffers' contents (rows, slot map, accepted counts) are read at
+ *     each replay.  Make one call of each entry point on a device before
+ *     capturing (it sets kernel attributes once).
  *   - `dev_status` (nullable): a device int32 into which kernels OR the
  *     KDA_DEV_* bits for input faults they detect (the faulty unit is
  *     skipped, never trapped).  The caller clears it.
