@@ -19,6 +19,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int io_size(int dtype) { return dtype == KDA_DTYPE_BF16 ? 2 : 4; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+size_t align1024(size_t x) { return (x + 1023) & ~size_t(1023); }
 
 int check_params(const kda_params* p)
 {
@@ -112,12 +113,27 @@ KDA_API const char* kda_status_string(int status)
     }
 }
 
+}  // extern "C"
+
+namespace kda {
+
+size_t prefill_workspace_bytes(const kda_params* p, int32_t N, int32_t T, bool allow_split)
+{
+    if (check_params(p) != KDA_OK || N < 0 || T < 0) return 0;
+    if (!chunk_supported(p)) return 0;
+    // the chunk kernel's longest-first schedule: one int32 per sequence
+    const size_t sched = align256((size_t)(N + 1) * sizeof(int32_t));
+    if (allow_split && chunk_split_wanted(p, N, T)) return align1024(sched) + chunk_split_bytes(N, p->num_heads);
+    return sched;
+}
+
+}  // namespace kda
+
+extern "C" {
+
 KDA_API size_t kda_prefill_workspace_bytes(const kda_params* p, int32_t N, int32_t T)
 {
-    (void)T;
-    if (check_params(p) != KDA_OK || N < 0) return 0;
-    // the chunk kernel's longest-first schedule: one int32 per sequence
-    return chunk_supported(p) ? align256((size_t)(N + 1) * sizeof(int32_t)) : 0;
+    return prefill_workspace_bytes(p, N, T, true);
 }
 
 KDA_API size_t kda_verify_log_bytes(const kda_params* p, int32_t B, int32_t W)
@@ -127,12 +143,13 @@ KDA_API size_t kda_verify_log_bytes(const kda_params* p, int32_t B, int32_t W)
     return log_float_bytes(p, B, W) + align256((size_t)B * W * conv_dim * io_size(p->io_dtype));
 }
 
-KDA_API int kda_prefill_varlen(const kda_params* p, const int32_t* cu_seqlens, int32_t N,
-                               int32_t T, const void* q, const void* k, const void* v,
-                               const void* gate, const void* beta, const void* out_gate,
-                               const int32_t* slots, void* conv_state, float* rec_state,
-                               void* out, void* workspace, size_t ws_bytes,
-                               int32_t* dev_status, cudaStream_t stream)
+}  // extern "C"
+
+int kda::prefill_varlen_impl(const kda_params* p, const int32_t* cu_seqlens, int32_t N, int32_t T,
+                             const void* q, const void* k, const void* v, const void* gate, const void* beta,
+                             const void* out_gate, const int32_t* slots, void* conv_state, float* rec_state,
+                             void* out, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                             cudaStream_t stream, bool allow_split)
 {
     int rc = check_params(p);
     if (rc != KDA_OK) return rc;
@@ -141,7 +158,7 @@ KDA_API int kda_prefill_varlen(const kda_params* p, const int32_t* cu_seqlens, i
     if ((rc = check_ptrs({cu_seqlens, conv_state, rec_state})) != KDA_OK) return rc;
     if (T > 0 && (rc = check_ptrs({q, k, v, gate, beta, out})) != KDA_OK) return rc;
     if ((rc = check_opt(out_gate)) != KDA_OK || (rc = check_opt(slots)) != KDA_OK) return rc;
-    const size_t need = kda_prefill_workspace_bytes(p, N, T);
+    const size_t need = prefill_workspace_bytes(p, N, T, allow_split);
     if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace))) return KDA_ERR_WORKSPACE;
     if ((rc = check_device()) != KDA_OK) return rc;
 
@@ -171,6 +188,8 @@ KDA_API int kda_prefill_varlen(const kda_params* p, const int32_t* cu_seqlens, i
         c.out = out;
         c.dev_status = dev_status;
         c.schedule = static_cast<int32_t*>(workspace);
+        if (allow_split && chunk_split_wanted(p, N, T))
+            c.split_ws = static_cast<unsigned char*>(workspace) + align1024(align256((size_t)(N + 1) * sizeof(int32_t)));
         return launch_chunk(p->io_dtype == KDA_DTYPE_BF16, c, stream) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
     }
     RecArgs a;
@@ -187,6 +206,19 @@ KDA_API int kda_prefill_varlen(const kda_params* p, const int32_t* cu_seqlens, i
     a.dev_status = dev_status;
     return launch_recurrent(REC_PREFILL, p->io_dtype == KDA_DTYPE_BF16, a, N * p->num_heads, stream) == cudaSuccess
                ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+extern "C" {
+
+KDA_API int kda_prefill_varlen(const kda_params* p, const int32_t* cu_seqlens, int32_t N,
+                               int32_t T, const void* q, const void* k, const void* v,
+                               const void* gate, const void* beta, const void* out_gate,
+                               const int32_t* slots, void* conv_state, float* rec_state,
+                               void* out, void* workspace, size_t ws_bytes,
+                               int32_t* dev_status, cudaStream_t stream)
+{
+    return prefill_varlen_impl(p, cu_seqlens, N, T, q, k, v, gate, beta, out_gate, slots, conv_state, rec_state,
+                               out, workspace, ws_bytes, dev_status, stream, true);
 }
 
 KDA_API int kda_decode(const kda_params* p, int32_t B, const void* q, const void* k,

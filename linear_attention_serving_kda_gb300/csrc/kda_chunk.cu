@@ -113,7 +113,8 @@ struct Misc {
     float rms[C];
     float X[32][33];          // solve scratch: A[H1,H0] inv(H0)
     uint64_t bar;             // tensor-core completion
-    uint64_t rbar;            // raw-row copies
+    uint64_t rbar;            // raw-row copies (split chain: third-product operands)
+    uint64_t bbar;            // split chain: fourth-product operands
     uint32_t tmem;
     int err;
 };
@@ -241,14 +242,593 @@ __device__ __forceinline__ void stage_chunk(unsigned char* sm, const RawMaps& m,
     ptx::tma_load_2d(sm + SM_RAWF, &m.f, h * D, c0, &ms.rbar, pol);
 }
 
+// The products are issued by ISSUERS threads (lane 0 of warps 0..3, one per
+// SM sub-partition), each owning a block of accumulator columns: a single
+// issuing thread cannot keep the tensor core busy with these small (N <= 96)
+// products.  Each accumulator still receives its MMAs in one thread's
+// program order, so every element sums the same terms in the same order.
+// All issuers commit to the same mbarrier (arrival count ISSUERS).
+constexpr int ISSUERS = 4;
+__device__ __forceinline__ int issuer(int tid) { return ((tid & 31) == 0 && tid < 32 * ISSUERS) ? tid >> 5 : -1; }
+
+// first product.  Both operands come from shared memory, whose bandwidth bounds
+// this product, so the A tile is not read twice by splitting N: issuer 0 runs
+// D1, issuer 1 D1c, the others only commit.
+__device__ __forceinline__ void issue_first(unsigned char* sm, uint32_t tmem, int q, uint64_t* bar)
+{
+    ptx::tc_fence_after();
+    const uint32_t id = ptx::idesc_tf32(128, 96);
+    const uint64_t dbh = dsc(sm, SM_B1H);
+    if (q == 0) {
+        const uint64_t dak = dsc(sm, SM_AX + 8192), dbl = dsc(sm, SM_B1L);
+#pragma unroll 4
+        for (int ks = 0; ks < 16; ++ks) {
+            const uint32_t ka = ((ks >> 2) * AX_KB + (ks & 3) * 32) >> 4, kb = ((ks >> 2) * B1_KB + (ks & 3) * 32) >> 4;
+            ptx::mma_tf32_ss(tmem + TM_D1, dak + ka, dbh + kb, id, ks > 0);
+            ptx::mma_tf32_ss(tmem + TM_D1, dak + ka, dbl + kb, id, 1);
+        }
+    } else if (q == 1) {
+        const uint64_t daq = dsc(sm, SM_AX);
+#pragma unroll 4
+        for (int ks = 0; ks < 16; ++ks) {
+            const uint32_t ka = ((ks >> 2) * AX_KB + (ks & 3) * 32) >> 4, kb = ((ks >> 2) * B1_KB + (ks & 3) * 32) >> 4;
+            ptx::mma_tf32_ss(tmem + TM_D1C, daq + ka, dbh + kb, id, ks > 0);
+        }
+    }
+    ptx::mma_commit(bar);
+}
+
+// second product.  Issuer q: W^T (q < 2) or U'^T (q >= 2), chunk rows [32 (q & 1), +32).
+__device__ __forceinline__ void issue_second(unsigned char* sm, uint32_t tmem, int q, uint64_t* bar)
+{
+    ptx::tc_fence_after();
+    const uint32_t id = ptx::idesc_tf32(128, 32);
+    const uint32_t hr = (q & 1) * 32, ho = (hr * 128) >> 4;
+    const uint64_t dt = dsc(sm, SM_T) + ho;
+#pragma unroll 4
+    for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t bd = dt + (((ks >> 2) * T64_KB + (ks & 3) * 32) >> 4);
+        if (q < 2) {
+            ptx::mma_tf32_ts(tmem + TM_WT + hr, tmem + TM_XT + ks * 8, bd, id, ks > 0);
+        } else {
+            ptx::mma_tf32_ts(tmem + TM_UT + hr, tmem + TM_YT + ks * 8, bd, id, ks > 0);
+            ptx::mma_tf32_ts(tmem + TM_UT + hr, tmem + TM_YL + ks * 8, bd, id, 1);
+        }
+    }
+    ptx::mma_commit(bar);
+}
+
+// The state-independent part of one chunk (all 512 threads): from the staged
+// raw rows (q, k, v with the HALO rows before the chunk, gate f) and beta in
+// shared memory, compute conv + SiLU, the gates and G, the first product (A
+// and P), the solve for T and the second product.  On return (true) the
+// tensor memory holds W^T and U'^T, shared memory the T, P (high, low),
+// Q o e^G (high, low) and K o e^{G_C - G} (high, low) tiles, and ms.gamma
+// holds e^{G_C}.  False: a tensor-core wait ran out (ms.err set).
+struct ThreadConst {
+    float wq[4], wk[4], wv[4];  // conv taps of this thread's q, k, v channel (4-tap form)
+    float dtc, ea;              // dt_bias of this key dim, exp(A_log) of the head
+};
+
+__device__ __forceinline__ ThreadConst thread_const(const ChunkArgs& a, int h, int col)
+{
+    ThreadConst t;
+    const int H = a.H, K = a.K;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int src = j - (4 - K);  // K < 4: the oldest taps are zero
+        t.wq[j] = src >= 0 ? a.conv_w[((size_t)0 * H * D + h * D + col) * K + src] : 0.f;
+        t.wk[j] = src >= 0 ? a.conv_w[((size_t)1 * H * D + h * D + col) * K + src] : 0.f;
+        t.wv[j] = src >= 0 ? a.conv_w[((size_t)2 * H * D + h * D + col) * K + src] : 0.f;
+    }
+    t.dtc = a.dt_bias[(size_t)h * D + col];
+    t.ea = expf(a.A_log[h]);
+    return t;
+}
+
+__device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const ChunkArgs& a, const ThreadConst& tc,
+                                            int nvalid, uint32_t tmem, uint32_t lane_base, uint32_t& ph)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int col = tid & (D - 1);
+    const int qq = tid >> 7;
+    const int half = qq >> 1;
+    const int lq = warp & 3;
+    const int r0 = RPT * qq;
+    const __nv_bfloat16* raw = reinterpret_cast<const __nv_bfloat16*>(sm + SM_RAW);
+    const __nv_bfloat16* rawf = reinterpret_cast<const __nv_bfloat16*>(sm + SM_RAWF);
+    const float* wq = tc.wq;
+    const float* wk = tc.wk;
+    const float* wv = tc.wv;
+    const float dtc = tc.dtc, ea = tc.ea;
+    // ---- prep: conv + SiLU, gate, running log-decay for this thread's column and 16 rows
+    float qv[RPT], kv[RPT], vv[RPT], G[RPT];
+    {
+        float xq[4], xk[4], xv[4];
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            xq[j] = __bfloat162float(raw[0 * RAWR * D + (r0 + j) * D + col]);
+            xk[j] = __bfloat162float(raw[1 * RAWR * D + (r0 + j) * D + col]);
+            xv[j] = __bfloat162float(raw[2 * RAWR * D + (r0 + j) * D + col]);
+        }
+        float run = 0.0f;
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int lr = r0 + r;
+            xq[3] = __bfloat162float(raw[0 * RAWR * D + (lr + 3) * D + col]);
+            xk[3] = __bfloat162float(raw[1 * RAWR * D + (lr + 3) * D + col]);
+            xv[3] = __bfloat162float(raw[2 * RAWR * D + (lr + 3) * D + col]);
+            float aq = 0.f, ak = 0.f, av = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                aq = __fmaf_rn(wq[j], xq[j], aq);
+                ak = __fmaf_rn(wk[j], xk[j], ak);
+                av = __fmaf_rn(wv[j], xv[j], av);
+            }
+            const bool ok = lr < nvalid;
+            qv[r] = ok ? siluf_(aq) : 0.0f;
+            kv[r] = ok ? siluf_(ak) : 0.0f;
+            vv[r] = ok ? siluf_(av) : 0.0f;
+            const float la = ok ? a.lb * sigmoidf_(ea * (__bfloat162float(rawf[lr * D + col]) + dtc)) : 0.0f;  // safe gate
+            run += la;
+            G[r] = run;
+#pragma unroll
+            for (int j = 0; j < 3; ++j) { xq[j] = xq[j + 1]; xk[j] = xk[j + 1]; xv[j] = xv[j + 1]; }
+        }
+    }
+    // row norms of q' and k' (this warp's 32 columns) and this quarter's log-decay total
+    {
+        float t[RPT];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) t[r] = qv[r] * qv[r];
+        const float pq = transpose_reduce16(t, lane);
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) t[r] = kv[r] * kv[r];
+        const float pk = transpose_reduce16(t, lane);
+        if (lane < 16) {
+            ms.npart[0][qq][lq][lane] = pq;
+            ms.npart[1][qq][lq][lane] = pk;
+        }
+        ms.gq[qq][col] = G[RPT - 1];
+    }
+    __syncthreads();
+    {
+        float off = 0.0f;
+        for (int q2 = 0; q2 < qq; ++q2) off += ms.gq[q2][col];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) G[r] += off;
+        if (qq == 1) ms.gx[0][col] = G[0];          // row 16
+        if (qq == 3) {
+            ms.gx[1][col] = G[0];                   // row 48
+            ms.gx[2][col] = G[RPT - 1];             // row 63 (G_C)
+            ms.gamma[col] = __expf(G[RPT - 1]);
+        }
+    }
+    if (tid < 2 * C) {
+        const int qk = tid / C, r = tid % C;
+        const float tot = ms.npart[qk][r >> 4][0][r & 15] + ms.npart[qk][r >> 4][1][r & 15] +
+                          ms.npart[qk][r >> 4][2][r & 15] + ms.npart[qk][r >> 4][3][r & 15];
+        ms.nrm[qk][r] = rsqrtf(tot + a.l2_eps);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        qv[r] *= ms.nrm[0][r0 + r];
+        kv[r] *= ms.nrm[1][r0 + r];
+    }
+
+    // ---- operands of the first and second products; q^ e^G and k^ e^{G_C - G}
+    // are formed here too and kept in registers until their tiles are free
+    const float Gm = ms.gx[half][col];   // reference row 16 (first half) or 48 (second half)
+    float qe[RPT], kdx[RPT];
+    {
+        const float Gm1 = ms.gx[1][col];
+        const float GC = ms.gx[2][col];
+        // the cross block (keys of the first half seen from the second half's
+        // reference) is written by the first half; the second half writes its
+        // own diagonal value a second time instead, which keeps this loop free
+        // of per-half code paths
+        const float Gx = half == 0 ? Gm1 : Gm;
+        const int xrow = half == 0 ? 64 : 0;
+        const float eGm = __expf(Gm);          // first half: e^{G_16} >= e^{-85}
+        const float cGC = __expf(GC - Gm);     // second half: e^{G_63 - G_48} >= e^{-75}
+        float xt[RPT], yt[RPT], yl[RPT];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int rr = r0 + r;
+            const float e = __expf(G[r] - Gm);
+            const float ie = __expf(Gm - G[r]);
+            const uint32_t o = swz(rr, col, AX_KB);
+            st_hi(sm, SM_AX + 8192 + o, kv[r] * e);
+            st_split(sm, SM_AX + 16384 + o, SM_AX + o, qv[r] * e);
+            st_split(sm, SM_B1H + swz(rr, col, B1_KB), SM_B1L + swz(rr, col, B1_KB), kv[r] * ie);
+            st_split(sm, SM_B1H + swz(xrow + rr, col, B1_KB), SM_B1L + swz(xrow + rr, col, B1_KB),
+                    kv[r] * __expf(Gx - G[r]));
+            // e^{G_r}: a product of two in-range factors in the first half; direct in the
+            // second (e^{G_48} may underflow).  e^{G_C - G_r}: direct in the first half
+            // (e^{G_C - G_16} may underflow); a product in the second.
+            const float eG = half == 0 ? e * eGm : __expf(G[r]);
+            const float edec = half == 0 ? __expf(GC - G[r]) : ie * cGC;
+            qe[r] = qv[r] * eG;
+            kdx[r] = kv[r] * edec;
+            const float be = ms.beta[rr];
+            xt[r] = tf32r(be * kv[r] * eG);
+            const float y = be * vv[r];
+            yt[r] = y;
+            yl[r] = tf32_lo(y);
+        }
+        ptx::tmem_st16(tmem + lane_base + TM_XT + RPT * qq, xt);
+        ptx::tmem_st16(tmem + lane_base + TM_YT + RPT * qq, yt);
+        ptx::tmem_st16(tmem + lane_base + TM_YL + RPT * qq, yl);
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+
+    // ---- first product: D1 = [K~; Q~hi](B1hi + B1lo)^T, D1c = [Q~lo; K~] B1hi^T
+    if (issuer(tid) >= 0) issue_first(sm, tmem, issuer(tid), &ms.bar);
+    if (!wait_mma(ms, ph, a.dev_status)) return false;
+
+    // ---- A (D1 lanes 0..63) and the D1c part of P.  D1 column of (row r,
+    // key row s): the first half reads its own block (column s), the second
+    // half its own block (column s >= 32) and, for s < 32, the cross block
+    // (column 64 + s).  Warp (lane quarter lq, column group qq) reads columns
+    // [32 qq, +32) for key rows [sb, sb + 32): group 0 serves rows r < 32,
+    // group 2 rows r >= 32 and group 1 all rows.
+    const int sb = qq == 1 ? 32 : 0;
+    const bool dact = qq == 1 || (qq == 0) == ((col & 63) < 32);
+    if (lq < 2 && qq < 3 && dact) {
+        float* akk = reinterpret_cast<float*>(sm + SM_AKK);
+        float* ptmp = reinterpret_cast<float*>(sm + SM_PTMP);
+        const int r = col;
+        const float br = ms.beta[r];
+        float v[32], w[32];
+        ptx::tmem_ld32(tmem + lane_base + TM_D1 + 32 * qq, v);
+        ptx::tmem_ld32(tmem + lane_base + TM_D1C + 32 * qq, w);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+            akk[r * 65 + sb + x] = sb + x < r ? br * v[x] : 0.0f;
+            ptmp[r * 65 + sb + x] = w[x];
+        }
+    }
+    __syncthreads();
+    // ---- P = D1 lanes 64..127 + PTMP, masked to s <= r, as high and low
+    // tiles (16-byte stores: four consecutive key rows share a swizzle chunk)
+    if (lq >= 2 && qq < 3 && dact) {
+        const float* ptmp = reinterpret_cast<const float*>(sm + SM_PTMP);
+        const int r = col - 64;
+        float v[32];
+        ptx::tmem_ld32(tmem + lane_base + TM_D1 + 32 * qq, v);
+        const uint32_t rowo = (uint32_t)((sb >> 5) * T64_KB + r * 128);
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+            float hi[4], lo[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int s2 = sb + 4 * c4 + u;
+                const float pv = s2 <= r ? v[4 * c4 + u] + ptmp[r * 65 + s2] : 0.0f;
+                hi[u] = pv;
+                lo[u] = tf32_lo(pv);
+            }
+            const uint32_t o = rowo + ((c4 ^ (r & 7)) << 4);
+            *reinterpret_cast<float4*>(sm + SM_PH + o) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<float4*>(sm + SM_PL + o) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+        }
+    }
+    // ---- Q o e^G and (K o e^{G_C - G})^T tiles for the later products
+    {
+        float kd[RPT], kl[RPT];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            st_raw(sm, SM_QE + swz(r0 + r, col, T64_KB), qe[r]);
+            kd[r] = kdx[r];
+            kl[r] = tf32_lo(kdx[r]);
+        }
+        // KD^T row col, key rows [16 qq, +16): K-block qq >> 1, 16-byte chunks 4 (qq & 1) + j
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int qd = 4 * (qq & 1) + j;
+            const uint32_t o = (qq >> 1) * 128 * 128 + col * 128 + ((qd ^ (col & 7)) << 4);
+            *reinterpret_cast<float4*>(sm + SM_KD + o) = make_float4(kd[4 * j], kd[4 * j + 1], kd[4 * j + 2], kd[4 * j + 3]);
+            *reinterpret_cast<float4*>(sm + SM_KDL + o) = make_float4(kl[4 * j], kl[4 * j + 1], kl[4 * j + 2], kl[4 * j + 3]);
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+
+    // ---- T = (I + A)^{-1} (unit lower triangular) in two levels.  The 32x32
+    // diagonal halves are inverted by column-oriented forward substitution, one
+    // row per lane and four columns per warp; the off-diagonal half follows as
+    // T[H1,H0] = -inv(H1) A[H1,H0] inv(H0).  Each value goes to the fp32 copy
+    // (operand of the later steps) and to the T operand tile as it is formed.
+    {
+        const float* akk = reinterpret_cast<const float*>(sm + SM_AKK);
+        float* ts = reinterpret_cast<float*>(sm + SM_TS);
+        {
+            const int hb = warp >> 3, cb = (warp & 7) * 4, rb = 32 * hb;
+            float av[31];  // this lane's row of A inside the half, zero on and above the diagonal
+#pragma unroll
+            for (int j = 0; j < 31; ++j) av[j] = lane > j ? akk[(rb + lane) * 65 + rb + j] : 0.0f;
+            float x[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) x[c] = lane == cb + c ? 1.0f : 0.0f;
+            // x_j is final once the steps before j are done (steps j < c add
+            // exact zeros to column c)
+#pragma unroll
+            for (int j = 0; j < 31; ++j) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) x[c] = __fmaf_rn(-av[j], __shfl_sync(0xffffffffu, x[c], j), x[c]);
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                ts[(rb + lane) * 65 + rb + cb + c] = x[c];
+                st_hi(sm, SM_T + swz(rb + lane, rb + cb + c, T64_KB), x[c]);
+            }
+            // the block above the diagonal, rows [0, 32) x columns [32, 64), is zero
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int e = tid + e2 * NT;
+                st_raw(sm, SM_T + swz(e >> 5, 32 + (e & 31), T64_KB), 0.0f);
+            }
+        }
+        __syncthreads();
+        {   // X = A[H1,H0] inv(H0).  inv(H0) is stored with its zeros above the
+            // diagonal, so column y may start at any z <= y: at y rounded down to 4.
+            // Warp w takes columns w and 31 - w, lane = row of X.
+            const int y0 = warp, y1 = 31 - warp;
+            const float* arow = akk + (32 + lane) * 65;
+            float s0 = 0.0f, s1 = 0.0f;
+            for (int z4 = y0 & ~3; z4 < (y1 & ~3); z4 += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) s0 = __fmaf_rn(arow[z4 + u], ts[(z4 + u) * 65 + y0], s0);
+            }
+            for (int z4 = y1 & ~3; z4 < 32; z4 += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float az = arow[z4 + u];
+                    s0 = __fmaf_rn(az, ts[(z4 + u) * 65 + y0], s0);
+                    s1 = __fmaf_rn(az, ts[(z4 + u) * 65 + y1], s1);
+                }
+            }
+            ms.X[lane][y0] = s0;
+            ms.X[lane][y1] = s1;
+        }
+        __syncthreads();
+        {   // T[H1,H0] = -inv(H1) X.  inv(H1) is stored with its zeros above the
+            // diagonal, so row x may end at any z >= x: at x rounded up to 4.
+            // Warp w takes rows w and 31 - w, lane = column.
+            const int x0 = warp, x1 = 31 - warp;
+            const float* t0 = ts + (32 + x0) * 65 + 32;
+            const float* t1 = ts + (32 + x1) * 65 + 32;
+            float s0 = 0.0f, s1 = 0.0f;
+            for (int z4 = 0; z4 <= x0; z4 += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float xz = ms.X[z4 + u][lane];
+                    s0 = __fmaf_rn(t0[z4 + u], xz, s0);
+                    s1 = __fmaf_rn(t1[z4 + u], xz, s1);
+                }
+            }
+            for (int z4 = (x0 | 3) + 1; z4 <= x1; z4 += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) s1 = __fmaf_rn(t1[z4 + u], ms.X[z4 + u][lane], s1);
+            }
+            st_hi(sm, SM_T + swz(32 + x0, lane, T64_KB), -s0);
+            st_hi(sm, SM_T + swz(32 + x1, lane, T64_KB), -s1);
+        }
+    }
+    // the low part of the QE tile (over the dead A and P scratch)
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) st_raw(sm, SM_QEL + swz(r0 + r, col, T64_KB), tf32_lo(qe[r]));
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+
+    // ---- second product: W^T = X^T T^T, U'^T = (Y + Ylo)^T T^T
+    if (issuer(tid) >= 0) issue_second(sm, tmem, issuer(tid), &ms.bar);
+    if (!wait_mma(ms, ph, a.dev_status)) return false;
+    return true;
+}
+
+// ---- inter-chunk steps shared by the fused kernel and the chain role of the
+// split kernel; `t*` arguments are TMEM addresses (this warp's lane quarter
+// included), `o*` shared-memory tile offsets.
+
+// S_lo = S - S_hi for this thread's 32 key dims
+__device__ __forceinline__ void state_low(uint32_t t_st, uint32_t t_sl)
+{
+    float s[32];
+    ptx::tmem_ld32(t_st, s);
+#pragma unroll
+    for (int x = 0; x < 32; ++x) s[x] -= __uint_as_float(__float_as_uint(s[x]) & 0xFFFFE000u);
+    ptx::tmem_st32(t_sl, s);
+}
+
+// -W tile (rounded to TF32) from W^T: this thread's 16 rows of column col
+__device__ __forceinline__ void store_neg_w(unsigned char* sm, uint32_t o_nw, uint32_t t_wt, int qq, int col)
+{
+    float v[RPT];
+    ptx::tmem_ld16(t_wt, v);
+#pragma unroll
+    for (int x = 0; x < RPT; ++x) st_hi(sm, o_nw + swz(RPT * qq + x, col, T64_KB), -v[x]);
+}
+
+// third product: U^T = U'^T - (S_hi + S_lo)^T W^T ; O^T = S^T (Q o e^G)^T (split).
+// Issuer q: U^T (q < 2) or O^T (q >= 2), chunk rows [32 (q & 1), +32).
+__device__ __forceinline__ void issue_third(unsigned char* sm, uint32_t tmem, int q, uint32_t o_nw, uint32_t o_qe,
+                                            uint32_t o_qel, uint32_t c_ut, uint32_t c_st, uint32_t c_sl,
+                                            uint32_t c_ot, uint64_t* bar)
+{
+    ptx::tc_fence_after();
+    const uint32_t id = ptx::idesc_tf32(128, 32);
+    const uint32_t hr = (q & 1) * 32, ho = (hr * 128) >> 4;  // N-half: TMEM columns, tile rows
+    if (q < 2) {
+        const uint64_t dnw = dsc(sm, o_nw) + ho;
+#pragma unroll 4
+        for (int ks = 0; ks < 16; ++ks) {
+            const uint32_t kb = ((ks >> 2) * T64_KB + (ks & 3) * 32) >> 4;
+            ptx::mma_tf32_ts(tmem + c_ut + hr, tmem + c_st + ks * 8, dnw + kb, id, 1);
+            ptx::mma_tf32_ts(tmem + c_ut + hr, tmem + c_sl + ks * 8, dnw + kb, id, 1);
+        }
+    } else {
+        const uint64_t dqe = dsc(sm, o_qe) + ho, dql = dsc(sm, o_qel) + ho;
+#pragma unroll 4
+        for (int ks = 0; ks < 16; ++ks) {
+            const uint32_t kb = ((ks >> 2) * T64_KB + (ks & 3) * 32) >> 4;
+            ptx::mma_tf32_ts(tmem + c_ot + hr, tmem + c_st + ks * 8, dqe + kb, id, ks > 0);
+            ptx::mma_tf32_ts(tmem + c_ot + hr, tmem + c_sl + ks * 8, dqe + kb, id, 1);
+            ptx::mma_tf32_ts(tmem + c_ot + hr, tmem + c_st + ks * 8, dql + kb, id, 1);
+        }
+    }
+    ptx::mma_commit(bar);
+}
+
+// S^T <- S^T Diag(gamma); U^T stays as the high part of U, its low part beside it
+__device__ __forceinline__ void rescale_split(uint32_t t_st, uint32_t t_ut, uint32_t t_ul, const float* gam32)
+{
+    float v[32];
+    ptx::tmem_ld32(t_st, v);
+#pragma unroll
+    for (int x = 0; x < 32; ++x) v[x] *= gam32[x];
+    ptx::tmem_st32(t_st, v);
+    float u[RPT];
+    ptx::tmem_ld16(t_ut, u);
+#pragma unroll
+    for (int x = 0; x < RPT; ++x) u[x] = tf32_lo(u[x]);
+    ptx::tmem_st16(t_ul, u);
+}
+
+// fourth product: O^T += U^T P^T ; S^T += U^T (K o e^{G_C - G}) (both split).
+// Issuer q: O^T chunk rows [32 q, +32) (q < 2) or S^T key dims [64 (q & 1), +64).
+__device__ __forceinline__ void issue_fourth(unsigned char* sm, uint32_t tmem, int q, uint32_t o_ph, uint32_t o_pl,
+                                             uint32_t o_kd, uint32_t o_kdl, uint32_t c_ut, uint32_t c_ul,
+                                             uint32_t c_st, uint32_t c_ot, uint64_t* bar)
+{
+    ptx::tc_fence_after();
+    if (q < 2) {
+        const uint32_t id = ptx::idesc_tf32(128, 32), hr = q * 32, ho = (hr * 128) >> 4;
+        const uint64_t dph = dsc(sm, o_ph) + ho, dpl = dsc(sm, o_pl) + ho;
+#pragma unroll 4
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t kb = ((ks >> 2) * T64_KB + (ks & 3) * 32) >> 4;
+            ptx::mma_tf32_ts(tmem + c_ot + hr, tmem + c_ut + ks * 8, dph + kb, id, 1);
+            ptx::mma_tf32_ts(tmem + c_ot + hr, tmem + c_ul + ks * 8, dph + kb, id, 1);
+            ptx::mma_tf32_ts(tmem + c_ot + hr, tmem + c_ut + ks * 8, dpl + kb, id, 1);
+        }
+    } else {
+        const uint32_t id = ptx::idesc_tf32(128, 64), hr = (q & 1) * 64, ho = (hr * 128) >> 4;
+        const uint64_t dkd = dsc(sm, o_kd) + ho, dkl = dsc(sm, o_kdl) + ho;
+#pragma unroll 4
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t kb = ((ks >> 2) * 128 * 128 + (ks & 3) * 32) >> 4;
+            ptx::mma_tf32_ts(tmem + c_st + hr, tmem + c_ut + ks * 8, dkd + kb, id, 1);
+            ptx::mma_tf32_ts(tmem + c_st + hr, tmem + c_ul + ks * 8, dkd + kb, id, 1);
+            ptx::mma_tf32_ts(tmem + c_st + hr, tmem + c_ut + ks * 8, dkl + kb, id, 1);
+        }
+    }
+    ptx::mma_commit(bar);
+}
+
+// the output gate of this thread's 16 rows (bf16 bits, two rows per register)
+__device__ __forceinline__ void load_gate_bits(uint32_t (&gp)[RPT / 2], const ChunkArgs& a, int c0, int r0,
+                                               int nvalid, int h, int col)
+{
+#pragma unroll
+    for (int x = 0; x < RPT / 2; ++x) gp[x] = 0u;
+    if (a.g != nullptr) {
+        const unsigned short* gb = static_cast<const unsigned short*>(a.g);
+#pragma unroll
+        for (int x = 0; x < RPT; ++x) {
+            const int r = r0 + x;
+            const uint32_t bits = r < nvalid ? gb[((size_t)(c0 + r) * a.H + h) * D + col] : 0u;
+            gp[x >> 1] |= bits << (16 * (x & 1));
+        }
+    }
+}
+
+// outputs of this thread's 16 rows (lane j = col), optional gated RMSNorm
+// (all threads; two block barriers when gated)
+__device__ __forceinline__ void write_outputs(Misc& ms, const ChunkArgs& a, uint32_t t_ot,
+                                              const uint32_t (&gp)[RPT / 2], int c0, int nvalid, int h, float nw)
+{
+    const int tid = threadIdx.x, lane = tid & 31, lq = (tid >> 5) & 3, qq = tid >> 7, col = tid & (D - 1);
+    const int r0 = RPT * qq, H = a.H;
+    float o[RPT];
+    ptx::tmem_ld16(t_ot, o);
+#pragma unroll
+    for (int x = 0; x < RPT; ++x) o[x] *= a.scale;
+    if (a.g != nullptr) {
+        float t[RPT];
+#pragma unroll
+        for (int x = 0; x < RPT; ++x) t[x] = o[x] * o[x];
+        const float pr = transpose_reduce16(t, lane);
+        if (lane < 16) ms.epart[qq][lq][lane] = pr;
+        __syncthreads();
+        if (tid < C) {
+            const int r = tid;
+            const float tot = ms.epart[r >> 4][0][r & 15] + ms.epart[r >> 4][1][r & 15] +
+                              ms.epart[r >> 4][2][r & 15] + ms.epart[r >> 4][3][r & 15];
+            ms.rms[r] = rsqrtf(tot * (1.0f / D) + a.norm_eps);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int x = 0; x < RPT; ++x) {
+            const float gx = __uint_as_float((x & 1) ? (gp[x >> 1] & 0xFFFF0000u) : (gp[x >> 1] << 16));
+            o[x] = o[x] * ms.rms[r0 + x] * nw * sigmoidf_(gx);
+        }
+    }
+    const size_t ob = ((size_t)(c0 + r0) * H + h) * D + col;
+    if (a.out_bf16) {
+        __nv_bfloat16* ou = static_cast<__nv_bfloat16*>(a.out);
+#pragma unroll
+        for (int x = 0; x < RPT; ++x)
+            if (r0 + x < nvalid) ou[ob + (size_t)x * H * D] = __float2bfloat16_rn(o[x]);
+    } else {
+        float* ou = static_cast<float*>(a.out);
+#pragma unroll
+        for (int x = 0; x < RPT; ++x)
+            if (r0 + x < nvalid) ou[ob + (size_t)x * H * D] = o[x];
+    }
+}
+
+// a segment's first chunk: the rows before it are the carried conv state
+// (oldest first; zero where K - 1 < HALO)
+__device__ __forceinline__ void patch_halo(unsigned char* sm, const ChunkArgs& a, int slot, int h)
+{
+    const int H = a.H, K = a.K, conv_dim = 3 * H * D;
+    const __nv_bfloat16* cs = static_cast<const __nv_bfloat16*>(a.conv_state);
+    __nv_bfloat16* rw = reinterpret_cast<__nv_bfloat16*>(sm + SM_RAW);
+    for (int idx = threadIdx.x; idx < 3 * HALO * D; idx += NT) {
+        const int tsel = idx / (HALO * D), sr = (idx / D) % HALO, cc = idx % D;
+        const int cr = (K - 1) - HALO + sr;
+        rw[tsel * RAWR * D + sr * D + cc] =
+            cr >= 0 ? cs[((size_t)slot * (K - 1) + cr) * conv_dim + (size_t)tsel * H * D + h * D + cc]
+                    : __float2bfloat16_rn(0.0f);
+    }
+}
+
+// wait (thread 0, bounded) for the raw-row copies of parity rph; all threads
+// then observe the completed phase.  False: the wait ran out (ms.err set).
+__device__ __forceinline__ bool wait_rows(Misc& ms, uint32_t& rph, int32_t* dev_status)
+{
+    if (threadIdx.x == 0 && !ptx::mbar_wait(&ms.rbar, rph)) {
+        ms.err = 1;
+        flag_status(dev_status, KDA_DEV_TIMEOUT);
+    }
+    __syncthreads();
+    if (ms.err) return false;
+    (void)ptx::mbar_try_wait(&ms.rbar, rph);  // completed: makes the copied rows visible to this thread
+    rph ^= 1u;
+    return true;
+}
+
 __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, const __grid_constant__ RawMaps maps)
 {
     extern __shared__ __align__(1024) unsigned char sm[];
     Misc& ms = *reinterpret_cast<Misc*>(sm + SM_MISC);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int col = tid & (D - 1);  // channel / key dim / value dim / TMEM lane of this thread
     const int qq = tid >> 7;        // quarter: chunk rows [16 qq, 16 qq + 16); also the TMEM column group
-    const int half = qq >> 1;       // 32-row half holding those rows
     const int lq = warp & 3;        // TMEM lane quarter of this warp (lanes 32 lq ..)
     const int H = a.H, K = a.K;
     const int conv_dim = 3 * H * D;
@@ -274,11 +854,10 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
     }
 
     const __nv_bfloat16* bg = static_cast<const __nv_bfloat16*>(a.b);
-    const __nv_bfloat16* gg = static_cast<const __nv_bfloat16*>(a.g);
     __nv_bfloat16* cs = static_cast<__nv_bfloat16*>(a.conv_state);
 
     if (tid == 0) {
-        ptx::mbar_init(&ms.bar, 1);
+        ptx::mbar_init(&ms.bar, ISSUERS);
         ptx::mbar_init(&ms.rbar, 1);
         ptx::fence_mbar_init();
         ms.err = 0;
@@ -294,17 +873,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
     uint32_t rph = 0;        // parity of the raw-row copies being waited for
     bool rpending = true;    // raw-row copies issued and not yet waited for
 
-    // ---- per-CTA constants: this thread's conv taps (4-tap form) and gate params
-    float wq[4], wk[4], wv[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int src = j - (4 - K);  // K < 4: the oldest taps are zero
-        wq[j] = src >= 0 ? a.conv_w[((size_t)0 * H * D + h * D + col) * K + src] : 0.f;
-        wk[j] = src >= 0 ? a.conv_w[((size_t)1 * H * D + h * D + col) * K + src] : 0.f;
-        wv[j] = src >= 0 ? a.conv_w[((size_t)2 * H * D + h * D + col) * K + src] : 0.f;
-    }
-    const float dtc = a.dt_bias[(size_t)h * D + col];
-    const float ea = expf(a.A_log[h]);
+    const ThreadConst tc = thread_const(a, h, col);
     const float nw = a.norm_w ? a.norm_w[col] : 1.0f;
 
     // ---- initial state -> TMEM S^T (lane j = col, key dims [32 qq, +32))
@@ -325,33 +894,15 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
         const int r0 = RPT * qq;
 
         if (tid < C) ms.beta[tid] = tid < nvalid ? sigmoidf_(bnext) : 0.0f;
-        if (tid == 0 && !ptx::mbar_wait(&ms.rbar, rph)) {
-            ms.err = 1;
-            flag_status(a.dev_status, KDA_DEV_TIMEOUT);
-        }
-        __syncthreads();
-        if (ms.err) break;
-        (void)ptx::mbar_try_wait(&ms.rbar, rph);  // completed: makes the copied rows visible to this thread
-        rph ^= 1u;
+        if (!wait_rows(ms, rph, a.dev_status)) break;
         rpending = false;
-
-        const __nv_bfloat16* raw = reinterpret_cast<const __nv_bfloat16*>(sm + SM_RAW);
-        const __nv_bfloat16* rawf = reinterpret_cast<const __nv_bfloat16*>(sm + SM_RAWF);
         if (ch == 0) {
-            // a segment's first chunk: the rows before it are the carried conv
-            // state (oldest first; zero where K - 1 < HALO)
-            __nv_bfloat16* rw = reinterpret_cast<__nv_bfloat16*>(sm + SM_RAW);
-            for (int idx = tid; idx < 3 * HALO * D; idx += NT) {
-                const int tsel = idx / (HALO * D), sr = (idx / D) % HALO, cc = idx % D;
-                const int cr = (K - 1) - HALO + sr;
-                rw[tsel * RAWR * D + sr * D + cc] =
-                    cr >= 0 ? cs[((size_t)slot * (K - 1) + cr) * conv_dim + (size_t)tsel * H * D + h * D + cc]
-                            : __float2bfloat16_rn(0.0f);
-            }
+            patch_halo(sm, a, slot, h);
             __syncthreads();
         }
         if (ch == nchunks - 1) {
             // the new conv state: the sequence's last K-1 raw rows
+            const __nv_bfloat16* raw = reinterpret_cast<const __nv_bfloat16*>(sm + SM_RAW);
             for (int idx = tid; idx < 3 * D * (K - 1); idx += NT) {
                 const int r = idx / (3 * D), c = idx % (3 * D), tsel = c / D, cc = c % D;
                 const int sr = HALO + nvalid - (K - 1) + r;
@@ -360,346 +911,17 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
             }
         }
 
-        // ---- prep: conv + SiLU, gate, running log-decay for this thread's column and 16 rows
-        float qv[RPT], kv[RPT], vv[RPT], G[RPT];
-        {
-            float xq[4], xk[4], xv[4];
-#pragma unroll
-            for (int j = 0; j < 3; ++j) {
-                xq[j] = __bfloat162float(raw[0 * RAWR * D + (r0 + j) * D + col]);
-                xk[j] = __bfloat162float(raw[1 * RAWR * D + (r0 + j) * D + col]);
-                xv[j] = __bfloat162float(raw[2 * RAWR * D + (r0 + j) * D + col]);
-            }
-            float run = 0.0f;
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) {
-                const int lr = r0 + r;
-                xq[3] = __bfloat162float(raw[0 * RAWR * D + (lr + 3) * D + col]);
-                xk[3] = __bfloat162float(raw[1 * RAWR * D + (lr + 3) * D + col]);
-                xv[3] = __bfloat162float(raw[2 * RAWR * D + (lr + 3) * D + col]);
-                float aq = 0.f, ak = 0.f, av = 0.f;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    aq = __fmaf_rn(wq[j], xq[j], aq);
-                    ak = __fmaf_rn(wk[j], xk[j], ak);
-                    av = __fmaf_rn(wv[j], xv[j], av);
-                }
-                const bool ok = lr < nvalid;
-                qv[r] = ok ? siluf_(aq) : 0.0f;
-                kv[r] = ok ? siluf_(ak) : 0.0f;
-                vv[r] = ok ? siluf_(av) : 0.0f;
-                const float la = ok ? a.lb * sigmoidf_(ea * (__bfloat162float(rawf[lr * D + col]) + dtc)) : 0.0f;  // safe gate
-                run += la;
-                G[r] = run;
-#pragma unroll
-                for (int j = 0; j < 3; ++j) { xq[j] = xq[j + 1]; xk[j] = xk[j + 1]; xv[j] = xv[j + 1]; }
-            }
-        }
-        // row norms of q' and k' (this warp's 32 columns) and this quarter's log-decay total
-        {
-            float t[RPT];
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) t[r] = qv[r] * qv[r];
-            const float pq = transpose_reduce16(t, lane);
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) t[r] = kv[r] * kv[r];
-            const float pk = transpose_reduce16(t, lane);
-            if (lane < 16) {
-                ms.npart[0][qq][lq][lane] = pq;
-                ms.npart[1][qq][lq][lane] = pk;
-            }
-            ms.gq[qq][col] = G[RPT - 1];
-        }
-        __syncthreads();
-        {
-            float off = 0.0f;
-            for (int q2 = 0; q2 < qq; ++q2) off += ms.gq[q2][col];
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) G[r] += off;
-            if (qq == 1) ms.gx[0][col] = G[0];          // row 16
-            if (qq == 3) {
-                ms.gx[1][col] = G[0];                   // row 48
-                ms.gx[2][col] = G[RPT - 1];             // row 63 (G_C)
-                ms.gamma[col] = __expf(G[RPT - 1]);
-            }
-        }
-        if (tid < 2 * C) {
-            const int qk = tid / C, r = tid % C;
-            const float tot = ms.npart[qk][r >> 4][0][r & 15] + ms.npart[qk][r >> 4][1][r & 15] +
-                              ms.npart[qk][r >> 4][2][r & 15] + ms.npart[qk][r >> 4][3][r & 15];
-            ms.nrm[qk][r] = rsqrtf(tot + a.l2_eps);
-        }
-        __syncthreads();
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-            qv[r] *= ms.nrm[0][r0 + r];
-            kv[r] *= ms.nrm[1][r0 + r];
-        }
-
-        // ---- operands of the first and second products; q^ e^G and k^ e^{G_C - G}
-        // are formed here too and kept in registers until their tiles are free
-        const float Gm = ms.gx[half][col];   // reference row 16 (first half) or 48 (second half)
-        float qe[RPT], kdx[RPT];
-        {
-            const float Gm1 = ms.gx[1][col];
-            const float GC = ms.gx[2][col];
-            // the cross block (keys of the first half seen from the second half's
-            // reference) is written by the first half; the second half writes its
-            // own diagonal value a second time instead, which keeps this loop free
-            // of per-half code paths
-            const float Gx = half == 0 ? Gm1 : Gm;
-            const int xrow = half == 0 ? 64 : 0;
-            const float eGm = __expf(Gm);          // first half: e^{G_16} >= e^{-85}
-            const float cGC = __expf(GC - Gm);     // second half: e^{G_63 - G_48} >= e^{-75}
-            float xt[RPT], yt[RPT], yl[RPT];
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) {
-                const int rr = r0 + r;
-                const float e = __expf(G[r] - Gm);
-                const float ie = __expf(Gm - G[r]);
-                const uint32_t o = swz(rr, col, AX_KB);
-                st_hi(sm, SM_AX + 8192 + o, kv[r] * e);
-                st_split(sm, SM_AX + 16384 + o, SM_AX + o, qv[r] * e);
-                st_split(sm, SM_B1H + swz(rr, col, B1_KB), SM_B1L + swz(rr, col, B1_KB), kv[r] * ie);
-                st_split(sm, SM_B1H + swz(xrow + rr, col, B1_KB), SM_B1L + swz(xrow + rr, col, B1_KB),
-                        kv[r] * __expf(Gx - G[r]));
-                // e^{G_r}: a product of two in-range factors in the first half; direct in the
-                // second (e^{G_48} may underflow).  e^{G_C - G_r}: direct in the first half
-                // (e^{G_C - G_16} may underflow); a product in the second.
-                const float eG = half == 0 ? e * eGm : __expf(G[r]);
-                const float edec = half == 0 ? __expf(GC - G[r]) : ie * cGC;
-                qe[r] = qv[r] * eG;
-                kdx[r] = kv[r] * edec;
-                const float be = ms.beta[rr];
-                xt[r] = tf32r(be * kv[r] * eG);
-                const float y = be * vv[r];
-                yt[r] = y;
-                yl[r] = tf32_lo(y);
-            }
-            ptx::tmem_st16(tmem + lane_base + TM_XT + RPT * qq, xt);
-            ptx::tmem_st16(tmem + lane_base + TM_YT + RPT * qq, yt);
-            ptx::tmem_st16(tmem + lane_base + TM_YL + RPT * qq, yl);
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        __syncthreads();
-
-        // ---- first product: D1 = [K~; Q~hi](B1hi + B1lo)^T, D1c = [Q~lo; K~] B1hi^T
-        if (tid == 0) {
-            ptx::tc_fence_after();
-            const uint32_t id = ptx::idesc_tf32(128, 96);
-#pragma unroll 1
-            for (int ks = 0; ks < 16; ++ks) {
-                const int ka = (ks >> 2) * AX_KB + (ks & 3) * 32, kb = (ks >> 2) * B1_KB + (ks & 3) * 32;
-                ptx::mma_tf32_ss(tmem + TM_D1, dsc(sm, SM_AX + 8192 + ka), dsc(sm, SM_B1H + kb), id, ks > 0);
-                ptx::mma_tf32_ss(tmem + TM_D1, dsc(sm, SM_AX + 8192 + ka), dsc(sm, SM_B1L + kb), id, 1);
-                ptx::mma_tf32_ss(tmem + TM_D1C, dsc(sm, SM_AX + ka), dsc(sm, SM_B1H + kb), id, ks > 0);
-            }
-            ptx::mma_commit(&ms.bar);
-        }
-        if (!wait_mma(ms, ph, a.dev_status)) break;
-
-        // ---- A (D1 lanes 0..63) and the D1c part of P.  D1 column of (row r,
-        // key row s): the first half reads its own block (column s), the second
-        // half its own block (column s >= 32) and, for s < 32, the cross block
-        // (column 64 + s).  Warp (lane quarter lq, column group qq) reads columns
-        // [32 qq, +32) for key rows [sb, sb + 32): group 0 serves rows r < 32,
-        // group 2 rows r >= 32 and group 1 all rows.
-        const int sb = qq == 1 ? 32 : 0;
-        const bool dact = qq == 1 || (qq == 0) == ((col & 63) < 32);
-        if (lq < 2 && qq < 3 && dact) {
-            float* akk = reinterpret_cast<float*>(sm + SM_AKK);
-            float* ptmp = reinterpret_cast<float*>(sm + SM_PTMP);
-            const int r = col;
-            const float br = ms.beta[r];
-            float v[32], w[32];
-            ptx::tmem_ld32(tmem + lane_base + TM_D1 + 32 * qq, v);
-            ptx::tmem_ld32(tmem + lane_base + TM_D1C + 32 * qq, w);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) {
-                akk[r * 65 + sb + x] = sb + x < r ? br * v[x] : 0.0f;
-                ptmp[r * 65 + sb + x] = w[x];
-            }
-        }
-        __syncthreads();
-        // ---- P = D1 lanes 64..127 + PTMP, masked to s <= r, as high and low
-        // tiles (16-byte stores: four consecutive key rows share a swizzle chunk)
-        if (lq >= 2 && qq < 3 && dact) {
-            const float* ptmp = reinterpret_cast<const float*>(sm + SM_PTMP);
-            const int r = col - 64;
-            float v[32];
-            ptx::tmem_ld32(tmem + lane_base + TM_D1 + 32 * qq, v);
-            const uint32_t rowo = (uint32_t)((sb >> 5) * T64_KB + r * 128);
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-                float hi[4], lo[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int s2 = sb + 4 * c4 + u;
-                    const float pv = s2 <= r ? v[4 * c4 + u] + ptmp[r * 65 + s2] : 0.0f;
-                    hi[u] = pv;
-                    lo[u] = tf32_lo(pv);
-                }
-                const uint32_t o = rowo + ((c4 ^ (r & 7)) << 4);
-                *reinterpret_cast<float4*>(sm + SM_PH + o) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<float4*>(sm + SM_PL + o) = make_float4(lo[0], lo[1], lo[2], lo[3]);
-            }
-        }
-        // ---- Q o e^G and (K o e^{G_C - G})^T tiles for the later products
-        {
-            float kd[RPT], kl[RPT];
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) {
-                st_raw(sm, SM_QE + swz(r0 + r, col, T64_KB), qe[r]);
-                kd[r] = kdx[r];
-                kl[r] = tf32_lo(kdx[r]);
-            }
-            // KD^T row col, key rows [16 qq, +16): K-block qq >> 1, 16-byte chunks 4 (qq & 1) + j
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int qd = 4 * (qq & 1) + j;
-                const uint32_t o = (qq >> 1) * 128 * 128 + col * 128 + ((qd ^ (col & 7)) << 4);
-                *reinterpret_cast<float4*>(sm + SM_KD + o) = make_float4(kd[4 * j], kd[4 * j + 1], kd[4 * j + 2], kd[4 * j + 3]);
-                *reinterpret_cast<float4*>(sm + SM_KDL + o) = make_float4(kl[4 * j], kl[4 * j + 1], kl[4 * j + 2], kl[4 * j + 3]);
-            }
-        }
-        ptx::tc_fence_before();
-        __syncthreads();
-
-        // ---- T = (I + A)^{-1} (unit lower triangular) in two levels.  The 32x32
-        // diagonal halves are inverted by column-oriented forward substitution, one
-        // row per lane and four columns per warp; the off-diagonal half follows as
-        // T[H1,H0] = -inv(H1) A[H1,H0] inv(H0).  Each value goes to the fp32 copy
-        // (operand of the later steps) and to the T operand tile as it is formed.
-        {
-            const float* akk = reinterpret_cast<const float*>(sm + SM_AKK);
-            float* ts = reinterpret_cast<float*>(sm + SM_TS);
-            {
-                const int hb = warp >> 3, cb = (warp & 7) * 4, rb = 32 * hb;
-                float av[31];  // this lane's row of A inside the half, zero on and above the diagonal
-#pragma unroll
-                for (int j = 0; j < 31; ++j) av[j] = lane > j ? akk[(rb + lane) * 65 + rb + j] : 0.0f;
-                float x[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) x[c] = lane == cb + c ? 1.0f : 0.0f;
-                // x_j is final once the steps before j are done (steps j < c add
-                // exact zeros to column c)
-#pragma unroll
-                for (int j = 0; j < 31; ++j) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) x[c] = __fmaf_rn(-av[j], __shfl_sync(0xffffffffu, x[c], j), x[c]);
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    ts[(rb + lane) * 65 + rb + cb + c] = x[c];
-                    st_hi(sm, SM_T + swz(rb + lane, rb + cb + c, T64_KB), x[c]);
-                }
-                // the block above the diagonal, rows [0, 32) x columns [32, 64), is zero
-#pragma unroll
-                for (int e2 = 0; e2 < 2; ++e2) {
-                    const int e = tid + e2 * NT;
-                    st_raw(sm, SM_T + swz(e >> 5, 32 + (e & 31), T64_KB), 0.0f);
-                }
-            }
-            __syncthreads();
-            {   // X = A[H1,H0] inv(H0).  inv(H0) is stored with its zeros above the
-                // diagonal, so column y may start at any z <= y: at y rounded down to 4.
-                // Warp w takes columns w and 31 - w, lane = row of X.
-                const int y0 = warp, y1 = 31 - warp;
-                const float* arow = akk + (32 + lane) * 65;
-                float s0 = 0.0f, s1 = 0.0f;
-                for (int z4 = y0 & ~3; z4 < (y1 & ~3); z4 += 4) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) s0 = __fmaf_rn(arow[z4 + u], ts[(z4 + u) * 65 + y0], s0);
-                }
-                for (int z4 = y1 & ~3; z4 < 32; z4 += 4) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float az = arow[z4 + u];
-                        s0 = __fmaf_rn(az, ts[(z4 + u) * 65 + y0], s0);
-                        s1 = __fmaf_rn(az, ts[(z4 + u) * 65 + y1], s1);
-                    }
-                }
-                ms.X[lane][y0] = s0;
-                ms.X[lane][y1] = s1;
-            }
-            __syncthreads();
-            {   // T[H1,H0] = -inv(H1) X.  inv(H1) is stored with its zeros above the
-                // diagonal, so row x may end at any z >= x: at x rounded up to 4.
-                // Warp w takes rows w and 31 - w, lane = column.
-                const int x0 = warp, x1 = 31 - warp;
-                const float* t0 = ts + (32 + x0) * 65 + 32;
-                const float* t1 = ts + (32 + x1) * 65 + 32;
-                float s0 = 0.0f, s1 = 0.0f;
-                for (int z4 = 0; z4 <= x0; z4 += 4) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float xz = ms.X[z4 + u][lane];
-                        s0 = __fmaf_rn(t0[z4 + u], xz, s0);
-                        s1 = __fmaf_rn(t1[z4 + u], xz, s1);
-                    }
-                }
-                for (int z4 = (x0 | 3) + 1; z4 <= x1; z4 += 4) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) s1 = __fmaf_rn(t1[z4 + u], ms.X[z4 + u][lane], s1);
-                }
-                st_hi(sm, SM_T + swz(32 + x0, lane, T64_KB), -s0);
-                st_hi(sm, SM_T + swz(32 + x1, lane, T64_KB), -s1);
-            }
-        }
-        // the low part of the QE tile (over the dead A and P scratch)
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) st_raw(sm, SM_QEL + swz(r0 + r, col, T64_KB), tf32_lo(qe[r]));
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        __syncthreads();
-
-        // ---- second product: W^T = X^T T^T, U'^T = (Y + Ylo)^T T^T
-        if (tid == 0) {
-            ptx::tc_fence_after();
-            const uint32_t id = ptx::idesc_tf32(128, 64);
-#pragma unroll 1
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t bd = dsc(sm, SM_T + (ks >> 2) * T64_KB + (ks & 3) * 32);
-                ptx::mma_tf32_ts(tmem + TM_WT, tmem + TM_XT + ks * 8, bd, id, ks > 0);
-                ptx::mma_tf32_ts(tmem + TM_UT, tmem + TM_YT + ks * 8, bd, id, ks > 0);
-                ptx::mma_tf32_ts(tmem + TM_UT, tmem + TM_YL + ks * 8, bd, id, 1);
-            }
-            ptx::mma_commit(&ms.bar);
-        }
-        if (!wait_mma(ms, ph, a.dev_status)) break;
+        if (!chunk_intra(sm, ms, a, tc, nvalid, tmem, lane_base, ph)) break;
 
         // ---- -W tile from W^T (lane i = col, rows [16 qq, +16)); S_lo = S - S_hi (key dims [32 qq, +32))
-        {
-            float v[RPT];
-            ptx::tmem_ld16(tmem + lane_base + TM_WT + RPT * qq, v);
-#pragma unroll
-            for (int x = 0; x < RPT; ++x) st_hi(sm, SM_NW + swz(RPT * qq + x, col, T64_KB), -v[x]);
-            float s[32];
-            ptx::tmem_ld32(tmem + lane_base + TM_ST + 32 * qq, s);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) s[x] -= __uint_as_float(__float_as_uint(s[x]) & 0xFFFFE000u);
-            ptx::tmem_st32(tmem + lane_base + TM_SL + 32 * qq, s);
-        }
+        store_neg_w(sm, SM_NW, tmem + lane_base + TM_WT + RPT * qq, qq, col);
+        state_low(tmem + lane_base + TM_ST + 32 * qq, tmem + lane_base + TM_SL + 32 * qq);
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncthreads();
 
-        // ---- third product: U^T = U'^T - (S_hi + S_lo)^T W^T ; O^T = S^T (Q o e^G)^T (split)
-        if (tid == 0) {
-            ptx::tc_fence_after();
-            const uint32_t id = ptx::idesc_tf32(128, 64);
-#pragma unroll 1
-            for (int ks = 0; ks < 16; ++ks) {
-                const int kb = (ks >> 2) * T64_KB + (ks & 3) * 32;
-                ptx::mma_tf32_ts(tmem + TM_UT, tmem + TM_ST + ks * 8, dsc(sm, SM_NW + kb), id, 1);
-                ptx::mma_tf32_ts(tmem + TM_UT, tmem + TM_SL + ks * 8, dsc(sm, SM_NW + kb), id, 1);
-                ptx::mma_tf32_ts(tmem + TM_OT, tmem + TM_ST + ks * 8, dsc(sm, SM_QE + kb), id, ks > 0);
-                ptx::mma_tf32_ts(tmem + TM_OT, tmem + TM_SL + ks * 8, dsc(sm, SM_QE + kb), id, 1);
-                ptx::mma_tf32_ts(tmem + TM_OT, tmem + TM_ST + ks * 8, dsc(sm, SM_QEL + kb), id, 1);
-            }
-            ptx::mma_commit(&ms.bar);
-        }
+        if (issuer(tid) >= 0)
+            issue_third(sm, tmem, issuer(tid), SM_NW, SM_QE, SM_QEL, TM_UT, TM_ST, TM_SL, TM_OT, &ms.bar);
         if (!wait_mma(ms, ph, a.dev_status)) break;
 
         // the raw staging region is free from here: prefetch the next chunk's rows
@@ -709,98 +931,18 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
             if (tid < C && c0 + C + tid < seg1) bnext = __bfloat162float(bg[(size_t)(c0 + C + tid) * H + h]);
         }
 
-        // ---- S^T <- S^T Diag(e^{G_C}); U^T stays as the high part of U, its low part beside it
-        {
-            float v[32];
-            const uint32_t ta = tmem + lane_base + TM_ST + 32 * qq;
-            ptx::tmem_ld32(ta, v);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) v[x] *= ms.gamma[32 * qq + x];
-            ptx::tmem_st32(ta, v);
-            float u[RPT];
-            ptx::tmem_ld16(tmem + lane_base + TM_UT + RPT * qq, u);
-#pragma unroll
-            for (int x = 0; x < RPT; ++x) u[x] = tf32_lo(u[x]);
-            ptx::tmem_st16(tmem + lane_base + TM_UL + RPT * qq, u);
-        }
+        rescale_split(tmem + lane_base + TM_ST + 32 * qq, tmem + lane_base + TM_UT + RPT * qq,
+                      tmem + lane_base + TM_UL + RPT * qq, &ms.gamma[32 * qq]);
         ptx::tc_fence_before();
         __syncthreads();
 
-        // ---- fourth product: O^T += U^T P^T ; S^T += U^T (K o e^{G_C - G}) (both split)
-        if (tid == 0) {
-            ptx::tc_fence_after();
-            const uint32_t id64 = ptx::idesc_tf32(128, 64), id128 = ptx::idesc_tf32(128, 128);
-#pragma unroll 1
-            for (int ks = 0; ks < 8; ++ks) {
-                const int kb = (ks >> 2) * T64_KB + (ks & 3) * 32;
-                ptx::mma_tf32_ts(tmem + TM_OT, tmem + TM_UT + ks * 8, dsc(sm, SM_PH + kb), id64, 1);
-                ptx::mma_tf32_ts(tmem + TM_OT, tmem + TM_UL + ks * 8, dsc(sm, SM_PH + kb), id64, 1);
-                ptx::mma_tf32_ts(tmem + TM_OT, tmem + TM_UT + ks * 8, dsc(sm, SM_PL + kb), id64, 1);
-            }
-#pragma unroll 1
-            for (int ks = 0; ks < 8; ++ks) {
-                const int kb = (ks >> 2) * 128 * 128 + (ks & 3) * 32;
-                ptx::mma_tf32_ts(tmem + TM_ST, tmem + TM_UT + ks * 8, dsc(sm, SM_KD + kb), id128, 1);
-                ptx::mma_tf32_ts(tmem + TM_ST, tmem + TM_UL + ks * 8, dsc(sm, SM_KD + kb), id128, 1);
-                ptx::mma_tf32_ts(tmem + TM_ST, tmem + TM_UT + ks * 8, dsc(sm, SM_KDL + kb), id128, 1);
-            }
-            ptx::mma_commit(&ms.bar);
-        }
-        // the output gate of this chunk's rows (bf16 bits, two rows per register),
-        // loaded while the product runs
+        if (issuer(tid) >= 0)
+            issue_fourth(sm, tmem, issuer(tid), SM_PH, SM_PL, SM_KD, SM_KDL, TM_UT, TM_UL, TM_ST, TM_OT, &ms.bar);
         uint32_t gp[RPT / 2];
-#pragma unroll
-        for (int x = 0; x < RPT / 2; ++x) gp[x] = 0u;
-        if (gg != nullptr) {
-            const unsigned short* gb = reinterpret_cast<const unsigned short*>(gg);
-#pragma unroll
-            for (int x = 0; x < RPT; ++x) {
-                const int r = r0 + x;
-                const uint32_t bits = r < nvalid ? gb[((size_t)(c0 + r) * H + h) * D + col] : 0u;
-                gp[x >> 1] |= bits << (16 * (x & 1));
-            }
-        }
+        load_gate_bits(gp, a, c0, r0, nvalid, h, col);  // while the product runs
         if (!wait_mma(ms, ph, a.dev_status)) break;
 
-        // ---- outputs (lane j = col, rows [16 qq, +16)), optional gated RMSNorm
-        {
-            float o[RPT];
-            ptx::tmem_ld16(tmem + lane_base + TM_OT + RPT * qq, o);
-#pragma unroll
-            for (int x = 0; x < RPT; ++x) o[x] *= a.scale;
-            if (gg != nullptr) {
-                float t[RPT];
-#pragma unroll
-                for (int x = 0; x < RPT; ++x) t[x] = o[x] * o[x];
-                const float pr = transpose_reduce16(t, lane);
-                if (lane < 16) ms.epart[qq][lq][lane] = pr;
-                __syncthreads();
-                if (tid < C) {
-                    const int r = tid;
-                    const float tot = ms.epart[r >> 4][0][r & 15] + ms.epart[r >> 4][1][r & 15] +
-                                      ms.epart[r >> 4][2][r & 15] + ms.epart[r >> 4][3][r & 15];
-                    ms.rms[r] = rsqrtf(tot * (1.0f / D) + a.norm_eps);
-                }
-                __syncthreads();
-#pragma unroll
-                for (int x = 0; x < RPT; ++x) {
-                    const float gx = __uint_as_float((x & 1) ? (gp[x >> 1] & 0xFFFF0000u) : (gp[x >> 1] << 16));
-                    o[x] = o[x] * ms.rms[r0 + x] * nw * sigmoidf_(gx);
-                }
-            }
-            const size_t ob = ((size_t)(c0 + r0) * H + h) * D + col;
-            if (a.out_bf16) {
-                __nv_bfloat16* ou = static_cast<__nv_bfloat16*>(a.out);
-#pragma unroll
-                for (int x = 0; x < RPT; ++x)
-                    if (r0 + x < nvalid) ou[ob + (size_t)x * H * D] = __float2bfloat16_rn(o[x]);
-            } else {
-                float* ou = static_cast<float*>(a.out);
-#pragma unroll
-                for (int x = 0; x < RPT; ++x)
-                    if (r0 + x < nvalid) ou[ob + (size_t)x * H * D] = o[x];
-            }
-        }
+        write_outputs(ms, a, tmem + lane_base + TM_OT + RPT * qq, gp, c0, nvalid, h, nw);
         ptx::tc_fence_before();
         __syncthreads();
     }
@@ -820,7 +962,377 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
     if (warp == 0) ptx::tmem_dealloc(tmem, TM_COLS);
 }
 
+// ------------------------------------------------------------------------
+// Split prefill for few (sequence, head) chains (long prompts): one persistent
+// cooperative grid, one CTA per SM.  CTA b < NC runs chain b: only the
+// state-dependent products (third and fourth) and the outputs, chunk after
+// chunk.  The other CTAs are producers: they take (chain, chunk) tasks in
+// chunk-major order, run the state-independent part of the chunk
+// (chunk_intra) and publish its operands -- -W, Q o e^G (high, low), P (high,
+// low), K o e^{G_C - G} (high, low) in the shared-memory tile layout, U'^T and
+// e^{G_C} -- in a ring of SPLIT_RING slots per chain, with a release flag.
+// The chain waits for the flag, bulk-copies the tiles and returns the slot
+// (a consumed counter the producer waits on before reusing it).  Both sides
+// run the same instructions as the fused kernel on the same values, so the
+// results have the fused kernel's bits.  All waits are bounded.
+
+constexpr int SPLIT_RING = 8;
+// slot layout (bytes): third-product operands [0, 96 KiB), fourth-product
+// operands [96 KiB, 192 KiB), then U'^T and e^{G_C}
+constexpr uint32_t SL_NW = 0, SL_QE = 32768, SL_QEL = 65536;
+constexpr uint32_t SL_PH = 98304, SL_PL = 114688, SL_KD = 131072, SL_KDL = 163840;
+constexpr uint32_t SL_UT = 196608;   // U'^T: [quarter][lane][16] fp32
+constexpr uint32_t SL_GAM = 229376;  // e^{G_C}: [128] fp32
+constexpr uint32_t SLOT_BYTES = 230400;
+constexpr uint32_t SL_A_BYTES = 98304, SL_B_BYTES = 98304;
+// chain shared-memory tiles: the slot's first 192 KiB, same offsets
+// chain tensor memory: S^T, S_lo^T, U^T, U_lo^T, two O^T blocks (chunks alternate)
+constexpr uint32_t CT_ST = 0, CT_SL = 128, CT_UT = 256, CT_UL = 320, CT_OT0 = 384, CT_OT1 = 448;
+static_assert(SL_A_BYTES + SL_B_BYTES <= (uint32_t)SM_MISC, "chain tiles overlap the scalars");
+
+struct SplitArgs {
+    int* ready;            // [NC][SPLIT_RING]: chunk index + 1 published in the slot
+    int* consumed;         // [NC]: chunks the chain has finished reading
+    unsigned char* ring;   // [NC][SPLIT_RING][SLOT_BYTES]
+    int NC;                // chains = N * H
+};
+
+__device__ __forceinline__ unsigned char* slot_ptr(const SplitArgs& sp, int u, int c)
+{
+    return sp.ring + ((size_t)u * SPLIT_RING + (c % SPLIT_RING)) * SLOT_BYTES;
+}
+
+// a chain unit's sequence range; false when the unit is skipped (and flagged)
+__device__ __forceinline__ bool split_unit(const ChunkArgs& a, int u, int& slot, int& seg0, int& seg1, bool flag)
+{
+    const int seq = u / a.H;
+    slot = a.slots ? a.slots[seq] : seq;
+    if (slot < 0) return false;
+    if (slot >= a.num_slots) {
+        if (flag) flag_status(a.dev_status, KDA_DEV_BAD_SLOT);
+        return false;
+    }
+    seg0 = a.cu_seqlens[seq];
+    seg1 = a.cu_seqlens[seq + 1];
+    if (seg0 < 0 || seg1 < seg0 || seg1 > a.T) {
+        if (flag) flag_status(a.dev_status, KDA_DEV_BAD_SEQLENS);
+        return false;
+    }
+    return seg1 > seg0;
+}
+
+__device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, const RawMaps& maps,
+                               const SplitArgs& sp, uint32_t tmem)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lq = warp & 3, qq = tid >> 7, col = tid & (D - 1);
+    const uint32_t lane_base = (uint32_t)(lq * 32) << 16;
+    const int H = a.H, NC = sp.NC;
+    const int p = blockIdx.x - NC, NP = gridDim.x - NC;
+    int maxc = 0;
+    for (int u = 0; u < NC; u += H) {
+        int slot, s0, s1;
+        if (split_unit(a, u, slot, s0, s1, false)) maxc = max(maxc, (s1 - s0 + C - 1) / C);
+    }
+    uint32_t ph = 0, rph = 0;
+    int cur_h = -1;
+    ThreadConst tc;
+    const __nv_bfloat16* bg = static_cast<const __nv_bfloat16*>(a.b);
+    for (int t = p; t < maxc * NC && !ms.err; t += NP) {
+        const int c = t / NC, u = t % NC, h = u % H;
+        int slot, seg0, seg1;
+        if (!split_unit(a, u, slot, seg0, seg1, false)) continue;
+        const int c0 = seg0 + c * C;
+        if (c0 >= seg1) continue;
+        const int nvalid = min(C, seg1 - c0);
+        if (h != cur_h) {
+            tc = thread_const(a, h, col);
+            cur_h = h;
+        }
+        if (tid == 0) {
+            // the slot is free once the chain has read chunk c - SPLIT_RING
+            if (c >= SPLIT_RING && !ptx::wait_flag_ge(&sp.consumed[u], c - SPLIT_RING + 1)) {
+                ms.err = 1;
+                flag_status(a.dev_status, KDA_DEV_TIMEOUT);
+            } else {
+                stage_chunk(sm, maps, ms, c0, h);
+            }
+        }
+        if (tid < C) ms.beta[tid] = tid < nvalid ? sigmoidf_(__bfloat162float(bg[(size_t)(c0 + tid) * H + h])) : 0.0f;
+        __syncthreads();
+        if (ms.err) break;
+        if (!wait_rows(ms, rph, a.dev_status)) break;
+        if (c == 0) {
+            patch_halo(sm, a, slot, h);
+            __syncthreads();
+        }
+        if (!chunk_intra(sm, ms, a, tc, nvalid, tmem, lane_base, ph)) break;
+
+        // publish: tiles by bulk copies, U'^T and e^{G_C} by plain stores
+        unsigned char* dst = slot_ptr(sp, u, c);
+        store_neg_w(sm, SM_NW, tmem + lane_base + TM_WT + RPT * qq, qq, col);
+        {
+            float v[RPT];
+            ptx::tmem_ld16(tmem + lane_base + TM_UT + RPT * qq, v);
+            float4* ut = reinterpret_cast<float4*>(dst + SL_UT + ((size_t)qq * D + col) * RPT * 4);
+#pragma unroll
+            for (int j = 0; j < RPT / 4; ++j) ut[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            if (tid < D) reinterpret_cast<float*>(dst + SL_GAM)[tid] = ms.gamma[tid];
+        }
+        ptx::fence_proxy_async_smem();
+        __threadfence();
+        ptx::tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            ptx::bulk_s2g(dst + SL_NW, sm + SM_NW, 32768);
+            ptx::bulk_s2g(dst + SL_QE, sm + SM_QE, 32768);
+            ptx::bulk_s2g(dst + SL_QEL, sm + SM_QEL, 32768);
+            ptx::bulk_s2g(dst + SL_PH, sm + SM_PH, 16384);
+            ptx::bulk_s2g(dst + SL_PL, sm + SM_PL, 16384);
+            ptx::bulk_s2g(dst + SL_KD, sm + SM_KD, 32768);
+            ptx::bulk_s2g(dst + SL_KDL, sm + SM_KDL, 32768);
+            ptx::bulk_commit();
+            ptx::bulk_wait_all();
+            ptx::fence_proxy_async_global();
+            __threadfence();
+            ptx::st_release_gpu(&sp.ready[u * SPLIT_RING + c % SPLIT_RING], c + 1);
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+        ptx::tc_fence_after();
+    }
+    (void)rph;
+}
+
+// bulk-copy one half of a published slot into the chain's tiles
+__device__ __forceinline__ void chain_fetch(unsigned char* sm, uint64_t* bar, const unsigned char* src,
+                                            uint32_t off, uint32_t bytes)
+{
+    ptx::mbar_arrive_expect_tx(bar, bytes);
+    for (uint32_t o = 0; o < bytes; o += 32768)
+        ptx::bulk_g2s(sm + off + o, src + off + o, min(32768u, bytes - o), bar);
+}
+
+__device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, const SplitArgs& sp, uint32_t tmem,
+                            int u, int slot, int seg0, int seg1)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lq = warp & 3, qq = tid >> 7, col = tid & (D - 1);
+    const uint32_t lane_base = (uint32_t)(lq * 32) << 16;
+    const int H = a.H, K = a.K, h = u % H, r0 = RPT * qq;
+    const int nchunks = (seg1 - seg0 + C - 1) / C;
+    const float nw = a.norm_w ? a.norm_w[col] : 1.0f;
+    uint32_t ph = 0;
+    bool pend_a = false, pend_b = false;
+
+    {   // initial state -> TMEM S^T
+        const float* Sg = a.rec_state + ((size_t)slot * H + h) * D * D;
+        float v[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) v[x] = Sg[(size_t)(32 * qq + x) * D + col];
+        ptx::tmem_st32(tmem + lane_base + CT_ST + 32 * qq, v);
+    }
+
+    // Wait (one thread, bounded, acquire) for chunk c's slot.  The block barrier
+    // that follows every call orders the other threads' reads of the slot
+    // after that acquire.  Thread 128 issues no products, so it can wait while
+    // the issuers are busy.
+    auto acquire_by = [&](int c, int who) {
+        if (tid == who && !ptx::wait_flag_ge(&sp.ready[u * SPLIT_RING + c % SPLIT_RING], c + 1)) {
+            ms.err = 1;
+            flag_status(a.dev_status, KDA_DEV_TIMEOUT);
+        }
+    };
+    // U'^T (16 values of this thread) and e^{G_C} (tid < D) of chunk c, into registers
+    float up[RPT], gam = 0.0f;
+    auto load_ut = [&](int c) {
+        const unsigned char* src = slot_ptr(sp, u, c);
+        const float4* ut = reinterpret_cast<const float4*>(src + SL_UT + ((size_t)qq * D + col) * RPT * 4);
+#pragma unroll
+        for (int j = 0; j < RPT / 4; ++j) {
+            const float4 x = ut[j];
+            up[4 * j] = x.x; up[4 * j + 1] = x.y; up[4 * j + 2] = x.z; up[4 * j + 3] = x.w;
+        }
+        if (tid < D) gam = reinterpret_cast<const float*>(src + SL_GAM)[tid];
+    };
+
+    // The outputs of chunk c are written while the third product of chunk c + 1
+    // runs (O^T alternates between two TMEM column blocks), and chunk c + 1's
+    // slot is acquired and its U'^T loaded meanwhile too.
+    bool mma_pending = false;
+    acquire_by(0, 0);
+    __syncthreads();
+    if (!ms.err) {
+        if (tid == 0) {
+            ptx::fence_proxy_async_global();
+            chain_fetch(sm, &ms.rbar, slot_ptr(sp, u, 0), 0, SL_A_BYTES);
+            chain_fetch(sm, &ms.bbar, slot_ptr(sp, u, 0), SL_A_BYTES, SL_B_BYTES);
+        }
+        pend_a = pend_b = true;
+        load_ut(0);
+    }
+    uint32_t gp[RPT / 2];   // output gate of the chunk whose outputs are pending (bf16 bits, 2 per register)
+    int prev_c0 = 0, prev_nvalid = 0;
+    bool have_prev = false;
+    for (int c = 0; c < nchunks && !ms.err; ++c) {
+        const int c0 = seg0 + c * C;
+        const int nvalid = min(C, seg1 - c0);
+        const uint32_t c_ot = (c & 1) ? CT_OT1 : CT_OT0;
+        ptx::tmem_st16(tmem + lane_base + CT_UT + RPT * qq, up);
+        if (tid < D) ms.gamma[tid] = gam;
+        // this chunk's output gate rows: loaded now, packed after the third product
+        uint32_t graw[RPT];
+        {
+            const unsigned short* gb = static_cast<const unsigned short*>(a.g);
+#pragma unroll
+            for (int x = 0; x < RPT; ++x)
+                graw[x] = (gb != nullptr && r0 + x < nvalid) ? gb[((size_t)(c0 + r0 + x) * H + h) * D + col] : 0u;
+        }
+        state_low(tmem + lane_base + CT_ST + 32 * qq, tmem + lane_base + CT_SL + 32 * qq);
+        if (tid == 0 && !ptx::mbar_wait(&ms.rbar, c & 1)) {
+            ms.err = 1;
+            flag_status(a.dev_status, KDA_DEV_TIMEOUT);
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+        if (ms.err) break;
+        pend_a = false;
+        if (issuer(tid) >= 0) {
+            (void)ptx::mbar_try_wait(&ms.rbar, c & 1);  // completed: the tiles are visible to this issuer
+            issue_third(sm, tmem, issuer(tid), SL_NW, SL_QE, SL_QEL, CT_UT, CT_ST, CT_SL, c_ot, &ms.bar);
+        }
+        mma_pending = true;
+        // while the third product runs: chunk c + 1's slot, the previous chunk's outputs
+        if (c + 1 < nchunks) acquire_by(c + 1, 128);
+        if (have_prev) {
+            write_outputs(ms, a, tmem + lane_base + (c_ot ^ (CT_OT0 ^ CT_OT1)) + RPT * qq, gp, prev_c0,
+                          prev_nvalid, h, nw);
+            have_prev = false;
+        }
+        __syncthreads();
+        if (ms.err) break;
+        if (c + 1 < nchunks) load_ut(c + 1);
+        if (!wait_mma(ms, ph, a.dev_status)) break;
+        mma_pending = false;
+
+        // the third-product tiles are free: fetch chunk c + 1's
+        if (c + 1 < nchunks) {
+            if (tid == 0) {
+                ptx::fence_proxy_async_global();
+                chain_fetch(sm, &ms.rbar, slot_ptr(sp, u, c + 1), 0, SL_A_BYTES);
+            }
+            pend_a = true;
+        }
+
+        rescale_split(tmem + lane_base + CT_ST + 32 * qq, tmem + lane_base + CT_UT + RPT * qq,
+                      tmem + lane_base + CT_UL + RPT * qq, &ms.gamma[32 * qq]);
+        if (tid == 0 && !ptx::mbar_wait(&ms.bbar, c & 1)) {
+            ms.err = 1;
+            flag_status(a.dev_status, KDA_DEV_TIMEOUT);
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+        if (ms.err) break;
+        pend_b = false;
+        if (issuer(tid) >= 0) {
+            (void)ptx::mbar_try_wait(&ms.bbar, c & 1);
+            issue_fourth(sm, tmem, issuer(tid), SL_PH, SL_PL, SL_KD, SL_KDL, CT_UT, CT_UL, CT_ST, c_ot, &ms.bar);
+        }
+        mma_pending = true;
+#pragma unroll
+        for (int x = 0; x < RPT / 2; ++x) gp[x] = graw[2 * x] | (graw[2 * x + 1] << 16);
+        // chunk c's slot is read (both tile copies have landed, U'^T and e^{G_C}
+        // are in registers): hand it back (a thread that issues no products)
+        if (tid == 128) ptx::st_release_gpu(&sp.consumed[u], c + 1);
+        if (!wait_mma(ms, ph, a.dev_status)) break;
+        mma_pending = false;
+
+        // fetch chunk c + 1's fourth-product tiles
+        if (tid == 0 && c + 1 < nchunks) chain_fetch(sm, &ms.bbar, slot_ptr(sp, u, c + 1), SL_A_BYTES, SL_B_BYTES);
+        if (c + 1 < nchunks) pend_b = true;
+        have_prev = true;
+        prev_c0 = c0;
+        prev_nvalid = nvalid;
+    }
+    if (have_prev && !ms.err) {
+        const uint32_t c_ot = ((nchunks - 1) & 1) ? CT_OT1 : CT_OT0;
+        write_outputs(ms, a, tmem + lane_base + c_ot + RPT * qq, gp, prev_c0, prev_nvalid, h, nw);
+    }
+    if (tid == 0 && mma_pending) (void)ptx::mbar_wait(&ms.bar, ph);  // after a failed wait: let the products end
+
+    // nothing may land in shared memory after the CTA ends
+    if (tid == 0) {
+        if (pend_a) (void)ptx::mbar_wait(&ms.rbar, 0), (void)ptx::mbar_wait(&ms.rbar, 1);
+        if (pend_b) (void)ptx::mbar_wait(&ms.bbar, 0), (void)ptx::mbar_wait(&ms.bbar, 1);
+    }
+    if (!ms.err) {
+        float* Sg = a.rec_state + ((size_t)slot * H + h) * D * D;
+        float v[32];
+        ptx::tmem_ld32(tmem + lane_base + CT_ST + 32 * qq, v);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) Sg[(size_t)(32 * qq + x) * D + col] = v[x];
+        // the new conv state: the last K-1 raw rows of the sequence, older ones
+        // from the carried state (each thread walks its channels' rows in order,
+        // so a row is read before it is overwritten)
+        const int len = seg1 - seg0, conv_dim = 3 * H * D;
+        __nv_bfloat16* cs = static_cast<__nv_bfloat16*>(a.conv_state);
+        for (int c = tid; c < 3 * D; c += NT) {
+            const int tsel = c / D, cc = c % D;
+            const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(tsel == 0 ? a.q : (tsel == 1 ? a.k : a.v));
+            for (int r = 0; r < K - 1; ++r) {
+                const int sr = len - (K - 1) + r;  // row of the sequence, or < 0: carried row sr + K - 1
+                const size_t ch = (size_t)tsel * H * D + h * D + cc;
+                cs[((size_t)slot * (K - 1) + r) * conv_dim + ch] =
+                    sr >= 0 ? src[((size_t)(seg0 + sr) * H + h) * D + cc]
+                            : cs[((size_t)slot * (K - 1) + sr + K - 1) * conv_dim + ch];
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(NT, 1)
+    kda_chunk_split_kernel(const ChunkArgs a, const __grid_constant__ RawMaps maps, const SplitArgs sp)
+{
+    extern __shared__ __align__(1024) unsigned char sm[];
+    Misc& ms = *reinterpret_cast<Misc*>(sm + SM_MISC);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const bool chain = (int)blockIdx.x < sp.NC;
+    int slot = 0, seg0 = 0, seg1 = 0;
+    if (chain && !split_unit(a, blockIdx.x, slot, seg0, seg1, tid == 0)) return;
+    if ((ptx::smem_u32(sm) & 1023u) != 0) {
+        if (tid == 0) flag_status(a.dev_status, KDA_DEV_TIMEOUT);
+        return;
+    }
+    if (tid == 0) {
+        ptx::mbar_init(&ms.bar, ISSUERS);
+        ptx::mbar_init(&ms.rbar, 1);
+        ptx::mbar_init(&ms.bbar, 1);
+        ptx::fence_mbar_init();
+        ms.err = 0;
+    }
+    if (warp == 0) ptx::tmem_alloc(&ms.tmem, TM_COLS);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = ms.tmem;
+    if (chain) split_chain(sm, ms, a, sp, tmem, blockIdx.x, slot, seg0, seg1);
+    else split_producer(sm, ms, a, maps, sp, tmem);
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) ptx::tmem_dealloc(tmem, TM_COLS);
+}
+
 }  // namespace chk
+
+bool chunk_split_wanted(const kda_params* p, int N, int T)
+{
+    return chunk_supported(p) && (long long)N * p->num_heads <= 64 && T >= 1024;
+}
+
+size_t chunk_split_bytes(int N, int H)
+{
+    const size_t nc = (size_t)N * H;
+    const size_t flags = (nc * (chk::SPLIT_RING + 1) * sizeof(int) + 1023) & ~size_t(1023);
+    return flags + nc * chk::SPLIT_RING * chk::SLOT_BYTES;
+}
 
 bool chunk_supported(const kda_params* p)
 {
@@ -882,6 +1394,35 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
         if (!encode_rows(&maps.q, a.q, a.H, a.T, chk::RAWR) || !encode_rows(&maps.k, a.k, a.H, a.T, chk::RAWR) ||
             !encode_rows(&maps.v, a.v, a.H, a.T, chk::RAWR) || !encode_rows(&maps.f, a.f, a.H, a.T, chk::C))
             return cudaErrorInvalidValue;
+    }
+    if (a.split_ws) {
+        // split path: one cooperative grid of one CTA per SM, chains first
+        static bool split_attr[128];
+        int sms = 0, per_sm = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (dev >= 0 && dev < 128 && !split_attr[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(chk::kda_chunk_split_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, chk::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+            split_attr[dev] = true;
+        }
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chk::kda_chunk_split_kernel, chk::NT, chk::SMEM_BYTES);
+        const int nc = a.N * a.H;
+        if (per_sm >= 1 && 2 * nc <= sms) {
+            chk::SplitArgs sp;
+            const size_t flags = ((size_t)nc * (chk::SPLIT_RING + 1) * sizeof(int) + 1023) & ~size_t(1023);
+            sp.ready = reinterpret_cast<int*>(a.split_ws);
+            sp.consumed = sp.ready + (size_t)nc * chk::SPLIT_RING;
+            sp.ring = a.split_ws + flags;
+            sp.NC = nc;
+            cudaError_t e = cudaMemsetAsync(a.split_ws, 0, flags, st);
+            if (e != cudaSuccess) return e;
+            ChunkArgs aa = a;
+            void* args[] = {&aa, &maps, &sp};
+            return cudaLaunchCooperativeKernel((const void*)chk::kda_chunk_split_kernel, dim3(sms), dim3(chk::NT),
+                                               args, chk::SMEM_BYTES, st);
+        }
+        // too few SMs for producers beside the chains: the fused kernel below
     }
     if (a.schedule) chk::kda_chunk_schedule_kernel<<<1, 256, 0, st>>>(a.cu_seqlens, a.N, a.schedule);
     chk::kda_chunk_kernel<<<a.N * a.H, chk::NT, chk::SMEM_BYTES, st>>>(a, maps);

@@ -67,6 +67,7 @@ struct ChunkArgs {
     void* out;
     int32_t* dev_status;
     int32_t* schedule;  // workspace: sequence order, longest first
+    unsigned char* split_ws;  // workspace of the split (producer / chain) path, or null: fused kernel
 };
 
 cudaError_t launch_recurrent(int mode, int io_bf16, const RecArgs& a, int units, cudaStream_t st);
@@ -74,6 +75,18 @@ cudaError_t launch_commit(int io_bf16, const CommitArgs& a, cudaStream_t st);
 
 // Chunk kernel: returns cudaErrorNotSupported when the shape is not covered.
 bool chunk_supported(const kda_params* p);
+// Few long chains (N * H <= 64 and T >= 1024 rows): the split path, whose
+// workspace holds a ring of published chunk operands per chain.
+bool chunk_split_wanted(const kda_params* p, int N, int T);
+size_t chunk_split_bytes(int N, int H);  // flags + ring, 1 KiB aligned parts
+
+// kda_prefill_varlen with the split path allowed or not (the built-in
+// workspace of the allocation-free entry point is too small for it).
+int prefill_varlen_impl(const kda_params* p, const int32_t* cu_seqlens, int32_t N, int32_t T, const void* q,
+                        const void* k, const void* v, const void* gate, const void* beta, const void* out_gate,
+                        const int32_t* slots, void* conv_state, float* rec_state, void* out, void* workspace,
+                        size_t ws_bytes, int32_t* dev_status, cudaStream_t stream, bool allow_split);
+size_t prefill_workspace_bytes(const kda_params* p, int32_t N, int32_t T, bool allow_split);
 cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st);
 
 }  // namespace kda

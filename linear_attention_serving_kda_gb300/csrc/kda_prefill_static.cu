@@ -58,15 +58,16 @@ KDA_API int kda_prefill_varlen_static_ws(const kda_params* p, const int32_t* cu_
                                          const int32_t* slots, void* conv_state, float* rec_state,
                                          void* out, int32_t* dev_status, cudaStream_t stream)
 {
-    const size_t need = kda_prefill_workspace_bytes(p, N, T);
+    // the fused chunk path only: the split path's ring does not fit the built-in workspace
+    const size_t need = kda::prefill_workspace_bytes(p, N, T, false);
     if (need > kStaticWorkspaceBytes) return KDA_ERR_WORKSPACE;
     void* ws = nullptr;
     if (need > 0) {
         const int rc = scratch_address(&ws);
         if (rc != KDA_OK) return rc;
     }
-    return kda_prefill_varlen(p, cu_seqlens, N, T, q, k, v, gate, beta, out_gate, slots, conv_state,
-                              rec_state, out, ws, need > 0 ? kStaticWorkspaceBytes : 0, dev_status, stream);
+    return kda::prefill_varlen_impl(p, cu_seqlens, N, T, q, k, v, gate, beta, out_gate, slots, conv_state, rec_state,
+                                    out, ws, need > 0 ? kStaticWorkspaceBytes : 0, dev_status, stream, false);
 }
 
 }  // extern "C"

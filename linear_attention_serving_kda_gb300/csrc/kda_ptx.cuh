@@ -94,6 +94,42 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
         : "memory");
 }
 
+// 1-D bulk copy shared -> global in the current bulk group (16-byte aligned
+// addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until every committed bulk group has completed its writes
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// order this thread's async-proxy and generic-proxy accesses to global memory
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait (with back-off) until *p >= want; false when the limit runs out.
+__device__ __forceinline__ bool wait_flag_ge(const int* p, int want, uint32_t limit = (1u << 25))
+{
+    for (uint32_t i = 0; i < limit; ++i) {
+        if (ld_acquire_gpu(p) >= want) return true;
+        __nanosleep(64);
+    }
+    return false;
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;

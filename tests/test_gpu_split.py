@@ -1,0 +1,85 @@
+"""The split (producer / chain) prefill path for few long chains.
+
+With N * H <= 64 and T >= 1024 rows, kda_prefill_varlen runs one persistent
+grid in which producer CTAs compute each chunk's state-independent operands
+and chain CTAs apply them in order.  Both run the fused kernel's instructions
+on the same values, so the results must have the fused kernel's bits; the
+allocation-free entry point always takes the fused kernel, which gives the
+reference here.
+"""
+import numpy as np
+import pytest
+import torch
+
+from linear_attention_serving_kda_gb300 import kda as K
+from linear_attention_serving_kda_gb300 import workloads as W
+from linear_attention_serving_kda_gb300.runtime import DeviceCase
+from tests.parity import assert_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _fused(dc):
+    wl = dc.wl
+    return K.kda_prefill_varlen_static_ws(dc.params(), dc.cu_seqlens, wl.N, wl.T, dc.q, dc.k, dc.v, dc.f, dc.b,
+                                          dc.g, dc.slots, dc.conv_state, dc.rec_state, dc.out, dc.dev_status)
+
+
+def _both(wl, out_dtype=W.BF16, **kw):
+    p = DeviceCase(wl, out_dtype=out_dtype, **kw)
+    assert K.kda_prefill_workspace_bytes(p.params(), wl.N, wl.T) > 10 * 2**20, "not the split path"
+    K.check(p.prefill())
+    f = DeviceCase(wl, out_dtype=out_dtype, **kw)
+    K.check(_fused(f))
+    torch.cuda.synchronize()
+    assert int(p.dev_status.item()) == 0 and int(f.dev_status.item()) == 0
+    return p, f
+
+
+CASES = [
+    # lens, H, out_gate, init
+    ([1500, 700, 0, 1100], 8, True, "random"),
+    ([4096], 16, False, "zero"),
+    ([1, 63, 1025, 130], 4, True, "random"),
+]
+
+
+@pytest.mark.parametrize("lens,H,og,init", CASES)
+def test_split_has_fused_bits(cuda_lib, lens, H, og, init):
+    wl = W.make_workload("split", 800 + sum(lens) + H, lens, H=H, d=128, K=4, io_dtype=W.BF16,
+                         gate_mode=W.SAFE, lower_bound=-5.0, out_gate=og, init_state=init)
+    p, f = _both(wl)
+    assert torch.equal(p.out[:wl.T], f.out[:wl.T])
+    assert torch.equal(p.rec_state, f.rec_state)
+    assert torch.equal(p.conv_state, f.conv_state)
+
+
+def test_split_against_oracle(cuda_lib, oracle_mod):
+    """Every (sequence, head) of a small split-path case against the oracle."""
+    lens, H = [1100, 200, 77], 2
+    wl = W.make_workload("split_o", 811, lens, H=H, d=128, K=3, io_dtype=W.BF16, gate_mode=W.SAFE,
+                         lower_bound=-5.0, out_gate=True, init_state="random")
+    dc = DeviceCase(wl, out_dtype=W.F32)
+    assert K.kda_prefill_workspace_bytes(dc.params(), wl.N, wl.T) > 10 * 2**20
+    K.check(dc.prefill())
+    torch.cuda.synchronize()
+    assert int(dc.dev_status.item()) == 0
+    ref = oracle_mod.forward(wl)
+    assert_close(to_np(dc.out[:wl.T]), ref["out"], "out")
+    assert_close(to_np(dc.rec_state), ref["rec_state"], "rec_state")
+    assert np.array_equal(to_np(dc.conv_state), ref["conv_state"].astype(np.float32))
+
+
+def test_split_slots(cuda_lib):
+    """A state pool with a skipped sequence: split and fused agree bit for bit,
+    and the skipped sequence's slot and rows are untouched."""
+    lens = [900, 500, 800]
+    wl = W.make_workload("split_s", 812, lens, H=4, d=128, K=4, io_dtype=W.BF16, gate_mode=W.SAFE,
+                         lower_bound=-5.0, out_gate=True, init_state="random")
+    slots = [2, -1, 0]
+    p, f = _both(wl, num_slots=4, slots=slots)
+    rs0 = DeviceCase(wl, num_slots=4, slots=slots).rec_state
+    assert torch.equal(p.rec_state, f.rec_state) and torch.equal(p.conv_state, f.conv_state)
+    assert torch.equal(p.rec_state[1], rs0[1]) and torch.equal(p.rec_state[3], rs0[3])
+    t0, t1 = 900, 1400
+    assert torch.equal(p.out[:t0], f.out[:t0]) and torch.equal(p.out[t1:wl.T], f.out[t1:wl.T])
