@@ -241,22 +241,32 @@ def leg_verify(kda, reps, stream):
     sets = [DeviceCase(wl, out_dtype=W.BF16) for _ in range(n_sets)]
     for s in sets:
         s.alloc_log()
-    tv, tc = [], []
+    logs2 = [torch.empty_like(s.log) for s in sets]
+    tv, tc, tcv = [], [], []
     for r in range(reps + 1):
         s = sets[r % n_sets]
         s.reset_states()
         torch.cuda.synchronize()
         dv = time_steps(lambda i: kda.check(s.verify(stream=stream)), 1, stream)[0]
         dcm = time_steps(lambda i: kda.check(s.commit(stream=stream)), 1, stream)[0]
+        # the next window in one call: commit this window's accepted rows, verify new rows
+        p = s.params()
+        lg2 = logs2[r % n_sets]
+        dcv = time_steps(lambda i: kda.check(kda.kda_commit_verify(
+            p, wl.N, wl.W, s.accepted, s.log, s.q, s.k, s.v, s.f, s.b, s.g, s.slots, s.conv_state,
+            s.rec_state, lg2, s.out, s.dev_status, stream)), 1, stream)[0]
         if r:
             tv += dv
             tc += dcm
-    mv, mc = statistics.median(tv), statistics.median(tc)
+            tcv += dcv
+    mv, mc, mcv = statistics.median(tv), statistics.median(tc), statistics.median(tcv)
     acc = int(wl.arrays["accepted"].sum())
     rows = wl.N * wl.W
     return {"workload": wl.name, "rows": rows, "accepted_rows": acc, "verify_ms": mv, "commit_ms": mc,
+            "commit_verify_ms": mcv,
             "rows_verified_per_s": rows / (mv * 1e-3),
-            "committed_tokens_per_s": acc / ((mv + mc) * 1e-3)}
+            "committed_tokens_per_s": acc / ((mv + mc) * 1e-3),
+            "committed_tokens_per_s_fused": acc / (mcv * 1e-3)}
 
 
 def e2e_decode(kda, steps, warmup, stream):

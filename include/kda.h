@@ -204,6 +204,33 @@ KDA_API int kda_commit(const kda_params* p, int32_t B, int32_t W, const int32_t*
                        const int32_t* slots, const void* log, void* conv_state,
                        float* rec_state, int32_t* dev_status, cudaStream_t stream);
 
+/*
+ * Commit and verify in one call: for each sequence b, first replay rows
+ * 0 .. accepted[b]-1 of the PREVIOUS window from log_prev onto its states and
+ * store the committed states (exactly what kda_commit does), then verify the
+ * NEW window's W draft rows on the committed states (exactly what
+ * kda_verify_window does), writing `out` and the new window's `log`.  The
+ * results carry the bits of kda_commit followed by kda_verify_window; the
+ * state is read once instead of twice (TensorFold #850, Oct 15 comment: the
+ * next window first replays the kept rows of the last one).
+ *   accepted: device int32 [B], rows of the previous window to keep, each in
+ *             [0, W]; a sequence with an out-of-range count is flagged
+ *             (KDA_DEV_BAD_ACCEPTED) and skipped entirely (no commit, no
+ *             outputs, no log rows).
+ *   log_prev: the previous window's log (kda_verify_window or
+ *             kda_commit_verify with the same p, B, W and slots); read only.
+ *   log:      this window's log, kda_verify_log_bytes(p, B, W) bytes; may be
+ *             the same buffer as log_prev (each sequence's rows are read
+ *             before they are rewritten).
+ * Other arguments as in kda_verify_window; conv_state and rec_state are
+ * updated in place by the commit.
+ */
+KDA_API int kda_commit_verify(const kda_params* p, int32_t B, int32_t W, const int32_t* accepted,
+                              const void* log_prev, const void* q, const void* k, const void* v,
+                              const void* gate, const void* beta, const void* out_gate,
+                              const int32_t* slots, void* conv_state, float* rec_state, void* log,
+                              void* out, int32_t* dev_status, cudaStream_t stream);
+
 /* Human-readable name of a return code. */
 KDA_API const char* kda_status_string(int status);
 

@@ -279,6 +279,42 @@ KDA_API int kda_verify_window(const kda_params* p, int32_t B, int32_t W, const v
                ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
+KDA_API int kda_commit_verify(const kda_params* p, int32_t B, int32_t W, const int32_t* accepted,
+                              const void* log_prev, const void* q, const void* k, const void* v,
+                              const void* gate, const void* beta, const void* out_gate,
+                              const int32_t* slots, void* conv_state, float* rec_state, void* log,
+                              void* out, int32_t* dev_status, cudaStream_t stream)
+{
+    int rc = check_params(p);
+    if (rc != KDA_OK) return rc;
+    if (B < 0 || W < 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (B == 0 || W == 0) return KDA_OK;
+    if ((rc = check_ptrs({accepted, log_prev, q, k, v, gate, beta, conv_state, rec_state, log, out})) != KDA_OK)
+        return rc;
+    if ((rc = check_opt(out_gate)) != KDA_OK || (rc = check_opt(slots)) != KDA_OK) return rc;
+    if ((rc = check_device()) != KDA_OK) return rc;
+    RecArgs a;
+    fill_common(a, p);
+    a.N = B;
+    a.W = W;
+    a.T = B * W;
+    a.q = q; a.k = k; a.v = v; a.f = gate; a.b = beta; a.g = out_gate;
+    a.slots = slots;
+    a.conv_state = conv_state;
+    a.rec_state = rec_state;
+    a.out = out;
+    a.log_f = static_cast<float*>(log);
+    a.log_raw = static_cast<char*>(log) + log_float_bytes(p, B, W);
+    a.accepted = accepted;
+    a.prev_log_f = static_cast<const float*>(log_prev);
+    a.prev_log_raw = static_cast<const char*>(log_prev) + log_float_bytes(p, B, W);
+    a.dev_status = dev_status;
+    return launch_recurrent(REC_COMMIT_VERIFY, p->io_dtype == KDA_DTYPE_BF16, a, B * p->num_heads, stream) ==
+                   cudaSuccess
+               ? KDA_OK
+               : KDA_ERR_LAUNCH;
+}
+
 KDA_API int kda_commit(const kda_params* p, int32_t B, int32_t W, const int32_t* accepted,
                        const int32_t* slots, const void* log, void* conv_state,
                        float* rec_state, int32_t* dev_status, cudaStream_t stream)

@@ -8,7 +8,9 @@
 
 namespace kda {
 
-enum RecMode { REC_PREFILL = 0, REC_DECODE = 1, REC_VERIFY = 2 };
+// REC_COMMIT_VERIFY: replay the accepted rows of the previous window's log,
+// store the committed states, then verify the new window on them.
+enum RecMode { REC_PREFILL = 0, REC_DECODE = 1, REC_VERIFY = 2, REC_COMMIT_VERIFY = 3 };
 
 // Arguments of the row-recurrent kernel (decode, verify window, and the
 // serial prefill used for the shapes the chunk kernel does not cover).
@@ -33,6 +35,10 @@ struct RecArgs {
     float* log_f;
     void* log_raw;
     int32_t* dev_status;
+    // REC_COMMIT_VERIFY: rows of the previous window to commit, and its log
+    const int32_t* accepted;
+    const float* prev_log_f;
+    const void* prev_log_raw;
 };
 
 struct CommitArgs {

@@ -274,12 +274,37 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_recurrent_kernel(const Rec
         row0 = seq * a.W;
         L = a.W;
     }
+    int acc = 0;  // REC_COMMIT_VERIFY: rows of the previous window to commit first
+    if (MODE == REC_COMMIT_VERIFY) {
+        acc = a.accepted[seq];
+        if (acc < 0 || acc > a.W) {
+            if (tid == 0 && h == 0) flag_status(a.dev_status, KDA_DEV_BAD_ACCEPTED);
+            return;
+        }
+    }
 
     // State tile first: its HBM stream overlaps the row preparation below.
     float* Sg = a.rec_state + ((size_t)slot * H + h) * D * D;
     const int r0 = warp * RPW, c0 = lane * CPT;
     float s[RPW][CPT];
     load_tile<D>(Sg, r0, c0, s);
+    if (MODE == REC_COMMIT_VERIFY && acc > 0) {
+        // commit: the same replay expression as kda_commit_kernel, so the
+        // committed state has the bits of `acc` serial decodes
+        for (int t = 0; t < acc; ++t) {
+            const float* lg = a.prev_log_f + (((size_t)seq * a.W + t) * H + h) * (3 * D);
+            float uc[CPT];
+#pragma unroll
+            for (int cc = 0; cc < CPT; ++cc) uc[cc] = lg[2 * D + c0 + cc];
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr) {
+                const float ai = lg[r0 + rr], ki = lg[D + r0 + rr];
+#pragma unroll
+                for (int cc = 0; cc < CPT; ++cc) s[rr][cc] = __fmaf_rn(ki, uc[cc], __fmul_rn(ai, s[rr][cc]));
+            }
+        }
+        store_tile<D>(Sg, r0, c0, s);
+    }
 
     const IO* q = static_cast<const IO*>(a.q);
     const IO* k = static_cast<const IO*>(a.k);
@@ -292,8 +317,23 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_recurrent_kernel(const Rec
     for (int c = tid; c < 3 * D; c += REC_THREADS) {
         const int ch = conv_channel<D>(c, h, H);
         for (int j = 0; j < K; ++j) sm.cw[c][j] = a.conv_w[(size_t)ch * K + j];
-        for (int r = 0; r < K - 1; ++r)
-            sm.win[ring(r - (K - 1))][c] = ldv(cs + ((size_t)slot * (K - 1) + r) * conv_dim + ch);
+        if (MODE == REC_COMMIT_VERIFY && acc > 0) {
+            // committed conv state: the last K-1 rows of [old state; accepted raw rows]
+            const IO* praw = static_cast<const IO*>(a.prev_log_raw);
+            float old[3], nw[3];
+            for (int r = 0; r < K - 1; ++r) old[r] = ldv(cs + ((size_t)slot * (K - 1) + r) * conv_dim + ch);
+            for (int r = 0; r < K - 1; ++r) {
+                const int src = acc - (K - 1) + r;  // window row, or < 0: old state row src + K - 1
+                nw[r] = src >= 0 ? ldv(praw + ((size_t)seq * a.W + src) * conv_dim + ch) : old[src + K - 1];
+            }
+            for (int r = 0; r < K - 1; ++r) {
+                stv(cs + ((size_t)slot * (K - 1) + r) * conv_dim + ch, nw[r]);
+                sm.win[ring(r - (K - 1))][c] = nw[r];
+            }
+        } else {
+            for (int r = 0; r < K - 1; ++r)
+                sm.win[ring(r - (K - 1))][c] = ldv(cs + ((size_t)slot * (K - 1) + r) * conv_dim + ch);
+        }
     }
     for (int i = tid; i < D; i += REC_THREADS) sm.dtb[i] = a.dt_bias[(size_t)h * D + i];
     RowConst rc{a.gate_mode, a.lb, expf(a.A_log[h]), a.l2_eps, a.norm_eps, a.scale, a.norm_w};
@@ -318,7 +358,7 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_recurrent_kernel(const Rec
         const float o = row_step<D>(sm, s, t, K, rc, bval, gval, g != nullptr);
         if (tid < D) store_out(a.out, rh * D + tid, o, a.out_bf16);
 
-        if (MODE == REC_VERIFY) {
+        if (MODE == REC_VERIFY || MODE == REC_COMMIT_VERIFY) {
             float* lg = a.log_f + (((size_t)seq * a.W + t) * H + h) * (3 * D);
             if (tid < D) {
                 lg[tid] = sm.alpha[tid];
@@ -331,7 +371,7 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_recurrent_kernel(const Rec
         __syncthreads();
     }
 
-    if (MODE != REC_VERIFY) {
+    if (MODE == REC_PREFILL || MODE == REC_DECODE) {
         store_tile<D>(Sg, r0, c0, s);
         // new conv state: the last K-1 raw rows (older ones from the old state)
         for (int c = tid; c < 3 * D; c += REC_THREADS) {
@@ -598,7 +638,8 @@ static cudaError_t launch_rec_d(int mode, const RecArgs& a, int units, cudaStrea
     dim3 grid(units), block(REC_THREADS);
     if (mode == REC_PREFILL) kda_recurrent_kernel<D, IO, REC_PREFILL><<<grid, block, 0, st>>>(a);
     else if (mode == REC_DECODE) kda_recurrent_kernel<D, IO, REC_DECODE><<<grid, block, 0, st>>>(a);
-    else kda_recurrent_kernel<D, IO, REC_VERIFY><<<grid, block, 0, st>>>(a);
+    else if (mode == REC_VERIFY) kda_recurrent_kernel<D, IO, REC_VERIFY><<<grid, block, 0, st>>>(a);
+    else kda_recurrent_kernel<D, IO, REC_COMMIT_VERIFY><<<grid, block, 0, st>>>(a);
     return cudaGetLastError();
 }
 

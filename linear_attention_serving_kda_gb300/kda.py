@@ -59,6 +59,7 @@ _SIG = {
     "kda_verify_window": (ctypes.c_int, [ctypes.POINTER(kda_params), _I32, _I32, _VP, _VP, _VP, _VP, _VP,
                                          _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "kda_verify_log_bytes": (ctypes.c_size_t, [ctypes.POINTER(kda_params), _I32, _I32]),
+    "kda_commit_verify": (ctypes.c_int, [ctypes.POINTER(kda_params), _I32, _I32] + [_VP] * 14 + [_VP]),
     "kda_commit": (ctypes.c_int, [ctypes.POINTER(kda_params), _I32, _I32, _VP, _VP, _VP, _VP, _VP,
                                   _VP, _VP]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -203,6 +204,15 @@ def kda_commit(params: Params, B: int, W: int, accepted, slots, log, conv_state,
     return load().kda_commit(
         ctypes.byref(params.c_struct()), B, W, _ptr(accepted), _ptr(slots), _ptr(log),
         _ptr(conv_state), _ptr(rec_state), _ptr(dev_status), _stream(stream))
+
+
+def kda_commit_verify(params: Params, B: int, W: int, accepted, log_prev, q, k, v, gate, beta, out_gate,
+                      slots, conv_state, rec_state, log, out, dev_status=None, stream=None) -> int:
+    """Commit the previous window's accepted rows, then verify a new window."""
+    return load().kda_commit_verify(
+        ctypes.byref(params.c_struct()), B, W, _ptr(accepted), _ptr(log_prev), _ptr(q), _ptr(k), _ptr(v),
+        _ptr(gate), _ptr(beta), _ptr(out_gate), _ptr(slots), _ptr(conv_state), _ptr(rec_state), _ptr(log),
+        _ptr(out), _ptr(dev_status), _stream(stream))
 
 
 class Prepared:

@@ -27,7 +27,7 @@ def _declared():
 
 def test_exports_every_declared_symbol(lib):
     names = _declared()
-    assert {"kda_prefill_varlen", "kda_decode", "kda_verify_window", "kda_commit"} <= set(names)
+    assert {"kda_prefill_varlen", "kda_decode", "kda_verify_window", "kda_commit", "kda_commit_verify"} <= set(names)
     raw = ctypes.CDLL(kbuild.LIB)
     for n in names:
         assert hasattr(raw, n), n
@@ -93,6 +93,14 @@ def test_pointer_checks(lib):
     assert kda.kda_verify_window(p, 2, 4, *([FAKE] * 5), None, None, FAKE, FAKE, None, FAKE, None, 0) \
         == kda.KDA_ERR_INVALID_ARGUMENT  # missing log
     assert kda.kda_commit(p, 2, 4, None, None, FAKE, FAKE, FAKE, None, 0) == kda.KDA_ERR_INVALID_ARGUMENT
+    # commit + verify: missing accepted counts, missing previous log, misaligned new log
+    cv = dict(accepted=FAKE, log_prev=FAKE, q=FAKE, k=FAKE, v=FAKE, gate=FAKE, beta=FAKE, out_gate=None,
+              slots=None, conv_state=FAKE, rec_state=FAKE, log=FAKE, out=FAKE)
+    for over in (dict(accepted=None), dict(log_prev=None), dict(log=FAKE + 4), dict(out_gate=FAKE + 8)):
+        args = {**cv, **over}
+        assert kda.kda_commit_verify(p, 2, 4, *args.values(), None, 0) == kda.KDA_ERR_INVALID_ARGUMENT, over
+    assert kda.kda_commit_verify(p, 0, 4, *([None] * 13), None, 0) == kda.KDA_OK  # empty batch: no-op
+    assert kda.kda_commit_verify(p, -1, 4, *cv.values(), None, 0) == kda.KDA_ERR_INVALID_ARGUMENT
 
 
 def test_sizes(lib):

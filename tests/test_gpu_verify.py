@@ -4,6 +4,7 @@ import numpy as np
 import pytest
 import torch
 
+from linear_attention_serving_kda_gb300 import kda as K
 from linear_attention_serving_kda_gb300 import workloads as W
 from linear_attention_serving_kda_gb300.runtime import DeviceCase
 from tests.parity import assert_bf16_within_one_ulp, assert_close, gather_rows, to_np
@@ -90,3 +91,81 @@ def test_commit_rejects_bad_accepted(cuda_lib):
     torch.cuda.synchronize()
     assert int(dc.dev_status.item()) & cuda_lib.KDA_DEV_BAD_ACCEPTED
     assert torch.equal(dc.rec_state, rs0)
+
+
+def _commit_verify(dc, accepted, log_prev, log_new):
+    wl = dc.wl
+    return K.kda_commit_verify(dc.params(), wl.N, wl.W, accepted, log_prev, dc.q, dc.k, dc.v, dc.f, dc.b, dc.g,
+                               dc.slots, dc.conv_state, dc.rec_state, log_new, dc.out, dc.dev_status)
+
+
+def _load_rows(dc, wl):
+    for nm in ("q", "k", "v", "f", "b", "g"):
+        t = getattr(dc, nm)
+        if t is not None:
+            t.copy_(wl.to_torch(nm, "cuda"))
+
+
+@pytest.mark.parametrize("d,io,gate,alias", [(128, W.BF16, W.SOFTPLUS, False), (128, W.BF16, W.SAFE, True),
+                                             (64, W.F32, W.SAFE, False), (32, W.BF16, W.SOFTPLUS, True)])
+def test_commit_verify_equals_separate_calls(cuda_lib, d, io, gate, alias):
+    """kda_commit_verify = kda_commit then kda_verify_window, bit for bit
+    (outputs, both states, the new log), also with the new log written over
+    the previous one."""
+    B, Wn, H = 5, 8, 3
+    kw = dict(H=H, d=d, K=4, io_dtype=io, gate_mode=gate, lower_bound=-5.0, out_gate=True,
+              init_state="random", W=Wn, accepted=True)
+    win1 = W.make_workload("cv1", 901 + d, [Wn] * B, **kw)
+    win2 = W.make_workload("cv2", 902 + d, [Wn] * B, **kw)
+    acc = torch.tensor([0, 3, 8, 1, 5], dtype=torch.int32, device="cuda")
+    sep = DeviceCase(win1, out_dtype=W.F32, num_slots=6, slots=[4, 0, 2, 5, 1])
+    fus = DeviceCase(win1, out_dtype=W.F32, num_slots=6, slots=[4, 0, 2, 5, 1])
+    for dc in (sep, fus):
+        dc.alloc_log()
+        K.check(dc.verify())
+    # separate calls: commit window 1, verify window 2
+    K.check(sep.commit(accepted=acc))
+    _load_rows(sep, win2)
+    K.check(sep.verify())
+    # one call
+    _load_rows(fus, win2)
+    log2 = fus.log if alias else torch.empty_like(fus.log)
+    K.check(_commit_verify(fus, acc, fus.log, log2))
+    torch.cuda.synchronize()
+    assert int(sep.dev_status.item()) == 0 and int(fus.dev_status.item()) == 0
+    assert torch.equal(fus.out[:B * Wn], sep.out[:B * Wn])
+    assert torch.equal(fus.rec_state, sep.rec_state)
+    assert torch.equal(fus.conv_state, sep.conv_state)
+    assert torch.equal(log2, sep.log)
+
+
+def test_commit_verify_bad_accepted(cuda_lib):
+    """An out-of-range accepted count is flagged and its sequence skipped; the
+    other sequences match the separate calls."""
+    B, Wn, H, d = 3, 4, 2, 64
+    kw = dict(H=H, d=d, K=4, io_dtype=W.F32, gate_mode=W.SAFE, lower_bound=-5.0, init_state="random", W=Wn,
+              accepted=True)
+    win1 = W.make_workload("cvb1", 911, [Wn] * B, **kw)
+    win2 = W.make_workload("cvb2", 912, [Wn] * B, **kw)
+    fus = DeviceCase(win1, out_dtype=W.F32)
+    sep = DeviceCase(win1, out_dtype=W.F32)
+    for dc in (fus, sep):
+        dc.alloc_log()
+        K.check(dc.verify())
+    rs0, cs0 = fus.rec_state.clone(), fus.conv_state.clone()
+    bad = torch.tensor([2, Wn + 1, 1], dtype=torch.int32, device="cuda")
+    good = torch.tensor([2, 0, 1], dtype=torch.int32, device="cuda")
+    _load_rows(fus, win2)
+    fus.out.fill_(float("nan"))
+    log2 = torch.empty_like(fus.log)
+    K.check(_commit_verify(fus, bad, fus.log, log2))
+    K.check(sep.commit(accepted=good))
+    _load_rows(sep, win2)
+    K.check(sep.verify())
+    torch.cuda.synchronize()
+    assert int(fus.dev_status.item()) & K.KDA_DEV_BAD_ACCEPTED
+    assert torch.equal(fus.rec_state[1], rs0[1]) and torch.equal(fus.conv_state[1], cs0[1])
+    assert torch.all(torch.isnan(fus.out[Wn:2 * Wn]))
+    for b in (0, 2):
+        assert torch.equal(fus.rec_state[b], sep.rec_state[b])
+        assert torch.equal(fus.out[b * Wn:(b + 1) * Wn], sep.out[b * Wn:(b + 1) * Wn])
