@@ -442,13 +442,22 @@ __device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const C
             st_hi(sm, SM_AX + 8192 + o, kv[r] * e);
             st_split(sm, SM_AX + 16384 + o, SM_AX + o, qv[r] * e);
             st_split(sm, SM_B1H + swz(rr, col, B1_KB), SM_B1L + swz(rr, col, B1_KB), kv[r] * ie);
-            st_split(sm, SM_B1H + swz(xrow + rr, col, B1_KB), SM_B1L + swz(xrow + rr, col, B1_KB),
-                    kv[r] * __expf(Gx - G[r]));
             // e^{G_r}: a product of two in-range factors in the first half; direct in the
             // second (e^{G_48} may underflow).  e^{G_C - G_r}: direct in the first half
-            // (e^{G_C - G_16} may underflow); a product in the second.
-            const float eG = half == 0 ? e * eGm : __expf(G[r]);
-            const float edec = half == 0 ? __expf(GC - G[r]) : ie * cGC;
+            // (e^{G_C - G_16} may underflow); a product in the second.  The cross
+            // factor is e^{G_48 - G_r} in the first half and e^{G_48 - G_r} = ie in
+            // the second.  (half is uniform over a warp: one side runs.)
+            float cross, eG, edec;
+            if (half == 0) {
+                cross = __expf(Gx - G[r]);
+                eG = e * eGm;
+                edec = __expf(GC - G[r]);
+            } else {
+                cross = ie;
+                eG = __expf(G[r]);
+                edec = ie * cGC;
+            }
+            st_split(sm, SM_B1H + swz(xrow + rr, col, B1_KB), SM_B1L + swz(xrow + rr, col, B1_KB), kv[r] * cross);
             qe[r] = qv[r] * eG;
             kdx[r] = kv[r] * edec;
             const float be = ms.beta[rr];
