@@ -18,10 +18,10 @@
 //
 // Decode at dk = dv = 128 -- the memory-bound serving step -- uses a
 // persistent kernel: one CTA per SM, a producer warp that streams each unit's
-// 64 KiB state, rows, conv history and parameters into a double-buffered
-// shared-memory stage with bulk async copies, and 8 consumer warps that run
-// row_step on the previous stage meanwhile and write the state back with
-// streaming stores.
+// 64 KiB state, rows, conv history and parameters into a ring of shared-memory
+// stages with bulk async copies, and 8 row warps that run row_step on a
+// loaded stage meanwhile and leave the new state in the stage, from where the
+// producer stores it back with one bulk copy before reusing the stage.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_ptx.cuh"
@@ -131,22 +131,44 @@ template <int D> __device__ __forceinline__ void store_tile(float* Sg, int r0, i
 // itself (identical operands in an identical order, so identical bits), which
 // leaves three barriers per row.
 template <int D>
+__device__ __forceinline__ float row_rest(RowSmem<D>& sm, float (&s)[RecShape<D>::RPW][RecShape<D>::CPT],
+                                          const RowConst& rc, float bval, float gval, bool has_g);
+
+// The row's first step: conv window + SiLU into sm.act, and the decay of each
+// key dim into sm.alpha.  win(c, j) is raw value j (oldest first, j = K-1 the
+// current row) of local channel c, fr(i) the gate of key dim i.
+template <int D, typename Win, typename Fr>
+__device__ __forceinline__ void row_conv(RowSmem<D>& sm, int K, const RowConst& rc, Win win, Fr fr)
+{
+    const int tid = threadIdx.x;
+    for (int c = tid; c < 3 * D; c += REC_THREADS) {
+        float acc = 0.0f;
+        for (int j = 0; j < K; ++j) acc = __fmaf_rn(sm.cw[c][j], win(c, j), acc);
+        sm.act[c] = siluf_(acc);
+    }
+    for (int i = tid; i < D; i += REC_THREADS)
+        sm.alpha[i] = __expf(log_alpha(rc.gate_mode, rc.lb, rc.ea, fr(i), sm.dtb[i]));
+    row_sync();
+}
+
+template <int D>
 __device__ __forceinline__ float row_step(RowSmem<D>& sm, float (&s)[RecShape<D>::RPW][RecShape<D>::CPT],
                                           int t, int K, const RowConst& rc, float bval, float gval, bool has_g)
+{
+    row_conv<D>(sm, K, rc, [&](int c, int j) { return sm.win[ring(t - K + 1 + j)][c]; },
+                [&](int i) { return sm.fr[i]; });
+    return row_rest<D>(sm, s, rc, bval, gval, has_g);
+}
+
+// The rest of the row (after row_conv): norms, beta, the delta rule on S and
+// the output of column tid.
+template <int D>
+__device__ __forceinline__ float row_rest(RowSmem<D>& sm, float (&s)[RecShape<D>::RPW][RecShape<D>::CPT],
+                                          const RowConst& rc, float bval, float gval, bool has_g)
 {
     constexpr int RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r0 = warp * RPW, c0 = lane * CPT;
-
-    // conv window + SiLU, and the decay of each key dim
-    for (int c = tid; c < 3 * D; c += REC_THREADS) {
-        float acc = 0.0f;
-        for (int j = 0; j < K; ++j) acc = __fmaf_rn(sm.cw[c][j], sm.win[ring(t - K + 1 + j)][c], acc);
-        sm.act[c] = siluf_(acc);
-    }
-    for (int i = tid; i < D; i += REC_THREADS)
-        sm.alpha[i] = __expf(log_alpha(rc.gate_mode, rc.lb, rc.ea, sm.fr[i], sm.dtb[i]));
-    row_sync();
 
     // q / k inverse L2 norms and beta (every warp; a butterfly sum leaves the
     // same bits in every lane)
@@ -400,7 +422,8 @@ template <typename IO> struct DecStage {
     IO hist[3][3][DEC_D];          // conv history [row][q|k|v][channel]
     float bval;                    // beta logit
     int slot;                      // state slot, or -1: skip the unit
-    int pad[2];
+    int head;                      // head of the unit (with slot: where the new state goes)
+    int pad;
 };
 
 template <typename IO> struct DecSmem {
@@ -446,15 +469,34 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) kda_decode_stream_kernel(const
     const bool has_g = g != nullptr;
 
     if (warp == REC_WARPS) {
-        // ---------------- producer
+        // ---------------- producer: loads each unit into a stage and, once the
+        // row warps have left the unit's new state in that stage, stores it back
+        // with one bulk copy before the stage takes the next unit
         if (lane != 0) return;
         const uint64_t pol = ptx::policy_evict_first();
+        // wait until the row warps are done with stage s (phase n) and write its state back
+        auto write_back = [&](int s, int n) -> bool {
+            if (!ptx::mbar_wait(&sm.empty[s], n & 1)) {
+                flag_status(a.dev_status, KDA_DEV_TIMEOUT);
+                return false;
+            }
+            DecStage<IO>& st = sm.stage[s];
+            if (st.slot >= 0) {
+                ptx::bulk_s2g(a.rec_state + ((size_t)st.slot * H + st.head) * D * D, st.S, D * D * 4);
+                // the new conv state: the window's last K-1 raw rows (history rows 1.., then the current row)
+                for (int r = 0; r < K - 1; ++r)
+                    for (int seg = 0; seg < 3; ++seg)
+                        ptx::bulk_s2g(cs + ((size_t)st.slot * (K - 1) + r) * conv_dim + (size_t)seg * H * D + st.head * D,
+                                      r + 1 < K - 1 ? st.hist[r + 1][seg] : st.rows[seg], D * sizeof(IO));
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();  // the stage may be refilled
+            }
+            return true;
+        };
+        const int count = u_end - u_begin;
         for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
             const int s = i % DEC_STAGES, n = i / DEC_STAGES;
-            if (n > 0 && !ptx::mbar_wait(&sm.empty[s], (n - 1) & 1)) {
-                flag_status(a.dev_status, KDA_DEV_TIMEOUT);
-                return;
-            }
+            if (n > 0 && !write_back(s, n - 1)) return;
             DecStage<IO>& st = sm.stage[s];
             const int h = u / N, seq = u % N;
             int slot = a.slots ? a.slots[seq] : seq;
@@ -482,8 +524,13 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) kda_decode_stream_kernel(const
                 st.bval = ldv(b + rh);
             }
             st.slot = slot;
+            st.head = h;
             ptx::mbar_arrive(&sm.full[s]);
         }
+        // the last units' states
+        for (int i = count > DEC_STAGES ? count - DEC_STAGES : 0; i < count; ++i)
+            if (!write_back(i % DEC_STAGES, i / DEC_STAGES)) return;
+        ptx::bulk_wait_all();
         return;
     }
 
@@ -512,31 +559,32 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) kda_decode_stream_kernel(const
         DecStage<IO>& st = sm.stage[s];
         const int slot = st.slot;
         float bval = 0.0f, gval = 0.0f;
-        if (slot >= 0) {
-            load_tile_smem<D>(st.S, r0, c0, sreg);
-            for (int c = tid; c < 3 * D; c += REC_THREADS) {
-                const int seg = c / D, ch = c % D;
-                for (int r = 0; r < K - 1; ++r) sm.row.win[ring(r - (K - 1))][c] = ldv(&st.hist[r][seg][ch]);
-                sm.row.win[ring(0)][c] = ldv(&st.rows[seg][ch]);
-            }
-            for (int c = tid; c < D; c += REC_THREADS) sm.row.fr[c] = ldv(&st.rows[3][c]);
-            bval = st.bval;
-            if (has_g && tid < D) gval = ldv(&st.rows[4][tid]);
+        if (slot < 0) {
+            row_sync();
+            if (tid == 0) ptx::mbar_arrive(&sm.empty[s]);  // nothing to write back
+            continue;
         }
-        row_sync();  // stage s fully read: hand it back to the producer
-        if (tid == 0) ptx::mbar_arrive(&sm.empty[s]);
-        if (slot < 0) continue;
-
-        const float o = row_step<D>(sm.row, sreg, 0, K, rc, bval, gval, has_g);
+        load_tile_smem<D>(st.S, r0, c0, sreg);
+        bval = st.bval;
+        if (has_g && tid < D) gval = ldv(&st.rows[4][tid]);
+        // the conv window straight from the stage: raw rows K-1 history rows, then the current row
+        row_conv<D>(sm.row, K, rc,
+                    [&](int c, int j) {
+                        const int seg = c / D, ch = c % D;
+                        return j < K - 1 ? ldv(&st.hist[j][seg][ch]) : ldv(&st.rows[seg][ch]);
+                    },
+                    [&](int i) { return ldv(&st.rows[3][i]); });
+        const float o = row_rest<D>(sm.row, sreg, rc, bval, gval, has_g);
         const size_t rh = (size_t)seq * H + h;
         if (tid < D) store_out(a.out, rh * D + tid, o, a.out_bf16);
-        store_tile<D>(a.rec_state + ((size_t)slot * H + h) * D * D, r0, c0, sreg);
-        for (int c = tid; c < 3 * D; c += REC_THREADS) {
-            const int ch = conv_channel<D>(c, h, H);
-            for (int r = 0; r < K - 1; ++r)
-                stv(cs + ((size_t)slot * (K - 1) + r) * conv_dim + ch, sm.row.win[ring(1 - (K - 1) + r)][c]);
-        }
-        row_sync();  // row arrays are rewritten by the next unit
+        // the new state goes back into the stage; the producer stores it with one bulk copy
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr)
+            *reinterpret_cast<float4*>(st.S + (r0 + rr) * D + c0) =
+                make_float4(sreg[rr][0], sreg[rr][1], sreg[rr][2], sreg[rr][3]);
+        ptx::fence_proxy_async_smem();
+        row_sync();  // row arrays are rewritten by the next unit; the stage's state is complete
+        if (tid == 0) ptx::mbar_arrive(&sm.empty[s]);
     }
 }
 
