@@ -226,8 +226,16 @@ def leg_prefill(kda, wl_fn, reps, stream):
     ms = statistics.median(durs)
     bpt = prefill_bytes_per_token_head(out=2, out_gate=wl.has_out_gate)
     alg = wl.T * wl.H * bpt + prefill_state_bytes(wl.N, wl.H)
+    # algorithmic tensor work: 5 C d + 6 d^2 FLOPs per (row, head) (chunk C = 64;
+    # triangles at half), measured against the dense bf16 tensor peak (the
+    # kernels run tf32, whose nominal dense rate is half of bf16's)
+    d = wl.dk
+    flops = wl.T * wl.H * (5 * 64 * d + 6 * d * d)
+    bf16_tflops = load_peaks()[1]
+    tf = flops / (ms * 1e-3) / 1e12
     return {"workload": wl.name, "tokens": wl.T, "ms": ms, "tokens_per_s": wl.T / (ms * 1e-3),
-            "alg_bytes": alg, "achieved_gbs": alg / (ms * 1e-3) / 1e9}
+            "alg_bytes": alg, "achieved_gbs": alg / (ms * 1e-3) / 1e9,
+            "alg_tflops": tf, "tf32_frac": tf / (bf16_tflops / 2.0)}
 
 
 def leg_verify(kda, reps, stream):
