@@ -1181,20 +1181,22 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
     uint32_t gp[RPT / 2];   // output gate of the chunk whose outputs are pending (bf16 bits, 2 per register)
     int prev_c0 = 0, prev_nvalid = 0;
     bool have_prev = false;
+    // output gate rows of a chunk, loaded one chunk ahead and packed after its products
+    uint32_t graw[RPT];
+    auto load_gate = [&](int c) {
+        const int cc0 = seg0 + c * C, nv = min(C, seg1 - cc0);
+        const unsigned short* gb = static_cast<const unsigned short*>(a.g);
+#pragma unroll
+        for (int x = 0; x < RPT; ++x)
+            graw[x] = (gb != nullptr && r0 + x < nv) ? gb[((size_t)(cc0 + r0 + x) * H + h) * D + col] : 0u;
+    };
+    load_gate(0);
     for (int c = 0; c < nchunks && !ms.err; ++c) {
         const int c0 = seg0 + c * C;
         const int nvalid = min(C, seg1 - c0);
         const uint32_t c_ot = (c & 1) ? CT_OT1 : CT_OT0;
         ptx::tmem_st16(tmem + lane_base + CT_UT + RPT * qq, up);
         if (tid < D) ms.gamma[tid] = gam;
-        // this chunk's output gate rows: loaded now, packed after the third product
-        uint32_t graw[RPT];
-        {
-            const unsigned short* gb = static_cast<const unsigned short*>(a.g);
-#pragma unroll
-            for (int x = 0; x < RPT; ++x)
-                graw[x] = (gb != nullptr && r0 + x < nvalid) ? gb[((size_t)(c0 + r0 + x) * H + h) * D + col] : 0u;
-        }
         state_low(tmem + lane_base + CT_ST + 32 * qq, tmem + lane_base + CT_SL + 32 * qq);
         if (tid == 0 && !ptx::mbar_wait(&ms.rbar, c & 1)) {
             ms.err = 1;
@@ -1248,6 +1250,7 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         mma_pending = true;
 #pragma unroll
         for (int x = 0; x < RPT / 2; ++x) gp[x] = graw[2 * x] | (graw[2 * x + 1] << 16);
+        if (c + 1 < nchunks) load_gate(c + 1);
         // chunk c's slot is read (both tile copies have landed, U'^T and e^{G_C}
         // are in registers): hand it back (a thread that issues no products)
         if (tid == 128) ptx::st_release_gpu(&sp.consumed[u], c + 1);
