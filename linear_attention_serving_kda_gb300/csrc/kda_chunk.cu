@@ -786,13 +786,23 @@ __device__ __forceinline__ void write_outputs(Misc& ms, const ChunkArgs& a, uint
             o[x] = o[x] * ms.rms[r0 + x] * nw * sigmoidf_(gx);
         }
     }
-    const size_t ob = ((size_t)(c0 + r0) * H + h) * D + col;
     if (a.out_bf16) {
-        __nv_bfloat16* ou = static_cast<__nv_bfloat16*>(a.out);
+        // bf16 pairs: lanes 2m and 2m+1 hold columns c and c+1; the even lane
+        // stores rows [r0, r0+8) and the odd lane rows [r0+8, r0+16), both as
+        // 4-byte (c, c+1) pairs, after one exchange per row
+        const bool odd = lane & 1;
+        const int cpair = col & ~1;
+        __nv_bfloat162* ou = static_cast<__nv_bfloat162*>(a.out);
 #pragma unroll
-        for (int x = 0; x < RPT; ++x)
-            if (r0 + x < nvalid) ou[ob + (size_t)x * H * D] = __float2bfloat16_rn(o[x]);
+        for (int x = 0; x < RPT / 2; ++x) {
+            const float send = odd ? o[x] : o[RPT / 2 + x];
+            const float got = __shfl_xor_sync(0xffffffffu, send, 1);
+            const int r = r0 + (odd ? RPT / 2 : 0) + x;
+            const float lo = odd ? got : o[x], hi = odd ? o[RPT / 2 + x] : got;
+            if (r < nvalid) ou[(((size_t)(c0 + r) * H + h) * D + cpair) >> 1] = __floats2bfloat162_rn(lo, hi);
+        }
     } else {
+        const size_t ob = ((size_t)(c0 + r0) * H + h) * D + col;
         float* ou = static_cast<float*>(a.out);
 #pragma unroll
         for (int x = 0; x < RPT; ++x)
