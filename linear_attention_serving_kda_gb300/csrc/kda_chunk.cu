@@ -755,6 +755,37 @@ __device__ __forceinline__ void load_gate_bits(uint32_t (&gp)[RPT / 2], const Ch
     }
 }
 
+// The output gate of a chunk as 4-byte (c, c+1) bf16 pairs of this thread's
+// column pair: rows [r0, r0+8) on even lanes, [r0+8, r0+16) on odd lanes
+// (half the load instructions of per-element loads).
+__device__ __forceinline__ void load_gate_words(uint32_t (&w)[RPT / 2], const ChunkArgs& a, int c0, int r0,
+                                                int nvalid, int h, int col)
+{
+    const int rb = r0 + ((col & 1) ? RPT / 2 : 0);
+    const uint32_t* gb = static_cast<const uint32_t*>(a.g);
+#pragma unroll
+    for (int x = 0; x < RPT / 2; ++x)
+        w[x] = (gb != nullptr && rb + x < nvalid) ? gb[(((size_t)(c0 + rb + x) * a.H + h) * D + (col & ~1)) >> 1] : 0u;
+}
+
+// This thread's column of the gate words above, after one lane exchange per
+// row pair: gp[k] holds rows r0 + 2k (low half) and r0 + 2k + 1 (high half).
+__device__ __forceinline__ void gate_bits_from_words(uint32_t (&gp)[RPT / 2], const uint32_t (&w)[RPT / 2], int col)
+{
+    const bool odd = col & 1;
+    uint32_t v[RPT];
+#pragma unroll
+    for (int x = 0; x < RPT / 2; ++x) {
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, w[x], 1);
+        // even lanes: own word for rows [r0, r0+8), the partner's for [r0+8, r0+16); low halves
+        // odd lanes: the partner's word for rows [r0, r0+8), own for [r0+8, r0+16); high halves
+        v[x] = odd ? (other >> 16) : (w[x] & 0xFFFFu);
+        v[RPT / 2 + x] = odd ? (w[x] >> 16) : (other & 0xFFFFu);
+    }
+#pragma unroll
+    for (int k = 0; k < RPT / 2; ++k) gp[k] = v[2 * k] | (v[2 * k + 1] << 16);
+}
+
 // outputs of this thread's 16 rows (lane j = col), optional gated RMSNorm
 // (all threads; two block barriers when gated)
 __device__ __forceinline__ void write_outputs(Misc& ms, const ChunkArgs& a, uint32_t t_ot,
@@ -1191,14 +1222,11 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
     uint32_t gp[RPT / 2];   // output gate of the chunk whose outputs are pending (bf16 bits, 2 per register)
     int prev_c0 = 0, prev_nvalid = 0;
     bool have_prev = false;
-    // output gate rows of a chunk, loaded one chunk ahead and packed after its products
-    uint32_t graw[RPT];
+    // output gate rows of a chunk, loaded one chunk ahead and unpacked after its products
+    uint32_t gw[RPT / 2];
     auto load_gate = [&](int c) {
-        const int cc0 = seg0 + c * C, nv = min(C, seg1 - cc0);
-        const unsigned short* gb = static_cast<const unsigned short*>(a.g);
-#pragma unroll
-        for (int x = 0; x < RPT; ++x)
-            graw[x] = (gb != nullptr && r0 + x < nv) ? gb[((size_t)(cc0 + r0 + x) * H + h) * D + col] : 0u;
+        const int cc0 = seg0 + c * C;
+        load_gate_words(gw, a, cc0, r0, min(C, seg1 - cc0), h, col);
     };
     load_gate(0);
     for (int c = 0; c < nchunks && !ms.err; ++c) {
@@ -1258,8 +1286,7 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
             issue_fourth(sm, tmem, issuer(tid), SL_PH, SL_PL, SL_KD, SL_KDL, CT_UT, CT_UL, CT_ST, c_ot, &ms.bar);
         }
         mma_pending = true;
-#pragma unroll
-        for (int x = 0; x < RPT / 2; ++x) gp[x] = graw[2 * x] | (graw[2 * x + 1] << 16);
+        gate_bits_from_words(gp, gw, col);
         if (c + 1 < nchunks) load_gate(c + 1);
         // chunk c's slot is read (both tile copies have landed, U'^T and e^{G_C}
         // are in registers): hand it back (a thread that issues no products)
