@@ -341,39 +341,61 @@ __device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const C
     const float* wk = tc.wk;
     const float* wv = tc.wv;
     const float dtc = tc.dtc, ea = tc.ea;
-    // ---- prep: conv + SiLU, gate, running log-decay for this thread's column and 16 rows
+    // ---- prep: conv + SiLU, gate, running log-decay for this thread's column and 16 rows,
+    // two rows at a time in packed f32x2 arithmetic
     float qv[RPT], kv[RPT], vv[RPT], G[RPT];
     {
-        float xq[4], xk[4], xv[4];
+        float xq[5], xk[5], xv[5];  // raw rows lr .. lr + 4 (lr + 3 is row r's own)
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
             xq[j] = __bfloat162float(raw[0 * RAWR * D + (r0 + j) * D + col]);
             xk[j] = __bfloat162float(raw[1 * RAWR * D + (r0 + j) * D + col]);
             xv[j] = __bfloat162float(raw[2 * RAWR * D + (r0 + j) * D + col]);
         }
+        const float2 dt2 = make_float2(dtc, dtc), ea2 = make_float2(ea, ea), lb2 = make_float2(a.lb, a.lb);
+        const float2 one2 = make_float2(1.0f, 1.0f);
         float run = 0.0f;
 #pragma unroll
-        for (int r = 0; r < RPT; ++r) {
+        for (int r = 0; r < RPT; r += 2) {
             const int lr = r0 + r;
-            xq[3] = __bfloat162float(raw[0 * RAWR * D + (lr + 3) * D + col]);
-            xk[3] = __bfloat162float(raw[1 * RAWR * D + (lr + 3) * D + col]);
-            xv[3] = __bfloat162float(raw[2 * RAWR * D + (lr + 3) * D + col]);
-            float aq = 0.f, ak = 0.f, av = 0.f;
+#pragma unroll
+            for (int j = 3; j < 5; ++j) {
+                xq[j] = __bfloat162float(raw[0 * RAWR * D + (lr + j) * D + col]);
+                xk[j] = __bfloat162float(raw[1 * RAWR * D + (lr + j) * D + col]);
+                xv[j] = __bfloat162float(raw[2 * RAWR * D + (lr + j) * D + col]);
+            }
+            float2 aq = make_float2(0.f, 0.f), ak = aq, av = aq;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                aq = __fmaf_rn(wq[j], xq[j], aq);
-                ak = __fmaf_rn(wk[j], xk[j], ak);
-                av = __fmaf_rn(wv[j], xv[j], av);
+                aq = __ffma2_rn(make_float2(wq[j], wq[j]), make_float2(xq[j], xq[j + 1]), aq);
+                ak = __ffma2_rn(make_float2(wk[j], wk[j]), make_float2(xk[j], xk[j + 1]), ak);
+                av = __ffma2_rn(make_float2(wv[j], wv[j]), make_float2(xv[j], xv[j + 1]), av);
             }
-            const bool ok = lr < nvalid;
-            qv[r] = ok ? siluf_(aq) : 0.0f;
-            kv[r] = ok ? siluf_(ak) : 0.0f;
-            vv[r] = ok ? siluf_(av) : 0.0f;
-            const float la = ok ? a.lb * sigmoidf_(ea * (__bfloat162float(rawf[lr * D + col]) + dtc)) : 0.0f;  // safe gate
-            run += la;
+            // SiLU: x / (1 + e^-x); the gate: lb * sigmoid(ea (f + dt))
+            const float2 dq = __fadd2_rn(one2, make_float2(__expf(-aq.x), __expf(-aq.y)));
+            const float2 dk = __fadd2_rn(one2, make_float2(__expf(-ak.x), __expf(-ak.y)));
+            const float2 dv = __fadd2_rn(one2, make_float2(__expf(-av.x), __expf(-av.y)));
+            const float2 sq = __fmul2_rn(aq, make_float2(__fdividef(1.0f, dq.x), __fdividef(1.0f, dq.y)));
+            const float2 sk = __fmul2_rn(ak, make_float2(__fdividef(1.0f, dk.x), __fdividef(1.0f, dk.y)));
+            const float2 sv = __fmul2_rn(av, make_float2(__fdividef(1.0f, dv.x), __fdividef(1.0f, dv.y)));
+            const float2 fz = __fmul2_rn(ea2, __fadd2_rn(make_float2(__bfloat162float(rawf[lr * D + col]),
+                                                                      __bfloat162float(rawf[(lr + 1) * D + col])),
+                                                          dt2));
+            const float2 gd = __fadd2_rn(one2, make_float2(__expf(-fz.x), __expf(-fz.y)));
+            const float2 la = __fmul2_rn(lb2, make_float2(__fdividef(1.0f, gd.x), __fdividef(1.0f, gd.y)));
+            const bool ok0 = lr < nvalid, ok1 = lr + 1 < nvalid;
+            qv[r] = ok0 ? sq.x : 0.0f;
+            kv[r] = ok0 ? sk.x : 0.0f;
+            vv[r] = ok0 ? sv.x : 0.0f;
+            qv[r + 1] = ok1 ? sq.y : 0.0f;
+            kv[r + 1] = ok1 ? sk.y : 0.0f;
+            vv[r + 1] = ok1 ? sv.y : 0.0f;
+            run += ok0 ? la.x : 0.0f;
             G[r] = run;
+            run += ok1 ? la.y : 0.0f;
+            G[r + 1] = run;
 #pragma unroll
-            for (int j = 0; j < 3; ++j) { xq[j] = xq[j + 1]; xk[j] = xk[j + 1]; xv[j] = xv[j + 1]; }
+            for (int j = 0; j < 3; ++j) { xq[j] = xq[j + 2]; xk[j] = xk[j + 2]; xv[j] = xv[j + 2]; }
         }
     }
     // row norms of q' and k' (this warp's 32 columns) and this quarter's log-decay total
