@@ -455,38 +455,71 @@ __device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const C
         const float eGm = __expf(Gm);          // first half: e^{G_16} >= e^{-85}
         const float cGC = __expf(GC - Gm);     // second half: e^{G_63 - G_48} >= e^{-75}
         float xt[RPT], yt[RPT], yl[RPT];
+        // two rows at a time in packed f32x2 arithmetic; the exponentials, TF32
+        // roundings and the stores (one address per element) stay per element
+        const float2 eGm2 = make_float2(eGm, eGm), cGC2 = make_float2(cGC, cGC);
+        const float2 mGm2 = make_float2(-Gm, -Gm);
+        auto lo2 = [](float2 x) {  // tf32_lo of both lanes: x - trunc(x)
+            return __fadd2_rn(x, make_float2(-__uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u),
+                                             -__uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u)));
+        };
 #pragma unroll
-        for (int r = 0; r < RPT; ++r) {
+        for (int r = 0; r < RPT; r += 2) {
             const int rr = r0 + r;
-            const float e = __expf(G[r] - Gm);
-            const float ie = __expf(Gm - G[r]);
-            const uint32_t o = swz(rr, col, AX_KB);
-            st_hi(sm, SM_AX + 8192 + o, kv[r] * e);
-            st_split(sm, SM_AX + 16384 + o, SM_AX + o, qv[r] * e);
-            st_split(sm, SM_B1H + swz(rr, col, B1_KB), SM_B1L + swz(rr, col, B1_KB), kv[r] * ie);
+            const float2 dg = __fadd2_rn(make_float2(G[r], G[r + 1]), mGm2);  // G - Gm
+            const float2 e = make_float2(__expf(dg.x), __expf(dg.y));
+            const float2 ie = make_float2(__expf(-dg.x), __expf(-dg.y));
+            const float2 k2 = make_float2(kv[r], kv[r + 1]), q2 = make_float2(qv[r], qv[r + 1]);
+            const float2 ke = __fmul2_rn(k2, e), qe2 = __fmul2_rn(q2, e), kie = __fmul2_rn(k2, ie);
+            const float2 qel = lo2(qe2), kiel = lo2(kie);
+            const uint32_t o0 = swz(rr, col, AX_KB), o1 = swz(rr + 1, col, AX_KB);
+            const uint32_t p0 = swz(rr, col, B1_KB), p1 = swz(rr + 1, col, B1_KB);
+            st_hi(sm, SM_AX + 8192 + o0, ke.x);
+            st_hi(sm, SM_AX + 8192 + o1, ke.y);
+            st_raw(sm, SM_AX + 16384 + o0, qe2.x);
+            st_raw(sm, SM_AX + 16384 + o1, qe2.y);
+            st_raw(sm, SM_AX + o0, qel.x);
+            st_raw(sm, SM_AX + o1, qel.y);
+            st_raw(sm, SM_B1H + p0, kie.x);
+            st_raw(sm, SM_B1H + p1, kie.y);
+            st_raw(sm, SM_B1L + p0, kiel.x);
+            st_raw(sm, SM_B1L + p1, kiel.y);
             // e^{G_r}: a product of two in-range factors in the first half; direct in the
             // second (e^{G_48} may underflow).  e^{G_C - G_r}: direct in the first half
             // (e^{G_C - G_16} may underflow); a product in the second.  The cross
             // factor is e^{G_48 - G_r} in the first half and e^{G_48 - G_r} = ie in
             // the second.  (half is uniform over a warp: one side runs.)
-            float cross, eG, edec;
+            float2 cross, eG, edec;
             if (half == 0) {
-                cross = __expf(Gx - G[r]);
-                eG = e * eGm;
-                edec = __expf(GC - G[r]);
+                cross = make_float2(__expf(Gx - G[r]), __expf(Gx - G[r + 1]));
+                eG = __fmul2_rn(e, eGm2);
+                edec = make_float2(__expf(GC - G[r]), __expf(GC - G[r + 1]));
             } else {
                 cross = ie;
-                eG = __expf(G[r]);
-                edec = ie * cGC;
+                eG = make_float2(__expf(G[r]), __expf(G[r + 1]));
+                edec = __fmul2_rn(ie, cGC2);
             }
-            st_split(sm, SM_B1H + swz(xrow + rr, col, B1_KB), SM_B1L + swz(xrow + rr, col, B1_KB), kv[r] * cross);
-            qe[r] = qv[r] * eG;
-            kdx[r] = kv[r] * edec;
-            const float be = ms.beta[rr];
-            xt[r] = tf32r(be * kv[r] * eG);
-            const float y = be * vv[r];
-            yt[r] = y;
-            yl[r] = tf32_lo(y);
+            const float2 kc = __fmul2_rn(k2, cross), kcl = lo2(kc);
+            const uint32_t x0 = swz(xrow + rr, col, B1_KB), x1 = swz(xrow + rr + 1, col, B1_KB);
+            st_raw(sm, SM_B1H + x0, kc.x);
+            st_raw(sm, SM_B1H + x1, kc.y);
+            st_raw(sm, SM_B1L + x0, kcl.x);
+            st_raw(sm, SM_B1L + x1, kcl.y);
+            const float2 qg = __fmul2_rn(q2, eG), kd2 = __fmul2_rn(k2, edec);
+            qe[r] = qg.x;
+            qe[r + 1] = qg.y;
+            kdx[r] = kd2.x;
+            kdx[r + 1] = kd2.y;
+            const float2 be = make_float2(ms.beta[rr], ms.beta[rr + 1]);
+            const float2 xg = __fmul2_rn(__fmul2_rn(be, k2), eG);
+            xt[r] = tf32r(xg.x);
+            xt[r + 1] = tf32r(xg.y);
+            const float2 y = __fmul2_rn(be, make_float2(vv[r], vv[r + 1]));
+            const float2 yl2 = lo2(y);
+            yt[r] = y.x;
+            yt[r + 1] = y.y;
+            yl[r] = yl2.x;
+            yl[r + 1] = yl2.y;
         }
         ptx::tmem_st16(tmem + lane_base + TM_XT + RPT * qq, xt);
         ptx::tmem_st16(tmem + lane_base + TM_YT + RPT * qq, yt);
