@@ -129,6 +129,8 @@ static_assert(SM_PH >= SM_T + 16384 && SM_PL >= SM_PH + 16384 && SM_QE >= SM_PL 
 static_assert(SM_QEL + 32768 <= SM_TS && SM_NW >= SM_QEL + 32768 && SM_NW + 32768 <= SM_PH,
               "late tiles overlap");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(offsetof(Misc, gamma) % 16 == 0 && SM_MISC % 16 == 0, "e^{G_C} is read as float4");
+static_assert(offsetof(Misc, rms) % 8 == 0, "row inverse norms are read as float2");
 
 // byte offset of element (row, k) in a K-major SW128 fp32 tile whose K-blocks
 // are `kbs` bytes apart (row 0 of the tile at offset 0)
@@ -704,7 +706,13 @@ __device__ __forceinline__ void state_low(uint32_t t_st, uint32_t t_sl)
     float s[32];
     ptx::tmem_ld32(t_st, s);
 #pragma unroll
-    for (int x = 0; x < 32; ++x) s[x] -= __uint_as_float(__float_as_uint(s[x]) & 0xFFFFE000u);
+    for (int x = 0; x < 32; x += 2) {
+        const float2 d = __fadd2_rn(make_float2(s[x], s[x + 1]),
+                                    make_float2(-__uint_as_float(__float_as_uint(s[x]) & 0xFFFFE000u),
+                                                -__uint_as_float(__float_as_uint(s[x + 1]) & 0xFFFFE000u)));
+        s[x] = d.x;
+        s[x + 1] = d.y;
+    }
     ptx::tmem_st32(t_sl, s);
 }
 
@@ -753,12 +761,23 @@ __device__ __forceinline__ void rescale_split(uint32_t t_st, uint32_t t_ut, uint
     float v[32];
     ptx::tmem_ld32(t_st, v);
 #pragma unroll
-    for (int x = 0; x < 32; ++x) v[x] *= gam32[x];
+    for (int x = 0; x < 32; x += 4) {
+        const float4 g4 = *reinterpret_cast<const float4*>(gam32 + x);
+        const float2 a2 = __fmul2_rn(make_float2(v[x], v[x + 1]), make_float2(g4.x, g4.y));
+        const float2 b2 = __fmul2_rn(make_float2(v[x + 2], v[x + 3]), make_float2(g4.z, g4.w));
+        v[x] = a2.x; v[x + 1] = a2.y; v[x + 2] = b2.x; v[x + 3] = b2.y;
+    }
     ptx::tmem_st32(t_st, v);
     float u[RPT];
     ptx::tmem_ld16(t_ut, u);
 #pragma unroll
-    for (int x = 0; x < RPT; ++x) u[x] = tf32_lo(u[x]);
+    for (int x = 0; x < RPT; x += 2) {
+        const float2 d = __fadd2_rn(make_float2(u[x], u[x + 1]),
+                                    make_float2(-__uint_as_float(__float_as_uint(u[x]) & 0xFFFFE000u),
+                                                -__uint_as_float(__float_as_uint(u[x + 1]) & 0xFFFFE000u)));
+        u[x] = d.x;
+        u[x + 1] = d.y;
+    }
     ptx::tmem_st16(t_ul, u);
 }
 
@@ -850,12 +869,21 @@ __device__ __forceinline__ void write_outputs(Misc& ms, const ChunkArgs& a, uint
     const int r0 = RPT * qq, H = a.H;
     float o[RPT];
     ptx::tmem_ld16(t_ot, o);
+    const float2 sc2 = make_float2(a.scale, a.scale);
 #pragma unroll
-    for (int x = 0; x < RPT; ++x) o[x] *= a.scale;
+    for (int x = 0; x < RPT; x += 2) {
+        const float2 y = __fmul2_rn(make_float2(o[x], o[x + 1]), sc2);
+        o[x] = y.x;
+        o[x + 1] = y.y;
+    }
     if (a.g != nullptr) {
         float t[RPT];
 #pragma unroll
-        for (int x = 0; x < RPT; ++x) t[x] = o[x] * o[x];
+        for (int x = 0; x < RPT; x += 2) {
+            const float2 y = __fmul2_rn(make_float2(o[x], o[x + 1]), make_float2(o[x], o[x + 1]));
+            t[x] = y.x;
+            t[x + 1] = y.y;
+        }
         const float pr = transpose_reduce16(t, lane);
         if (lane < 16) ms.epart[qq][lq][lane] = pr;
         __syncthreads();
@@ -866,10 +894,16 @@ __device__ __forceinline__ void write_outputs(Misc& ms, const ChunkArgs& a, uint
             ms.rms[r] = rsqrtf(tot * (1.0f / D) + a.norm_eps);
         }
         __syncthreads();
+        const float2 nw2 = make_float2(nw, nw);
 #pragma unroll
-        for (int x = 0; x < RPT; ++x) {
-            const float gx = __uint_as_float((x & 1) ? (gp[x >> 1] & 0xFFFF0000u) : (gp[x >> 1] << 16));
-            o[x] = o[x] * ms.rms[r0 + x] * nw * sigmoidf_(gx);
+        for (int x = 0; x < RPT; x += 2) {
+            // o * rms * w * sigmoid(g), two rows per packed operation
+            const float g0 = __uint_as_float(gp[x >> 1] << 16), g1 = __uint_as_float(gp[x >> 1] & 0xFFFF0000u);
+            const float2 rr = *reinterpret_cast<const float2*>(&ms.rms[r0 + x]);
+            const float2 y = __fmul2_rn(__fmul2_rn(make_float2(o[x], o[x + 1]), rr), nw2);
+            const float2 z = __fmul2_rn(y, make_float2(sigmoidf_(g0), sigmoidf_(g1)));
+            o[x] = z.x;
+            o[x + 1] = z.y;
         }
     }
     if (a.out_bf16) {
