@@ -860,14 +860,15 @@ __device__ __forceinline__ void gate_bits_from_words(uint32_t (&gp)[RPT / 2], co
     for (int k = 0; k < RPT / 2; ++k) gp[k] = v[2 * k] | (v[2 * k + 1] << 16);
 }
 
-// outputs of this thread's 16 rows (lane j = col), optional gated RMSNorm
-// (all threads; two block barriers when gated)
-__device__ __forceinline__ void write_outputs(Misc& ms, const ChunkArgs& a, uint32_t t_ot,
-                                              const uint32_t (&gp)[RPT / 2], int c0, int nvalid, int h, float nw)
+// Outputs of this thread's 16 rows (lane j = col), optional gated RMSNorm, in
+// two parts.  Part A (all threads) reads O^T, applies the scale and, when
+// gated, leaves each warp's partial sums of squares in ms.epart; the caller
+// then syncs the block.  Part B needs no block barrier: lanes 0..15 of every
+// warp form the inverse RMS of the quarter's 16 rows from the four partials
+// (the same sum in the same order in every warp) and the warp reads them back.
+__device__ __forceinline__ void write_outputs_a(Misc& ms, const ChunkArgs& a, uint32_t t_ot, float (&o)[RPT])
 {
-    const int tid = threadIdx.x, lane = tid & 31, lq = (tid >> 5) & 3, qq = tid >> 7, col = tid & (D - 1);
-    const int r0 = RPT * qq, H = a.H;
-    float o[RPT];
+    const int tid = threadIdx.x, lane = tid & 31, lq = (tid >> 5) & 3, qq = tid >> 7;
     ptx::tmem_ld16(t_ot, o);
     const float2 sc2 = make_float2(a.scale, a.scale);
 #pragma unroll
@@ -886,14 +887,21 @@ __device__ __forceinline__ void write_outputs(Misc& ms, const ChunkArgs& a, uint
         }
         const float pr = transpose_reduce16(t, lane);
         if (lane < 16) ms.epart[qq][lq][lane] = pr;
-        __syncthreads();
-        if (tid < C) {
-            const int r = tid;
-            const float tot = ms.epart[r >> 4][0][r & 15] + ms.epart[r >> 4][1][r & 15] +
-                              ms.epart[r >> 4][2][r & 15] + ms.epart[r >> 4][3][r & 15];
-            ms.rms[r] = rsqrtf(tot * (1.0f / D) + a.norm_eps);
+    }
+}
+
+__device__ __forceinline__ void write_outputs_b(Misc& ms, const ChunkArgs& a, float (&o)[RPT],
+                                                const uint32_t (&gp)[RPT / 2], int c0, int nvalid, int h, float nw)
+{
+    const int tid = threadIdx.x, lane = tid & 31, qq = tid >> 7, col = tid & (D - 1);
+    const int r0 = RPT * qq, H = a.H;
+    if (a.g != nullptr) {
+        if (lane < 16) {
+            const float tot = ms.epart[qq][0][lane] + ms.epart[qq][1][lane] + ms.epart[qq][2][lane] +
+                              ms.epart[qq][3][lane];
+            ms.rms[r0 + lane] = rsqrtf(tot * (1.0f / D) + a.norm_eps);  // same value from the quarter's 4 warps
         }
-        __syncthreads();
+        __syncwarp();
         const float2 nw2 = make_float2(nw, nw);
 #pragma unroll
         for (int x = 0; x < RPT; x += 2) {
@@ -1081,7 +1089,12 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
         load_gate_bits(gp, a, c0, r0, nvalid, h, col);  // while the product runs
         if (!wait_mma(ms, ph, a.dev_status)) break;
 
-        write_outputs(ms, a, tmem + lane_base + TM_OT + RPT * qq, gp, c0, nvalid, h, nw);
+        {
+            float o[RPT];
+            write_outputs_a(ms, a, tmem + lane_base + TM_OT + RPT * qq, o);
+            __syncthreads();
+            write_outputs_b(ms, a, o, gp, c0, nvalid, h, nw);
+        }
         ptx::tc_fence_before();
         __syncthreads();
     }
@@ -1325,6 +1338,9 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         ptx::tmem_st16(tmem + lane_base + CT_UT + RPT * qq, up);
         if (tid < D) ms.gamma[tid] = gam;
         state_low(tmem + lane_base + CT_ST + 32 * qq, tmem + lane_base + CT_SL + 32 * qq);
+        // the previous chunk's outputs, first part (its block barrier is the one below)
+        float o[RPT];
+        if (have_prev) write_outputs_a(ms, a, tmem + lane_base + (c_ot ^ (CT_OT0 ^ CT_OT1)) + RPT * qq, o);
         if (tid == 0 && !ptx::mbar_wait(&ms.rbar, c & 1)) {
             ms.err = 1;
             flag_status(a.dev_status, KDA_DEV_TIMEOUT);
@@ -1338,11 +1354,11 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
             issue_third(sm, tmem, issuer(tid), SL_NW, SL_QE, SL_QEL, CT_UT, CT_ST, CT_SL, c_ot, &ms.bar);
         }
         mma_pending = true;
-        // while the third product runs: chunk c + 1's slot, the previous chunk's outputs
+        // while the third product runs: chunk c + 1's slot, the rest of the previous
+        // chunk's outputs (warp-local: the issuing warps join when they are done)
         if (c + 1 < nchunks) acquire_by(c + 1, 128);
         if (have_prev) {
-            write_outputs(ms, a, tmem + lane_base + (c_ot ^ (CT_OT0 ^ CT_OT1)) + RPT * qq, gp, prev_c0,
-                          prev_nvalid, h, nw);
+            write_outputs_b(ms, a, o, gp, prev_c0, prev_nvalid, h, nw);
             have_prev = false;
         }
         __syncthreads();
@@ -1392,7 +1408,10 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
     }
     if (have_prev && !ms.err) {
         const uint32_t c_ot = ((nchunks - 1) & 1) ? CT_OT1 : CT_OT0;
-        write_outputs(ms, a, tmem + lane_base + c_ot + RPT * qq, gp, prev_c0, prev_nvalid, h, nw);
+        float o[RPT];
+        write_outputs_a(ms, a, tmem + lane_base + c_ot + RPT * qq, o);
+        __syncthreads();
+        write_outputs_b(ms, a, o, gp, prev_c0, prev_nvalid, h, nw);
     }
     if (tid == 0 && mma_pending) (void)ptx::mbar_wait(&ms.bar, ph);  // after a failed wait: let the products end
 
