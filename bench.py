@@ -105,25 +105,34 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(r[2] for r in rows), "reasons": reasons}
 
 
-def time_steps(fn, steps, stream, queue_ahead=True):
+def time_steps(fn, steps, stream, queue_ahead=True, per_step=True):
     """Per-step CUDA-event durations (ms) of fn(i) on `stream`, and the
     elapsed time of the whole sequence.  With queue_ahead the stream first
     sleeps on the GPU so the host can enqueue every step before the GPU
     reaches the first one: the events then time GPU execution, not host
-    launch overhead (which the end-to-end figure measures)."""
+    launch overhead (which the end-to-end figure measures).  Without
+    per_step only the first start and the last end are recorded (an event
+    between back-to-back launches adds a gap of its own); every step's
+    duration is then reported as the elapsed time over the steps."""
     import torch
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    n_ev = steps if per_step else 1
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     if queue_ahead:
         with torch.cuda.stream(stream):
             torch.cuda._sleep(int(2e6) + 200000 * steps)
     for i in range(steps):
-        starts[i].record(stream)
+        if per_step or i == 0:
+            starts[i if per_step else 0].record(stream)
         fn(i)
-        ends[i].record(stream)
+        if per_step or i == steps - 1:
+            ends[i if per_step else 0].record(stream)
     torch.cuda.synchronize()
-    return [s.elapsed_time(e) for s, e in zip(starts, ends)], starts[0].elapsed_time(ends[-1])
+    total = starts[0].elapsed_time(ends[-1])
+    if not per_step:
+        return [total / steps] * steps, total
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], total
 
 
 # ------------------------------------------------------- algorithmic bytes
@@ -194,6 +203,9 @@ def weak_scaling_value(tokens_per_rank_step: int, world: int, steps: int, total_
 
 
 def run_timed(step, steps, stream, dist):
+    """The timed region: K decode steps (one kernel launch each) between two
+    events; a launch's duration is taken as the region over K (gaps between
+    launches included)."""
     import torch
 
     torch.cuda.synchronize()
@@ -201,7 +213,7 @@ def run_timed(step, steps, stream, dist):
         dist.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    durs, total_ms = time_steps(step, steps, stream)
+    durs, total_ms = time_steps(step, steps, stream, per_step=False)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -278,11 +290,16 @@ def leg_verify(kda, reps, stream):
 
 
 def e2e_decode(kda, steps, warmup, stream):
-    """Same decode step through the public API, host buffers: the step's rows
-    come from one pinned host buffer (q, k, v, gate, beta and output gate packed
-    back to back, one host-to-device copy) and the output goes back to pinned
-    host memory, both inside the timed region.  The call is a pre-marshalled
-    `kda.Prepared` decode on the device copy of that buffer."""
+    """Same decode step through the public API, host buffers, as a serving
+    loop runs it: each step's rows come from pinned host memory (q, k, v,
+    gate, beta and output gate packed back to back, one host-to-device copy)
+    and its output goes back to pinned host memory, both inside the timed
+    region.  The copies run on their own streams, double-buffered, so the
+    upload of step i+1 and the download of step i overlap the decode of step
+    i; events order each buffer's reuse.  The call is a pre-marshalled
+    `kda.Prepared` decode on the device copy of the step's rows.  The timed
+    region runs from before the first upload to the end of the last
+    download, host launch overhead included (no queue-ahead)."""
     import torch
 
     from linear_attention_serving_kda_gb300 import workloads as W
@@ -296,37 +313,64 @@ def e2e_decode(kda, steps, warmup, stream):
     for nm in names:
         offs[nm] = off
         off += (srcs[nm].numel() * srcs[nm].element_size() + 255) // 256 * 256
-    host_in = torch.empty(off, dtype=torch.uint8).pin_memory()
-    dev_in = torch.empty(off, dtype=torch.uint8, device="cuda")
 
     def view(buf, nm):
         t = srcs[nm]
         n = t.numel() * t.element_size()
         return buf[offs[nm]:offs[nm] + n].view(t.dtype).view(t.shape)
 
+    NB = 2
+    host_in = torch.empty(off, dtype=torch.uint8).pin_memory()
     for nm in names:
         view(host_in, nm).copy_(srcs[nm])
-    dv = {nm: view(dev_in, nm) for nm in names}
-    host_out = torch.empty(dc.out.shape, dtype=dc.out.dtype).pin_memory()
+    dev_in = [torch.empty(off, dtype=torch.uint8, device="cuda") for _ in range(NB)]
+    dev_out = [torch.empty_like(dc.out) for _ in range(NB)]
+    host_out = [torch.empty(dc.out.shape, dtype=dc.out.dtype).pin_memory() for _ in range(NB)]
     h2d = sum(srcs[nm].numel() * srcs[nm].element_size() for nm in names)
-    d2h = host_out.numel() * host_out.element_size()
-    call = kda.Prepared("kda_decode", dc.params(), wl.N, dv["q"], dv["k"], dv["v"], dv["f"], dv["b"], dv["g"],
-                        None, dc.conv_state, dc.rec_state, dc.out, dc.dev_status, stream=stream)
+    d2h = host_out[0].numel() * host_out[0].element_size()
+    calls = []
+    for j in range(NB):
+        dv = {nm: view(dev_in[j], nm) for nm in names}
+        calls.append(kda.Prepared("kda_decode", dc.params(), wl.N, dv["q"], dv["k"], dv["v"], dv["f"], dv["b"],
+                                  dv["g"], None, dc.conv_state, dc.rec_state, dev_out[j], dc.dev_status,
+                                  stream=stream))
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    uploaded = [ev() for _ in range(NB)]   # rows of buffer j on the device
+    computed = [ev() for _ in range(NB)]   # decode on buffer j done (rows free, output ready)
+    fetched = [ev() for _ in range(NB)]    # output of buffer j copied back (output free)
 
     def step(i):
-        dev_in.copy_(host_in, non_blocking=True)
-        kda.check(call())
-        host_out.copy_(dc.out, non_blocking=True)
+        j = i % NB
+        with torch.cuda.stream(up):
+            if i >= NB:
+                up.wait_event(computed[j])
+            dev_in[j].copy_(host_in, non_blocking=True)
+            uploaded[j].record(up)
+        stream.wait_event(uploaded[j])
+        if i >= NB:
+            stream.wait_event(fetched[j])
+        kda.check(calls[j]())
+        computed[j].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(computed[j])
+            host_out[j].copy_(dev_out[j], non_blocking=True)
+            fetched[j].record(down)
 
-    with torch.cuda.stream(stream):
-        for i in range(warmup):
-            step(i)
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        _, total = time_steps(step, steps, stream, queue_ahead=False)
-    ms = total / steps
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(up)
+    for i in range(steps):
+        step(i)
+    stream.wait_stream(down)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
     return {"value": wl.N / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "pipeline": "upload of step i+1 and download of step i overlap the decode of step i"}
 
 
 # --------------------------------------------------------- CPU oracle legs
@@ -464,7 +508,8 @@ def main():
                    "l2": f"inputs rotate over {len(sets)} sets, {len(sets) * per_set / 1e6:.0f} MB > L2"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                      "frac": achieved / hbm_gbs, "traffic": traffic, "kernel": "kda_decode_stream_kernel<bf16>",
-                     "alg_bytes_per_launch": per_set, "peak_source": peak_src},
+                     "alg_bytes_per_launch": per_set, "peak_source": peak_src, "launch_ms": kernel_ms,
+                     "launch_ms_from": "CUDA events around the K timed launches, divided by K"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,

@@ -8,8 +8,9 @@
 // key-dim reductions per row (S'^T k and S^T q) are an in-register partial
 // over the warp's rows followed by a fixed-order sum over the 8 warps.
 //
-// Every kernel here runs one row through row_step(): the same expressions in
-// the same order -- S' = alpha * S (rounded), then S = fma(k, u, S') -- with
+// Every kernel here runs one row through row_conv, row_delta and row_out (in
+// row_step, or in that order with the state store between): the same
+// expressions in the same order -- S' = alpha * S (rounded), then S = fma(k, u, S') -- with
 // the same thread-to-element map and reduction trees.  So a verified row has
 // the bits of a decoded row, and a committed state the bits of serial decode
 // (TensorFold issue #850, Oct 15 comment: a window logs each row's decay,
@@ -17,11 +18,12 @@
 // one at a time; Oct 19 comment: preserve rounding, reduction order, replay).
 //
 // Decode at dk = dv = 128 -- the memory-bound serving step -- uses a
-// persistent kernel: one CTA per SM, a producer warp that streams each unit's
-// 64 KiB state, rows, conv history and parameters into a ring of shared-memory
-// stages with bulk async copies, and 8 row warps that run row_step on a
-// loaded stage meanwhile and leave the new state in the stage, from where the
-// producer stores it back with one bulk copy before reusing the stage.
+// persistent kernel: one CTA on each of ~27/32 of the SMs, a producer warp that
+// streams each unit's 64 KiB state, rows, conv history and parameters into a
+// ring of shared-memory stages with bulk async copies, and 8 row warps that
+// run the row on a loaded stage meanwhile and leave the new state in the
+// stage, from where the producer stores it back with one bulk copy before
+// reusing the stage.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_ptx.cuh"
@@ -44,6 +46,7 @@ template <int D> struct RowSmem {
     float alpha[D], fr[D];
     float red[REC_WARPS][D];  // cross-warp partial sums of S'^T k
     float red2[REC_WARPS][D]; // cross-warp partial sums of S^T q
+    float nrm[8];             // per-warp sums of squares: q' [0, D/32), k' [D/32, 2D/32)
     float scal[8];
 };
 
@@ -116,69 +119,71 @@ template <int D> __device__ __forceinline__ void store_tile(float* Sg, int r0, i
     }
 }
 
-// One row of the layer for one (sequence, head); called by all 256 threads.
-// On entry sm.win[ring(t)] holds the raw q|k|v row, the K-1 ring slots before
-// it the previous raw rows, sm.fr the gate row, sm.cw / sm.dtb the head's
-// parameters; bval is the beta logit and gval the output gate of column tid
-// (used when has_g).  On return S is updated in registers, sm.alpha holds the
-// row's decay, sm.act the post-SiLU q|k|v row, sm.scal[0..2] the q and k
-// inverse norms and beta, sm.red the per-warp partials of S'^T k (so the
-// normalised key is act[D + i] * scal[1] and the update u_j = beta (act[2D + j]
-// - sum_w red[w][j]), the same expressions as here), and the result is the
-// output of column tid (tid < D).  The caller syncs before the next row.
+// One row of the layer for one (sequence, head); called by all 256 threads,
+// in two steps.
 //
-// Every warp computes the norms, beta and the update of its own columns
-// itself (identical operands in an identical order, so identical bits), which
-// leaves three barriers per row.
-template <int D>
-__device__ __forceinline__ float row_rest(RowSmem<D>& sm, float (&s)[RecShape<D>::RPW][RecShape<D>::CPT],
-                                          const RowConst& rc, float bval, float gval, bool has_g);
-
-// The row's first step: conv window + SiLU into sm.act, and the decay of each
-// key dim into sm.alpha.  win(c, j) is raw value j (oldest first, j = K-1 the
-// current row) of local channel c, fr(i) the gate of key dim i.
+// row_conv: on entry sm.cw / sm.dtb hold the head's parameters; win(c, j) is
+// raw value j (oldest first, j = K-1 the current row) of local channel c
+// (q | k | v), fr(i) the gate of key dim i.  Leaves the post-SiLU q|k|v row in
+// sm.act, each key dim's decay in sm.alpha and per-warp sums of squares of q'
+// and k' in sm.nrm.  The 3D conv channels and the D decays are 4D items taken
+// round-robin by the threads (two each at D = 128); the q and k channels fill
+// whole warps of the first round.  The thread that takes item c < 3D must be
+// the one that loaded sm.cw[c] (item 3D + i: sm.dtb[i]) when the caller
+// relies on that instead of a barrier.
+//
+// row_delta: the q and k inverse norms and beta into sm.scal[0..2], the delta
+// rule on S (in registers: warp w owns rows [RPW w, +RPW), lane l columns
+// [CPT l, +CPT)), sm.red the per-warp partials of S'^T k (so the normalised key
+// is act[D + i] * scal[1] and the update u_j = beta (act[2D + j] - sum_w
+// red[w][j]), the same expressions as here), and sm.red2 the per-warp partials
+// of S^T q.  No barrier after the last step: the caller may store S first.
+//
+// row_out: the output of column tid (tid < D), with the optional
+// sigmoid-gated RMSNorm; gval is the output gate of column tid.
+//
+// Every warp forms the norms, beta and the update of its own columns itself
+// from the same shared values in the same order (identical bits everywhere).
+// Decode, verify and commit use these functions and the expressions they log,
+// so a verified row has the bits of a decoded one.
 template <int D, typename Win, typename Fr>
 __device__ __forceinline__ void row_conv(RowSmem<D>& sm, int K, const RowConst& rc, Win win, Fr fr)
 {
-    const int tid = threadIdx.x;
-    for (int c = tid; c < 3 * D; c += REC_THREADS) {
-        float acc = 0.0f;
-        for (int j = 0; j < K; ++j) acc = __fmaf_rn(sm.cw[c][j], win(c, j), acc);
-        sm.act[c] = siluf_(acc);
+    const int tid = threadIdx.x, lane = tid & 31;
+    for (int it = tid; it < 4 * D; it += REC_THREADS) {
+        if (it < 3 * D) {
+            float acc = 0.0f;
+            for (int j = 0; j < K; ++j) acc = __fmaf_rn(sm.cw[it][j], win(it, j), acc);
+            const float x = siluf_(acc);
+            sm.act[it] = x;
+            if (it < 2 * D) {  // warp-uniform: D is a multiple of 32
+                const float ss = warp_sum(x * x);
+                if (lane == 0) sm.nrm[it >> 5] = ss;
+            }
+        } else {
+            const int i = it - 3 * D;
+            sm.alpha[i] = __expf(log_alpha(rc.gate_mode, rc.lb, rc.ea, fr(i), sm.dtb[i]));
+        }
     }
-    for (int i = tid; i < D; i += REC_THREADS)
-        sm.alpha[i] = __expf(log_alpha(rc.gate_mode, rc.lb, rc.ea, fr(i), sm.dtb[i]));
     row_sync();
 }
 
 template <int D>
-__device__ __forceinline__ float row_step(RowSmem<D>& sm, float (&s)[RecShape<D>::RPW][RecShape<D>::CPT],
-                                          int t, int K, const RowConst& rc, float bval, float gval, bool has_g)
+__device__ __forceinline__ void row_delta(RowSmem<D>& sm, float (&s)[RecShape<D>::RPW][RecShape<D>::CPT],
+                                          const RowConst& rc, float bval)
 {
-    row_conv<D>(sm, K, rc, [&](int c, int j) { return sm.win[ring(t - K + 1 + j)][c]; },
-                [&](int i) { return sm.fr[i]; });
-    return row_rest<D>(sm, s, rc, bval, gval, has_g);
-}
-
-// The rest of the row (after row_conv): norms, beta, the delta rule on S and
-// the output of column tid.
-template <int D>
-__device__ __forceinline__ float row_rest(RowSmem<D>& sm, float (&s)[RecShape<D>::RPW][RecShape<D>::CPT],
-                                          const RowConst& rc, float bval, float gval, bool has_g)
-{
-    constexpr int RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT;
+    constexpr int RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT, NP = D / 32;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r0 = warp * RPW, c0 = lane * CPT;
 
-    // q / k inverse L2 norms and beta (every warp; a butterfly sum leaves the
-    // same bits in every lane)
-    float ssq = 0.0f, ssk = 0.0f;
-    for (int c = lane; c < D; c += 32) {
-        ssq = __fmaf_rn(sm.act[c], sm.act[c], ssq);
-        ssk = __fmaf_rn(sm.act[D + c], sm.act[D + c], ssk);
+    float sq = 0.0f, sk = 0.0f;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+        sq += sm.nrm[p];
+        sk += sm.nrm[NP + p];
     }
-    const float rq = rsqrtf(warp_sum(ssq) + rc.l2_eps);
-    const float rk = rsqrtf(warp_sum(ssk) + rc.l2_eps);
+    const float rq = rsqrtf(sq + rc.l2_eps);
+    const float rk = rsqrtf(sk + rc.l2_eps);
     const float beta = sigmoidf_(bval);
     if (tid == 0) {
         sm.scal[0] = rq;
@@ -186,48 +191,93 @@ __device__ __forceinline__ float row_rest(RowSmem<D>& sm, float (&s)[RecShape<D>
         sm.scal[2] = beta;
     }
 
-    // S' = Diag(alpha) S ; kv = S'^T k (partial over this warp's rows)
-    float part[CPT];
+    // S' = Diag(alpha) S ; kv = S'^T k (partial over this warp's rows).  Column
+    // pairs in packed f32x2 arithmetic: the same rounded operations per element.
+    float kr[RPW], part[CPT];
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) kr[rr] = sm.act[D + r0 + rr] * rk;
 #pragma unroll
     for (int cc = 0; cc < CPT; ++cc) part[cc] = 0.0f;
 #pragma unroll
     for (int rr = 0; rr < RPW; ++rr) {
-        const float ai = sm.alpha[r0 + rr], ki = sm.act[D + r0 + rr] * rk;
+        const float ai = sm.alpha[r0 + rr];
+        if constexpr (CPT % 2 == 0) {
 #pragma unroll
-        for (int cc = 0; cc < CPT; ++cc) {
-            s[rr][cc] = __fmul_rn(ai, s[rr][cc]);
-            part[cc] = __fmaf_rn(s[rr][cc], ki, part[cc]);
+            for (int cc = 0; cc < CPT; cc += 2) {
+                const float2 sp = __fmul2_rn(make_float2(ai, ai), make_float2(s[rr][cc], s[rr][cc + 1]));
+                const float2 pp = __ffma2_rn(sp, make_float2(kr[rr], kr[rr]), make_float2(part[cc], part[cc + 1]));
+                s[rr][cc] = sp.x;
+                s[rr][cc + 1] = sp.y;
+                part[cc] = pp.x;
+                part[cc + 1] = pp.y;
+            }
+        } else {
+#pragma unroll
+            for (int cc = 0; cc < CPT; ++cc) {
+                s[rr][cc] = __fmul_rn(ai, s[rr][cc]);
+                part[cc] = __fmaf_rn(s[rr][cc], kr[rr], part[cc]);
+            }
         }
     }
 #pragma unroll
     for (int cc = 0; cc < CPT; ++cc) sm.red[warp][c0 + cc] = part[cc];
     row_sync();
 
-    // u of this thread's columns: the 8 partials summed in warp order
-    float uc[CPT];
+    // u of this thread's columns: the partials summed in warp order
+    float uc[CPT], kv[CPT];
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) kv[cc] = 0.0f;
+#pragma unroll
+    for (int w = 0; w < REC_WARPS; ++w) {
+        if constexpr (CPT == 4) {
+            const float4 r4 = *reinterpret_cast<const float4*>(&sm.red[w][c0]);
+            kv[0] += r4.x;
+            kv[1] += r4.y;
+            kv[2] += r4.z;
+            kv[3] += r4.w;
+        } else {
+#pragma unroll
+            for (int cc = 0; cc < CPT; ++cc) kv[cc] += sm.red[w][c0 + cc];
+        }
+    }
 #pragma unroll
     for (int cc = 0; cc < CPT; ++cc) {
-        float kv = 0.0f;
-#pragma unroll
-        for (int w = 0; w < REC_WARPS; ++w) kv += sm.red[w][c0 + cc];
-        uc[cc] = beta * (sm.act[2 * D + c0 + cc] - kv);
+        uc[cc] = beta * (sm.act[2 * D + c0 + cc] - kv[cc]);
         part[cc] = 0.0f;
     }
 
     // S = S' + k u^T ; o = S^T q (partial)
 #pragma unroll
     for (int rr = 0; rr < RPW; ++rr) {
-        const float ki = sm.act[D + r0 + rr] * rk, qi = sm.act[r0 + rr] * rq;
+        const float qi = sm.act[r0 + rr] * rq;
+        if constexpr (CPT % 2 == 0) {
 #pragma unroll
-        for (int cc = 0; cc < CPT; ++cc) {
-            s[rr][cc] = __fmaf_rn(ki, uc[cc], s[rr][cc]);
-            part[cc] = __fmaf_rn(s[rr][cc], qi, part[cc]);
+            for (int cc = 0; cc < CPT; cc += 2) {
+                const float2 sn = __ffma2_rn(make_float2(kr[rr], kr[rr]), make_float2(uc[cc], uc[cc + 1]),
+                                             make_float2(s[rr][cc], s[rr][cc + 1]));
+                const float2 pp = __ffma2_rn(sn, make_float2(qi, qi), make_float2(part[cc], part[cc + 1]));
+                s[rr][cc] = sn.x;
+                s[rr][cc + 1] = sn.y;
+                part[cc] = pp.x;
+                part[cc + 1] = pp.y;
+            }
+        } else {
+#pragma unroll
+            for (int cc = 0; cc < CPT; ++cc) {
+                s[rr][cc] = __fmaf_rn(kr[rr], uc[cc], s[rr][cc]);
+                part[cc] = __fmaf_rn(s[rr][cc], qi, part[cc]);
+            }
         }
     }
 #pragma unroll
     for (int cc = 0; cc < CPT; ++cc) sm.red2[warp][c0 + cc] = part[cc];
-    row_sync();
+}
 
+template <int D>
+__device__ __forceinline__ float row_out(RowSmem<D>& sm, const RowConst& rc, float gval, bool has_g)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    row_sync();
     float o = 0.0f;
     if (tid < D) {
 #pragma unroll
@@ -249,6 +299,17 @@ __device__ __forceinline__ float row_rest(RowSmem<D>& sm, float (&s)[RecShape<D>
         }
     }
     return o;
+}
+
+// conv, delta rule and output of a row whose raw values sit in the window ring
+template <int D>
+__device__ __forceinline__ float row_step(RowSmem<D>& sm, float (&s)[RecShape<D>::RPW][RecShape<D>::CPT],
+                                          int t, int K, const RowConst& rc, float bval, float gval, bool has_g)
+{
+    row_conv<D>(sm, K, rc, [&](int c, int j) { return sm.win[ring(t - K + 1 + j)][c]; },
+                [&](int i) { return sm.fr[i]; });
+    row_delta<D>(sm, s, rc, bval);
+    return row_out<D>(sm, rc, gval, has_g);
 }
 
 // The update u_j of the last row_step (column j), from what it left in shared memory.
@@ -452,7 +513,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) kda_decode_stream_kernel(const
     if (tid == 0) {
         for (int s = 0; s < DEC_STAGES; ++s) {
             ptx::mbar_init(&sm.full[s], 1);
-            ptx::mbar_init(&sm.empty[s], 1);
+            ptx::mbar_init(&sm.empty[s], REC_WARPS);  // one arrival per row warp
         }
         ptx::fence_mbar_init();
     }
@@ -543,12 +604,16 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) kda_decode_stream_kernel(const
         const int s = i % DEC_STAGES, n = i / DEC_STAGES;
         const int h = u / N, seq = u % N;
         if (h != cur_head) {
-            // this head's conv taps, dt_bias and decay scale (L2-resident)
-            for (int c = tid; c < 3 * D; c += REC_THREADS) {
-                const int ch = conv_channel<D>(c, h, H);
-                for (int j = 0; j < K; ++j) sm.row.cw[c][j] = a.conv_w[(size_t)ch * K + j];
+            // this head's conv taps, dt_bias and decay scale (L2-resident), each
+            // loaded by the thread whose row_conv item reads it: no barrier needed
+            for (int it = tid; it < 4 * D; it += REC_THREADS) {
+                if (it < 3 * D) {
+                    const int ch = conv_channel<D>(it, h, H);
+                    for (int j = 0; j < K; ++j) sm.row.cw[it][j] = a.conv_w[(size_t)ch * K + j];
+                } else {
+                    sm.row.dtb[it - 3 * D] = a.dt_bias[(size_t)h * D + it - 3 * D];
+                }
             }
-            for (int c = tid; c < D; c += REC_THREADS) sm.row.dtb[c] = a.dt_bias[(size_t)h * D + c];
             rc.ea = expf(a.A_log[h]);
             cur_head = h;
         }
@@ -560,8 +625,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) kda_decode_stream_kernel(const
         const int slot = st.slot;
         float bval = 0.0f, gval = 0.0f;
         if (slot < 0) {
-            row_sync();
-            if (tid == 0) ptx::mbar_arrive(&sm.empty[s]);  // nothing to write back
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sm.empty[s]);  // nothing to write back
             continue;
         }
         load_tile_smem<D>(st.S, r0, c0, sreg);
@@ -574,17 +639,22 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) kda_decode_stream_kernel(const
                         return j < K - 1 ? ldv(&st.hist[j][seg][ch]) : ldv(&st.rows[seg][ch]);
                     },
                     [&](int i) { return ldv(&st.rows[3][i]); });
-        const float o = row_rest<D>(sm.row, sreg, rc, bval, gval, has_g);
-        const size_t rh = (size_t)seq * H + h;
-        if (tid < D) store_out(a.out, rh * D + tid, o, a.out_bf16);
-        // the new state goes back into the stage; the producer stores it with one bulk copy
+        row_delta<D>(sm.row, sreg, rc, bval);
+        // the new state goes back into the stage (the producer stores it with one
+        // bulk copy); the stores drain while the output step runs
 #pragma unroll
         for (int rr = 0; rr < RPW; ++rr)
             *reinterpret_cast<float4*>(st.S + (r0 + rr) * D + c0) =
                 make_float4(sreg[rr][0], sreg[rr][1], sreg[rr][2], sreg[rr][3]);
+        const float o = row_out<D>(sm.row, rc, gval, has_g);
+        const size_t rh = (size_t)seq * H + h;
+        if (tid < D) store_out(a.out, rh * D + tid, o, a.out_bf16);
+        // Each warp hands its part of the stage back.  No block barrier: the next
+        // unit's first writes to the row arrays come after its first barrier,
+        // which every warp reaches only after the reads of this unit.
         ptx::fence_proxy_async_smem();
-        row_sync();  // row arrays are rewritten by the next unit; the stage's state is complete
-        if (tid == 0) ptx::mbar_arrive(&sm.empty[s]);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.empty[s]);
     }
 }
 
@@ -675,7 +745,12 @@ template <typename IO> static cudaError_t launch_decode_stream(const RecArgs& a,
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    const int grid = units < sm_count() ? units : sm_count();
+    // Streaming CTAs: about 27/32 of the SMs (128 of the 152 on GB300).  Measured:
+    // more concurrent state streams lower the total HBM rate (B = 256 decode:
+    // 6.24 TB/s with 128 CTAs, 5.86 TB/s with 152), while below ~112 CTAs the
+    // per-SM stream rate (~50 GB/s) becomes the limit.
+    const int cap = sm_count() * 27 / 32 > 0 ? sm_count() * 27 / 32 : 1;
+    const int grid = units < cap ? units : cap;
     kda_decode_stream_kernel<IO><<<grid, DEC_THREADS, smem, st>>>(a);
     return cudaGetLastError();
 }
