@@ -289,5 +289,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
         : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel on the stream begin
+// launching, and wait until the previous kernel has completed and its memory
+// operations are visible (a no-op when launched without the attribute).
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace ptx
 }  // namespace kda

@@ -517,8 +517,14 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) kda_decode_stream_kernel(const
         }
         ptx::fence_mbar_init();
     }
+    __syncthreads();  // barrier initialisation visible to every thread
+    // Programmatic dependent launch: the next kernel on the stream may start its
+    // prologue now; every thread here waits for the previous kernel's completion
+    // (and its memory) before its first global access.
+    ptx::grid_launch_dependents();
+    ptx::grid_dependency_wait();
+    // gain of column tid: read back only by the same thread (row_out)
     for (int c = tid; c < D; c += DEC_THREADS) sm.normw[c] = a.norm_w ? a.norm_w[c] : 1.0f;
-    __syncthreads();
 
     const IO* q = static_cast<const IO*>(a.q);
     const IO* k = static_cast<const IO*>(a.k);
@@ -751,8 +757,19 @@ template <typename IO> static cudaError_t launch_decode_stream(const RecArgs& a,
     // per-SM stream rate (~50 GB/s) becomes the limit.
     const int cap = sm_count() * 27 / 32 > 0 ? sm_count() * 27 / 32 : 1;
     const int grid = units < cap ? units : cap;
-    kda_decode_stream_kernel<IO><<<grid, DEC_THREADS, smem, st>>>(a);
-    return cudaGetLastError();
+    // launched as a programmatic dependent of the previous kernel on the stream:
+    // the launch and the prologue overlap that kernel's tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(DEC_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kda_decode_stream_kernel<IO>, a);
 }
 
 template <int D, typename IO>
