@@ -251,11 +251,23 @@ __device__ __forceinline__ void stage_chunk(unsigned char* sm, const RawMaps& m,
 // program order, so every element sums the same terms in the same order.
 // All issuers commit to the same mbarrier (arrival count ISSUERS).
 constexpr int ISSUERS = 4;
+// Unrolling of the issue loops (4 by default).  Measured: full unrolling made
+// the fused kernel slower (code size) and did not speed up the split chain,
+// whose issue rate is set by the tensor pipe and by the other warps sharing
+// the sub-partitions while it issues.
+#ifndef KDA_ISSUE_UNROLL
+#define KDA_ISSUE_UNROLL 4
+#endif
+#ifndef KDA_CHAIN_UNROLL
+#define KDA_CHAIN_UNROLL 4
+#endif
+constexpr int ISSUE_UNROLL = KDA_ISSUE_UNROLL, CHAIN_UNROLL = KDA_CHAIN_UNROLL;
 __device__ __forceinline__ int issuer(int tid) { return ((tid & 31) == 0 && tid < 32 * ISSUERS) ? tid >> 5 : -1; }
 
 // first product.  Both operands come from shared memory, whose bandwidth bounds
 // this product, so the A tile is not read twice by splitting N: issuer 0 runs
 // D1, issuer 1 D1c, the others only commit.
+template <int UNR>
 __device__ __forceinline__ void issue_first(unsigned char* sm, uint32_t tmem, int q, uint64_t* bar)
 {
     ptx::tc_fence_after();
@@ -263,7 +275,7 @@ __device__ __forceinline__ void issue_first(unsigned char* sm, uint32_t tmem, in
     const uint64_t dbh = dsc(sm, SM_B1H);
     if (q == 0) {
         const uint64_t dak = dsc(sm, SM_AX + 8192), dbl = dsc(sm, SM_B1L);
-#pragma unroll 4
+#pragma unroll UNR
         for (int ks = 0; ks < 16; ++ks) {
             const uint32_t ka = ((ks >> 2) * AX_KB + (ks & 3) * 32) >> 4, kb = ((ks >> 2) * B1_KB + (ks & 3) * 32) >> 4;
             ptx::mma_tf32_ss(tmem + TM_D1, dak + ka, dbh + kb, id, ks > 0);
@@ -271,7 +283,7 @@ __device__ __forceinline__ void issue_first(unsigned char* sm, uint32_t tmem, in
         }
     } else if (q == 1) {
         const uint64_t daq = dsc(sm, SM_AX);
-#pragma unroll 4
+#pragma unroll UNR
         for (int ks = 0; ks < 16; ++ks) {
             const uint32_t ka = ((ks >> 2) * AX_KB + (ks & 3) * 32) >> 4, kb = ((ks >> 2) * B1_KB + (ks & 3) * 32) >> 4;
             ptx::mma_tf32_ss(tmem + TM_D1C, daq + ka, dbh + kb, id, ks > 0);
@@ -281,13 +293,14 @@ __device__ __forceinline__ void issue_first(unsigned char* sm, uint32_t tmem, in
 }
 
 // second product.  Issuer q: W^T (q < 2) or U'^T (q >= 2), chunk rows [32 (q & 1), +32).
+template <int UNR>
 __device__ __forceinline__ void issue_second(unsigned char* sm, uint32_t tmem, int q, uint64_t* bar)
 {
     ptx::tc_fence_after();
     const uint32_t id = ptx::idesc_tf32(128, 32);
     const uint32_t hr = (q & 1) * 32, ho = (hr * 128) >> 4;
     const uint64_t dt = dsc(sm, SM_T) + ho;
-#pragma unroll 4
+#pragma unroll UNR
     for (int ks = 0; ks < 8; ++ks) {
         const uint64_t bd = dt + (((ks >> 2) * T64_KB + (ks & 3) * 32) >> 4);
         if (q < 2) {
@@ -532,7 +545,7 @@ __device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const C
     __syncthreads();
 
     // ---- first product: D1 = [K~; Q~hi](B1hi + B1lo)^T, D1c = [Q~lo; K~] B1hi^T
-    if (issuer(tid) >= 0) issue_first(sm, tmem, issuer(tid), &ms.bar);
+    if (issuer(tid) >= 0) issue_first<ISSUE_UNROLL>(sm, tmem, issuer(tid), &ms.bar);
     if (!wait_mma(ms, ph, a.dev_status)) return false;
 
     // ---- A (D1 lanes 0..63) and the D1c part of P.  D1 column of (row r,
@@ -691,7 +704,7 @@ __device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const C
     __syncthreads();
 
     // ---- second product: W^T = X^T T^T, U'^T = (Y + Ylo)^T T^T
-    if (issuer(tid) >= 0) issue_second(sm, tmem, issuer(tid), &ms.bar);
+    if (issuer(tid) >= 0) issue_second<ISSUE_UNROLL>(sm, tmem, issuer(tid), &ms.bar);
     if (!wait_mma(ms, ph, a.dev_status)) return false;
     return true;
 }
@@ -727,6 +740,7 @@ __device__ __forceinline__ void store_neg_w(unsigned char* sm, uint32_t o_nw, ui
 
 // third product: U^T = U'^T - (S_hi + S_lo)^T W^T ; O^T = S^T (Q o e^G)^T (split).
 // Issuer q: U^T (q < 2) or O^T (q >= 2), chunk rows [32 (q & 1), +32).
+template <int UNR>
 __device__ __forceinline__ void issue_third(unsigned char* sm, uint32_t tmem, int q, uint32_t o_nw, uint32_t o_qe,
                                             uint32_t o_qel, uint32_t c_ut, uint32_t c_st, uint32_t c_sl,
                                             uint32_t c_ot, uint64_t* bar)
@@ -736,7 +750,7 @@ __device__ __forceinline__ void issue_third(unsigned char* sm, uint32_t tmem, in
     const uint32_t hr = (q & 1) * 32, ho = (hr * 128) >> 4;  // N-half: TMEM columns, tile rows
     if (q < 2) {
         const uint64_t dnw = dsc(sm, o_nw) + ho;
-#pragma unroll 4
+#pragma unroll UNR
         for (int ks = 0; ks < 16; ++ks) {
             const uint32_t kb = ((ks >> 2) * T64_KB + (ks & 3) * 32) >> 4;
             ptx::mma_tf32_ts(tmem + c_ut + hr, tmem + c_st + ks * 8, dnw + kb, id, 1);
@@ -744,7 +758,7 @@ __device__ __forceinline__ void issue_third(unsigned char* sm, uint32_t tmem, in
         }
     } else {
         const uint64_t dqe = dsc(sm, o_qe) + ho, dql = dsc(sm, o_qel) + ho;
-#pragma unroll 4
+#pragma unroll UNR
         for (int ks = 0; ks < 16; ++ks) {
             const uint32_t kb = ((ks >> 2) * T64_KB + (ks & 3) * 32) >> 4;
             ptx::mma_tf32_ts(tmem + c_ot + hr, tmem + c_st + ks * 8, dqe + kb, id, ks > 0);
@@ -783,6 +797,7 @@ __device__ __forceinline__ void rescale_split(uint32_t t_st, uint32_t t_ut, uint
 
 // fourth product: O^T += U^T P^T ; S^T += U^T (K o e^{G_C - G}) (both split).
 // Issuer q: O^T chunk rows [32 q, +32) (q < 2) or S^T key dims [64 (q & 1), +64).
+template <int UNR>
 __device__ __forceinline__ void issue_fourth(unsigned char* sm, uint32_t tmem, int q, uint32_t o_ph, uint32_t o_pl,
                                              uint32_t o_kd, uint32_t o_kdl, uint32_t c_ut, uint32_t c_ul,
                                              uint32_t c_st, uint32_t c_ot, uint64_t* bar)
@@ -791,7 +806,7 @@ __device__ __forceinline__ void issue_fourth(unsigned char* sm, uint32_t tmem, i
     if (q < 2) {
         const uint32_t id = ptx::idesc_tf32(128, 32), hr = q * 32, ho = (hr * 128) >> 4;
         const uint64_t dph = dsc(sm, o_ph) + ho, dpl = dsc(sm, o_pl) + ho;
-#pragma unroll 4
+#pragma unroll UNR
         for (int ks = 0; ks < 8; ++ks) {
             const uint32_t kb = ((ks >> 2) * T64_KB + (ks & 3) * 32) >> 4;
             ptx::mma_tf32_ts(tmem + c_ot + hr, tmem + c_ut + ks * 8, dph + kb, id, 1);
@@ -801,7 +816,7 @@ __device__ __forceinline__ void issue_fourth(unsigned char* sm, uint32_t tmem, i
     } else {
         const uint32_t id = ptx::idesc_tf32(128, 64), hr = (q & 1) * 64, ho = (hr * 128) >> 4;
         const uint64_t dkd = dsc(sm, o_kd) + ho, dkl = dsc(sm, o_kdl) + ho;
-#pragma unroll 4
+#pragma unroll UNR
         for (int ks = 0; ks < 8; ++ks) {
             const uint32_t kb = ((ks >> 2) * 128 * 128 + (ks & 3) * 32) >> 4;
             ptx::mma_tf32_ts(tmem + c_st + hr, tmem + c_ut + ks * 8, dkd + kb, id, 1);
@@ -1068,7 +1083,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
         __syncthreads();
 
         if (issuer(tid) >= 0)
-            issue_third(sm, tmem, issuer(tid), SM_NW, SM_QE, SM_QEL, TM_UT, TM_ST, TM_SL, TM_OT, &ms.bar);
+            issue_third<ISSUE_UNROLL>(sm, tmem, issuer(tid), SM_NW, SM_QE, SM_QEL, TM_UT, TM_ST, TM_SL, TM_OT, &ms.bar);
         if (!wait_mma(ms, ph, a.dev_status)) break;
 
         // the raw staging region is free from here: prefetch the next chunk's rows
@@ -1084,7 +1099,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
         __syncthreads();
 
         if (issuer(tid) >= 0)
-            issue_fourth(sm, tmem, issuer(tid), SM_PH, SM_PL, SM_KD, SM_KDL, TM_UT, TM_UL, TM_ST, TM_OT, &ms.bar);
+            issue_fourth<ISSUE_UNROLL>(sm, tmem, issuer(tid), SM_PH, SM_PL, SM_KD, SM_KDL, TM_UT, TM_UL, TM_ST, TM_OT, &ms.bar);
         uint32_t gp[RPT / 2];
         load_gate_bits(gp, a, c0, r0, nvalid, h, col);  // while the product runs
         if (!wait_mma(ms, ph, a.dev_status)) break;
@@ -1306,9 +1321,11 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         if (tid < D) gam = reinterpret_cast<const float*>(src + SL_GAM)[tid];
     };
 
-    // The outputs of chunk c are written while the third product of chunk c + 1
-    // runs (O^T alternates between two TMEM column blocks), and chunk c + 1's
-    // slot is acquired and its U'^T loaded meanwhile too.
+    // The outputs of chunk c are formed while the products of chunk c + 1 run
+    // (O^T alternates between two TMEM column blocks): O^T is read and the norm
+    // partials formed while the third product runs, the norm and the stores
+    // while the fourth runs, whose issuers have half the MMAs.  Chunk c + 1's
+    // slot is acquired and its U'^T loaded during the third product too.
     bool mma_pending = false;
     acquire_by(0, 0);
     __syncthreads();
@@ -1338,9 +1355,6 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         ptx::tmem_st16(tmem + lane_base + CT_UT + RPT * qq, up);
         if (tid < D) ms.gamma[tid] = gam;
         state_low(tmem + lane_base + CT_ST + 32 * qq, tmem + lane_base + CT_SL + 32 * qq);
-        // the previous chunk's outputs, first part (its block barrier is the one below)
-        float o[RPT];
-        if (have_prev) write_outputs_a(ms, a, tmem + lane_base + (c_ot ^ (CT_OT0 ^ CT_OT1)) + RPT * qq, o);
         if (tid == 0 && !ptx::mbar_wait(&ms.rbar, c & 1)) {
             ms.err = 1;
             flag_status(a.dev_status, KDA_DEV_TIMEOUT);
@@ -1351,16 +1365,15 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         pend_a = false;
         if (issuer(tid) >= 0) {
             (void)ptx::mbar_try_wait(&ms.rbar, c & 1);  // completed: the tiles are visible to this issuer
-            issue_third(sm, tmem, issuer(tid), SL_NW, SL_QE, SL_QEL, CT_UT, CT_ST, CT_SL, c_ot, &ms.bar);
+            issue_third<CHAIN_UNROLL>(sm, tmem, issuer(tid), SL_NW, SL_QE, SL_QEL, CT_UT, CT_ST, CT_SL, c_ot, &ms.bar);
         }
         mma_pending = true;
-        // while the third product runs: chunk c + 1's slot, the rest of the previous
-        // chunk's outputs (warp-local: the issuing warps join when they are done)
+        // while the third product runs: the previous chunk's O^T and norm
+        // partials (the barrier of the wait below orders them before part B),
+        // chunk c + 1's slot and U'^T
+        float o[RPT];
+        if (have_prev) write_outputs_a(ms, a, tmem + lane_base + (c_ot ^ (CT_OT0 ^ CT_OT1)) + RPT * qq, o);
         if (c + 1 < nchunks) acquire_by(c + 1, 128);
-        if (have_prev) {
-            write_outputs_b(ms, a, o, gp, prev_c0, prev_nvalid, h, nw);
-            have_prev = false;
-        }
         __syncthreads();
         if (ms.err) break;
         if (c + 1 < nchunks) load_ut(c + 1);
@@ -1388,9 +1401,15 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         pend_b = false;
         if (issuer(tid) >= 0) {
             (void)ptx::mbar_try_wait(&ms.bbar, c & 1);
-            issue_fourth(sm, tmem, issuer(tid), SL_PH, SL_PL, SL_KD, SL_KDL, CT_UT, CT_UL, CT_ST, c_ot, &ms.bar);
+            issue_fourth<CHAIN_UNROLL>(sm, tmem, issuer(tid), SL_PH, SL_PL, SL_KD, SL_KDL, CT_UT, CT_UL, CT_ST, c_ot, &ms.bar);
         }
         mma_pending = true;
+        // while the fourth product runs: the rest of the previous chunk's outputs
+        // (warp-local), then chunk c's output gate
+        if (have_prev) {
+            write_outputs_b(ms, a, o, gp, prev_c0, prev_nvalid, h, nw);
+            have_prev = false;
+        }
         gate_bits_from_words(gp, gw, col);
         if (c + 1 < nchunks) load_gate(c + 1);
         // chunk c's slot is read (both tile copies have landed, U'^T and e^{G_C}
