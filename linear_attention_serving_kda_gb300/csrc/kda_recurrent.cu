@@ -322,6 +322,87 @@ template <int D> __device__ __forceinline__ float row_update(const RowSmem<D>& s
 }
 
 // ------------------------------------------------------------------------
+// Staged window rows.  A verify window's draft rows (q, k, v, gate f, output
+// gate g) are copied into shared memory in blocks of VWB rows with 16-byte
+// cp.async pieces, the next block while the current one runs, so no row of
+// the window waits on a global load; a commit's log rows (alpha | k^ | u) are
+// staged the same way before they are replayed.  The values are the ones the
+// per-row global loads would read, so the arithmetic and its bits are
+// unchanged.
+
+constexpr int VWB = 8;  // window rows per staged block
+
+template <int D, typename IO> struct VerBuf {
+    IO rows[VWB][5][D];  // q, k, v, f, g of each row of the block
+    float bv[VWB];       // beta logits
+};
+
+template <int D, typename IO> struct VerSmem {
+    VerBuf<D, IO> buf[2];      // double-buffered blocks
+    float plog[VWB][3 * D];    // a block of log rows to replay (commit)
+};
+
+// Issue the copies of window rows [t0, t0 + nr) of unit (seq, h) into vb (all
+// threads; one commit group).  The beta logits are returned as raw values of
+// the threads tid < nr, to be written into vb.bv when the block is published,
+// so no thread waits on their load here.
+template <int D, typename IO>
+__device__ __forceinline__ IO stage_window_rows(VerBuf<D, IO>& vb, const RecArgs& a, int seq, int h, int t0, int nr)
+{
+    constexpr int EPP = 16 / (int)sizeof(IO);  // elements per 16-byte piece
+    constexpr int PIECES = D / EPP;            // pieces per row
+    const int ntens = a.g != nullptr ? 5 : 4;
+    for (int idx = threadIdx.x; idx < nr * ntens * PIECES; idx += REC_THREADS) {
+        const int piece = idx % PIECES, rest = idx / PIECES, tens = rest % ntens, r = rest / ntens;
+        const size_t rh = ((size_t)seq * a.W + t0 + r) * a.H + h;
+        const void* base = tens == 0 ? a.q : tens == 1 ? a.k : tens == 2 ? a.v : tens == 3 ? a.f : a.g;
+        ptx::cp_async16(&vb.rows[r][tens][piece * EPP], static_cast<const IO*>(base) + rh * D + piece * EPP, 16);
+    }
+    ptx::cp_async_commit();
+    const IO* b = static_cast<const IO*>(a.b);
+    IO braw{};
+    if (threadIdx.x < nr) braw = b[((size_t)seq * a.W + t0 + threadIdx.x) * a.H + h];
+    return braw;
+}
+
+// Issue the copies of log rows [t0, t0 + nr) (alpha | k^ | u, fp32) of unit
+// (seq, h) into plog (all threads; one commit group).
+template <int D>
+__device__ __forceinline__ void stage_log_rows(float (&plog)[VWB][3 * D], const float* log_f, int W, int H, int seq,
+                                               int h, int t0, int nr)
+{
+    constexpr int PIECES = 3 * D / 4;
+    for (int idx = threadIdx.x; idx < nr * PIECES; idx += REC_THREADS) {
+        const int piece = idx % PIECES, r = idx / PIECES;
+        ptx::cp_async16(&plog[r][piece * 4], log_f + (((size_t)seq * W + t0 + r) * H + h) * (3 * D) + piece * 4, 16);
+    }
+    ptx::cp_async_commit();
+}
+
+// Replay staged log rows [0, nr) onto this thread's part of the state:
+// S <- fma(k^, u, alpha * S), the expression of the decoded row.
+template <int D>
+__device__ __forceinline__ void replay_log_rows(const float (&plog)[VWB][3 * D], int nr,
+                                                float (&s)[RecShape<D>::RPW][RecShape<D>::CPT])
+{
+    constexpr int RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r0 = warp * RPW, c0 = lane * CPT;
+    for (int t = 0; t < nr; ++t) {
+        const float* lg = plog[t];
+        float uc[CPT];
+#pragma unroll
+        for (int cc = 0; cc < CPT; ++cc) uc[cc] = lg[2 * D + c0 + cc];
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr) {
+            const float ai = lg[r0 + rr], ki = lg[D + r0 + rr];
+#pragma unroll
+            for (int cc = 0; cc < CPT; ++cc) s[rr][cc] = __fmaf_rn(ki, uc[cc], __fmul_rn(ai, s[rr][cc]));
+        }
+    }
+}
+
+// ------------------------------------------------------------------------
 // Register kernel: one CTA per unit, all of the unit's rows.
 
 template <int D, typename IO, int MODE>
@@ -366,7 +447,17 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_recurrent_kernel(const Rec
         }
     }
 
-    // State tile first: its HBM stream overlaps the row preparation below.
+    constexpr bool WINDOW = MODE == REC_VERIFY || MODE == REC_COMMIT_VERIFY;
+    extern __shared__ __align__(16) unsigned char rec_dyn_smem[];
+    VerSmem<D, IO>& vs = *reinterpret_cast<VerSmem<D, IO>*>(rec_dyn_smem);  // window modes only
+    // Staged copies first (the previous window's log rows to commit, then the
+    // first block of this window's rows), then the state tile: all in flight together.
+    const int nblk = WINDOW ? (L + VWB - 1) / VWB : 0;
+    IO bnext{};  // beta logit (raw) of row tid of the next staged block
+    if (MODE == REC_COMMIT_VERIFY && acc > 0)
+        stage_log_rows<D>(vs.plog, a.prev_log_f, a.W, H, seq, h, 0, min(acc, VWB));
+    if (WINDOW) bnext = stage_window_rows<D, IO>(vs.buf[0], a, seq, h, 0, min(L, VWB));
+
     float* Sg = a.rec_state + ((size_t)slot * H + h) * D * D;
     const int r0 = warp * RPW, c0 = lane * CPT;
     float s[RPW][CPT];
@@ -374,17 +465,17 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_recurrent_kernel(const Rec
     if (MODE == REC_COMMIT_VERIFY && acc > 0) {
         // commit: the same replay expression as kda_commit_kernel, so the
         // committed state has the bits of `acc` serial decodes
-        for (int t = 0; t < acc; ++t) {
-            const float* lg = a.prev_log_f + (((size_t)seq * a.W + t) * H + h) * (3 * D);
-            float uc[CPT];
-#pragma unroll
-            for (int cc = 0; cc < CPT; ++cc) uc[cc] = lg[2 * D + c0 + cc];
-#pragma unroll
-            for (int rr = 0; rr < RPW; ++rr) {
-                const float ai = lg[r0 + rr], ki = lg[D + r0 + rr];
-#pragma unroll
-                for (int cc = 0; cc < CPT; ++cc) s[rr][cc] = __fmaf_rn(ki, uc[cc], __fmul_rn(ai, s[rr][cc]));
+        for (int t0 = 0; t0 < acc; t0 += VWB) {
+            const int nr = min(VWB, acc - t0);
+            if (t0 == 0) {
+                ptx::cp_async_wait_prev();  // the log rows (the window rows may still be in flight)
+            } else {
+                stage_log_rows<D>(vs.plog, a.prev_log_f, a.W, H, seq, h, t0, nr);
+                ptx::cp_async_wait_all();
             }
+            __syncthreads();
+            replay_log_rows<D>(vs.plog, nr, s);
+            __syncthreads();  // plog may be refilled
         }
         store_tile<D>(Sg, r0, c0, s);
     }
@@ -426,16 +517,36 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_recurrent_kernel(const Rec
         const size_t row = (size_t)row0 + t;
         const size_t rh = row * H + h;
         const int cur = ring(t);
-        for (int c = tid; c < 3 * D; c += REC_THREADS) {
-            float x;
-            if (c < D) x = ldv(q + rh * D + c);
-            else if (c < 2 * D) x = ldv(k + rh * D + (c - D));
-            else x = ldv(v + rh * D + (c - 2 * D));
-            sm.win[cur][c] = x;
+        float bval, gval;
+        if constexpr (WINDOW) {
+            // rows of the window from the staged block (t / VWB)
+            const int blk = t / VWB, r = t % VWB;
+            VerBuf<D, IO>& vb = vs.buf[blk & 1];
+            if (r == 0) {
+                if (tid < min(VWB, L - blk * VWB)) vb.bv[tid] = Io<IO>::ld(&bnext);
+                ptx::cp_async_wait_all();
+                __syncthreads();
+                // the other buffer's rows are done: prefetch the next block into it
+                if (blk + 1 < nblk)
+                    bnext = stage_window_rows<D, IO>(vs.buf[(blk + 1) & 1], a, seq, h, (blk + 1) * VWB,
+                                                     min(VWB, L - (blk + 1) * VWB));
+            }
+            for (int c = tid; c < 3 * D; c += REC_THREADS) sm.win[cur][c] = ldv(&vb.rows[r][c / D][c % D]);
+            for (int i = tid; i < D; i += REC_THREADS) sm.fr[i] = ldv(&vb.rows[r][3][i]);
+            bval = vb.bv[r];
+            gval = (g != nullptr && tid < D) ? ldv(&vb.rows[r][4][tid]) : 0.0f;
+        } else {
+            for (int c = tid; c < 3 * D; c += REC_THREADS) {
+                float x;
+                if (c < D) x = ldv(q + rh * D + c);
+                else if (c < 2 * D) x = ldv(k + rh * D + (c - D));
+                else x = ldv(v + rh * D + (c - 2 * D));
+                sm.win[cur][c] = x;
+            }
+            for (int i = tid; i < D; i += REC_THREADS) sm.fr[i] = ldv(f + rh * D + i);
+            bval = ldv(b + rh);
+            gval = (g != nullptr && tid < D) ? ldv(g + rh * D + tid) : 0.0f;
         }
-        for (int i = tid; i < D; i += REC_THREADS) sm.fr[i] = ldv(f + rh * D + i);
-        const float bval = ldv(b + rh);
-        const float gval = (g != nullptr && tid < D) ? ldv(g + rh * D + tid) : 0.0f;
         __syncthreads();
 
         const float o = row_step<D>(sm, s, t, K, rc, bval, gval, g != nullptr);
@@ -688,21 +799,20 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_commit_kernel(const Commit
     }
     if (acc == 0) return;
 
+    // the log rows to replay, staged in blocks of VWB (the first in flight with the state loads)
+    __shared__ __align__(16) float plog[VWB][3 * D];
+    stage_log_rows<D>(plog, a.log_f, W, H, seq, h, 0, min(acc, VWB));
     float* Sg = a.rec_state + ((size_t)slot * H + h) * D * D;
     const int r0 = warp * RPW, c0 = lane * CPT;
     float s[RPW][CPT];
     load_tile<D>(Sg, r0, c0, s);
-    for (int t = 0; t < acc; ++t) {
-        const float* lg = a.log_f + (((size_t)seq * W + t) * H + h) * (3 * D);
-        float uc[CPT];
-#pragma unroll
-        for (int cc = 0; cc < CPT; ++cc) uc[cc] = lg[2 * D + c0 + cc];
-#pragma unroll
-        for (int rr = 0; rr < RPW; ++rr) {
-            const float ai = lg[r0 + rr], ki = lg[D + r0 + rr];
-#pragma unroll
-            for (int cc = 0; cc < CPT; ++cc) s[rr][cc] = __fmaf_rn(ki, uc[cc], __fmul_rn(ai, s[rr][cc]));
-        }
+    for (int t0 = 0; t0 < acc; t0 += VWB) {
+        const int nr = min(VWB, acc - t0);
+        if (t0 > 0) stage_log_rows<D>(plog, a.log_f, W, H, seq, h, t0, nr);
+        ptx::cp_async_wait_all();
+        __syncthreads();
+        replay_log_rows<D>(plog, nr, s);
+        __syncthreads();  // plog may be refilled
     }
     store_tile<D>(Sg, r0, c0, s);
 
@@ -772,14 +882,31 @@ template <typename IO> static cudaError_t launch_decode_stream(const RecArgs& a,
     return cudaLaunchKernelEx(&cfg, kda_decode_stream_kernel<IO>, a);
 }
 
+// The window modes stage rows in dynamic shared memory (VerSmem).
+template <int D, typename IO, int MODE> static cudaError_t launch_window(const RecArgs& a, int units, cudaStream_t st)
+{
+    static bool attr_done[128];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int smem = (int)sizeof(VerSmem<D, IO>);
+    if (dev >= 0 && dev < 128 && !attr_done[dev]) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kda_recurrent_kernel<D, IO, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    kda_recurrent_kernel<D, IO, MODE><<<dim3(units), dim3(REC_THREADS), smem, st>>>(a);
+    return cudaGetLastError();
+}
+
 template <int D, typename IO>
 static cudaError_t launch_rec_d(int mode, const RecArgs& a, int units, cudaStream_t st)
 {
     dim3 grid(units), block(REC_THREADS);
     if (mode == REC_PREFILL) kda_recurrent_kernel<D, IO, REC_PREFILL><<<grid, block, 0, st>>>(a);
     else if (mode == REC_DECODE) kda_recurrent_kernel<D, IO, REC_DECODE><<<grid, block, 0, st>>>(a);
-    else if (mode == REC_VERIFY) kda_recurrent_kernel<D, IO, REC_VERIFY><<<grid, block, 0, st>>>(a);
-    else kda_recurrent_kernel<D, IO, REC_COMMIT_VERIFY><<<grid, block, 0, st>>>(a);
+    else if (mode == REC_VERIFY) return launch_window<D, IO, REC_VERIFY>(a, units, st);
+    else return launch_window<D, IO, REC_COMMIT_VERIFY>(a, units, st);
     return cudaGetLastError();
 }
 
