@@ -776,6 +776,340 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) kda_decode_stream_kernel(const
 }
 
 // ------------------------------------------------------------------------
+// Verify window at dk = dv = 128 with warp-local rows.
+//
+// The register kernel's thread tiles (16 key dims x 4 value dims, the key
+// dims of tile (m, .) being [16m, 16m + 16)) are assigned so that the eight
+// tiles of a value-dim block share a warp: warp w holds value dims [16w, +16),
+// lane l = 4m + c key dims [16m, +16) of value dims [16w + 4c, +4).  Each
+// thread forms the register kernel's partial sums of S'^T k and S^T q over its
+// 16 key dims, and their sum over the eight key-dim blocks -- in block order,
+// as the register kernel sums its warps -- is read back from a per-warp
+// scratch after a warp barrier.  So a row needs no block barrier.  The parts of
+// a row that do not depend on the state (conv, SiLU, sums of squares, decay)
+// run for a staged block of rows at a time before its rows, and the gated norm
+// after them.  Every value is formed by the register kernel's expressions in
+// its order, so verified rows, their log and the committed states have the
+// bits of decoded rows.
+
+constexpr int VWD = 128;
+
+template <typename IO> struct VwBuf {
+    IO rows[VWB][5][VWD];   // q, k, v, f, g of each row of the block
+    IO halo[3][3][VWD];     // raw q|k|v rows 3, 2, 1 before the block (before the window: the conv history)
+    float bv[VWB];          // beta logits
+};
+
+template <typename IO> struct VwSmem {
+    VwBuf<IO> buf[2];                 // double-buffered staged blocks
+    float plog[VWB][3 * VWD];         // log rows to replay (commit first)
+    float cw[3 * VWD][4];             // conv taps (4-tap form, oldest first)
+    float dtb[VWD];                   // dt_bias of this head
+    float act[VWB][3 * VWD];          // post-SiLU q', k', v' of the block's rows
+    float alpha[VWB][VWD];            // decays of the block's rows
+    float nrm[VWB][8];                // per-32-channel sums of squares of q', k'
+    float o[VWB][VWD];                // outputs before the gated norm
+    float esum[VWB][4];               // gated norm: per-32-column sums of squares
+    float red[REC_WARPS][8][16];      // per-warp scratch: [key block][value dim] partials of S'^T k
+    float red2[REC_WARPS][8][16];     // the same for S^T q
+};
+
+// Source of history row r (0 = oldest of the K-1) of the conv state the
+// window starts from: the stored conv state, or -- after committing `acc`
+// rows of the previous window -- its last K-1 rows of [old state; accepted rows].
+template <typename IO>
+__device__ __forceinline__ const IO* vw_hist_row(const RecArgs& a, int seq, int slot, int acc, int r, int seg, int h)
+{
+    const int K = a.K, conv_dim = 3 * a.H * VWD;
+    const int src = acc - (K - 1) + r;  // previous window row, or < 0: old state row src + K - 1
+    const size_t chan = (size_t)seg * a.H * VWD + (size_t)h * VWD;
+    if (src >= 0) return static_cast<const IO*>(a.prev_log_raw) + ((size_t)seq * a.W + src) * conv_dim + chan;
+    return static_cast<const IO*>(a.conv_state) + ((size_t)slot * (K - 1) + src + K - 1) * conv_dim + chan;
+}
+
+// Issue the copies of window rows [t0, t0 + nr) and of the three raw rows
+// before them (all threads; one commit group).  Returns the raw beta logit of
+// row t0 + tid (tid < nr), to be published in vb.bv with the block.
+template <typename IO>
+__device__ __forceinline__ IO vw_stage(VwBuf<IO>& vb, const RecArgs& a, int seq, int h, int slot, int acc, int t0,
+                                       int nr)
+{
+    constexpr int EPP = 16 / (int)sizeof(IO), PIECES = VWD / EPP;
+    const int ntens = a.g != nullptr ? 5 : 4;
+    for (int idx = threadIdx.x; idx < nr * ntens * PIECES; idx += REC_THREADS) {
+        const int piece = idx % PIECES, rest = idx / PIECES, tens = rest % ntens, r = rest / ntens;
+        const size_t rh = ((size_t)seq * a.W + t0 + r) * a.H + h;
+        const void* base = tens == 0 ? a.q : tens == 1 ? a.k : tens == 2 ? a.v : tens == 3 ? a.f : a.g;
+        ptx::cp_async16(&vb.rows[r][tens][piece * EPP], static_cast<const IO*>(base) + rh * VWD + piece * EPP, 16);
+    }
+    for (int idx = threadIdx.x; idx < 9 * PIECES; idx += REC_THREADS) {
+        const int piece = idx % PIECES, seg = (idx / PIECES) % 3, hr = idx / (3 * PIECES);
+        const int x = t0 - 3 + hr;  // window row of this halo row
+        const IO* src;
+        if (x >= 0) {
+            const void* base = seg == 0 ? a.q : seg == 1 ? a.k : a.v;
+            src = static_cast<const IO*>(base) + (((size_t)seq * a.W + x) * a.H + h) * VWD;
+        } else {
+            const int r = x + a.K - 1;  // history row; r < 0: a tap the conv does not have
+            if (r < 0) continue;
+            src = vw_hist_row<IO>(a, seq, slot, acc, r, seg, h);
+        }
+        ptx::cp_async16(&vb.halo[hr][seg][piece * EPP], src + piece * EPP, 16);
+    }
+    ptx::cp_async_commit();
+    const IO* b = static_cast<const IO*>(a.b);
+    IO braw{};
+    if (threadIdx.x < nr) braw = b[((size_t)seq * a.W + t0 + threadIdx.x) * a.H + h];
+    return braw;
+}
+
+template <typename IO, int MODE>
+__global__ void __launch_bounds__(REC_THREADS, 2) kda_verify_warp_kernel(const RecArgs a)
+{
+    extern __shared__ __align__(16) unsigned char vw_dyn_smem[];
+    VwSmem<IO>& sm = *reinterpret_cast<VwSmem<IO>*>(vw_dyn_smem);
+    constexpr int D = VWD, RPW = 16, CPT = 4, EPP = 16 / (int)sizeof(IO);
+    constexpr bool CV = MODE == REC_COMMIT_VERIFY;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int m = lane >> 2, cq = lane & 3;
+    const int r0 = RPW * m, c0 = 16 * warp + CPT * cq;  // this thread's tile: key dims [r0, +16), value dims [c0, +4)
+    const int H = a.H, K = a.K, W = a.W;
+    const int seq = blockIdx.x / H, h = blockIdx.x % H;
+    const int conv_dim = 3 * H * D;
+    const bool has_g = a.g != nullptr;
+
+    const int slot = a.slots ? a.slots[seq] : seq;
+    if (slot < 0) return;  // padding sequence: nothing to do
+    if (slot >= a.num_slots) {
+        if (tid == 0) flag_status(a.dev_status, KDA_DEV_BAD_SLOT);
+        return;
+    }
+    int acc = 0;  // commit first: rows of the previous window to replay
+    if (CV) {
+        acc = a.accepted[seq];
+        if (acc < 0 || acc > W) {
+            if (tid == 0 && h == 0) flag_status(a.dev_status, KDA_DEV_BAD_ACCEPTED);
+            return;
+        }
+    }
+
+    // staged copies first (the log rows to commit, the first block of rows with
+    // the conv history before it), then the parameters and the state tile
+    const int nblk = (W + VWB - 1) / VWB;
+    if (CV && acc > 0) stage_log_rows<D>(sm.plog, a.prev_log_f, W, H, seq, h, 0, min(acc, VWB));
+    IO bnext = vw_stage<IO>(sm.buf[0], a, seq, h, slot, acc, 0, min(W, VWB));
+    for (int c = tid; c < 3 * D; c += REC_THREADS) {
+        const int ch = conv_channel<D>(c, h, H);
+        for (int j = 0; j < K; ++j) sm.cw[c][j] = a.conv_w[(size_t)ch * K + j];
+    }
+    for (int i = tid; i < D; i += REC_THREADS) sm.dtb[i] = a.dt_bias[(size_t)h * D + i];
+    const RowConst rc{a.gate_mode, a.lb, expf(a.A_log[h]), a.l2_eps, a.norm_eps, a.scale, a.norm_w};
+
+    float* Sg = a.rec_state + ((size_t)slot * H + h) * D * D;
+    float s[RPW][CPT];
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) {
+        const float4 x = ld_stream4(Sg + (size_t)(r0 + rr) * D + c0);
+        s[rr][0] = x.x; s[rr][1] = x.y; s[rr][2] = x.z; s[rr][3] = x.w;
+    }
+    if (CV && acc > 0) {
+        // commit: S <- fma(k^, u, alpha * S) per logged row, the decoded row's expression
+        for (int t0 = 0; t0 < acc; t0 += VWB) {
+            const int nr = min(VWB, acc - t0);
+            if (t0 == 0) {
+                ptx::cp_async_wait_prev();  // the log rows; the window rows may still be in flight
+            } else {
+                stage_log_rows<D>(sm.plog, a.prev_log_f, W, H, seq, h, t0, nr);
+                ptx::cp_async_wait_all();
+            }
+            __syncthreads();
+            for (int t = 0; t < nr; ++t) {
+                const float* lg = sm.plog[t];
+                const float4 u4 = *reinterpret_cast<const float4*>(lg + 2 * D + c0);
+                const float uc[CPT] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+                for (int rr = 0; rr < RPW; ++rr) {
+                    const float ai = lg[r0 + rr], ki = lg[D + r0 + rr];
+#pragma unroll
+                    for (int cc = 0; cc < CPT; ++cc) s[rr][cc] = __fmaf_rn(ki, uc[cc], __fmul_rn(ai, s[rr][cc]));
+                }
+            }
+            __syncthreads();  // plog may be refilled
+        }
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr)
+            st_stream4(Sg + (size_t)(r0 + rr) * D + c0, make_float4(s[rr][0], s[rr][1], s[rr][2], s[rr][3]));
+    }
+
+    IO* cs = static_cast<IO*>(a.conv_state);
+    IO* lraw = static_cast<IO*>(a.log_raw);
+    for (int blk = 0; blk < nblk; ++blk) {
+        const int t0 = blk * VWB, nr = min(VWB, W - t0);
+        VwBuf<IO>& vb = sm.buf[blk & 1];
+        if (tid < nr) vb.bv[tid] = Io<IO>::ld(&bnext);
+        ptx::cp_async_wait_all();
+        __syncthreads();  // the block is staged; the previous block (rows, epilogue) is done
+        if (blk + 1 < nblk) bnext = vw_stage<IO>(sm.buf[(blk + 1) & 1], a, seq, h, slot, acc, t0 + VWB, min(VWB, W - t0 - VWB));
+
+        if (CV && blk == 0 && acc > 0) {
+            // the committed conv state: the history rows the window starts from
+            for (int idx = tid; idx < 3 * (K - 1) * (D / EPP); idx += REC_THREADS) {
+                const int piece = idx % (D / EPP), seg = (idx / (D / EPP)) % 3, r = idx / (3 * (D / EPP));
+                *reinterpret_cast<int4*>(cs + ((size_t)slot * (K - 1) + r) * conv_dim + (size_t)seg * H * D + h * D +
+                                         piece * EPP) =
+                    *reinterpret_cast<const int4*>(&vb.halo[r + 4 - K][seg][piece * EPP]);
+            }
+        }
+        // the raw q|k|v rows of the window into the log
+        for (int idx = tid; idx < nr * 3 * (D / EPP); idx += REC_THREADS) {
+            const int piece = idx % (D / EPP), seg = (idx / (D / EPP)) % 3, t = idx / (3 * (D / EPP));
+            *reinterpret_cast<int4*>(lraw + ((size_t)seq * W + t0 + t) * conv_dim + (size_t)seg * H * D + h * D +
+                                     piece * EPP) = *reinterpret_cast<const int4*>(&vb.rows[t][seg][piece * EPP]);
+        }
+        // ---- state-independent part of the block's rows (the register kernel's row_conv)
+        for (int e = tid; e < nr * 4 * D; e += REC_THREADS) {
+            const int t = e / (4 * D), it = e % (4 * D);
+            if (it < 3 * D) {
+                const int seg = it / D, ch = it % D;
+                float accv = 0.0f;
+                for (int j = 0; j < K; ++j) {
+                    const int xl = t - K + 1 + j;  // raw row of tap j, relative to the block's first row
+                    const float xv = xl >= 0 ? ldv(&vb.rows[xl][seg][ch]) : ldv(&vb.halo[xl + 3][seg][ch]);
+                    accv = __fmaf_rn(sm.cw[it][j], xv, accv);
+                }
+                const float x = siluf_(accv);
+                sm.act[t][it] = x;
+                if (it < 2 * D) {  // warp-uniform: 32 consecutive channels of one row
+                    const float ss = warp_sum(x * x);
+                    if (lane == 0) sm.nrm[t][it >> 5] = ss;
+                }
+            } else {
+                const int i = it - 3 * D;
+                sm.alpha[t][i] = __expf(log_alpha(rc.gate_mode, rc.lb, rc.ea, ldv(&vb.rows[t][3][i]), sm.dtb[i]));
+            }
+        }
+        __syncthreads();
+        // decay and normalised key of each row into the log
+        for (int e = tid; e < nr * D; e += REC_THREADS) {
+            const int t = e / D, i = e % D;
+            float sk = 0.0f;
+#pragma unroll
+            for (int p = 0; p < D / 32; ++p) sk += sm.nrm[t][D / 32 + p];
+            const float rk = rsqrtf(sk + rc.l2_eps);
+            float* lg = a.log_f + (((size_t)seq * W + t0 + t) * H + h) * (3 * D);
+            lg[i] = sm.alpha[t][i];
+            lg[D + i] = sm.act[t][D + i] * rk;
+        }
+
+        // ---- the rows: the delta rule on the register state, sums inside the warp
+        for (int t = 0; t < nr; ++t) {
+            float sq = 0.0f, sk = 0.0f;
+#pragma unroll
+            for (int p = 0; p < D / 32; ++p) {
+                sq += sm.nrm[t][p];
+                sk += sm.nrm[t][D / 32 + p];
+            }
+            const float rq = rsqrtf(sq + rc.l2_eps);
+            const float rk = rsqrtf(sk + rc.l2_eps);
+            const float beta = sigmoidf_(vb.bv[t]);
+            float kr[RPW], part[CPT];
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr) kr[rr] = sm.act[t][D + r0 + rr] * rk;
+#pragma unroll
+            for (int cc = 0; cc < CPT; ++cc) part[cc] = 0.0f;
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr) {
+                const float ai = sm.alpha[t][r0 + rr];
+#pragma unroll
+                for (int cc = 0; cc < CPT; cc += 2) {
+                    const float2 sp = __fmul2_rn(make_float2(ai, ai), make_float2(s[rr][cc], s[rr][cc + 1]));
+                    const float2 pp = __ffma2_rn(sp, make_float2(kr[rr], kr[rr]), make_float2(part[cc], part[cc + 1]));
+                    s[rr][cc] = sp.x;
+                    s[rr][cc + 1] = sp.y;
+                    part[cc] = pp.x;
+                    part[cc + 1] = pp.y;
+                }
+            }
+            *reinterpret_cast<float4*>(&sm.red[warp][m][CPT * cq]) = make_float4(part[0], part[1], part[2], part[3]);
+            __syncwarp();
+            float kv[CPT] = {0.0f, 0.0f, 0.0f, 0.0f}, uc[CPT];
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb) {  // key-dim blocks in order
+                const float4 r4 = *reinterpret_cast<const float4*>(&sm.red[warp][mb][CPT * cq]);
+                kv[0] += r4.x;
+                kv[1] += r4.y;
+                kv[2] += r4.z;
+                kv[3] += r4.w;
+            }
+#pragma unroll
+            for (int cc = 0; cc < CPT; ++cc) {
+                uc[cc] = beta * (sm.act[t][2 * D + c0 + cc] - kv[cc]);
+                part[cc] = 0.0f;
+            }
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr) {
+                const float qi = sm.act[t][r0 + rr] * rq;
+#pragma unroll
+                for (int cc = 0; cc < CPT; cc += 2) {
+                    const float2 sn = __ffma2_rn(make_float2(kr[rr], kr[rr]), make_float2(uc[cc], uc[cc + 1]),
+                                                 make_float2(s[rr][cc], s[rr][cc + 1]));
+                    const float2 pp = __ffma2_rn(sn, make_float2(qi, qi), make_float2(part[cc], part[cc + 1]));
+                    s[rr][cc] = sn.x;
+                    s[rr][cc + 1] = sn.y;
+                    part[cc] = pp.x;
+                    part[cc + 1] = pp.y;
+                }
+            }
+            *reinterpret_cast<float4*>(&sm.red2[warp][m][CPT * cq]) = make_float4(part[0], part[1], part[2], part[3]);
+            __syncwarp();
+            if (m == 0) {
+                float o[CPT] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int mb = 0; mb < 8; ++mb) {
+                    const float4 r4 = *reinterpret_cast<const float4*>(&sm.red2[warp][mb][CPT * cq]);
+                    o[0] += r4.x;
+                    o[1] += r4.y;
+                    o[2] += r4.z;
+                    o[3] += r4.w;
+                }
+#pragma unroll
+                for (int cc = 0; cc < CPT; ++cc) o[cc] *= rc.scale;
+                const size_t rh = ((size_t)seq * W + t0 + t) * H + h;
+                *reinterpret_cast<float4*>(a.log_f + rh * (3 * D) + 2 * D + c0) = make_float4(uc[0], uc[1], uc[2], uc[3]);
+                if (has_g) {
+                    *reinterpret_cast<float4*>(&sm.o[t][c0]) = make_float4(o[0], o[1], o[2], o[3]);
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < CPT; ++cc) store_out(a.out, rh * D + c0 + cc, o[cc], a.out_bf16);
+                }
+            }
+        }
+
+        // ---- sigmoid-gated RMSNorm of the block's outputs (the register kernel's row_out)
+        if (has_g) {
+            __syncthreads();
+            for (int task = warp; task < nr * (D / 32); task += REC_WARPS) {
+                const int t = task / (D / 32), p = task % (D / 32);
+                const float ov = sm.o[t][32 * p + lane];
+                const float ss = warp_sum(ov * ov);
+                if (lane == 0) sm.esum[t][p] = ss;
+            }
+            __syncthreads();
+            for (int e = tid; e < nr * D; e += REC_THREADS) {
+                const int t = e / D, j = e % D;
+                float tot = 0.0f;
+#pragma unroll
+                for (int p = 0; p < D / 32; ++p) tot += sm.esum[t][p];
+                const float r = rsqrtf(tot * (1.0f / D) + rc.norm_eps);
+                const float wn = rc.norm_w ? rc.norm_w[j] : 1.0f;
+                const float y = sm.o[t][j] * r * wn * sigmoidf_(ldv(&vb.rows[t][4][j]));
+                store_out(a.out, (((size_t)seq * W + t0 + t) * H + h) * D + j, y, a.out_bf16);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------
 // Commit: replay the accepted prefix of a verify window from its log.
 
 template <int D, typename IO>
@@ -899,9 +1233,30 @@ template <int D, typename IO, int MODE> static cudaError_t launch_window(const R
     return cudaGetLastError();
 }
 
+// Verify windows at dk = dv = 128: the warp-local kernel (dynamic shared memory VwSmem).
+template <typename IO, int MODE> static cudaError_t launch_verify_warp(const RecArgs& a, int units, cudaStream_t st)
+{
+    static bool attr_done[128];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int smem = (int)sizeof(VwSmem<IO>);
+    if (dev >= 0 && dev < 128 && !attr_done[dev]) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kda_verify_warp_kernel<IO, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    kda_verify_warp_kernel<IO, MODE><<<dim3(units), dim3(REC_THREADS), smem, st>>>(a);
+    return cudaGetLastError();
+}
+
 template <int D, typename IO>
 static cudaError_t launch_rec_d(int mode, const RecArgs& a, int units, cudaStream_t st)
 {
+    if constexpr (D == VWD) {
+        if (mode == REC_VERIFY) return launch_verify_warp<IO, REC_VERIFY>(a, units, st);
+        if (mode == REC_COMMIT_VERIFY) return launch_verify_warp<IO, REC_COMMIT_VERIFY>(a, units, st);
+    }
     dim3 grid(units), block(REC_THREADS);
     if (mode == REC_PREFILL) kda_recurrent_kernel<D, IO, REC_PREFILL><<<grid, block, 0, st>>>(a);
     else if (mode == REC_DECODE) kda_recurrent_kernel<D, IO, REC_DECODE><<<grid, block, 0, st>>>(a);

@@ -80,6 +80,19 @@ def test_verify_commit_shapes(cuda_lib, oracle_mod, d, io, gate, K, og):
     _check_window(cuda_lib, oracle_mod, wl, out_dtype=W.BF16 if io == W.BF16 else W.F32)
 
 
+@pytest.mark.parametrize("Wn,io,gate,og", [(1, W.BF16, W.SAFE, True), (13, W.BF16, W.SOFTPLUS, True),
+                                         (17, W.F32, W.SAFE, False)])
+def test_verify_commit_window_lengths(cuda_lib, oracle_mod, Wn, io, gate, og):
+    """dk = dv = 128 windows of one row and of several staged 8-row blocks with
+    a ragged last block: serial-decode bits and oracle tolerance."""
+    B = 4
+    wl = W.make_workload(f"verw{Wn}", 300 + Wn, [Wn] * B, H=3, d=128, K=4, io_dtype=io,
+                         gate_mode=gate, lower_bound=-5.0, out_gate=og, init_state="random",
+                         W=Wn, accepted=True)
+    wl.arrays["accepted"][:2] = [Wn, Wn - 1]
+    _check_window(cuda_lib, oracle_mod, wl, out_dtype=W.BF16 if io == W.BF16 else W.F32)
+
+
 def test_commit_rejects_bad_accepted(cuda_lib):
     wl = W.make_workload("badacc", 99, [4] * 2, H=2, d=32, K=4, io_dtype=W.F32,
                          gate_mode=W.SAFE, init_state="random", W=4, accepted=True)
@@ -128,6 +141,35 @@ def test_commit_verify_equals_separate_calls(cuda_lib, d, io, gate, alias):
     _load_rows(sep, win2)
     K.check(sep.verify())
     # one call
+    _load_rows(fus, win2)
+    log2 = fus.log if alias else torch.empty_like(fus.log)
+    K.check(_commit_verify(fus, acc, fus.log, log2))
+    torch.cuda.synchronize()
+    assert int(sep.dev_status.item()) == 0 and int(fus.dev_status.item()) == 0
+    assert torch.equal(fus.out[:B * Wn], sep.out[:B * Wn])
+    assert torch.equal(fus.rec_state, sep.rec_state)
+    assert torch.equal(fus.conv_state, sep.conv_state)
+    assert torch.equal(log2, sep.log)
+
+
+@pytest.mark.parametrize("Wn,alias", [(12, True), (9, False)])
+def test_commit_verify_long_windows(cuda_lib, Wn, alias):
+    """Commit of more than one staged block of log rows fused into the next
+    verify (dk = dv = 128) = the separate calls, bit for bit."""
+    B, H, d = 4, 2, 128
+    kw = dict(H=H, d=d, K=4, io_dtype=W.BF16, gate_mode=W.SAFE, lower_bound=-5.0, out_gate=True,
+              init_state="random", W=Wn, accepted=True)
+    win1 = W.make_workload("cvl1", 921 + Wn, [Wn] * B, **kw)
+    win2 = W.make_workload("cvl2", 922 + Wn, [Wn] * B, **kw)
+    acc = torch.tensor([Wn, 9, 0, 3], dtype=torch.int32, device="cuda")
+    sep = DeviceCase(win1, out_dtype=W.F32)
+    fus = DeviceCase(win1, out_dtype=W.F32)
+    for dc in (sep, fus):
+        dc.alloc_log()
+        K.check(dc.verify())
+    K.check(sep.commit(accepted=acc))
+    _load_rows(sep, win2)
+    K.check(sep.verify())
     _load_rows(fus, win2)
     log2 = fus.log if alias else torch.empty_like(fus.log)
     K.check(_commit_verify(fus, acc, fus.log, log2))
