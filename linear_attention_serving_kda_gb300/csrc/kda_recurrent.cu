@@ -800,14 +800,23 @@ template <typename IO> struct VwBuf {
     float bv[VWB];          // beta logits
 };
 
+// Key-dim arrays of a row are padded by 4 floats every 16 (index i -> vw_pad(i)),
+// so the eight 16-float key-dim blocks a warp reads at once start in distinct
+// bank groups (float4 reads without conflicts).
+constexpr int VWP = VWD + VWD / 4;
+__device__ __forceinline__ int vw_pad(int i) { return i + 4 * (i >> 4); }
+
 template <typename IO> struct VwSmem {
     VwBuf<IO> buf[2];                 // double-buffered staged blocks
     float plog[VWB][3 * VWD];         // log rows to replay (commit first)
-    float cw[3 * VWD][4];             // conv taps (4-tap form, oldest first)
+    float cw[3 * VWD][4];             // conv taps (K-tap form, oldest first)
     float dtb[VWD];                   // dt_bias of this head
-    float act[VWB][3 * VWD];          // post-SiLU q', k', v' of the block's rows
-    float alpha[VWB][VWD];            // decays of the block's rows
+    float qp[VWB][VWP];               // post-SiLU q' of the block's rows (padded key dims)
+    float kp[VWB][VWP];               // post-SiLU k' (padded key dims)
+    float ap[VWB][VWP];               // decays (padded key dims)
+    float vp[VWB][VWD];               // post-SiLU v'
     float nrm[VWB][8];                // per-32-channel sums of squares of q', k'
+    float rs[VWB][4];                 // per row: q and k inverse norms, beta
     float o[VWB][VWD];                // outputs before the gated norm
     float esum[VWB][4];               // gated norm: per-32-column sums of squares
     float red[REC_WARPS][8][16];      // per-warp scratch: [key block][value dim] partials of S'^T k
@@ -861,6 +870,47 @@ __device__ __forceinline__ IO vw_stage(VwBuf<IO>& vb, const RecArgs& a, int seq,
     IO braw{};
     if (threadIdx.x < nr) braw = b[((size_t)seq * a.W + t0 + threadIdx.x) * a.H + h];
     return braw;
+}
+
+// State-independent part of rows [0, nr) of a staged block for one conv
+// channel `it` (q | k | v) of this thread: the register kernel's row_conv
+// expressions -- acc = fma(w_j, x_{t-K+1+j}, acc) over j = 0..K-1 from 0,
+// SiLU, and for q and k the warp's sum of squares over its 32 consecutive
+// channels -- with the raw values in a sliding window of registers.
+template <int KK, typename IO>
+__device__ __forceinline__ void vw_conv_channel(VwSmem<IO>& sm, const VwBuf<IO>& vb, int it, int nr, int lane)
+{
+    constexpr int D = VWD;
+    const int seg = it / D, ch = it % D;
+    float w[KK], xs[KK];
+#pragma unroll
+    for (int j = 0; j < KK; ++j) w[j] = sm.cw[it][j];
+#pragma unroll
+    for (int j = 1; j < KK; ++j) xs[j] = ldv(&vb.halo[3 - KK + j][seg][ch]);  // rows j - KK .. -1
+    for (int t = 0; t < nr; ++t) {
+#pragma unroll
+        for (int j = 0; j + 1 < KK; ++j) xs[j] = xs[j + 1];
+        xs[KK - 1] = ldv(&vb.rows[t][seg][ch]);
+        float accv = 0.0f;
+#pragma unroll
+        for (int j = 0; j < KK; ++j) accv = __fmaf_rn(w[j], xs[j], accv);
+        const float x = siluf_(accv);
+        if (seg == 2) {
+            sm.vp[t][ch] = x;
+        } else {  // warp-uniform: a warp holds 32 consecutive q or k channels
+            (seg == 0 ? sm.qp : sm.kp)[t][vw_pad(ch)] = x;
+            const float ss = warp_sum(x * x);
+            if (lane == 0) sm.nrm[t][it >> 5] = ss;
+        }
+    }
+}
+
+template <typename IO>
+__device__ __forceinline__ void vw_conv(VwSmem<IO>& sm, const VwBuf<IO>& vb, int K, int it, int nr, int lane)
+{
+    if (K == 4) vw_conv_channel<4, IO>(sm, vb, it, nr, lane);
+    else if (K == 3) vw_conv_channel<3, IO>(sm, vb, it, nr, lane);
+    else vw_conv_channel<2, IO>(sm, vb, it, nr, lane);
 }
 
 template <typename IO, int MODE>
@@ -966,60 +1016,57 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_verify_warp_kernel(const R
             *reinterpret_cast<int4*>(lraw + ((size_t)seq * W + t0 + t) * conv_dim + (size_t)seg * H * D + h * D +
                                      piece * EPP) = *reinterpret_cast<const int4*>(&vb.rows[t][seg][piece * EPP]);
         }
-        // ---- state-independent part of the block's rows (the register kernel's row_conv)
-        for (int e = tid; e < nr * 4 * D; e += REC_THREADS) {
-            const int t = e / (4 * D), it = e % (4 * D);
-            if (it < 3 * D) {
-                const int seg = it / D, ch = it % D;
-                float accv = 0.0f;
-                for (int j = 0; j < K; ++j) {
-                    const int xl = t - K + 1 + j;  // raw row of tap j, relative to the block's first row
-                    const float xv = xl >= 0 ? ldv(&vb.rows[xl][seg][ch]) : ldv(&vb.halo[xl + 3][seg][ch]);
-                    accv = __fmaf_rn(sm.cw[it][j], xv, accv);
-                }
-                const float x = siluf_(accv);
-                sm.act[t][it] = x;
-                if (it < 2 * D) {  // warp-uniform: 32 consecutive channels of one row
-                    const float ss = warp_sum(x * x);
-                    if (lane == 0) sm.nrm[t][it >> 5] = ss;
-                }
-            } else {
-                const int i = it - 3 * D;
-                sm.alpha[t][i] = __expf(log_alpha(rc.gate_mode, rc.lb, rc.ea, ldv(&vb.rows[t][3][i]), sm.dtb[i]));
+        // ---- state-independent part of the block's rows: conv channels (q, k
+        // on every warp, v on warps 0-3) and decays (warps 4-7)
+        vw_conv<IO>(sm, vb, K, tid, nr, lane);
+        if (tid < D) {
+            vw_conv<IO>(sm, vb, K, 2 * D + tid, nr, lane);
+        } else {
+            const int i = tid - D;
+            const float dti = sm.dtb[i];
+            for (int t = 0; t < nr; ++t)
+                sm.ap[t][vw_pad(i)] = __expf(log_alpha(rc.gate_mode, rc.lb, rc.ea, ldv(&vb.rows[t][3][i]), dti));
+        }
+        __syncthreads();
+        if (tid < nr) {  // the register kernel's norms and beta of row tid
+            float sq = 0.0f, sk = 0.0f;
+#pragma unroll
+            for (int p = 0; p < D / 32; ++p) {
+                sq += sm.nrm[tid][p];
+                sk += sm.nrm[tid][D / 32 + p];
             }
+            sm.rs[tid][0] = rsqrtf(sq + rc.l2_eps);
+            sm.rs[tid][1] = rsqrtf(sk + rc.l2_eps);
+            sm.rs[tid][2] = sigmoidf_(vb.bv[tid]);
         }
         __syncthreads();
         // decay and normalised key of each row into the log
         for (int e = tid; e < nr * D; e += REC_THREADS) {
             const int t = e / D, i = e % D;
-            float sk = 0.0f;
-#pragma unroll
-            for (int p = 0; p < D / 32; ++p) sk += sm.nrm[t][D / 32 + p];
-            const float rk = rsqrtf(sk + rc.l2_eps);
             float* lg = a.log_f + (((size_t)seq * W + t0 + t) * H + h) * (3 * D);
-            lg[i] = sm.alpha[t][i];
-            lg[D + i] = sm.act[t][D + i] * rk;
+            lg[i] = sm.ap[t][vw_pad(i)];
+            lg[D + i] = sm.kp[t][vw_pad(i)] * sm.rs[t][1];
         }
 
         // ---- the rows: the delta rule on the register state, sums inside the warp
         for (int t = 0; t < nr; ++t) {
-            float sq = 0.0f, sk = 0.0f;
+            const float4 sc = *reinterpret_cast<const float4*>(&sm.rs[t][0]);
+            const float rq = sc.x, rk = sc.y, beta = sc.z;
+            float kr[RPW], av[RPW], part[CPT];
 #pragma unroll
-            for (int p = 0; p < D / 32; ++p) {
-                sq += sm.nrm[t][p];
-                sk += sm.nrm[t][D / 32 + p];
+            for (int u = 0; u < RPW; u += 4) {
+                const float4 k4 = *reinterpret_cast<const float4*>(&sm.kp[t][vw_pad(r0) + u]);
+                const float4 a4 = *reinterpret_cast<const float4*>(&sm.ap[t][vw_pad(r0) + u]);
+                const float2 ka = __fmul2_rn(make_float2(k4.x, k4.y), make_float2(rk, rk));
+                const float2 kb = __fmul2_rn(make_float2(k4.z, k4.w), make_float2(rk, rk));
+                kr[u] = ka.x; kr[u + 1] = ka.y; kr[u + 2] = kb.x; kr[u + 3] = kb.y;
+                av[u] = a4.x; av[u + 1] = a4.y; av[u + 2] = a4.z; av[u + 3] = a4.w;
             }
-            const float rq = rsqrtf(sq + rc.l2_eps);
-            const float rk = rsqrtf(sk + rc.l2_eps);
-            const float beta = sigmoidf_(vb.bv[t]);
-            float kr[RPW], part[CPT];
-#pragma unroll
-            for (int rr = 0; rr < RPW; ++rr) kr[rr] = sm.act[t][D + r0 + rr] * rk;
 #pragma unroll
             for (int cc = 0; cc < CPT; ++cc) part[cc] = 0.0f;
 #pragma unroll
             for (int rr = 0; rr < RPW; ++rr) {
-                const float ai = sm.alpha[t][r0 + rr];
+                const float ai = av[rr];
 #pragma unroll
                 for (int cc = 0; cc < CPT; cc += 2) {
                     const float2 sp = __fmul2_rn(make_float2(ai, ai), make_float2(s[rr][cc], s[rr][cc + 1]));
@@ -1032,23 +1079,29 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_verify_warp_kernel(const R
             }
             *reinterpret_cast<float4*>(&sm.red[warp][m][CPT * cq]) = make_float4(part[0], part[1], part[2], part[3]);
             __syncwarp();
-            float kv[CPT] = {0.0f, 0.0f, 0.0f, 0.0f}, uc[CPT];
+            float2 kv01 = make_float2(0.0f, 0.0f), kv23 = kv01;
 #pragma unroll
             for (int mb = 0; mb < 8; ++mb) {  // key-dim blocks in order
                 const float4 r4 = *reinterpret_cast<const float4*>(&sm.red[warp][mb][CPT * cq]);
-                kv[0] += r4.x;
-                kv[1] += r4.y;
-                kv[2] += r4.z;
-                kv[3] += r4.w;
+                kv01 = __fadd2_rn(kv01, make_float2(r4.x, r4.y));
+                kv23 = __fadd2_rn(kv23, make_float2(r4.z, r4.w));
             }
+            const float4 v4 = *reinterpret_cast<const float4*>(&sm.vp[t][c0]);
+            const float2 u01 = __fmul2_rn(make_float2(beta, beta), __fadd2_rn(make_float2(v4.x, v4.y), make_float2(-kv01.x, -kv01.y)));
+            const float2 u23 = __fmul2_rn(make_float2(beta, beta), __fadd2_rn(make_float2(v4.z, v4.w), make_float2(-kv23.x, -kv23.y)));
+            const float uc[CPT] = {u01.x, u01.y, u23.x, u23.y};
 #pragma unroll
-            for (int cc = 0; cc < CPT; ++cc) {
-                uc[cc] = beta * (sm.act[t][2 * D + c0 + cc] - kv[cc]);
-                part[cc] = 0.0f;
+            for (int cc = 0; cc < CPT; ++cc) part[cc] = 0.0f;
+#pragma unroll
+            for (int u = 0; u < RPW; u += 4) {  // q^ of the tile's key dims
+                const float4 q4 = *reinterpret_cast<const float4*>(&sm.qp[t][vw_pad(r0) + u]);
+                const float2 qa = __fmul2_rn(make_float2(q4.x, q4.y), make_float2(rq, rq));
+                const float2 qb = __fmul2_rn(make_float2(q4.z, q4.w), make_float2(rq, rq));
+                av[u] = qa.x; av[u + 1] = qa.y; av[u + 2] = qb.x; av[u + 3] = qb.y;
             }
 #pragma unroll
             for (int rr = 0; rr < RPW; ++rr) {
-                const float qi = sm.act[t][r0 + rr] * rq;
+                const float qi = av[rr];
 #pragma unroll
                 for (int cc = 0; cc < CPT; cc += 2) {
                     const float2 sn = __ffma2_rn(make_float2(kr[rr], kr[rr]), make_float2(uc[cc], uc[cc + 1]),
@@ -1063,24 +1116,24 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_verify_warp_kernel(const R
             *reinterpret_cast<float4*>(&sm.red2[warp][m][CPT * cq]) = make_float4(part[0], part[1], part[2], part[3]);
             __syncwarp();
             if (m == 0) {
-                float o[CPT] = {0.0f, 0.0f, 0.0f, 0.0f};
+                float2 o01 = make_float2(0.0f, 0.0f), o23 = o01;
 #pragma unroll
                 for (int mb = 0; mb < 8; ++mb) {
                     const float4 r4 = *reinterpret_cast<const float4*>(&sm.red2[warp][mb][CPT * cq]);
-                    o[0] += r4.x;
-                    o[1] += r4.y;
-                    o[2] += r4.z;
-                    o[3] += r4.w;
+                    o01 = __fadd2_rn(o01, make_float2(r4.x, r4.y));
+                    o23 = __fadd2_rn(o23, make_float2(r4.z, r4.w));
                 }
-#pragma unroll
-                for (int cc = 0; cc < CPT; ++cc) o[cc] *= rc.scale;
+                o01 = __fmul2_rn(o01, make_float2(rc.scale, rc.scale));
+                o23 = __fmul2_rn(o23, make_float2(rc.scale, rc.scale));
                 const size_t rh = ((size_t)seq * W + t0 + t) * H + h;
                 *reinterpret_cast<float4*>(a.log_f + rh * (3 * D) + 2 * D + c0) = make_float4(uc[0], uc[1], uc[2], uc[3]);
                 if (has_g) {
-                    *reinterpret_cast<float4*>(&sm.o[t][c0]) = make_float4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<float4*>(&sm.o[t][c0]) = make_float4(o01.x, o01.y, o23.x, o23.y);
                 } else {
-#pragma unroll
-                    for (int cc = 0; cc < CPT; ++cc) store_out(a.out, rh * D + c0 + cc, o[cc], a.out_bf16);
+                    store_out(a.out, rh * D + c0, o01.x, a.out_bf16);
+                    store_out(a.out, rh * D + c0 + 1, o01.y, a.out_bf16);
+                    store_out(a.out, rh * D + c0 + 2, o23.x, a.out_bf16);
+                    store_out(a.out, rh * D + c0 + 3, o23.y, a.out_bf16);
                 }
             }
         }
