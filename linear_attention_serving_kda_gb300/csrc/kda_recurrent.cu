@@ -1218,6 +1218,164 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_commit_kernel(const Commit
 }
 
 // ------------------------------------------------------------------------
+// Streaming commit (D = 128): persistent CTAs, a producer warp and 8 replay
+// warps.  The producer bulk-copies each unit's state, its accepted log rows
+// and the source rows of its new conv state into a stage; the replay warps
+// apply S <- fma(k^, u, alpha * S) row after row -- decode's per-element
+// expression -- and leave the state in the stage, from where the producer
+// stores it and the conv rows back with bulk copies before the stage takes
+// its next unit.  Units with nothing accepted move no data.
+
+constexpr int CMT_WMAX = 16;   // log rows a stage holds (longer windows run kda_commit_kernel)
+constexpr int CMT_STAGES = 2;
+
+template <typename IO> struct CmtStage {
+    float S[DEC_D * DEC_D];        // the unit's state, row-major (64 KiB)
+    float lg[CMT_WMAX][3 * DEC_D]; // accepted log rows: alpha | k^ | u
+    IO conv[3][3][DEC_D];          // new conv-state rows [row][q|k|v][channel]
+    int slot, acc, head, pad;
+};
+
+template <typename IO> struct CmtSmem {
+    CmtStage<IO> stage[CMT_STAGES];
+    uint64_t full[CMT_STAGES], empty[CMT_STAGES];
+};
+
+template <typename IO>
+__global__ void __launch_bounds__(DEC_THREADS, 1) kda_commit_stream_kernel(const CommitArgs a)
+{
+    extern __shared__ __align__(128) unsigned char cmt_smem[];
+    CmtSmem<IO>& sm = *reinterpret_cast<CmtSmem<IO>*>(cmt_smem);
+    constexpr int D = DEC_D, RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.H, K = a.K, W = a.W, N = a.B;
+    const int conv_dim = 3 * H * D;
+    const int units = N * H;
+    const int u_begin = (int)(((long long)units * blockIdx.x) / gridDim.x);
+    const int u_end = (int)(((long long)units * (blockIdx.x + 1)) / gridDim.x);
+
+    if (tid == 0) {
+        for (int s = 0; s < CMT_STAGES; ++s) {
+            ptx::mbar_init(&sm.full[s], 1);
+            ptx::mbar_init(&sm.empty[s], REC_WARPS);  // one arrival per replay warp
+        }
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    // programmatic dependent launch: the prologue may overlap the previous
+    // kernel (the verify that wrote the log); data is read only after it completes
+    ptx::grid_launch_dependents();
+    ptx::grid_dependency_wait();
+    IO* cs = static_cast<IO*>(a.conv_state);
+    const IO* raw = static_cast<const IO*>(a.log_raw);
+
+    if (warp == REC_WARPS) {
+        // ---------------- producer
+        if (lane != 0) return;
+        const uint64_t pol = ptx::policy_evict_first();
+        auto write_back = [&](int s, int n) -> bool {
+            if (!ptx::mbar_wait(&sm.empty[s], n & 1)) {
+                flag_status(a.dev_status, KDA_DEV_TIMEOUT);
+                return false;
+            }
+            const CmtStage<IO>& st = sm.stage[s];
+            if (st.acc > 0) {
+                ptx::bulk_s2g(a.rec_state + ((size_t)st.slot * H + st.head) * D * D, st.S, D * D * 4);
+                for (int r = 0; r < K - 1; ++r)
+                    for (int seg = 0; seg < 3; ++seg)
+                        ptx::bulk_s2g(cs + ((size_t)st.slot * (K - 1) + r) * conv_dim + (size_t)seg * H * D + st.head * D,
+                                      st.conv[r][seg], D * sizeof(IO));
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();  // the stage may be refilled
+            }
+            return true;
+        };
+        const int count = u_end - u_begin;
+        for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
+            const int s = i % CMT_STAGES, n = i / CMT_STAGES;
+            if (n > 0 && !write_back(s, n - 1)) return;
+            CmtStage<IO>& st = sm.stage[s];
+            const int h = u / N, seq = u % N;
+            int slot = a.slots ? a.slots[seq] : seq;
+            int acc = 0;
+            if (slot >= a.num_slots) {
+                flag_status(a.dev_status, KDA_DEV_BAD_SLOT);
+                slot = -1;
+            }
+            if (slot >= 0) {
+                acc = a.accepted[seq];
+                if (acc < 0 || acc > W) {
+                    if (h == 0) flag_status(a.dev_status, KDA_DEV_BAD_ACCEPTED);
+                    acc = 0;
+                }
+            }
+            // the stage's fields first: the arrival below publishes them with the copies
+            st.slot = slot;
+            st.acc = acc;
+            st.head = h;
+            if (acc > 0) {
+                const uint32_t rowb = D * sizeof(IO);
+                const uint32_t bytes = D * D * 4 + (uint32_t)acc * 3 * D * 4 + (uint32_t)(K - 1) * 3 * rowb;
+                asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(ptx::smem_u32(&sm.full[s])),
+                             "r"(bytes) : "memory");
+                ptx::bulk_g2s_stream(st.S, a.rec_state + ((size_t)slot * H + h) * D * D, D * D * 4, &sm.full[s], pol);
+                for (int t = 0; t < acc; ++t)
+                    ptx::bulk_g2s(st.lg[t], a.log_f + (((size_t)seq * W + t) * H + h) * (3 * D), 3 * D * 4, &sm.full[s]);
+                // the new conv state: the last K-1 rows of [old state; accepted raw rows]
+                for (int r = 0; r < K - 1; ++r) {
+                    const int src = acc - (K - 1) + r;  // window row, or < 0: old state row src + K - 1
+                    for (int seg = 0; seg < 3; ++seg) {
+                        const size_t chan = (size_t)seg * H * D + (size_t)h * D;
+                        const IO* from = src >= 0 ? raw + ((size_t)seq * W + src) * conv_dim + chan
+                                                  : cs + ((size_t)slot * (K - 1) + src + K - 1) * conv_dim + chan;
+                        ptx::bulk_g2s(st.conv[r][seg], from, rowb, &sm.full[s]);
+                    }
+                }
+            }
+            ptx::mbar_arrive(&sm.full[s]);
+        }
+        for (int i = count > CMT_STAGES ? count - CMT_STAGES : 0; i < count; ++i)
+            if (!write_back(i % CMT_STAGES, i / CMT_STAGES)) return;
+        ptx::bulk_wait_all();
+        return;
+    }
+
+    // ---------------- replay warps (warp w: rows [16w, +16), lane l: columns [4l, +4))
+    const int r0 = warp * RPW, c0 = lane * CPT;
+    for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
+        const int s = i % CMT_STAGES, n = i / CMT_STAGES;
+        if (!ptx::mbar_wait(&sm.full[s], n & 1)) {
+            if (lane == 0) flag_status(a.dev_status, KDA_DEV_TIMEOUT);
+            return;
+        }
+        CmtStage<IO>& st = sm.stage[s];
+        const int acc = st.acc;
+        if (acc > 0) {
+            float sreg[RPW][CPT];
+            load_tile_smem<D>(st.S, r0, c0, sreg);
+            for (int t = 0; t < acc; ++t) {
+                const float* lg = st.lg[t];
+                const float4 u4 = *reinterpret_cast<const float4*>(lg + 2 * D + c0);
+                const float uc[CPT] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+                for (int rr = 0; rr < RPW; ++rr) {
+                    const float ai = lg[r0 + rr], ki = lg[D + r0 + rr];
+#pragma unroll
+                    for (int cc = 0; cc < CPT; ++cc) sreg[rr][cc] = __fmaf_rn(ki, uc[cc], __fmul_rn(ai, sreg[rr][cc]));
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr)
+                *reinterpret_cast<float4*>(st.S + (r0 + rr) * D + c0) =
+                    make_float4(sreg[rr][0], sreg[rr][1], sreg[rr][2], sreg[rr][3]);
+            ptx::fence_proxy_async_smem();  // the producer's bulk store reads these writes
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.empty[s]);
+    }
+}
+
+// ------------------------------------------------------------------------
 // launchers
 
 static int sm_count()
@@ -1332,10 +1490,41 @@ cudaError_t launch_recurrent(int mode, int io_bf16, const RecArgs& a, int units,
     }
 }
 
+static_assert(sizeof(CmtSmem<__nv_bfloat16>) <= 232448, "commit stage buffers exceed shared memory");
+static_assert(sizeof(CmtSmem<float>) <= 232448, "commit stage buffers exceed shared memory");
+
+template <typename IO> static cudaError_t launch_commit_stream(const CommitArgs& a, int units, cudaStream_t st)
+{
+    static bool attr_done[128];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int smem = (int)sizeof(CmtSmem<IO>);
+    if (dev >= 0 && dev < 128 && !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kda_commit_stream_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    // as many streaming CTAs as the decode kernel (27/32 of the SMs)
+    const int cap = sm_count() * 27 / 32 > 0 ? sm_count() * 27 / 32 : 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(units < cap ? units : cap);
+    cfg.blockDim = dim3(DEC_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kda_commit_stream_kernel<IO>, a);
+}
+
 cudaError_t launch_commit(int io_bf16, const CommitArgs& a, cudaStream_t st)
 {
     const int units = a.B * a.H;
     if (units <= 0) return cudaSuccess;
+    if (a.D == DEC_D && a.W <= CMT_WMAX)
+        return io_bf16 ? launch_commit_stream<__nv_bfloat16>(a, units, st) : launch_commit_stream<float>(a, units, st);
     dim3 grid(units), block(REC_THREADS);
     switch (a.D) {
     case 32: if (io_bf16) kda_commit_kernel<32, __nv_bfloat16><<<grid, block, 0, st>>>(a); else kda_commit_kernel<32, float><<<grid, block, 0, st>>>(a); break;

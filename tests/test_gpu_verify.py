@@ -93,17 +93,20 @@ def test_verify_commit_window_lengths(cuda_lib, oracle_mod, Wn, io, gate, og):
     _check_window(cuda_lib, oracle_mod, wl, out_dtype=W.BF16 if io == W.BF16 else W.F32)
 
 
-def test_commit_rejects_bad_accepted(cuda_lib):
-    wl = W.make_workload("badacc", 99, [4] * 2, H=2, d=32, K=4, io_dtype=W.F32,
+@pytest.mark.parametrize("d,io", [(32, W.F32), (128, W.BF16)])
+def test_commit_rejects_bad_accepted(cuda_lib, d, io):
+    wl = W.make_workload("badacc", 99, [4] * 3, H=2, d=d, K=4, io_dtype=io,
                          gate_mode=W.SAFE, init_state="random", W=4, accepted=True)
     dc = DeviceCase(wl)
     cuda_lib.check(dc.verify())
-    rs0 = dc.rec_state.clone()
-    bad = torch.tensor([9, -1], dtype=torch.int32, device="cuda")
+    rs0, cs0 = dc.rec_state.clone(), dc.conv_state.clone()
+    bad = torch.tensor([9, -1, 2], dtype=torch.int32, device="cuda")
     cuda_lib.check(dc.commit(accepted=bad))
     torch.cuda.synchronize()
     assert int(dc.dev_status.item()) & cuda_lib.KDA_DEV_BAD_ACCEPTED
-    assert torch.equal(dc.rec_state, rs0)
+    # the bad sequences keep their states; the good one commits its two rows
+    assert torch.equal(dc.rec_state[:2], rs0[:2]) and torch.equal(dc.conv_state[:2], cs0[:2])
+    assert not torch.equal(dc.rec_state[2], rs0[2])
 
 
 def _commit_verify(dc, accepted, log_prev, log_new):
