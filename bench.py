@@ -282,11 +282,26 @@ def leg_verify(kda, reps, stream):
     mv, mc, mcv = statistics.median(tv), statistics.median(tc), statistics.median(tcv)
     acc = int(wl.arrays["accepted"].sum())
     rows = wl.N * wl.W
+    # algorithmic HBM bytes per launch (each state, row, log entry moved once)
+    io, d, H, Wn, K = 2, wl.dk, wl.H, wl.W, wl.K
+    state = d * d * 4
+    conv = (K - 1) * 3 * d * io                                  # one head's conv history
+    row_in = (4 * d + 1) * io + (d * io if wl.has_out_gate else 0)  # q, k, v, f, beta (, g)
+    row_io = row_in + d * 2 + 3 * d * 4 + 3 * d * io             # + bf16 out + log (alpha|k^|u, raw row)
+    per_acc = [int(x) for x in wl.arrays["accepted"]]
+    v_bytes = wl.N * H * (state + conv + Wn * row_io)
+    c_bytes = sum(H * (2 * state + a * 3 * d * 4 + 2 * conv) for a in per_acc if a > 0)
+    cv_bytes = v_bytes + sum(H * (state + a * 3 * d * 4 + conv) for a in per_acc if a > 0)
+    hbm_gbs = load_peaks()[0]
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
     return {"workload": wl.name, "rows": rows, "accepted_rows": acc, "verify_ms": mv, "commit_ms": mc,
             "commit_verify_ms": mcv,
             "rows_verified_per_s": rows / (mv * 1e-3),
             "committed_tokens_per_s": acc / ((mv + mc) * 1e-3),
-            "committed_tokens_per_s_fused": acc / (mcv * 1e-3)}
+            "committed_tokens_per_s_fused": acc / (mcv * 1e-3),
+            "alg_bytes": {"verify": v_bytes, "commit": c_bytes, "commit_verify": cv_bytes},
+            "hbm_frac": {"verify": gbs(v_bytes, mv) / hbm_gbs, "commit": gbs(c_bytes, mc) / hbm_gbs,
+                         "commit_verify": gbs(cv_bytes, mcv) / hbm_gbs}}
 
 
 def e2e_decode(kda, steps, warmup, stream):
