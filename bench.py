@@ -421,9 +421,12 @@ def measured_traffic():
     try:
         with open(tpath) as fh:
             rec = json.load(fh)
-        with open(os.path.join(ROOT, rec["source"]), "rb") as fh:
-            if hashlib.sha256(fh.read()).hexdigest() != rec["source_sha256"]:
-                return None
+        h = hashlib.sha256()
+        for src in rec["sources"]:  # the kernel's source files, in this order
+            with open(os.path.join(ROOT, src), "rb") as fh:
+                h.update(fh.read())
+        if h.hexdigest() != rec["sources_sha256"]:
+            return None
         return rec["bytes_per_launch"]
     except Exception:
         return None

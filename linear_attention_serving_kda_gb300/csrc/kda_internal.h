@@ -78,6 +78,8 @@ struct ChunkArgs {
 
 cudaError_t launch_recurrent(int mode, int io_bf16, const RecArgs& a, int units, cudaStream_t st);
 cudaError_t launch_commit(int io_bf16, const CommitArgs& a, cudaStream_t st);
+// streaming decode at dk = dv = 128 (kda_decode.cu)
+cudaError_t launch_decode_stream_d128(int io_bf16, const RecArgs& a, int units, cudaStream_t st);
 
 // Chunk kernel: returns cudaErrorNotSupported when the shape is not covered.
 bool chunk_supported(const kda_params* p);

@@ -1,325 +1,14 @@
-// kda_recurrent.cu -- row-recurrent KDA kernels for sm_103a: decode rows,
-// verify windows, the serial prefill, and the verify commit.
-//
-// A (sequence, head) unit is processed by 256 threads.  The fp32 dk x dv
-// state lives in registers while the unit's rows run: warp w holds rows
-// [w*D/8, (w+1)*D/8) and lane l holds columns [l*D/32, (l+1)*D/32), so each
-// warp touches whole D-float rows (coalesced, vector accesses) and the two
-// key-dim reductions per row (S'^T k and S^T q) are an in-register partial
-// over the warp's rows followed by a fixed-order sum over the 8 warps.
-//
-// Every kernel here runs one row through row_conv, row_delta and row_out (in
-// row_step, or in that order with the state store between): the same
-// expressions in the same order -- S' = alpha * S (rounded), then S = fma(k, u, S') -- with
-// the same thread-to-element map and reduction trees.  So a verified row has
-// the bits of a decoded row, and a committed state the bits of serial decode
-// (TensorFold issue #850, Oct 15 comment: a window logs each row's decay,
-// normalized key and update, and replaying them gives the bits of rows decoded
-// one at a time; Oct 19 comment: preserve rounding, reduction order, replay).
-//
-// Decode at dk = dv = 128 -- the memory-bound serving step -- uses a
-// persistent kernel: one CTA on each of ~27/32 of the SMs, a producer warp that
-// streams each unit's 64 KiB state, rows, conv history and parameters into a
-// ring of shared-memory stages with bulk async copies, and 8 row warps that
-// run the row on a loaded stage meanwhile and leave the new state in the
-// stage, from where the producer stores it back with one bulk copy before
-// reusing the stage.
-#include "kda_common.cuh"
-#include "kda_internal.h"
-#include "kda_ptx.cuh"
+// kda_recurrent.cu -- row-recurrent KDA kernels for sm_103a: verify windows
+// (and commit fused into the next window), commit, and the serial prefill for
+// the shapes the chunk kernel does not take.  Rows follow kda_row.cuh, so they
+// carry decode's bits.  At dk = dv = 128 verify windows regroup the thread
+// tiles so that a row's sums stay inside a warp (kda_verify_warp_kernel) and
+// commit streams through shared-memory stages like decode
+// (kda_commit_stream_kernel); other widths run the register kernel, one CTA
+// per unit.
+#include "kda_row.cuh"
 
 namespace kda {
-
-constexpr int REC_THREADS = 256;
-constexpr int REC_WARPS = REC_THREADS / 32;
-
-template <int D> struct RecShape {
-    static constexpr int CPT = D / 32;        // state columns per lane
-    static constexpr int RPW = D / REC_WARPS; // state rows per warp
-};
-
-template <int D> struct RowSmem {
-    float win[4][3 * D];      // ring of the last 4 raw conv rows (this head's q|k|v channels)
-    float cw[3 * D][4];       // conv taps
-    float dtb[D];             // dt_bias of this head
-    float act[3 * D];         // post-SiLU q', k', v'
-    float alpha[D], fr[D];
-    float red[REC_WARPS][D];  // cross-warp partial sums of S'^T k
-    float red2[REC_WARPS][D]; // cross-warp partial sums of S^T q
-    float nrm[8];             // per-warp sums of squares: q' [0, D/32), k' [D/32, 2D/32)
-    float scal[8];
-};
-
-struct RowConst {
-    int gate_mode;
-    float lb, ea, l2_eps, norm_eps, scale;
-    const float* norm_w;
-};
-
-__device__ __forceinline__ int ring(int x) { return x & 3; }
-
-// Barrier over the 256 row threads only (a streaming CTA also has a producer warp).
-__device__ __forceinline__ void row_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-// Global channel of local channel c (q | k | v of head h) in the conv layout.
-template <int D> __device__ __forceinline__ int conv_channel(int c, int h, int H)
-{
-    if (c < D) return h * D + c;
-    if (c < 2 * D) return H * D + h * D + (c - D);
-    return 2 * H * D + h * D + (c - 2 * D);
-}
-
-template <int D, typename Src>
-__device__ __forceinline__ void load_tile(const Src* Sg, int r0, int c0,
-                                          float (&s)[RecShape<D>::RPW][RecShape<D>::CPT])
-{
-    constexpr int RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT;
-#pragma unroll
-    for (int rr = 0; rr < RPW; ++rr) {
-        const float* p = Sg + (size_t)(r0 + rr) * D + c0;
-        if constexpr (CPT == 4) {
-            float4 x = ld_stream4(p);
-            s[rr][0] = x.x; s[rr][1] = x.y; s[rr][2] = x.z; s[rr][3] = x.w;
-        } else if constexpr (CPT == 2) {
-            float2 x = __ldcs(reinterpret_cast<const float2*>(p));
-            s[rr][0] = x.x; s[rr][1] = x.y;
-        } else {
-            s[rr][0] = __ldcs(p);
-        }
-    }
-}
-
-template <int D>
-__device__ __forceinline__ void load_tile_smem(const float* Ss, int r0, int c0,
-                                               float (&s)[RecShape<D>::RPW][RecShape<D>::CPT])
-{
-    constexpr int RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT;
-    static_assert(CPT == 4, "shared-memory tile path is for D = 128");
-#pragma unroll
-    for (int rr = 0; rr < RPW; ++rr) {
-        float4 x = *reinterpret_cast<const float4*>(Ss + (r0 + rr) * D + c0);
-        s[rr][0] = x.x; s[rr][1] = x.y; s[rr][2] = x.z; s[rr][3] = x.w;
-    }
-}
-
-template <int D> __device__ __forceinline__ void store_tile(float* Sg, int r0, int c0,
-                                                            const float (&s)[RecShape<D>::RPW][RecShape<D>::CPT])
-{
-    constexpr int RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT;
-#pragma unroll
-    for (int rr = 0; rr < RPW; ++rr) {
-        float* p = Sg + (size_t)(r0 + rr) * D + c0;
-        if constexpr (CPT == 4) {
-            st_stream4(p, make_float4(s[rr][0], s[rr][1], s[rr][2], s[rr][3]));
-        } else if constexpr (CPT == 2) {
-            __stcs(reinterpret_cast<float2*>(p), make_float2(s[rr][0], s[rr][1]));
-        } else {
-            __stcs(p, s[rr][0]);
-        }
-    }
-}
-
-// One row of the layer for one (sequence, head); called by all 256 threads,
-// in two steps.
-//
-// row_conv: on entry sm.cw / sm.dtb hold the head's parameters; win(c, j) is
-// raw value j (oldest first, j = K-1 the current row) of local channel c
-// (q | k | v), fr(i) the gate of key dim i.  Leaves the post-SiLU q|k|v row in
-// sm.act, each key dim's decay in sm.alpha and per-warp sums of squares of q'
-// and k' in sm.nrm.  The 3D conv channels and the D decays are 4D items taken
-// round-robin by the threads (two each at D = 128); the q and k channels fill
-// whole warps of the first round.  The thread that takes item c < 3D must be
-// the one that loaded sm.cw[c] (item 3D + i: sm.dtb[i]) when the caller
-// relies on that instead of a barrier.
-//
-// row_delta: the q and k inverse norms and beta into sm.scal[0..2], the delta
-// rule on S (in registers: warp w owns rows [RPW w, +RPW), lane l columns
-// [CPT l, +CPT)), sm.red the per-warp partials of S'^T k (so the normalised key
-// is act[D + i] * scal[1] and the update u_j = beta (act[2D + j] - sum_w
-// red[w][j]), the same expressions as here), and sm.red2 the per-warp partials
-// of S^T q.  No barrier after the last step: the caller may store S first.
-//
-// row_out: the output of column tid (tid < D), with the optional
-// sigmoid-gated RMSNorm; gval is the output gate of column tid.
-//
-// Every warp forms the norms, beta and the update of its own columns itself
-// from the same shared values in the same order (identical bits everywhere).
-// Decode, verify and commit use these functions and the expressions they log,
-// so a verified row has the bits of a decoded one.
-template <int D, typename Win, typename Fr>
-__device__ __forceinline__ void row_conv(RowSmem<D>& sm, int K, const RowConst& rc, Win win, Fr fr)
-{
-    const int tid = threadIdx.x, lane = tid & 31;
-    for (int it = tid; it < 4 * D; it += REC_THREADS) {
-        if (it < 3 * D) {
-            float acc = 0.0f;
-            for (int j = 0; j < K; ++j) acc = __fmaf_rn(sm.cw[it][j], win(it, j), acc);
-            const float x = siluf_(acc);
-            sm.act[it] = x;
-            if (it < 2 * D) {  // warp-uniform: D is a multiple of 32
-                const float ss = warp_sum(x * x);
-                if (lane == 0) sm.nrm[it >> 5] = ss;
-            }
-        } else {
-            const int i = it - 3 * D;
-            sm.alpha[i] = __expf(log_alpha(rc.gate_mode, rc.lb, rc.ea, fr(i), sm.dtb[i]));
-        }
-    }
-    row_sync();
-}
-
-template <int D>
-__device__ __forceinline__ void row_delta(RowSmem<D>& sm, float (&s)[RecShape<D>::RPW][RecShape<D>::CPT],
-                                          const RowConst& rc, float bval)
-{
-    constexpr int RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT, NP = D / 32;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r0 = warp * RPW, c0 = lane * CPT;
-
-    float sq = 0.0f, sk = 0.0f;
-#pragma unroll
-    for (int p = 0; p < NP; ++p) {
-        sq += sm.nrm[p];
-        sk += sm.nrm[NP + p];
-    }
-    const float rq = rsqrtf(sq + rc.l2_eps);
-    const float rk = rsqrtf(sk + rc.l2_eps);
-    const float beta = sigmoidf_(bval);
-    if (tid == 0) {
-        sm.scal[0] = rq;
-        sm.scal[1] = rk;
-        sm.scal[2] = beta;
-    }
-
-    // S' = Diag(alpha) S ; kv = S'^T k (partial over this warp's rows).  Column
-    // pairs in packed f32x2 arithmetic: the same rounded operations per element.
-    float kr[RPW], part[CPT];
-#pragma unroll
-    for (int rr = 0; rr < RPW; ++rr) kr[rr] = sm.act[D + r0 + rr] * rk;
-#pragma unroll
-    for (int cc = 0; cc < CPT; ++cc) part[cc] = 0.0f;
-#pragma unroll
-    for (int rr = 0; rr < RPW; ++rr) {
-        const float ai = sm.alpha[r0 + rr];
-        if constexpr (CPT % 2 == 0) {
-#pragma unroll
-            for (int cc = 0; cc < CPT; cc += 2) {
-                const float2 sp = __fmul2_rn(make_float2(ai, ai), make_float2(s[rr][cc], s[rr][cc + 1]));
-                const float2 pp = __ffma2_rn(sp, make_float2(kr[rr], kr[rr]), make_float2(part[cc], part[cc + 1]));
-                s[rr][cc] = sp.x;
-                s[rr][cc + 1] = sp.y;
-                part[cc] = pp.x;
-                part[cc + 1] = pp.y;
-            }
-        } else {
-#pragma unroll
-            for (int cc = 0; cc < CPT; ++cc) {
-                s[rr][cc] = __fmul_rn(ai, s[rr][cc]);
-                part[cc] = __fmaf_rn(s[rr][cc], kr[rr], part[cc]);
-            }
-        }
-    }
-#pragma unroll
-    for (int cc = 0; cc < CPT; ++cc) sm.red[warp][c0 + cc] = part[cc];
-    row_sync();
-
-    // u of this thread's columns: the partials summed in warp order
-    float uc[CPT], kv[CPT];
-#pragma unroll
-    for (int cc = 0; cc < CPT; ++cc) kv[cc] = 0.0f;
-#pragma unroll
-    for (int w = 0; w < REC_WARPS; ++w) {
-        if constexpr (CPT == 4) {
-            const float4 r4 = *reinterpret_cast<const float4*>(&sm.red[w][c0]);
-            kv[0] += r4.x;
-            kv[1] += r4.y;
-            kv[2] += r4.z;
-            kv[3] += r4.w;
-        } else {
-#pragma unroll
-            for (int cc = 0; cc < CPT; ++cc) kv[cc] += sm.red[w][c0 + cc];
-        }
-    }
-#pragma unroll
-    for (int cc = 0; cc < CPT; ++cc) {
-        uc[cc] = beta * (sm.act[2 * D + c0 + cc] - kv[cc]);
-        part[cc] = 0.0f;
-    }
-
-    // S = S' + k u^T ; o = S^T q (partial)
-#pragma unroll
-    for (int rr = 0; rr < RPW; ++rr) {
-        const float qi = sm.act[r0 + rr] * rq;
-        if constexpr (CPT % 2 == 0) {
-#pragma unroll
-            for (int cc = 0; cc < CPT; cc += 2) {
-                const float2 sn = __ffma2_rn(make_float2(kr[rr], kr[rr]), make_float2(uc[cc], uc[cc + 1]),
-                                             make_float2(s[rr][cc], s[rr][cc + 1]));
-                const float2 pp = __ffma2_rn(sn, make_float2(qi, qi), make_float2(part[cc], part[cc + 1]));
-                s[rr][cc] = sn.x;
-                s[rr][cc + 1] = sn.y;
-                part[cc] = pp.x;
-                part[cc + 1] = pp.y;
-            }
-        } else {
-#pragma unroll
-            for (int cc = 0; cc < CPT; ++cc) {
-                s[rr][cc] = __fmaf_rn(kr[rr], uc[cc], s[rr][cc]);
-                part[cc] = __fmaf_rn(s[rr][cc], qi, part[cc]);
-            }
-        }
-    }
-#pragma unroll
-    for (int cc = 0; cc < CPT; ++cc) sm.red2[warp][c0 + cc] = part[cc];
-}
-
-template <int D>
-__device__ __forceinline__ float row_out(RowSmem<D>& sm, const RowConst& rc, float gval, bool has_g)
-{
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    row_sync();
-    float o = 0.0f;
-    if (tid < D) {
-#pragma unroll
-        for (int w = 0; w < REC_WARPS; ++w) o += sm.red2[w][tid];
-        o *= rc.scale;
-    }
-    if (has_g) {
-        // sigmoid-gated RMSNorm over the head's D outputs
-        float sq = tid < D ? o * o : 0.0f;
-        sq = warp_sum(sq);
-        if (lane == 0 && warp < D / 32) sm.scal[4 + warp] = sq;
-        row_sync();
-        if (tid < D) {
-            float tot = 0.0f;
-            for (int w = 0; w < D / 32; ++w) tot += sm.scal[4 + w];
-            const float r = rsqrtf(tot * (1.0f / D) + rc.norm_eps);
-            const float w = rc.norm_w ? rc.norm_w[tid] : 1.0f;
-            o = o * r * w * sigmoidf_(gval);
-        }
-    }
-    return o;
-}
-
-// conv, delta rule and output of a row whose raw values sit in the window ring
-template <int D>
-__device__ __forceinline__ float row_step(RowSmem<D>& sm, float (&s)[RecShape<D>::RPW][RecShape<D>::CPT],
-                                          int t, int K, const RowConst& rc, float bval, float gval, bool has_g)
-{
-    row_conv<D>(sm, K, rc, [&](int c, int j) { return sm.win[ring(t - K + 1 + j)][c]; },
-                [&](int i) { return sm.fr[i]; });
-    row_delta<D>(sm, s, rc, bval);
-    return row_out<D>(sm, rc, gval, has_g);
-}
-
-// The update u_j of the last row_step (column j), from what it left in shared memory.
-template <int D> __device__ __forceinline__ float row_update(const RowSmem<D>& sm, int j)
-{
-    float kv = 0.0f;
-#pragma unroll
-    for (int w = 0; w < REC_WARPS; ++w) kv += sm.red[w][j];
-    return sm.scal[2] * (sm.act[2 * D + j] - kv);
-}
 
 // ------------------------------------------------------------------------
 // Staged window rows.  A verify window's draft rows (q, k, v, gate f, output
@@ -573,205 +262,6 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_recurrent_kernel(const Rec
             for (int r = 0; r < K - 1; ++r)
                 stv(cs + ((size_t)slot * (K - 1) + r) * conv_dim + ch, sm.win[ring(L - (K - 1) + r)][c]);
         }
-    }
-}
-
-// ------------------------------------------------------------------------
-// Streaming decode (D = 128): persistent CTAs, producer warp + 8 consumer warps.
-//
-// CTA c owns a contiguous, head-major range of units (u = head * N + seq), so
-// a CTA meets at most a couple of heads and loads each head's conv taps and
-// dt_bias once.  The producer keeps DEC_STAGES units in flight.
-
-constexpr int DEC_D = 128;
-constexpr int DEC_THREADS = REC_THREADS + 32;
-// three stages fit in shared memory with bf16 rows, two with fp32 rows
-template <typename IO> constexpr int dec_stages() { return sizeof(IO) == 2 ? 3 : 2; }
-
-template <typename IO> struct DecStage {
-    float S[DEC_D * DEC_D];        // the unit's state, row-major (64 KiB)
-    IO rows[5][DEC_D];             // raw q, k, v, gate, output-gate rows
-    IO hist[3][3][DEC_D];          // conv history [row][q|k|v][channel]
-    float bval;                    // beta logit
-    int slot;                      // state slot, or -1: skip the unit
-    int head;                      // head of the unit (with slot: where the new state goes)
-    int pad;
-};
-
-template <typename IO> struct DecSmem {
-    static constexpr int STAGES = dec_stages<IO>();
-    DecStage<IO> stage[STAGES];
-    RowSmem<DEC_D> row;
-    float normw[DEC_D];
-    uint64_t full[STAGES], empty[STAGES];
-};
-
-template <typename IO>
-__global__ void __launch_bounds__(DEC_THREADS, 1) kda_decode_stream_kernel(const RecArgs a)
-{
-    extern __shared__ __align__(128) unsigned char dyn_smem[];
-    DecSmem<IO>& sm = *reinterpret_cast<DecSmem<IO>*>(dyn_smem);
-    constexpr int D = DEC_D;
-    constexpr int DEC_STAGES = DecSmem<IO>::STAGES;
-    constexpr int RPW = RecShape<D>::RPW, CPT = RecShape<D>::CPT;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int H = a.H, K = a.K, N = a.N;
-    const int conv_dim = H * 3 * D;
-    const int units = N * H;
-    const int u_begin = (int)(((long long)units * blockIdx.x) / gridDim.x);
-    const int u_end = (int)(((long long)units * (blockIdx.x + 1)) / gridDim.x);
-
-    if (tid == 0) {
-        for (int s = 0; s < DEC_STAGES; ++s) {
-            ptx::mbar_init(&sm.full[s], 1);
-            ptx::mbar_init(&sm.empty[s], REC_WARPS);  // one arrival per row warp
-        }
-        ptx::fence_mbar_init();
-    }
-    __syncthreads();  // barrier initialisation visible to every thread
-    // Programmatic dependent launch: the next kernel on the stream may start its
-    // prologue now; every thread here waits for the previous kernel's completion
-    // (and its memory) before its first global access.
-    ptx::grid_launch_dependents();
-    ptx::grid_dependency_wait();
-    // gain of column tid: read back only by the same thread (row_out)
-    for (int c = tid; c < D; c += DEC_THREADS) sm.normw[c] = a.norm_w ? a.norm_w[c] : 1.0f;
-
-    const IO* q = static_cast<const IO*>(a.q);
-    const IO* k = static_cast<const IO*>(a.k);
-    const IO* v = static_cast<const IO*>(a.v);
-    const IO* f = static_cast<const IO*>(a.f);
-    const IO* b = static_cast<const IO*>(a.b);
-    const IO* g = static_cast<const IO*>(a.g);
-    IO* cs = static_cast<IO*>(a.conv_state);
-    const bool has_g = g != nullptr;
-
-    if (warp == REC_WARPS) {
-        // ---------------- producer: loads each unit into a stage and, once the
-        // row warps have left the unit's new state in that stage, stores it back
-        // with one bulk copy before the stage takes the next unit
-        if (lane != 0) return;
-        const uint64_t pol = ptx::policy_evict_first();
-        // wait until the row warps are done with stage s (phase n) and write its state back
-        auto write_back = [&](int s, int n) -> bool {
-            if (!ptx::mbar_wait(&sm.empty[s], n & 1)) {
-                flag_status(a.dev_status, KDA_DEV_TIMEOUT);
-                return false;
-            }
-            DecStage<IO>& st = sm.stage[s];
-            if (st.slot >= 0) {
-                ptx::bulk_s2g(a.rec_state + ((size_t)st.slot * H + st.head) * D * D, st.S, D * D * 4);
-                // the new conv state: the window's last K-1 raw rows (history rows 1.., then the current row)
-                for (int r = 0; r < K - 1; ++r)
-                    for (int seg = 0; seg < 3; ++seg)
-                        ptx::bulk_s2g(cs + ((size_t)st.slot * (K - 1) + r) * conv_dim + (size_t)seg * H * D + st.head * D,
-                                      r + 1 < K - 1 ? st.hist[r + 1][seg] : st.rows[seg], D * sizeof(IO));
-                ptx::bulk_commit();
-                ptx::bulk_wait_read_all();  // the stage may be refilled
-            }
-            return true;
-        };
-        const int count = u_end - u_begin;
-        for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
-            const int s = i % DEC_STAGES, n = i / DEC_STAGES;
-            if (n > 0 && !write_back(s, n - 1)) return;
-            DecStage<IO>& st = sm.stage[s];
-            const int h = u / N, seq = u % N;
-            int slot = a.slots ? a.slots[seq] : seq;
-            if (slot >= a.num_slots) {
-                flag_status(a.dev_status, KDA_DEV_BAD_SLOT);
-                slot = -1;
-            }
-            if (slot >= 0) {
-                const uint32_t rowb = D * sizeof(IO);
-                const uint32_t bytes = D * D * 4 + (has_g ? 5 : 4) * rowb + 3 * (K - 1) * rowb;
-                asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(ptx::smem_u32(&sm.full[s])),
-                             "r"(bytes) : "memory");
-                ptx::bulk_g2s_stream(st.S, a.rec_state + ((size_t)slot * H + h) * D * D, D * D * 4, &sm.full[s], pol);
-                const size_t rh = (size_t)seq * H + h;
-                ptx::bulk_g2s(st.rows[0], q + rh * D, rowb, &sm.full[s]);
-                ptx::bulk_g2s(st.rows[1], k + rh * D, rowb, &sm.full[s]);
-                ptx::bulk_g2s(st.rows[2], v + rh * D, rowb, &sm.full[s]);
-                ptx::bulk_g2s(st.rows[3], f + rh * D, rowb, &sm.full[s]);
-                if (has_g) ptx::bulk_g2s(st.rows[4], g + rh * D, rowb, &sm.full[s]);
-                for (int r = 0; r < K - 1; ++r)
-                    for (int seg = 0; seg < 3; ++seg)
-                        ptx::bulk_g2s(st.hist[r][seg],
-                                      cs + ((size_t)slot * (K - 1) + r) * conv_dim + (size_t)seg * H * D + h * D,
-                                      rowb, &sm.full[s]);
-                st.bval = ldv(b + rh);
-            }
-            st.slot = slot;
-            st.head = h;
-            ptx::mbar_arrive(&sm.full[s]);
-        }
-        // the last units' states
-        for (int i = count > DEC_STAGES ? count - DEC_STAGES : 0; i < count; ++i)
-            if (!write_back(i % DEC_STAGES, i / DEC_STAGES)) return;
-        ptx::bulk_wait_all();
-        return;
-    }
-
-    // ---------------- consumers (256 threads)
-    const int r0 = warp * RPW, c0 = lane * CPT;
-    float sreg[RPW][CPT];
-    int cur_head = -1;
-    RowConst rc{a.gate_mode, a.lb, 0.0f, a.l2_eps, a.norm_eps, a.scale, sm.normw};
-    for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
-        const int s = i % DEC_STAGES, n = i / DEC_STAGES;
-        const int h = u / N, seq = u % N;
-        if (h != cur_head) {
-            // this head's conv taps, dt_bias and decay scale (L2-resident), each
-            // loaded by the thread whose row_conv item reads it: no barrier needed
-            for (int it = tid; it < 4 * D; it += REC_THREADS) {
-                if (it < 3 * D) {
-                    const int ch = conv_channel<D>(it, h, H);
-                    for (int j = 0; j < K; ++j) sm.row.cw[it][j] = a.conv_w[(size_t)ch * K + j];
-                } else {
-                    sm.row.dtb[it - 3 * D] = a.dt_bias[(size_t)h * D + it - 3 * D];
-                }
-            }
-            rc.ea = expf(a.A_log[h]);
-            cur_head = h;
-        }
-        if (!ptx::mbar_wait(&sm.full[s], n & 1)) {
-            if (tid == 0) flag_status(a.dev_status, KDA_DEV_TIMEOUT);
-            return;
-        }
-        DecStage<IO>& st = sm.stage[s];
-        const int slot = st.slot;
-        float bval = 0.0f, gval = 0.0f;
-        if (slot < 0) {
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&sm.empty[s]);  // nothing to write back
-            continue;
-        }
-        load_tile_smem<D>(st.S, r0, c0, sreg);
-        bval = st.bval;
-        if (has_g && tid < D) gval = ldv(&st.rows[4][tid]);
-        // the conv window straight from the stage: raw rows K-1 history rows, then the current row
-        row_conv<D>(sm.row, K, rc,
-                    [&](int c, int j) {
-                        const int seg = c / D, ch = c % D;
-                        return j < K - 1 ? ldv(&st.hist[j][seg][ch]) : ldv(&st.rows[seg][ch]);
-                    },
-                    [&](int i) { return ldv(&st.rows[3][i]); });
-        row_delta<D>(sm.row, sreg, rc, bval);
-        // the new state goes back into the stage (the producer stores it with one
-        // bulk copy); the stores drain while the output step runs
-#pragma unroll
-        for (int rr = 0; rr < RPW; ++rr)
-            *reinterpret_cast<float4*>(st.S + (r0 + rr) * D + c0) =
-                make_float4(sreg[rr][0], sreg[rr][1], sreg[rr][2], sreg[rr][3]);
-        const float o = row_out<D>(sm.row, rc, gval, has_g);
-        const size_t rh = (size_t)seq * H + h;
-        if (tid < D) store_out(a.out, rh * D + tid, o, a.out_bf16);
-        // Each warp hands its part of the stage back.  No block barrier: the next
-        // unit's first writes to the row arrays come after its first barrier,
-        // which every warp reaches only after the reads of this unit.
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm.empty[s]);
     }
 }
 
@@ -1378,54 +868,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) kda_commit_stream_kernel(const
 // ------------------------------------------------------------------------
 // launchers
 
-static int sm_count()
-{
-    static int n[128];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 128) return 148;
-    if (n[dev] == 0) {
-        int c = 0;
-        cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
-        n[dev] = c > 0 ? c : 148;
-    }
-    return n[dev];
-}
 
-static_assert(sizeof(DecSmem<__nv_bfloat16>) <= 232448, "decode stage buffers exceed shared memory");
-static_assert(sizeof(DecSmem<float>) <= 232448, "decode stage buffers exceed shared memory");
 
-template <typename IO> static cudaError_t launch_decode_stream(const RecArgs& a, int units, cudaStream_t st)
-{
-    static bool attr_done[128];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const int smem = (int)sizeof(DecSmem<IO>);
-    if (dev >= 0 && dev < 128 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kda_decode_stream_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
-    // Streaming CTAs: about 27/32 of the SMs (128 of the 152 on GB300).  Measured:
-    // more concurrent state streams lower the total HBM rate (B = 256 decode:
-    // 6.24 TB/s with 128 CTAs, 5.86 TB/s with 152), while below ~112 CTAs the
-    // per-SM stream rate (~50 GB/s) becomes the limit.
-    const int cap = sm_count() * 27 / 32 > 0 ? sm_count() * 27 / 32 : 1;
-    const int grid = units < cap ? units : cap;
-    // launched as a programmatic dependent of the previous kernel on the stream:
-    // the launch and the prologue overlap that kernel's tail
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(DEC_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kda_decode_stream_kernel<IO>, a);
-}
 
 // The window modes stage rows in dynamic shared memory (VerSmem).
 template <int D, typename IO, int MODE> static cudaError_t launch_window(const RecArgs& a, int units, cudaStream_t st)
@@ -1484,7 +928,7 @@ cudaError_t launch_recurrent(int mode, int io_bf16, const RecArgs& a, int units,
     case 64: return io_bf16 ? launch_rec_d<64, __nv_bfloat16>(mode, a, units, st) : launch_rec_d<64, float>(mode, a, units, st);
     case 128:
         if (mode == REC_DECODE)
-            return io_bf16 ? launch_decode_stream<__nv_bfloat16>(a, units, st) : launch_decode_stream<float>(a, units, st);
+            return launch_decode_stream_d128(io_bf16, a, units, st);
         return io_bf16 ? launch_rec_d<128, __nv_bfloat16>(mode, a, units, st) : launch_rec_d<128, float>(mode, a, units, st);
     default: return cudaErrorInvalidValue;
     }

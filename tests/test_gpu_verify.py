@@ -214,3 +214,46 @@ def test_commit_verify_bad_accepted(cuda_lib):
     for b in (0, 2):
         assert torch.equal(fus.rec_state[b], sep.rec_state[b])
         assert torch.equal(fus.out[b * Wn:(b + 1) * Wn], sep.out[b * Wn:(b + 1) * Wn])
+
+
+def test_verify_slot_map_negative_and_bad(cuda_lib):
+    """dk = dv = 128 verify, commit and commit+verify with a slot map: a
+    negative slot skips its sequence (outputs and state untouched), a slot past
+    the pool is flagged and skipped, and the other sequences equal the same
+    window run with valid slots."""
+    B, Wn, H = 4, 6, 2
+    wl = W.make_workload("vslot", 77, [Wn] * B, H=H, d=128, K=4, io_dtype=W.BF16, gate_mode=W.SOFTPLUS,
+                         lower_bound=-5.0, out_gate=True, init_state="random", W=Wn, accepted=True)
+    ref = DeviceCase(wl, out_dtype=W.F32, num_slots=5, slots=[3, 0, 1, 2])
+    dc = DeviceCase(wl, out_dtype=W.F32, num_slots=5, slots=[3, -1, 1, 9])
+    for c in (ref, dc):
+        c.alloc_log()
+    dc.out.fill_(float("nan"))
+    rs0, cs0 = dc.rec_state.clone(), dc.conv_state.clone()
+    K.check(ref.verify())
+    K.check(dc.verify())
+    torch.cuda.synchronize()
+    assert int(dc.dev_status.item()) & K.KDA_DEV_BAD_SLOT
+    for b in (1, 3):
+        assert torch.all(torch.isnan(dc.out[b * Wn:(b + 1) * Wn]))
+    for b in (0, 2):
+        assert torch.equal(dc.out[b * Wn:(b + 1) * Wn], ref.out[b * Wn:(b + 1) * Wn])
+    # commit, then commit fused into a second verify of the same rows
+    acc = torch.tensor([3, 5, Wn, 2], dtype=torch.int32, device="cuda")
+    K.check(ref.commit(accepted=acc))
+    K.check(dc.commit(accepted=acc))
+    torch.cuda.synchronize()
+    assert torch.equal(dc.rec_state[0], rs0[0]) and torch.equal(dc.conv_state[0], cs0[0])  # slot 0: unused
+    for sl in (3, 1):
+        assert torch.equal(dc.rec_state[sl], ref.rec_state[sl])
+        assert torch.equal(dc.conv_state[sl], ref.conv_state[sl])
+    dc.out.fill_(float("nan"))
+    log2r, log2d = torch.empty_like(ref.log), torch.empty_like(dc.log)
+    K.check(_commit_verify(ref, acc, ref.log, log2r))
+    K.check(_commit_verify(dc, acc, dc.log, log2d))
+    torch.cuda.synchronize()
+    for b, sl in ((0, 3), (2, 1)):
+        assert torch.equal(dc.out[b * Wn:(b + 1) * Wn], ref.out[b * Wn:(b + 1) * Wn])
+        assert torch.equal(dc.rec_state[sl], ref.rec_state[sl])
+    for b in (1, 3):
+        assert torch.all(torch.isnan(dc.out[b * Wn:(b + 1) * Wn]))
