@@ -81,10 +81,12 @@ def test_verify_commit_shapes(cuda_lib, oracle_mod, d, io, gate, K, og):
 
 
 @pytest.mark.parametrize("Wn,io,gate,og", [(1, W.BF16, W.SAFE, True), (13, W.BF16, W.SOFTPLUS, True),
-                                         (17, W.F32, W.SAFE, False)])
+                                         (16, W.BF16, W.SAFE, False), (17, W.F32, W.SAFE, False)])
 def test_verify_commit_window_lengths(cuda_lib, oracle_mod, Wn, io, gate, og):
     """dk = dv = 128 windows of one row and of several staged 8-row blocks with
-    a ragged last block: serial-decode bits and oracle tolerance."""
+    a ragged last block, and the longest window the streaming commit stages
+    (16 rows; 17 commits through the per-unit kernel): serial-decode bits and
+    oracle tolerance."""
     B = 4
     wl = W.make_workload(f"verw{Wn}", 300 + Wn, [Wn] * B, H=3, d=128, K=4, io_dtype=io,
                          gate_mode=gate, lower_bound=-5.0, out_gate=og, init_state="random",
