@@ -1135,27 +1135,136 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
 // state-dependent products (third and fourth) and the outputs, chunk after
 // chunk.  The other CTAs are producers: they take (chain, chunk) tasks in
 // chunk-major order, run the state-independent part of the chunk
-// (chunk_intra) and publish its operands -- -W, Q o e^G (high, low), P (high,
-// low), K o e^{G_C - G} (high, low) in the shared-memory tile layout, U'^T and
-// e^{G_C} -- in a ring of SPLIT_RING slots per chain, with a release flag.
-// The chain waits for the flag, bulk-copies the tiles and returns the slot
-// (a consumed counter the producer waits on before reusing it).  Both sides
-// run the same instructions as the fused kernel on the same values, so the
-// results have the fused kernel's bits.  All waits are bounded.
+// (chunk_intra, the fused kernel's steps) and publish its operands -- -W,
+// Q o e^G, P and (K o e^{G_C - G})^T as bf16 high and low tiles, U'^T and
+// e^{G_C} in fp32 -- in a ring of SPLIT_RING slots per chain, with a release
+// flag.  The chain waits for the flag, bulk-copies the tiles and returns the
+// slot (a consumed counter the producer waits on before reusing it).  The
+// chain's products split S^T and U^T into bf16 high and low parts too and run
+// three-term bf16 products (kind::f16, fp32 accumulation): twice the tf32
+// tensor rate and half the published bytes, at an operand precision of 2^-16
+// (the tf32 splits of the fused kernel reach 2^-20; its single tf32 operands,
+// -W among them, 2^-12).  All waits are bounded.
 
 constexpr int SPLIT_RING = 8;
-// slot layout (bytes): third-product operands [0, 96 KiB), fourth-product
-// operands [96 KiB, 192 KiB), then U'^T and e^{G_C}
-constexpr uint32_t SL_NW = 0, SL_QE = 32768, SL_QEL = 65536;
-constexpr uint32_t SL_PH = 98304, SL_PL = 114688, SL_KD = 131072, SL_KDL = 163840;
-constexpr uint32_t SL_UT = 196608;   // U'^T: [quarter][lane][16] fp32
-constexpr uint32_t SL_GAM = 229376;  // e^{G_C}: [128] fp32
-constexpr uint32_t SLOT_BYTES = 230400;
-constexpr uint32_t SL_A_BYTES = 98304, SL_B_BYTES = 98304;
-// chain shared-memory tiles: the slot's first 192 KiB, same offsets
-// chain tensor memory: S^T, S_lo^T, U^T, U_lo^T, two O^T blocks (chunks alternate)
-constexpr uint32_t CT_ST = 0, CT_SL = 128, CT_UT = 256, CT_UL = 320, CT_OT0 = 384, CT_OT1 = 448;
+// Slot layout (bytes).  The chain's products run on bf16 operands split into a
+// high and a low part (x = hi + lo to within 2^-16 |x|; three-term products
+// hi*hi + hi*lo + lo*hi accumulate in fp32 at the bf16 tensor rate), in
+// K-major 128-byte-swizzled tiles of 64 bf16 per row: third-product operands
+// [0, 64 KiB) (-W and Q o e^G, 64 rows x 128 key dims), fourth-product
+// operands [64 KiB, 112 KiB) (P, 64 x 64, and (K o e^{G_C - G})^T, 128 key
+// dims x 64 rows), then U'^T and e^{G_C} in fp32.
+constexpr uint32_t SL_NWH = 0, SL_NWL = 16384, SL_QEH = 32768, SL_QEL = 49152;
+constexpr uint32_t SL_PH = 65536, SL_PL = 73728, SL_KDH = 81920, SL_KDL = 98304;
+constexpr uint32_t SL_UT = 114688;   // U'^T: [quarter][lane][16] fp32
+constexpr uint32_t SL_GAM = 147456;  // e^{G_C}: [128] fp32
+constexpr uint32_t SLOT_BYTES = 147968;
+constexpr uint32_t SL_A_BYTES = 65536, SL_B_BYTES = 49152;
+constexpr uint32_t BT64_KB = 8192;   // K-block stride of a 64-row bf16 tile
+constexpr uint32_t BT128_KB = 16384; // K-block stride of a 128-row bf16 tile
+// chain tile shared memory: the slot's first 112 KiB, same offsets.  Chain
+// tensor memory: S^T (fp32), S^T high and low (bf16 pairs), U^T (fp32), U^T
+// high and low (bf16 pairs), two O^T blocks (chunks alternate)
+constexpr uint32_t CT_ST = 0, CT_SH = 128, CT_SL = 192, CT_UT = 256, CT_UH = 320, CT_UL = 352;
+constexpr uint32_t CT_OT0 = 384, CT_OT1 = 448;
 static_assert(SL_A_BYTES + SL_B_BYTES <= (uint32_t)SM_MISC, "chain tiles overlap the scalars");
+static_assert(SLOT_BYTES % 16 == 0 && SL_UT % 16 == 0 && SL_GAM % 16 == 0, "bulk copies need 16-byte pieces");
+
+// byte offset of bf16 element (row, k) in a K-major SW128 bf16 tile (64 per
+// 128-byte row) whose K-blocks are `kbs` bytes apart
+__device__ __forceinline__ uint32_t swz16(int row, int k, int kbs)
+{
+    return (uint32_t)((k >> 6) * kbs + row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) + (k & 7) * 2);
+}
+
+// bf16 high and low parts of (x0, x1) as packed pairs (x0 in the low half):
+// hi = RN(x), lo = RN(x - hi); x - hi is exact in fp32
+__device__ __forceinline__ void bf16_split2(float x0, float x1, uint32_t& hi, uint32_t& lo)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// chain: S^T -> bf16 high and low pairs (this thread's 32 key dims)
+__device__ __forceinline__ void state_split16(uint32_t t_st, uint32_t t_sh, uint32_t t_sl)
+{
+    float s[32];
+    ptx::tmem_ld32(t_st, s);
+    uint32_t hi[16], lo[16];
+#pragma unroll
+    for (int x = 0; x < 16; ++x) bf16_split2(s[2 * x], s[2 * x + 1], hi[x], lo[x]);
+    ptx::tmem_st16u(t_sh, hi);
+    ptx::tmem_st16u(t_sl, lo);
+}
+
+// chain: S^T <- S^T Diag(gamma); U^T -> bf16 high and low pairs (this thread's 16 rows)
+__device__ __forceinline__ void rescale_split16(uint32_t t_st, uint32_t t_ut, uint32_t t_uh, uint32_t t_ul,
+                                                const float* gam32)
+{
+    float v[32];
+    ptx::tmem_ld32(t_st, v);
+#pragma unroll
+    for (int x = 0; x < 32; x += 4) {
+        const float4 g4 = *reinterpret_cast<const float4*>(gam32 + x);
+        const float2 a2 = __fmul2_rn(make_float2(v[x], v[x + 1]), make_float2(g4.x, g4.y));
+        const float2 b2 = __fmul2_rn(make_float2(v[x + 2], v[x + 3]), make_float2(g4.z, g4.w));
+        v[x] = a2.x; v[x + 1] = a2.y; v[x + 2] = b2.x; v[x + 3] = b2.y;
+    }
+    ptx::tmem_st32(t_st, v);
+    float u[RPT];
+    ptx::tmem_ld16(t_ut, u);
+    uint32_t hi[RPT / 2], lo[RPT / 2];
+#pragma unroll
+    for (int x = 0; x < RPT / 2; ++x) bf16_split2(u[2 * x], u[2 * x + 1], hi[x], lo[x]);
+    ptx::tmem_st8(t_uh, hi);
+    ptx::tmem_st8(t_ul, lo);
+}
+
+// chain, third product: U^T += S^T (-W)^T (issuer 0) and O^T = S^T (Q o e^G)^T
+// (issuer 1), all 64 chunk rows each (few large MMAs: the MMA count, not the
+// FLOPs, bounds these small products); three bf16 terms per K step.
+template <int UNR>
+__device__ __forceinline__ void issue_third16(unsigned char* sm, uint32_t tmem, int q, uint32_t c_ot, uint64_t* bar)
+{
+    ptx::tc_fence_after();
+    if (q < 2) {
+        const uint32_t id = ptx::idesc_bf16(128, 64);
+        const uint32_t c_d = q == 0 ? CT_UT : c_ot;
+        const uint64_t bh = dsc(sm, q == 0 ? SL_NWH : SL_QEH), bl = dsc(sm, q == 0 ? SL_NWL : SL_QEL);
+#pragma unroll UNR
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t kb = ((ks >> 2) * BT64_KB + (ks & 3) * 32) >> 4;
+            ptx::mma_bf16_ts(tmem + c_d, tmem + CT_SH + ks * 8, bh + kb, id, q == 0 || ks > 0);
+            ptx::mma_bf16_ts(tmem + c_d, tmem + CT_SH + ks * 8, bl + kb, id, 1);
+            ptx::mma_bf16_ts(tmem + c_d, tmem + CT_SL + ks * 8, bh + kb, id, 1);
+        }
+    }
+    ptx::mma_commit(bar);
+}
+
+// chain, fourth product: O^T += U^T P^T (issuer 0, all 64 chunk rows) and
+// S^T += U^T (K o e^{G_C - G}) (issuer 1, all 128 key dims).
+template <int UNR>
+__device__ __forceinline__ void issue_fourth16(unsigned char* sm, uint32_t tmem, int q, uint32_t c_ot, uint64_t* bar)
+{
+    ptx::tc_fence_after();
+    if (q < 2) {
+        const uint32_t id = q == 0 ? ptx::idesc_bf16(128, 64) : ptx::idesc_bf16(128, 128);
+        const uint32_t c_d = q == 0 ? c_ot : CT_ST;
+        const uint64_t bh = dsc(sm, q == 0 ? SL_PH : SL_KDH), bl = dsc(sm, q == 0 ? SL_PL : SL_KDL);
+#pragma unroll UNR
+        for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t kb = (ks * 32) >> 4;
+            ptx::mma_bf16_ts(tmem + c_d, tmem + CT_UH + ks * 8, bh + kb, id, 1);
+            ptx::mma_bf16_ts(tmem + c_d, tmem + CT_UH + ks * 8, bl + kb, id, 1);
+            ptx::mma_bf16_ts(tmem + c_d, tmem + CT_UL + ks * 8, bh + kb, id, 1);
+        }
+    }
+    ptx::mma_commit(bar);
+}
 
 struct SplitArgs {
     int* ready;            // [NC][SPLIT_RING]: chunk index + 1 published in the slot
@@ -1234,29 +1343,73 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
         }
         if (!chunk_intra(sm, ms, a, tc, nvalid, tmem, lane_base, ph)) break;
 
-        // publish: tiles by bulk copies, U'^T and e^{G_C} by plain stores
+        // publish: the chain's operands as bf16 high and low tiles (bulk copies),
+        // U'^T and e^{G_C} in fp32 (plain stores)
         unsigned char* dst = slot_ptr(sp, u, c);
-        store_neg_w(sm, SM_NW, tmem + lane_base + TM_WT + RPT * qq, qq, col);
         {
-            float v[RPT];
-            ptx::tmem_ld16(tmem + lane_base + TM_UT + RPT * qq, v);
-            float4* ut = reinterpret_cast<float4*>(dst + SL_UT + ((size_t)qq * D + col) * RPT * 4);
+            float w[RPT];  // W^T: key dim col, chunk rows [16 qq, +16)
+            ptx::tmem_ld16(tmem + lane_base + TM_WT + RPT * qq, w);
+            {
+                float v[RPT];
+                ptx::tmem_ld16(tmem + lane_base + TM_UT + RPT * qq, v);
+                float4* ut = reinterpret_cast<float4*>(dst + SL_UT + ((size_t)qq * D + col) * RPT * 4);
 #pragma unroll
-            for (int j = 0; j < RPT / 4; ++j) ut[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-            if (tid < D) reinterpret_cast<float*>(dst + SL_GAM)[tid] = ms.gamma[tid];
+                for (int j = 0; j < RPT / 4; ++j) ut[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                if (tid < D) reinterpret_cast<float*>(dst + SL_GAM)[tid] = ms.gamma[tid];
+            }
+            // the fp32 tiles into registers, four consecutive K elements at a time:
+            // Q o e^G (64 x 128), P (64 x 64), (K o e^{G_C - G})^T (128 x 64)
+            float4 qe4[4], p4[2], kd4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int e = tid + NT * j;
+                qe4[j] = *reinterpret_cast<const float4*>(sm + SM_QE + swz(e >> 5, (e & 31) * 4, T64_KB));
+                kd4[j] = *reinterpret_cast<const float4*>(sm + SM_KD + swz(e >> 4, (e & 15) * 4, 128 * 128));
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int e = tid + NT * j;
+                p4[j] = *reinterpret_cast<const float4*>(sm + SM_PH + swz(e >> 4, (e & 15) * 4, T64_KB));
+            }
+            __syncthreads();  // the fp32 tiles are read: the bf16 tiles may overwrite them
+            auto put4 = [&](uint32_t off_hi, uint32_t off_lo, float4 x) {
+                uint2 hi, lo;
+                bf16_split2(x.x, x.y, hi.x, lo.x);
+                bf16_split2(x.z, x.w, hi.y, lo.y);
+                *reinterpret_cast<uint2*>(sm + off_hi) = hi;
+                *reinterpret_cast<uint2*>(sm + off_lo) = lo;
+            };
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int e = tid + NT * j;
+                const uint32_t oq = swz16(e >> 5, (e & 31) * 4, BT64_KB), ok = swz16(e >> 4, (e & 15) * 4, BT128_KB);
+                put4(SL_QEH + oq, SL_QEL + oq, qe4[j]);
+                put4(SL_KDH + ok, SL_KDL + ok, kd4[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int e = tid + NT * j;
+                const uint32_t op = swz16(e >> 4, (e & 15) * 4, BT64_KB);
+                put4(SL_PH + op, SL_PL + op, p4[j]);
+            }
+            // -W: rows [16 qq, +16) of key dim col
+#pragma unroll
+            for (int x = 0; x < RPT; x += 2) {
+                uint32_t hi, lo;
+                bf16_split2(-w[x], -w[x + 1], hi, lo);
+                const uint32_t o0 = swz16(RPT * qq + x, col, BT64_KB), o1 = swz16(RPT * qq + x + 1, col, BT64_KB);
+                *reinterpret_cast<uint16_t*>(sm + SL_NWH + o0) = (uint16_t)(hi & 0xFFFFu);
+                *reinterpret_cast<uint16_t*>(sm + SL_NWH + o1) = (uint16_t)(hi >> 16);
+                *reinterpret_cast<uint16_t*>(sm + SL_NWL + o0) = (uint16_t)(lo & 0xFFFFu);
+                *reinterpret_cast<uint16_t*>(sm + SL_NWL + o1) = (uint16_t)(lo >> 16);
+            }
         }
         ptx::fence_proxy_async_smem();
         __threadfence();
         ptx::tc_fence_before();
         __syncthreads();
         if (tid == 0) {
-            ptx::bulk_s2g(dst + SL_NW, sm + SM_NW, 32768);
-            ptx::bulk_s2g(dst + SL_QE, sm + SM_QE, 32768);
-            ptx::bulk_s2g(dst + SL_QEL, sm + SM_QEL, 32768);
-            ptx::bulk_s2g(dst + SL_PH, sm + SM_PH, 16384);
-            ptx::bulk_s2g(dst + SL_PL, sm + SM_PL, 16384);
-            ptx::bulk_s2g(dst + SL_KD, sm + SM_KD, 32768);
-            ptx::bulk_s2g(dst + SL_KDL, sm + SM_KDL, 32768);
+            for (uint32_t o = 0; o < SL_A_BYTES + SL_B_BYTES; o += 16384) ptx::bulk_s2g(dst + o, sm + o, 16384);
             ptx::bulk_commit();
             ptx::bulk_wait_all();
             ptx::fence_proxy_async_global();
@@ -1354,7 +1507,8 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         const uint32_t c_ot = (c & 1) ? CT_OT1 : CT_OT0;
         ptx::tmem_st16(tmem + lane_base + CT_UT + RPT * qq, up);
         if (tid < D) ms.gamma[tid] = gam;
-        state_low(tmem + lane_base + CT_ST + 32 * qq, tmem + lane_base + CT_SL + 32 * qq);
+        state_split16(tmem + lane_base + CT_ST + 32 * qq, tmem + lane_base + CT_SH + 16 * qq,
+                      tmem + lane_base + CT_SL + 16 * qq);
         if (tid == 0 && !ptx::mbar_wait(&ms.rbar, c & 1)) {
             ms.err = 1;
             flag_status(a.dev_status, KDA_DEV_TIMEOUT);
@@ -1365,7 +1519,7 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         pend_a = false;
         if (issuer(tid) >= 0) {
             (void)ptx::mbar_try_wait(&ms.rbar, c & 1);  // completed: the tiles are visible to this issuer
-            issue_third<CHAIN_UNROLL>(sm, tmem, issuer(tid), SL_NW, SL_QE, SL_QEL, CT_UT, CT_ST, CT_SL, c_ot, &ms.bar);
+            issue_third16<CHAIN_UNROLL>(sm, tmem, issuer(tid), c_ot, &ms.bar);
         }
         mma_pending = true;
         // while the third product runs: the previous chunk's O^T and norm
@@ -1389,8 +1543,8 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
             pend_a = true;
         }
 
-        rescale_split(tmem + lane_base + CT_ST + 32 * qq, tmem + lane_base + CT_UT + RPT * qq,
-                      tmem + lane_base + CT_UL + RPT * qq, &ms.gamma[32 * qq]);
+        rescale_split16(tmem + lane_base + CT_ST + 32 * qq, tmem + lane_base + CT_UT + RPT * qq,
+                        tmem + lane_base + CT_UH + 8 * qq, tmem + lane_base + CT_UL + 8 * qq, &ms.gamma[32 * qq]);
         if (tid == 0 && !ptx::mbar_wait(&ms.bbar, c & 1)) {
             ms.err = 1;
             flag_status(a.dev_status, KDA_DEV_TIMEOUT);
@@ -1401,7 +1555,7 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         pend_b = false;
         if (issuer(tid) >= 0) {
             (void)ptx::mbar_try_wait(&ms.bbar, c & 1);
-            issue_fourth<CHAIN_UNROLL>(sm, tmem, issuer(tid), SL_PH, SL_PL, SL_KD, SL_KDL, CT_UT, CT_UL, CT_ST, c_ot, &ms.bar);
+            issue_fourth16<CHAIN_UNROLL>(sm, tmem, issuer(tid), c_ot, &ms.bar);
         }
         mma_pending = true;
         // while the fourth product runs: the rest of the previous chunk's outputs
