@@ -116,15 +116,18 @@ def test_sizes(lib):
 def test_split_workspace_size(lib):
     """Few long chains (N * H <= 64, T >= 1024 rows) take the split path:
     the schedule, then one release flag per ring slot plus one consumed
-    counter per chain, then 8 slots of 230400 bytes per chain (each slot: the
-    seven operand tiles of a chunk, U'^T and e^{G_C})."""
+    counter per chain, then 8 slots of 147968 bytes per chain (each slot: the
+    chain's operand tiles of a chunk as bf16 high and low parts, then U'^T and
+    e^{G_C} in fp32)."""
     p = _params(io_dtype=kda.KDA_DTYPE_BF16)  # H = 4
     N, nc = 2, 8
     sched = 1024                      # 3 int32 rounded to 256, then to 1 KiB
     flags = 1024                      # nc * 9 int32 = 288 bytes, rounded to 1 KiB
-    slot = 3 * 32768 + 2 * 16384 + 2 * 32768 + 32768 + 512  # tiles, U'^T, e^{G_C}
-    assert slot <= 230400
-    assert kda.kda_prefill_workspace_bytes(p, N, 1024) == sched + flags + nc * 8 * 230400
+    # -W and Q o e^G (64 x 128), P (64 x 64), (K o e^{G_C - G})^T (128 x 64), hi and lo,
+    # 2 bytes each; U'^T (128 x 64 fp32); e^{G_C} (128 fp32)
+    slot = 2 * 2 * (64 * 128 + 64 * 128 + 64 * 64 + 128 * 64) + 128 * 64 * 4 + 128 * 4
+    assert slot == 147968
+    assert kda.kda_prefill_workspace_bytes(p, N, 1024) == sched + flags + nc * 8 * slot
     assert kda.kda_prefill_workspace_bytes(p, N, 1023) == 256          # short: fused path
     assert kda.kda_prefill_workspace_bytes(p, 17, 4096) == 256 * 1     # 68 chains: fused path
     assert kda.kda_prefill_workspace_bytes(_params(gate_mode=kda.KDA_GATE_SOFTPLUS), N, 4096) == 0
