@@ -259,3 +259,26 @@ def test_verify_slot_map_negative_and_bad(cuda_lib):
         assert torch.equal(dc.rec_state[sl], ref.rec_state[sl])
     for b in (1, 3):
         assert torch.all(torch.isnan(dc.out[b * Wn:(b + 1) * Wn]))
+
+
+def _sweep_cases(n=12, seed=2024):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        d = 128 if i < 8 else int(rng.choice([32, 64]))
+        cases.append(dict(d=d, Wn=int(rng.integers(1, 21)), B=int(rng.integers(1, 4)), H=int(rng.integers(1, 3)),
+                          K=int(rng.integers(2, 5)), gate=[W.SAFE, W.SOFTPLUS][i % 2],
+                          io=[W.BF16, W.F32][(i // 2) % 2], og=bool(rng.integers(0, 2)), seed=5000 + i))
+    return cases
+
+
+@pytest.mark.parametrize("case", _sweep_cases(), ids=lambda c: f"d{c['d']}w{c['Wn']}b{c['B']}h{c['H']}k{c['K']}")
+def test_verify_commit_sweep(cuda_lib, oracle_mod, case):
+    """Seeded sweep of window lengths, batch sizes, head counts, conv taps,
+    gates, row types and output gates: verify and commit against serial
+    decode (bits) and the oracle."""
+    c = case
+    wl = W.make_workload(f"vsweep{c['seed']}", c["seed"], [c["Wn"]] * c["B"], H=c["H"], d=c["d"], K=c["K"],
+                         io_dtype=c["io"], gate_mode=c["gate"], lower_bound=-5.0, out_gate=c["og"],
+                         init_state="random", W=c["Wn"], accepted=True)
+    _check_window(cuda_lib, oracle_mod, wl, out_dtype=W.BF16 if c["io"] == W.BF16 else W.F32)
