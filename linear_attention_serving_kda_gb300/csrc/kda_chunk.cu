@@ -13,30 +13,30 @@
 // which is the gated delta rule unrolled over the chunk (exact in real
 // arithmetic).
 //
-// Tensor cores.  Every product is an M = 128 tcgen05.mma (kind::tf32, fp32
-// accumulation in tensor memory) in a transposed form whose M dimension is a
-// key or value dim: the state lives in TMEM as S^T (lane = value dim j,
-// column = key dim i) and, like U^T, feeds later MMAs straight from TMEM as
-// the A operand; B operands are K-major 128-byte-swizzled shared-memory tiles.
+// Tensor cores.  Every product is an M = 128 tcgen05.mma (fp32 accumulation
+// in tensor memory) in a transposed form whose M dimension is a key or value
+// dim: the state lives in TMEM as S^T (lane = value dim j, column = key dim i)
+// and, like U^T, feeds later MMAs straight from TMEM as the A operand; B
+// operands are K-major 128-byte-swizzled shared-memory tiles.
 //
 // Precision.  Outputs are dominated by the most recent rows (o_r ~ P_rr u_r),
 // a chain of products whose TF32 operand roundings (2^-11 each) would leave
 // the largest outputs ~1e-3 off -- too much for a per-element bound of a few
-// thousandths of the output RMS.  So the operands on that chain are split:
-// the high part is x itself as the tensor core reads it (the low 13 mantissa
-// bits dropped) and the low part the exact remainder, itself read truncated
-// (x = hi + lo to within 2^-20 |x|):
+// thousandths of the output RMS.  So the operands on that chain are split.
+// The first two products run on tf32 (kind::tf32): the high part is x itself
+// as the tensor core reads it (the low 13 mantissa bits dropped) and the low
+// part the exact remainder, itself read truncated (x = hi + lo to within
+// 2^-20 |x|):
 //     P (and A)  = [K~; Q~hi] (B1hi + B1lo)^T + [Q~lo; K~] B1hi^T
 //     U'         = T (Y + Ylo)                    (Y = Diag(beta) V)
-//     P U        = P_hi U_hi + P_hi U_lo + P_lo U_hi
-//     K~^T U     = KD_hi U_hi + KD_hi U_lo + KD_lo U_hi   (the state update)
-//     (Q o e^G) S = QE_hi S_hi + QE_hi S_lo + QE_lo S_hi  (long prompts: the
-//                  carried state dominates the outputs)
-//     W S        = W (S_hi + S_lo)        (the state read truncated would bias
-//                  U when the decay is weak and the state grows)
-// (S in TMEM and U in TMEM are split the same way in place).  The remaining
-// products (W and T) are single TF32 with operands rounded to nearest.  The
-// two A operands of the first product share their K~ rows: within each
+// with W = X T single TF32 (operands rounded to nearest).  The third and
+// fourth products run on bf16 (kind::f16: 16 K elements per MMA, half the
+// MMA chain of each accumulator): every operand is split into bf16 high and
+// low parts (x = hi + lo to within 2^-16 |x|) and a product sums hi*hi +
+// hi*lo + lo*hi:
+//     U = U' - W S,  (Q o e^G) S   (S^T split in TMEM; -W, Q o e^G tiles)
+//     P U,  (K o e^{G_C - G})^T U  (U^T split in TMEM; P, KD tiles)
+// The two A operands of the first product share their K~ rows: within each
 // 24 KiB K-block the layout is [Q~lo | K~ | Q~hi] (64 rows each),
 // and the tiles start at the first and the second 64-row slot.
 //
@@ -49,8 +49,9 @@
 //
 // TMEM (512 columns): S^T [0,128); X^T [128,192), Y^T [192,256),
 // Ylo^T [256,320), D1 [320,416), D1c [416,512) until the first product is
-// read; then W^T [320,384), U'^T -> U^T (hi) [384,448), O^T [128,192),
-// S^T low part [192,320), U^T low part [448,512).
+// read; then W^T [320,384), U'^T -> U^T [384,448), O^T [128,192), S^T high
+// and low bf16 pairs [192,256), [256,320), U^T high and low pairs [448,480),
+// [480,512).
 //
 // Staging.  A chunk's raw rows (q, k, v with the three rows before it, and
 // the gate rows) arrive as four 2-D tensor copies issued by one thread, the
@@ -242,6 +243,148 @@ __device__ __forceinline__ void stage_chunk(unsigned char* sm, const RawMaps& m,
     ptx::tma_load_2d(sm + SM_RAW + RAW_T, &m.k, h * D, c0 - HALO, &ms.rbar, pol);
     ptx::tma_load_2d(sm + SM_RAW + 2 * RAW_T, &m.v, h * D, c0 - HALO, &ms.rbar, pol);
     ptx::tma_load_2d(sm + SM_RAWF, &m.f, h * D, c0, &ms.rbar, pol);
+}
+
+// ---- bf16 operands of the third and fourth products.  Each operand x is
+// split into bf16 high and low parts (x = hi + lo to within 2^-16 |x|) and a
+// product sums hi*hi + hi*lo + lo*hi in fp32 (kind::f16): 16 K elements per
+// MMA halve each accumulator's chain of MMAs against tf32.  Tiles are K-major
+// and 128-byte swizzled with 64 bf16 per row; in tensor memory an A operand
+// holds two bf16 per 32-bit column, the even k in the low half.
+constexpr uint32_t BT64_KB = 8192;   // K-block stride of a 64-row bf16 tile
+constexpr uint32_t BT128_KB = 16384; // K-block stride of a 128-row bf16 tile
+
+// shared-memory offsets of the high and low tiles: -W and Q o e^G (64 rows x
+// 128 key dims), P (64 x 64), (K o e^{G_C - G})^T (128 key dims x 64 rows)
+struct Bf16Tiles {
+    uint32_t nwh, nwl, qeh, qel, ph, pl, kdh, kdl;
+};
+// tensor-memory columns: S^T (fp32), S^T high and low (bf16 pairs), U^T (fp32),
+// U^T high and low (bf16 pairs)
+struct Bf16Tmem {
+    uint32_t st, sh, sl, ut, uh, ul;
+};
+// the fused kernel's tiles (in the regions of the fp32 tiles they replace) and
+// columns (S^T pairs over the dead Y^T / Ylo^T, U^T pairs after U^T)
+constexpr uint32_t TM_SH = 192, TM_SL16 = 256, TM_UH = 448, TM_UL16 = 480;
+constexpr Bf16Tiles FUSED_TILES{SM_NW, SM_NW + 16384, SM_QE, SM_QE + 16384, SM_PH, SM_PH + 8192, SM_KD, SM_KD + 16384};
+constexpr Bf16Tmem FUSED_TMEM{TM_ST, TM_SH, TM_SL16, TM_UT, TM_UH, TM_UL16};
+static_assert(SM_NW % 1024 == 0 && SM_QE % 1024 == 0 && SM_PH % 1024 == 0 && SM_KD % 1024 == 0,
+              "bf16 tiles need 1 KiB-aligned bases");
+
+// byte offset of bf16 element (row, k) in a K-major SW128 bf16 tile (64 per
+// 128-byte row) whose K-blocks are `kbs` bytes apart
+__device__ __forceinline__ uint32_t swz16(int row, int k, int kbs)
+{
+    return (uint32_t)((k >> 6) * kbs + row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) + (k & 7) * 2);
+}
+
+// bf16 high and low parts of (x0, x1) as packed pairs (x0 in the low half):
+// hi = RN(x), lo = RN(x - hi); x - hi is exact in fp32
+__device__ __forceinline__ void bf16_split2(float x0, float x1, uint32_t& hi, uint32_t& lo)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// S^T -> bf16 high and low pairs (this thread's 32 key dims)
+__device__ __forceinline__ void state_split16(uint32_t t_st, uint32_t t_sh, uint32_t t_sl)
+{
+    float s[32];
+    ptx::tmem_ld32(t_st, s);
+    uint32_t hi[16], lo[16];
+#pragma unroll
+    for (int x = 0; x < 16; ++x) bf16_split2(s[2 * x], s[2 * x + 1], hi[x], lo[x]);
+    ptx::tmem_st16u(t_sh, hi);
+    ptx::tmem_st16u(t_sl, lo);
+}
+
+// S^T <- S^T Diag(gamma); U^T -> bf16 high and low pairs (this thread's 16 rows)
+__device__ __forceinline__ void rescale_split16(uint32_t t_st, uint32_t t_ut, uint32_t t_uh, uint32_t t_ul,
+                                                const float* gam32)
+{
+    float v[32];
+    ptx::tmem_ld32(t_st, v);
+#pragma unroll
+    for (int x = 0; x < 32; x += 4) {
+        const float4 g4 = *reinterpret_cast<const float4*>(gam32 + x);
+        const float2 a2 = __fmul2_rn(make_float2(v[x], v[x + 1]), make_float2(g4.x, g4.y));
+        const float2 b2 = __fmul2_rn(make_float2(v[x + 2], v[x + 3]), make_float2(g4.z, g4.w));
+        v[x] = a2.x; v[x + 1] = a2.y; v[x + 2] = b2.x; v[x + 3] = b2.y;
+    }
+    ptx::tmem_st32(t_st, v);
+    float u[RPT];
+    ptx::tmem_ld16(t_ut, u);
+    uint32_t hi[RPT / 2], lo[RPT / 2];
+#pragma unroll
+    for (int x = 0; x < RPT / 2; ++x) bf16_split2(u[2 * x], u[2 * x + 1], hi[x], lo[x]);
+    ptx::tmem_st8(t_uh, hi);
+    ptx::tmem_st8(t_ul, lo);
+}
+
+// -W as bf16 high and low tiles from W^T: this thread's 16 rows of key dim col
+__device__ __forceinline__ void store_neg_w16(unsigned char* sm, const Bf16Tiles tl, uint32_t t_wt, int qq, int col)
+{
+    float w[RPT];
+    ptx::tmem_ld16(t_wt, w);
+#pragma unroll
+    for (int x = 0; x < RPT; x += 2) {
+        uint32_t hi, lo;
+        bf16_split2(-w[x], -w[x + 1], hi, lo);
+        const uint32_t o0 = swz16(RPT * qq + x, col, BT64_KB), o1 = swz16(RPT * qq + x + 1, col, BT64_KB);
+        *reinterpret_cast<uint16_t*>(sm + tl.nwh + o0) = (uint16_t)(hi & 0xFFFFu);
+        *reinterpret_cast<uint16_t*>(sm + tl.nwh + o1) = (uint16_t)(hi >> 16);
+        *reinterpret_cast<uint16_t*>(sm + tl.nwl + o0) = (uint16_t)(lo & 0xFFFFu);
+        *reinterpret_cast<uint16_t*>(sm + tl.nwl + o1) = (uint16_t)(lo >> 16);
+    }
+}
+
+// third product: U^T += S^T (-W)^T (issuer 0) and O^T = S^T (Q o e^G)^T
+// (issuer 1), all 64 chunk rows each (few large MMAs: each accumulator's MMAs
+// are a chain in one thread); three bf16 terms per K step.
+template <int UNR>
+__device__ __forceinline__ void issue_third16(unsigned char* sm, uint32_t tmem, int q, const Bf16Tiles tl,
+                                              const Bf16Tmem tm, uint32_t c_ot, uint64_t* bar)
+{
+    ptx::tc_fence_after();
+    if (q < 2) {
+        const uint32_t id = ptx::idesc_bf16(128, 64);
+        const uint32_t c_d = q == 0 ? tm.ut : c_ot;
+        const uint64_t bh = dsc(sm, q == 0 ? tl.nwh : tl.qeh), bl = dsc(sm, q == 0 ? tl.nwl : tl.qel);
+#pragma unroll UNR
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t kb = ((ks >> 2) * BT64_KB + (ks & 3) * 32) >> 4;
+            ptx::mma_bf16_ts(tmem + c_d, tmem + tm.sh + ks * 8, bh + kb, id, q == 0 || ks > 0);
+            ptx::mma_bf16_ts(tmem + c_d, tmem + tm.sh + ks * 8, bl + kb, id, 1);
+            ptx::mma_bf16_ts(tmem + c_d, tmem + tm.sl + ks * 8, bh + kb, id, 1);
+        }
+    }
+    ptx::mma_commit(bar);
+}
+
+// fourth product: O^T += U^T P^T (issuer 0, all 64 chunk rows) and
+// S^T += U^T (K o e^{G_C - G}) (issuer 1, all 128 key dims).
+template <int UNR>
+__device__ __forceinline__ void issue_fourth16(unsigned char* sm, uint32_t tmem, int q, const Bf16Tiles tl,
+                                               const Bf16Tmem tm, uint32_t c_ot, uint64_t* bar)
+{
+    ptx::tc_fence_after();
+    if (q < 2) {
+        const uint32_t id = q == 0 ? ptx::idesc_bf16(128, 64) : ptx::idesc_bf16(128, 128);
+        const uint32_t c_d = q == 0 ? c_ot : tm.st;
+        const uint64_t bh = dsc(sm, q == 0 ? tl.ph : tl.kdh), bl = dsc(sm, q == 0 ? tl.pl : tl.kdl);
+#pragma unroll UNR
+        for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t kb = (ks * 32) >> 4;
+            ptx::mma_bf16_ts(tmem + c_d, tmem + tm.uh + ks * 8, bh + kb, id, 1);
+            ptx::mma_bf16_ts(tmem + c_d, tmem + tm.uh + ks * 8, bl + kb, id, 1);
+            ptx::mma_bf16_ts(tmem + c_d, tmem + tm.ul + ks * 8, bh + kb, id, 1);
+        }
+    }
+    ptx::mma_commit(bar);
 }
 
 // The products are issued by ISSUERS threads (lane 0 of warps 0..3, one per
@@ -578,38 +721,44 @@ __device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const C
         const int r = col - 64;
         float v[32];
         ptx::tmem_ld32(tmem + lane_base + TM_D1 + 32 * qq, v);
-        const uint32_t rowo = (uint32_t)((sb >> 5) * T64_KB + r * 128);
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-            float hi[4], lo[4];
+            float pv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int s2 = sb + 4 * c4 + u;
-                const float pv = s2 <= r ? v[4 * c4 + u] + ptmp[r * 65 + s2] : 0.0f;
-                hi[u] = pv;
-                lo[u] = tf32_lo(pv);
+                pv[u] = s2 <= r ? v[4 * c4 + u] + ptmp[r * 65 + s2] : 0.0f;
             }
-            const uint32_t o = rowo + ((c4 ^ (r & 7)) << 4);
-            *reinterpret_cast<float4*>(sm + SM_PH + o) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<float4*>(sm + SM_PL + o) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            uint2 hi, lo;
+            bf16_split2(pv[0], pv[1], hi.x, lo.x);
+            bf16_split2(pv[2], pv[3], hi.y, lo.y);
+            const uint32_t o = swz16(r, sb + 4 * c4, BT64_KB);
+            *reinterpret_cast<uint2*>(sm + FUSED_TILES.ph + o) = hi;
+            *reinterpret_cast<uint2*>(sm + FUSED_TILES.pl + o) = lo;
         }
     }
-    // ---- Q o e^G and (K o e^{G_C - G})^T tiles for the later products
+    // ---- Q o e^G and (K o e^{G_C - G})^T as bf16 high and low tiles for the
+    // third and fourth products
     {
-        float kd[RPT], kl[RPT];
 #pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-            st_raw(sm, SM_QE + swz(r0 + r, col, T64_KB), qe[r]);
-            kd[r] = kdx[r];
-            kl[r] = tf32_lo(kdx[r]);
+        for (int r = 0; r < RPT; r += 2) {  // element (row r0 + r, key dim col)
+            uint32_t hi, lo;
+            bf16_split2(qe[r], qe[r + 1], hi, lo);
+            const uint32_t o0 = swz16(r0 + r, col, BT64_KB), o1 = swz16(r0 + r + 1, col, BT64_KB);
+            *reinterpret_cast<uint16_t*>(sm + FUSED_TILES.qeh + o0) = (uint16_t)(hi & 0xFFFFu);
+            *reinterpret_cast<uint16_t*>(sm + FUSED_TILES.qeh + o1) = (uint16_t)(hi >> 16);
+            *reinterpret_cast<uint16_t*>(sm + FUSED_TILES.qel + o0) = (uint16_t)(lo & 0xFFFFu);
+            *reinterpret_cast<uint16_t*>(sm + FUSED_TILES.qel + o1) = (uint16_t)(lo >> 16);
         }
-        // KD^T row col, key rows [16 qq, +16): K-block qq >> 1, 16-byte chunks 4 (qq & 1) + j
+        // KD^T row col, chunk rows [16 qq, +16) along K
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int qd = 4 * (qq & 1) + j;
-            const uint32_t o = (qq >> 1) * 128 * 128 + col * 128 + ((qd ^ (col & 7)) << 4);
-            *reinterpret_cast<float4*>(sm + SM_KD + o) = make_float4(kd[4 * j], kd[4 * j + 1], kd[4 * j + 2], kd[4 * j + 3]);
-            *reinterpret_cast<float4*>(sm + SM_KDL + o) = make_float4(kl[4 * j], kl[4 * j + 1], kl[4 * j + 2], kl[4 * j + 3]);
+            uint2 hi, lo;
+            bf16_split2(kdx[4 * j], kdx[4 * j + 1], hi.x, lo.x);
+            bf16_split2(kdx[4 * j + 2], kdx[4 * j + 3], hi.y, lo.y);
+            const uint32_t o = swz16(col, RPT * qq + 4 * j, BT128_KB);
+            *reinterpret_cast<uint2*>(sm + FUSED_TILES.kdh + o) = hi;
+            *reinterpret_cast<uint2*>(sm + FUSED_TILES.kdl + o) = lo;
         }
     }
     ptx::tc_fence_before();
@@ -696,9 +845,6 @@ __device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const C
             st_hi(sm, SM_T + swz(32 + x1, lane, T64_KB), -s1);
         }
     }
-    // the low part of the QE tile (over the dead A and P scratch)
-#pragma unroll
-    for (int r = 0; r < RPT; ++r) st_raw(sm, SM_QEL + swz(r0 + r, col, T64_KB), tf32_lo(qe[r]));
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncthreads();
@@ -712,120 +858,6 @@ __device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const C
 // ---- inter-chunk steps shared by the fused kernel and the chain role of the
 // split kernel; `t*` arguments are TMEM addresses (this warp's lane quarter
 // included), `o*` shared-memory tile offsets.
-
-// S_lo = S - S_hi for this thread's 32 key dims
-__device__ __forceinline__ void state_low(uint32_t t_st, uint32_t t_sl)
-{
-    float s[32];
-    ptx::tmem_ld32(t_st, s);
-#pragma unroll
-    for (int x = 0; x < 32; x += 2) {
-        const float2 d = __fadd2_rn(make_float2(s[x], s[x + 1]),
-                                    make_float2(-__uint_as_float(__float_as_uint(s[x]) & 0xFFFFE000u),
-                                                -__uint_as_float(__float_as_uint(s[x + 1]) & 0xFFFFE000u)));
-        s[x] = d.x;
-        s[x + 1] = d.y;
-    }
-    ptx::tmem_st32(t_sl, s);
-}
-
-// -W tile (rounded to TF32) from W^T: this thread's 16 rows of column col
-__device__ __forceinline__ void store_neg_w(unsigned char* sm, uint32_t o_nw, uint32_t t_wt, int qq, int col)
-{
-    float v[RPT];
-    ptx::tmem_ld16(t_wt, v);
-#pragma unroll
-    for (int x = 0; x < RPT; ++x) st_hi(sm, o_nw + swz(RPT * qq + x, col, T64_KB), -v[x]);
-}
-
-// third product: U^T = U'^T - (S_hi + S_lo)^T W^T ; O^T = S^T (Q o e^G)^T (split).
-// Issuer q: U^T (q < 2) or O^T (q >= 2), chunk rows [32 (q & 1), +32).
-template <int UNR>
-__device__ __forceinline__ void issue_third(unsigned char* sm, uint32_t tmem, int q, uint32_t o_nw, uint32_t o_qe,
-                                            uint32_t o_qel, uint32_t c_ut, uint32_t c_st, uint32_t c_sl,
-                                            uint32_t c_ot, uint64_t* bar)
-{
-    ptx::tc_fence_after();
-    const uint32_t id = ptx::idesc_tf32(128, 32);
-    const uint32_t hr = (q & 1) * 32, ho = (hr * 128) >> 4;  // N-half: TMEM columns, tile rows
-    if (q < 2) {
-        const uint64_t dnw = dsc(sm, o_nw) + ho;
-#pragma unroll UNR
-        for (int ks = 0; ks < 16; ++ks) {
-            const uint32_t kb = ((ks >> 2) * T64_KB + (ks & 3) * 32) >> 4;
-            ptx::mma_tf32_ts(tmem + c_ut + hr, tmem + c_st + ks * 8, dnw + kb, id, 1);
-            ptx::mma_tf32_ts(tmem + c_ut + hr, tmem + c_sl + ks * 8, dnw + kb, id, 1);
-        }
-    } else {
-        const uint64_t dqe = dsc(sm, o_qe) + ho, dql = dsc(sm, o_qel) + ho;
-#pragma unroll UNR
-        for (int ks = 0; ks < 16; ++ks) {
-            const uint32_t kb = ((ks >> 2) * T64_KB + (ks & 3) * 32) >> 4;
-            ptx::mma_tf32_ts(tmem + c_ot + hr, tmem + c_st + ks * 8, dqe + kb, id, ks > 0);
-            ptx::mma_tf32_ts(tmem + c_ot + hr, tmem + c_sl + ks * 8, dqe + kb, id, 1);
-            ptx::mma_tf32_ts(tmem + c_ot + hr, tmem + c_st + ks * 8, dql + kb, id, 1);
-        }
-    }
-    ptx::mma_commit(bar);
-}
-
-// S^T <- S^T Diag(gamma); U^T stays as the high part of U, its low part beside it
-__device__ __forceinline__ void rescale_split(uint32_t t_st, uint32_t t_ut, uint32_t t_ul, const float* gam32)
-{
-    float v[32];
-    ptx::tmem_ld32(t_st, v);
-#pragma unroll
-    for (int x = 0; x < 32; x += 4) {
-        const float4 g4 = *reinterpret_cast<const float4*>(gam32 + x);
-        const float2 a2 = __fmul2_rn(make_float2(v[x], v[x + 1]), make_float2(g4.x, g4.y));
-        const float2 b2 = __fmul2_rn(make_float2(v[x + 2], v[x + 3]), make_float2(g4.z, g4.w));
-        v[x] = a2.x; v[x + 1] = a2.y; v[x + 2] = b2.x; v[x + 3] = b2.y;
-    }
-    ptx::tmem_st32(t_st, v);
-    float u[RPT];
-    ptx::tmem_ld16(t_ut, u);
-#pragma unroll
-    for (int x = 0; x < RPT; x += 2) {
-        const float2 d = __fadd2_rn(make_float2(u[x], u[x + 1]),
-                                    make_float2(-__uint_as_float(__float_as_uint(u[x]) & 0xFFFFE000u),
-                                                -__uint_as_float(__float_as_uint(u[x + 1]) & 0xFFFFE000u)));
-        u[x] = d.x;
-        u[x + 1] = d.y;
-    }
-    ptx::tmem_st16(t_ul, u);
-}
-
-// fourth product: O^T += U^T P^T ; S^T += U^T (K o e^{G_C - G}) (both split).
-// Issuer q: O^T chunk rows [32 q, +32) (q < 2) or S^T key dims [64 (q & 1), +64).
-template <int UNR>
-__device__ __forceinline__ void issue_fourth(unsigned char* sm, uint32_t tmem, int q, uint32_t o_ph, uint32_t o_pl,
-                                             uint32_t o_kd, uint32_t o_kdl, uint32_t c_ut, uint32_t c_ul,
-                                             uint32_t c_st, uint32_t c_ot, uint64_t* bar)
-{
-    ptx::tc_fence_after();
-    if (q < 2) {
-        const uint32_t id = ptx::idesc_tf32(128, 32), hr = q * 32, ho = (hr * 128) >> 4;
-        const uint64_t dph = dsc(sm, o_ph) + ho, dpl = dsc(sm, o_pl) + ho;
-#pragma unroll UNR
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t kb = ((ks >> 2) * T64_KB + (ks & 3) * 32) >> 4;
-            ptx::mma_tf32_ts(tmem + c_ot + hr, tmem + c_ut + ks * 8, dph + kb, id, 1);
-            ptx::mma_tf32_ts(tmem + c_ot + hr, tmem + c_ul + ks * 8, dph + kb, id, 1);
-            ptx::mma_tf32_ts(tmem + c_ot + hr, tmem + c_ut + ks * 8, dpl + kb, id, 1);
-        }
-    } else {
-        const uint32_t id = ptx::idesc_tf32(128, 64), hr = (q & 1) * 64, ho = (hr * 128) >> 4;
-        const uint64_t dkd = dsc(sm, o_kd) + ho, dkl = dsc(sm, o_kdl) + ho;
-#pragma unroll UNR
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t kb = ((ks >> 2) * 128 * 128 + (ks & 3) * 32) >> 4;
-            ptx::mma_tf32_ts(tmem + c_st + hr, tmem + c_ut + ks * 8, dkd + kb, id, 1);
-            ptx::mma_tf32_ts(tmem + c_st + hr, tmem + c_ul + ks * 8, dkd + kb, id, 1);
-            ptx::mma_tf32_ts(tmem + c_st + hr, tmem + c_ut + ks * 8, dkl + kb, id, 1);
-        }
-    }
-    ptx::mma_commit(bar);
-}
 
 // the output gate of this thread's 16 rows (bf16 bits, two rows per register)
 __device__ __forceinline__ void load_gate_bits(uint32_t (&gp)[RPT / 2], const ChunkArgs& a, int c0, int r0,
@@ -1076,14 +1108,15 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
         if (!chunk_intra(sm, ms, a, tc, nvalid, tmem, lane_base, ph)) break;
 
         // ---- -W tile from W^T (lane i = col, rows [16 qq, +16)); S_lo = S - S_hi (key dims [32 qq, +32))
-        store_neg_w(sm, SM_NW, tmem + lane_base + TM_WT + RPT * qq, qq, col);
-        state_low(tmem + lane_base + TM_ST + 32 * qq, tmem + lane_base + TM_SL + 32 * qq);
+        store_neg_w16(sm, FUSED_TILES, tmem + lane_base + TM_WT + RPT * qq, qq, col);
+        state_split16(tmem + lane_base + TM_ST + 32 * qq, tmem + lane_base + TM_SH + 16 * qq,
+                      tmem + lane_base + TM_SL16 + 16 * qq);
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncthreads();
 
         if (issuer(tid) >= 0)
-            issue_third<ISSUE_UNROLL>(sm, tmem, issuer(tid), SM_NW, SM_QE, SM_QEL, TM_UT, TM_ST, TM_SL, TM_OT, &ms.bar);
+            issue_third16<ISSUE_UNROLL>(sm, tmem, issuer(tid), FUSED_TILES, FUSED_TMEM, TM_OT, &ms.bar);
         if (!wait_mma(ms, ph, a.dev_status)) break;
 
         // the raw staging region is free from here: prefetch the next chunk's rows
@@ -1093,13 +1126,13 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
             if (tid < C && c0 + C + tid < seg1) bnext = __bfloat162float(bg[(size_t)(c0 + C + tid) * H + h]);
         }
 
-        rescale_split(tmem + lane_base + TM_ST + 32 * qq, tmem + lane_base + TM_UT + RPT * qq,
-                      tmem + lane_base + TM_UL + RPT * qq, &ms.gamma[32 * qq]);
+        rescale_split16(tmem + lane_base + TM_ST + 32 * qq, tmem + lane_base + TM_UT + RPT * qq,
+                        tmem + lane_base + TM_UH + 8 * qq, tmem + lane_base + TM_UL16 + 8 * qq, &ms.gamma[32 * qq]);
         ptx::tc_fence_before();
         __syncthreads();
 
         if (issuer(tid) >= 0)
-            issue_fourth<ISSUE_UNROLL>(sm, tmem, issuer(tid), SM_PH, SM_PL, SM_KD, SM_KDL, TM_UT, TM_UL, TM_ST, TM_OT, &ms.bar);
+            issue_fourth16<ISSUE_UNROLL>(sm, tmem, issuer(tid), FUSED_TILES, FUSED_TMEM, TM_OT, &ms.bar);
         uint32_t gp[RPT / 2];
         load_gate_bits(gp, a, c0, r0, nvalid, h, col);  // while the product runs
         if (!wait_mma(ms, ph, a.dev_status)) break;
@@ -1139,12 +1172,11 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
 // Q o e^G, P and (K o e^{G_C - G})^T as bf16 high and low tiles, U'^T and
 // e^{G_C} in fp32 -- in a ring of SPLIT_RING slots per chain, with a release
 // flag.  The chain waits for the flag, bulk-copies the tiles and returns the
-// slot (a consumed counter the producer waits on before reusing it).  The
-// chain's products split S^T and U^T into bf16 high and low parts too and run
-// three-term bf16 products (kind::f16, fp32 accumulation): twice the tf32
-// tensor rate and half the published bytes, at an operand precision of 2^-16
-// (the tf32 splits of the fused kernel reach 2^-20; its single tf32 operands,
-// -W among them, 2^-12).  All waits are bounded.
+// slot (a consumed counter the producer waits on before reusing it).  Both
+// sides run the fused kernel's instructions on the same values (the producers
+// publish the bf16 tiles chunk_intra builds; the chain runs the fused kernel's
+// bf16 third and fourth products), so the results have the fused kernel's
+// bits.  All waits are bounded.
 
 constexpr int SPLIT_RING = 8;
 // Slot layout (bytes).  The chain's products run on bf16 operands split into a
@@ -1160,111 +1192,15 @@ constexpr uint32_t SL_UT = 114688;   // U'^T: [quarter][lane][16] fp32
 constexpr uint32_t SL_GAM = 147456;  // e^{G_C}: [128] fp32
 constexpr uint32_t SLOT_BYTES = 147968;
 constexpr uint32_t SL_A_BYTES = 65536, SL_B_BYTES = 49152;
-constexpr uint32_t BT64_KB = 8192;   // K-block stride of a 64-row bf16 tile
-constexpr uint32_t BT128_KB = 16384; // K-block stride of a 128-row bf16 tile
 // chain tile shared memory: the slot's first 112 KiB, same offsets.  Chain
 // tensor memory: S^T (fp32), S^T high and low (bf16 pairs), U^T (fp32), U^T
 // high and low (bf16 pairs), two O^T blocks (chunks alternate)
 constexpr uint32_t CT_ST = 0, CT_SH = 128, CT_SL = 192, CT_UT = 256, CT_UH = 320, CT_UL = 352;
 constexpr uint32_t CT_OT0 = 384, CT_OT1 = 448;
+constexpr Bf16Tiles CHAIN_TILES{SL_NWH, SL_NWL, SL_QEH, SL_QEL, SL_PH, SL_PL, SL_KDH, SL_KDL};
+constexpr Bf16Tmem CHAIN_TMEM{CT_ST, CT_SH, CT_SL, CT_UT, CT_UH, CT_UL};
 static_assert(SL_A_BYTES + SL_B_BYTES <= (uint32_t)SM_MISC, "chain tiles overlap the scalars");
 static_assert(SLOT_BYTES % 16 == 0 && SL_UT % 16 == 0 && SL_GAM % 16 == 0, "bulk copies need 16-byte pieces");
-
-// byte offset of bf16 element (row, k) in a K-major SW128 bf16 tile (64 per
-// 128-byte row) whose K-blocks are `kbs` bytes apart
-__device__ __forceinline__ uint32_t swz16(int row, int k, int kbs)
-{
-    return (uint32_t)((k >> 6) * kbs + row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) + (k & 7) * 2);
-}
-
-// bf16 high and low parts of (x0, x1) as packed pairs (x0 in the low half):
-// hi = RN(x), lo = RN(x - hi); x - hi is exact in fp32
-__device__ __forceinline__ void bf16_split2(float x0, float x1, uint32_t& hi, uint32_t& lo)
-{
-    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-    const float2 hf = __bfloat1622float2(h);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-    hi = *reinterpret_cast<const uint32_t*>(&h);
-    lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-
-// chain: S^T -> bf16 high and low pairs (this thread's 32 key dims)
-__device__ __forceinline__ void state_split16(uint32_t t_st, uint32_t t_sh, uint32_t t_sl)
-{
-    float s[32];
-    ptx::tmem_ld32(t_st, s);
-    uint32_t hi[16], lo[16];
-#pragma unroll
-    for (int x = 0; x < 16; ++x) bf16_split2(s[2 * x], s[2 * x + 1], hi[x], lo[x]);
-    ptx::tmem_st16u(t_sh, hi);
-    ptx::tmem_st16u(t_sl, lo);
-}
-
-// chain: S^T <- S^T Diag(gamma); U^T -> bf16 high and low pairs (this thread's 16 rows)
-__device__ __forceinline__ void rescale_split16(uint32_t t_st, uint32_t t_ut, uint32_t t_uh, uint32_t t_ul,
-                                                const float* gam32)
-{
-    float v[32];
-    ptx::tmem_ld32(t_st, v);
-#pragma unroll
-    for (int x = 0; x < 32; x += 4) {
-        const float4 g4 = *reinterpret_cast<const float4*>(gam32 + x);
-        const float2 a2 = __fmul2_rn(make_float2(v[x], v[x + 1]), make_float2(g4.x, g4.y));
-        const float2 b2 = __fmul2_rn(make_float2(v[x + 2], v[x + 3]), make_float2(g4.z, g4.w));
-        v[x] = a2.x; v[x + 1] = a2.y; v[x + 2] = b2.x; v[x + 3] = b2.y;
-    }
-    ptx::tmem_st32(t_st, v);
-    float u[RPT];
-    ptx::tmem_ld16(t_ut, u);
-    uint32_t hi[RPT / 2], lo[RPT / 2];
-#pragma unroll
-    for (int x = 0; x < RPT / 2; ++x) bf16_split2(u[2 * x], u[2 * x + 1], hi[x], lo[x]);
-    ptx::tmem_st8(t_uh, hi);
-    ptx::tmem_st8(t_ul, lo);
-}
-
-// chain, third product: U^T += S^T (-W)^T (issuer 0) and O^T = S^T (Q o e^G)^T
-// (issuer 1), all 64 chunk rows each (few large MMAs: the MMA count, not the
-// FLOPs, bounds these small products); three bf16 terms per K step.
-template <int UNR>
-__device__ __forceinline__ void issue_third16(unsigned char* sm, uint32_t tmem, int q, uint32_t c_ot, uint64_t* bar)
-{
-    ptx::tc_fence_after();
-    if (q < 2) {
-        const uint32_t id = ptx::idesc_bf16(128, 64);
-        const uint32_t c_d = q == 0 ? CT_UT : c_ot;
-        const uint64_t bh = dsc(sm, q == 0 ? SL_NWH : SL_QEH), bl = dsc(sm, q == 0 ? SL_NWL : SL_QEL);
-#pragma unroll UNR
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t kb = ((ks >> 2) * BT64_KB + (ks & 3) * 32) >> 4;
-            ptx::mma_bf16_ts(tmem + c_d, tmem + CT_SH + ks * 8, bh + kb, id, q == 0 || ks > 0);
-            ptx::mma_bf16_ts(tmem + c_d, tmem + CT_SH + ks * 8, bl + kb, id, 1);
-            ptx::mma_bf16_ts(tmem + c_d, tmem + CT_SL + ks * 8, bh + kb, id, 1);
-        }
-    }
-    ptx::mma_commit(bar);
-}
-
-// chain, fourth product: O^T += U^T P^T (issuer 0, all 64 chunk rows) and
-// S^T += U^T (K o e^{G_C - G}) (issuer 1, all 128 key dims).
-template <int UNR>
-__device__ __forceinline__ void issue_fourth16(unsigned char* sm, uint32_t tmem, int q, uint32_t c_ot, uint64_t* bar)
-{
-    ptx::tc_fence_after();
-    if (q < 2) {
-        const uint32_t id = q == 0 ? ptx::idesc_bf16(128, 64) : ptx::idesc_bf16(128, 128);
-        const uint32_t c_d = q == 0 ? c_ot : CT_ST;
-        const uint64_t bh = dsc(sm, q == 0 ? SL_PH : SL_KDH), bl = dsc(sm, q == 0 ? SL_PL : SL_KDL);
-#pragma unroll UNR
-        for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t kb = (ks * 32) >> 4;
-            ptx::mma_bf16_ts(tmem + c_d, tmem + CT_UH + ks * 8, bh + kb, id, 1);
-            ptx::mma_bf16_ts(tmem + c_d, tmem + CT_UH + ks * 8, bl + kb, id, 1);
-            ptx::mma_bf16_ts(tmem + c_d, tmem + CT_UL + ks * 8, bh + kb, id, 1);
-        }
-    }
-    ptx::mma_commit(bar);
-}
 
 struct SplitArgs {
     int* ready;            // [NC][SPLIT_RING]: chunk index + 1 published in the slot
@@ -1343,73 +1279,28 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
         }
         if (!chunk_intra(sm, ms, a, tc, nvalid, tmem, lane_base, ph)) break;
 
-        // publish: the chain's operands as bf16 high and low tiles (bulk copies),
-        // U'^T and e^{G_C} in fp32 (plain stores)
+        // publish: the chain's operands as the bf16 high and low tiles
+        // chunk_intra built (and -W from W^T), by bulk copies; U'^T and e^{G_C}
+        // in fp32 by plain stores
         unsigned char* dst = slot_ptr(sp, u, c);
+        store_neg_w16(sm, FUSED_TILES, tmem + lane_base + TM_WT + RPT * qq, qq, col);
         {
-            float w[RPT];  // W^T: key dim col, chunk rows [16 qq, +16)
-            ptx::tmem_ld16(tmem + lane_base + TM_WT + RPT * qq, w);
-            {
-                float v[RPT];
-                ptx::tmem_ld16(tmem + lane_base + TM_UT + RPT * qq, v);
-                float4* ut = reinterpret_cast<float4*>(dst + SL_UT + ((size_t)qq * D + col) * RPT * 4);
+            float v[RPT];
+            ptx::tmem_ld16(tmem + lane_base + TM_UT + RPT * qq, v);
+            float4* ut = reinterpret_cast<float4*>(dst + SL_UT + ((size_t)qq * D + col) * RPT * 4);
 #pragma unroll
-                for (int j = 0; j < RPT / 4; ++j) ut[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                if (tid < D) reinterpret_cast<float*>(dst + SL_GAM)[tid] = ms.gamma[tid];
-            }
-            // the fp32 tiles into registers, four consecutive K elements at a time:
-            // Q o e^G (64 x 128), P (64 x 64), (K o e^{G_C - G})^T (128 x 64)
-            float4 qe4[4], p4[2], kd4[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int e = tid + NT * j;
-                qe4[j] = *reinterpret_cast<const float4*>(sm + SM_QE + swz(e >> 5, (e & 31) * 4, T64_KB));
-                kd4[j] = *reinterpret_cast<const float4*>(sm + SM_KD + swz(e >> 4, (e & 15) * 4, 128 * 128));
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int e = tid + NT * j;
-                p4[j] = *reinterpret_cast<const float4*>(sm + SM_PH + swz(e >> 4, (e & 15) * 4, T64_KB));
-            }
-            __syncthreads();  // the fp32 tiles are read: the bf16 tiles may overwrite them
-            auto put4 = [&](uint32_t off_hi, uint32_t off_lo, float4 x) {
-                uint2 hi, lo;
-                bf16_split2(x.x, x.y, hi.x, lo.x);
-                bf16_split2(x.z, x.w, hi.y, lo.y);
-                *reinterpret_cast<uint2*>(sm + off_hi) = hi;
-                *reinterpret_cast<uint2*>(sm + off_lo) = lo;
-            };
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int e = tid + NT * j;
-                const uint32_t oq = swz16(e >> 5, (e & 31) * 4, BT64_KB), ok = swz16(e >> 4, (e & 15) * 4, BT128_KB);
-                put4(SL_QEH + oq, SL_QEL + oq, qe4[j]);
-                put4(SL_KDH + ok, SL_KDL + ok, kd4[j]);
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int e = tid + NT * j;
-                const uint32_t op = swz16(e >> 4, (e & 15) * 4, BT64_KB);
-                put4(SL_PH + op, SL_PL + op, p4[j]);
-            }
-            // -W: rows [16 qq, +16) of key dim col
-#pragma unroll
-            for (int x = 0; x < RPT; x += 2) {
-                uint32_t hi, lo;
-                bf16_split2(-w[x], -w[x + 1], hi, lo);
-                const uint32_t o0 = swz16(RPT * qq + x, col, BT64_KB), o1 = swz16(RPT * qq + x + 1, col, BT64_KB);
-                *reinterpret_cast<uint16_t*>(sm + SL_NWH + o0) = (uint16_t)(hi & 0xFFFFu);
-                *reinterpret_cast<uint16_t*>(sm + SL_NWH + o1) = (uint16_t)(hi >> 16);
-                *reinterpret_cast<uint16_t*>(sm + SL_NWL + o0) = (uint16_t)(lo & 0xFFFFu);
-                *reinterpret_cast<uint16_t*>(sm + SL_NWL + o1) = (uint16_t)(lo >> 16);
-            }
+            for (int j = 0; j < RPT / 4; ++j) ut[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            if (tid < D) reinterpret_cast<float*>(dst + SL_GAM)[tid] = ms.gamma[tid];
         }
         ptx::fence_proxy_async_smem();
         __threadfence();
         ptx::tc_fence_before();
         __syncthreads();
         if (tid == 0) {
-            for (uint32_t o = 0; o < SL_A_BYTES + SL_B_BYTES; o += 16384) ptx::bulk_s2g(dst + o, sm + o, 16384);
+            ptx::bulk_s2g(dst + SL_NWH, sm + FUSED_TILES.nwh, 32768);  // -W high, low
+            ptx::bulk_s2g(dst + SL_QEH, sm + FUSED_TILES.qeh, 32768);  // Q o e^G high, low
+            ptx::bulk_s2g(dst + SL_PH, sm + FUSED_TILES.ph, 16384);    // P high, low
+            ptx::bulk_s2g(dst + SL_KDH, sm + FUSED_TILES.kdh, 32768);  // (K o e^{G_C - G})^T high, low
             ptx::bulk_commit();
             ptx::bulk_wait_all();
             ptx::fence_proxy_async_global();
@@ -1519,7 +1410,7 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         pend_a = false;
         if (issuer(tid) >= 0) {
             (void)ptx::mbar_try_wait(&ms.rbar, c & 1);  // completed: the tiles are visible to this issuer
-            issue_third16<CHAIN_UNROLL>(sm, tmem, issuer(tid), c_ot, &ms.bar);
+            issue_third16<CHAIN_UNROLL>(sm, tmem, issuer(tid), CHAIN_TILES, CHAIN_TMEM, c_ot, &ms.bar);
         }
         mma_pending = true;
         // while the third product runs: the previous chunk's O^T and norm
@@ -1555,7 +1446,7 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         pend_b = false;
         if (issuer(tid) >= 0) {
             (void)ptx::mbar_try_wait(&ms.bbar, c & 1);
-            issue_fourth16<CHAIN_UNROLL>(sm, tmem, issuer(tid), c_ot, &ms.bar);
+            issue_fourth16<CHAIN_UNROLL>(sm, tmem, issuer(tid), CHAIN_TILES, CHAIN_TMEM, c_ot, &ms.bar);
         }
         mma_pending = true;
         // while the fourth product runs: the rest of the previous chunk's outputs

@@ -2,11 +2,12 @@
 
 With N * H <= 64 and T >= 1024 rows, kda_prefill_varlen runs one persistent
 grid in which producer CTAs compute each chunk's state-independent operands
-and chain CTAs apply them in order.  The producers run the fused kernel's
-steps; the chain's products run on bf16 high/low operand splits instead of
-tf32 ones, so the results are compared with the oracle and with the fused
-kernel (the allocation-free entry point always takes it) at the parity
-tolerance; conv states are copies and must match exactly.
+and chain CTAs apply them in order.  Both run the fused kernel's steps on
+the same values (the producers publish the bf16 tiles the fused kernel builds,
+and the chain runs its bf16 products), so the results must have the fused
+kernel's bits -- the allocation-free entry point always takes the fused
+kernel, which gives the reference here -- and stay within the parity
+tolerance of the oracle.
 """
 import numpy as np
 import pytest
@@ -63,12 +64,12 @@ def _units_close(oracle_mod, wl, dc, units, what):
 
 
 @pytest.mark.parametrize("lens,H,og,init", CASES)
-def test_split_against_oracle_and_fused(cuda_lib, oracle_mod, lens, H, og, init):
+def test_split_has_fused_bits_and_oracle_parity(cuda_lib, oracle_mod, lens, H, og, init):
     wl = W.make_workload("split", 800 + sum(lens) + H, lens, H=H, d=128, K=4, io_dtype=W.BF16,
                          gate_mode=W.SAFE, lower_bound=-5.0, out_gate=og, init_state=init)
     p, f = _both(wl, out_dtype=W.F32)
-    assert_close(to_np(p.out[:wl.T]), to_np(f.out[:wl.T]), "split vs fused out")
-    assert_close(to_np(p.rec_state), to_np(f.rec_state), "split vs fused state")
+    assert torch.equal(p.out[:wl.T], f.out[:wl.T])
+    assert torch.equal(p.rec_state, f.rec_state)
     assert torch.equal(p.conv_state, f.conv_state)
     units = [(s_, h) for s_ in range(wl.N) if lens[s_] > 0 for h in sorted({0, H - 1})]
     _units_close(oracle_mod, wl, p, units, "split vs oracle")
@@ -91,20 +92,16 @@ def test_split_against_oracle(cuda_lib, oracle_mod):
 
 
 def test_split_slots(cuda_lib):
-    """A state pool with a skipped sequence: split and fused agree within the
-    tolerance (conv states exactly), and the skipped sequence's slot and rows
-    are untouched."""
+    """A state pool with a skipped sequence: split and fused agree bit for
+    bit, and the skipped sequence's slot and rows are untouched."""
     lens = [900, 500, 800]
     wl = W.make_workload("split_s", 812, lens, H=4, d=128, K=4, io_dtype=W.BF16, gate_mode=W.SAFE,
                          lower_bound=-5.0, out_gate=True, init_state="random")
     slots = [2, -1, 0]
     p, f = _both(wl, out_dtype=W.F32, num_slots=4, slots=slots)
     rs0 = DeviceCase(wl, num_slots=4, slots=slots).rec_state
-    for sl in (2, 0):
-        assert_close(to_np(p.rec_state[sl]), to_np(f.rec_state[sl]), f"split vs fused state, slot {sl}")
-    assert torch.equal(p.conv_state, f.conv_state)
+    assert torch.equal(p.rec_state, f.rec_state) and torch.equal(p.conv_state, f.conv_state)
     assert torch.equal(p.rec_state[1], rs0[1]) and torch.equal(p.rec_state[3], rs0[3])
     t0, t1 = 900, 1400
     assert torch.all(torch.isnan(p.out[t0:t1]))
-    assert_close(to_np(p.out[:t0]), to_np(f.out[:t0]), "split vs fused out, seq 0")
-    assert_close(to_np(p.out[t1:wl.T]), to_np(f.out[t1:wl.T]), "split vs fused out, seq 2")
+    assert torch.equal(p.out[:t0], f.out[:t0]) and torch.equal(p.out[t1:wl.T], f.out[t1:wl.T])
