@@ -1107,7 +1107,8 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
 
         if (!chunk_intra(sm, ms, a, tc, nvalid, tmem, lane_base, ph)) break;
 
-        // ---- -W tile from W^T (lane i = col, rows [16 qq, +16)); S_lo = S - S_hi (key dims [32 qq, +32))
+        // ---- -W tile from W^T as bf16 high and low parts (lane i = col, rows [16 qq, +16));
+        // S^T as bf16 high and low pairs (key dims [32 qq, +32))
         store_neg_w16(sm, FUSED_TILES, tmem + lane_base + TM_WT + RPT * qq, qq, col);
         state_split16(tmem + lane_base + TM_ST + 32 * qq, tmem + lane_base + TM_SH + 16 * qq,
                       tmem + lane_base + TM_SL16 + 16 * qq);
