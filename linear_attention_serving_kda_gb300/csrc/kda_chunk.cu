@@ -77,7 +77,7 @@ constexpr int HALO = 3;
 constexpr int RAWR = C + HALO;  // staged raw rows per tensor
 
 constexpr uint32_t TM_ST = 0, TM_XT = 128, TM_YT = 192, TM_YL = 256, TM_D1 = 320, TM_D1C = 416;
-constexpr uint32_t TM_WT = 320, TM_UT = 384, TM_OT = 128, TM_SL = 192, TM_UL = 448;
+constexpr uint32_t TM_WT = 320, TM_UT = 384, TM_OT = 128;
 constexpr uint32_t TM_COLS = 512;
 
 // shared memory map (bytes); tiles 1 KiB aligned
@@ -264,13 +264,17 @@ struct Bf16Tiles {
 struct Bf16Tmem {
     uint32_t st, sh, sl, ut, uh, ul;
 };
-// the fused kernel's tiles (in the regions of the fp32 tiles they replace) and
+// the fused kernel's tiles (-W in the region of the first product's low B tile,
+// dead after it; the others in the regions of the fp32 tiles they replace, so
+// the raw-row staging region is free once the second product has read T) and
 // columns (S^T pairs over the dead Y^T / Ylo^T, U^T pairs after U^T)
 constexpr uint32_t TM_SH = 192, TM_SL16 = 256, TM_UH = 448, TM_UL16 = 480;
-constexpr Bf16Tiles FUSED_TILES{SM_NW, SM_NW + 16384, SM_QE, SM_QE + 16384, SM_PH, SM_PH + 8192, SM_KD, SM_KD + 16384};
+constexpr Bf16Tiles FUSED_TILES{SM_KDL, SM_KDL + 16384, SM_QE, SM_QE + 16384, SM_PH, SM_PH + 8192, SM_KD, SM_KD + 16384};
 constexpr Bf16Tmem FUSED_TMEM{TM_ST, TM_SH, TM_SL16, TM_UT, TM_UH, TM_UL16};
-static_assert(SM_NW % 1024 == 0 && SM_QE % 1024 == 0 && SM_PH % 1024 == 0 && SM_KD % 1024 == 0,
+static_assert(SM_KDL % 1024 == 0 && SM_QE % 1024 == 0 && SM_PH % 1024 == 0 && SM_KD % 1024 == 0,
               "bf16 tiles need 1 KiB-aligned bases");
+static_assert(SM_KDL + 32768 <= SM_MISC && SM_KD + 32768 <= SM_KDL && RAW_END <= SM_PH,
+              "-W (the low K-block region) and the staging region are free after the second product");
 
 // byte offset of bf16 element (row, k) in a K-major SW128 bf16 tile (64 per
 // 128-byte row) whose K-blocks are `kbs` bytes apart
@@ -484,13 +488,16 @@ __device__ __forceinline__ ThreadConst thread_const(const ChunkArgs& a, int h, i
     return t;
 }
 
-__device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const ChunkArgs& a, const ThreadConst& tc,
-                                            int nvalid, uint32_t tmem, uint32_t lane_base, uint32_t& ph)
+// The state-independent prep of a chunk: conv + SiLU, the gate and the running
+// log-decay G of this thread's column and 16 rows, the q/k row norms applied.
+// Registers and the prep scratch of ms only (e^{G_C} is stored by chunk_rest).
+__device__ __forceinline__ void chunk_prep(unsigned char* sm, Misc& ms, const ChunkArgs& a, const ThreadConst& tc,
+                                           int nvalid, float (&qv)[RPT], float (&kv)[RPT], float (&vv)[RPT],
+                                           float (&G)[RPT])
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int col = tid & (D - 1);
     const int qq = tid >> 7;
-    const int half = qq >> 1;
     const int lq = warp & 3;
     const int r0 = RPT * qq;
     const __nv_bfloat16* raw = reinterpret_cast<const __nv_bfloat16*>(sm + SM_RAW);
@@ -501,7 +508,6 @@ __device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const C
     const float dtc = tc.dtc, ea = tc.ea;
     // ---- prep: conv + SiLU, gate, running log-decay for this thread's column and 16 rows,
     // two rows at a time in packed f32x2 arithmetic
-    float qv[RPT], kv[RPT], vv[RPT], G[RPT];
     {
         float xq[5], xk[5], xv[5];  // raw rows lr .. lr + 4 (lr + 3 is row r's own)
 #pragma unroll
@@ -581,7 +587,6 @@ __device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const C
         if (qq == 3) {
             ms.gx[1][col] = G[0];                   // row 48
             ms.gx[2][col] = G[RPT - 1];             // row 63 (G_C)
-            ms.gamma[col] = __expf(G[RPT - 1]);
         }
     }
     if (tid < 2 * C) {
@@ -596,7 +601,23 @@ __device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const C
         qv[r] *= ms.nrm[0][r0 + r];
         kv[r] *= ms.nrm[1][r0 + r];
     }
+}
 
+// The rest of the state-independent part of a chunk, from the prep's
+// results: e^{G_C}, the operands, the first product, A and P, the solve for T
+// and the second product (see chunk_intra).
+__device__ __forceinline__ bool chunk_rest(unsigned char* sm, Misc& ms, const ChunkArgs& a, int nvalid, uint32_t tmem,
+                                           uint32_t lane_base, uint32_t& ph, float (&qv)[RPT], float (&kv)[RPT],
+                                           float (&vv)[RPT], float (&G)[RPT])
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int col = tid & (D - 1);
+    const int qq = tid >> 7;
+    const int half = qq >> 1;
+    const int lq = warp & 3;
+    const int r0 = RPT * qq;
+    (void)lq;
+    if (qq == 3) ms.gamma[col] = __expf(G[RPT - 1]);  // e^{G_C}; read after later block barriers
     // ---- operands of the first and second products; q^ e^G and k^ e^{G_C - G}
     // are formed here too and kept in registers until their tiles are free
     const float Gm = ms.gx[half][col];   // reference row 16 (first half) or 48 (second half)
@@ -855,6 +876,21 @@ __device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const C
     return true;
 }
 
+// The state-independent part of one chunk (all 512 threads): from the staged
+// raw rows (q, k, v with the HALO rows before the chunk, gate f) and beta in
+// shared memory, compute conv + SiLU, the gates and G, the first product (A
+// and P), the solve for T and the second product.  On return (true) the
+// tensor memory holds W^T and U'^T, shared memory the T tile and the bf16
+// high/low P, Q o e^G and (K o e^{G_C - G})^T tiles, and ms.gamma holds
+// e^{G_C}.  False: a tensor-core wait ran out (ms.err set).
+__device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const ChunkArgs& a, const ThreadConst& tc,
+                                            int nvalid, uint32_t tmem, uint32_t lane_base, uint32_t& ph)
+{
+    float qv[RPT], kv[RPT], vv[RPT], G[RPT];
+    chunk_prep(sm, ms, a, tc, nvalid, qv, kv, vv, G);
+    return chunk_rest(sm, ms, a, nvalid, tmem, lane_base, ph, qv, kv, vv, G);
+}
+
 // ---- inter-chunk steps shared by the fused kernel and the chain role of the
 // split kernel; `t*` arguments are TMEM addresses (this warp's lane quarter
 // included), `o*` shared-memory tile offsets.
@@ -1080,8 +1116,21 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
     }
 
     const int nchunks = (seg1 - seg0 + C - 1) / C;
+    // the new conv state: the sequence's last K-1 raw rows, from the staged rows
+    // of the last chunk (nv valid rows)
+    auto store_conv_state = [&](int nv) {
+        const __nv_bfloat16* raw = reinterpret_cast<const __nv_bfloat16*>(sm + SM_RAW);
+        for (int idx = tid; idx < 3 * D * (K - 1); idx += NT) {
+            const int r = idx / (3 * D), c = idx % (3 * D), tsel = c / D, cc = c % D;
+            const int sr = HALO + nv - (K - 1) + r;
+            cs[((size_t)slot * (K - 1) + r) * conv_dim + (size_t)tsel * H * D + h * D + cc] =
+                raw[tsel * RAWR * D + sr * D + cc];
+        }
+    };
     float bnext = 0.0f;  // beta logit of row `tid` of the next chunk
     if (tid < C && seg0 + tid < seg1) bnext = __bfloat162float(bg[(size_t)(seg0 + tid) * H + h]);
+    // A chunk's rows are staged as soon as the previous chunk's second product
+    // has freed the staging region (two products and the outputs ahead of their use).
     for (int ch = 0; ch < nchunks && !ms.err; ++ch) {
         const int c0 = seg0 + ch * C;
         const int nvalid = min(C, seg1 - c0);
@@ -1091,21 +1140,22 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
         if (!wait_rows(ms, rph, a.dev_status)) break;
         rpending = false;
         if (ch == 0) {
-            patch_halo(sm, a, slot, h);
+            patch_halo(sm, a, slot, h);  // a segment's first chunk: the rows before it are the conv state
             __syncthreads();
         }
-        if (ch == nchunks - 1) {
-            // the new conv state: the sequence's last K-1 raw rows
-            const __nv_bfloat16* raw = reinterpret_cast<const __nv_bfloat16*>(sm + SM_RAW);
-            for (int idx = tid; idx < 3 * D * (K - 1); idx += NT) {
-                const int r = idx / (3 * D), c = idx % (3 * D), tsel = c / D, cc = c % D;
-                const int sr = HALO + nvalid - (K - 1) + r;
-                cs[((size_t)slot * (K - 1) + r) * conv_dim + (size_t)tsel * H * D + h * D + cc] =
-                    raw[tsel * RAWR * D + sr * D + cc];
-            }
+        if (ch == nchunks - 1) store_conv_state(nvalid);
+        {
+            float qv[RPT], kv[RPT], vv[RPT], G[RPT];
+            chunk_prep(sm, ms, a, tc, nvalid, qv, kv, vv, G);
+            if (!chunk_rest(sm, ms, a, nvalid, tmem, lane_base, ph, qv, kv, vv, G)) break;
         }
 
-        if (!chunk_intra(sm, ms, a, tc, nvalid, tmem, lane_base, ph)) break;
+        // the staging region is free: the next chunk's rows
+        if (ch + 1 < nchunks) {
+            if (tid == 0) stage_chunk(sm, maps, ms, c0 + C, h);
+            rpending = true;
+            if (tid < C && c0 + C + tid < seg1) bnext = __bfloat162float(bg[(size_t)(c0 + C + tid) * H + h]);
+        }
 
         // ---- -W tile from W^T as bf16 high and low parts (lane i = col, rows [16 qq, +16));
         // S^T as bf16 high and low pairs (key dims [32 qq, +32))
@@ -1119,13 +1169,6 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
         if (issuer(tid) >= 0)
             issue_third16<ISSUE_UNROLL>(sm, tmem, issuer(tid), FUSED_TILES, FUSED_TMEM, TM_OT, &ms.bar);
         if (!wait_mma(ms, ph, a.dev_status)) break;
-
-        // the raw staging region is free from here: prefetch the next chunk's rows
-        if (ch + 1 < nchunks) {
-            if (tid == 0) stage_chunk(sm, maps, ms, c0 + C, h);
-            rpending = true;
-            if (tid < C && c0 + C + tid < seg1) bnext = __bfloat162float(bg[(size_t)(c0 + C + tid) * H + h]);
-        }
 
         rescale_split16(tmem + lane_base + TM_ST + 32 * qq, tmem + lane_base + TM_UT + RPT * qq,
                         tmem + lane_base + TM_UH + 8 * qq, tmem + lane_base + TM_UL16 + 8 * qq, &ms.gamma[32 * qq]);
