@@ -327,17 +327,18 @@ __device__ __forceinline__ const IO* vw_hist_row(const RecArgs& a, int seq, int 
 }
 
 // Issue the copies of window rows [t0, t0 + nr) and of the three raw rows
-// before them (all threads; one commit group).  Returns the raw beta logit of
-// row t0 + tid (tid < nr), to be published in vb.bv with the block.
+// before them (all threads; one commit group); window row x is token row
+// rbase + x.  Returns the raw beta logit of row t0 + tid (tid < nr), to be
+// published in vb.bv with the block.
 template <typename IO>
-__device__ __forceinline__ IO vw_stage(VwBuf<IO>& vb, const RecArgs& a, int seq, int h, int slot, int acc, int t0,
-                                       int nr)
+__device__ __forceinline__ IO vw_stage(VwBuf<IO>& vb, const RecArgs& a, int seq, int h, int slot, int acc,
+                                       int rbase, int t0, int nr)
 {
     constexpr int EPP = 16 / (int)sizeof(IO), PIECES = VWD / EPP;
     const int ntens = a.g != nullptr ? 5 : 4;
     for (int idx = threadIdx.x; idx < nr * ntens * PIECES; idx += REC_THREADS) {
         const int piece = idx % PIECES, rest = idx / PIECES, tens = rest % ntens, r = rest / ntens;
-        const size_t rh = ((size_t)seq * a.W + t0 + r) * a.H + h;
+        const size_t rh = ((size_t)rbase + t0 + r) * a.H + h;
         const void* base = tens == 0 ? a.q : tens == 1 ? a.k : tens == 2 ? a.v : tens == 3 ? a.f : a.g;
         ptx::cp_async16(&vb.rows[r][tens][piece * EPP], static_cast<const IO*>(base) + rh * VWD + piece * EPP, 16);
     }
@@ -347,7 +348,7 @@ __device__ __forceinline__ IO vw_stage(VwBuf<IO>& vb, const RecArgs& a, int seq,
         const IO* src;
         if (x >= 0) {
             const void* base = seg == 0 ? a.q : seg == 1 ? a.k : a.v;
-            src = static_cast<const IO*>(base) + (((size_t)seq * a.W + x) * a.H + h) * VWD;
+            src = static_cast<const IO*>(base) + (((size_t)rbase + x) * a.H + h) * VWD;
         } else {
             const int r = x + a.K - 1;  // history row; r < 0: a tap the conv does not have
             if (r < 0) continue;
@@ -358,7 +359,7 @@ __device__ __forceinline__ IO vw_stage(VwBuf<IO>& vb, const RecArgs& a, int seq,
     ptx::cp_async_commit();
     const IO* b = static_cast<const IO*>(a.b);
     IO braw{};
-    if (threadIdx.x < nr) braw = b[((size_t)seq * a.W + t0 + threadIdx.x) * a.H + h];
+    if (threadIdx.x < nr) braw = b[((size_t)rbase + t0 + threadIdx.x) * a.H + h];
     return braw;
 }
 
@@ -410,6 +411,7 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_verify_warp_kernel(const R
     VwSmem<IO>& sm = *reinterpret_cast<VwSmem<IO>*>(vw_dyn_smem);
     constexpr int D = VWD, RPW = 16, CPT = 4, EPP = 16 / (int)sizeof(IO);
     constexpr bool CV = MODE == REC_COMMIT_VERIFY;
+    constexpr bool PF = MODE == REC_PREFILL;  // a whole sequence: no log, the final states stored
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int m = lane >> 2, cq = lane & 3;
     const int r0 = RPW * m, c0 = 16 * warp + CPT * cq;  // this thread's tile: key dims [r0, +16), value dims [c0, +4)
@@ -424,6 +426,17 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_verify_warp_kernel(const R
         if (tid == 0) flag_status(a.dev_status, KDA_DEV_BAD_SLOT);
         return;
     }
+    int L = W, rbase = seq * W;  // rows of the window (prefill: of the sequence) and the token row of its first
+    if (PF) {
+        const int s0 = a.cu_seqlens[seq], s1 = a.cu_seqlens[seq + 1];
+        if (s0 < 0 || s1 < s0 || s1 > a.T) {
+            if (tid == 0) flag_status(a.dev_status, KDA_DEV_BAD_SEQLENS);
+            return;
+        }
+        rbase = s0;
+        L = s1 - s0;
+        if (L == 0) return;  // zero-length sequence: states unchanged
+    }
     int acc = 0;  // commit first: rows of the previous window to replay
     if (CV) {
         acc = a.accepted[seq];
@@ -435,9 +448,9 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_verify_warp_kernel(const R
 
     // staged copies first (the log rows to commit, the first block of rows with
     // the conv history before it), then the parameters and the state tile
-    const int nblk = (W + VWB - 1) / VWB;
+    const int nblk = (L + VWB - 1) / VWB;
     if (CV && acc > 0) stage_log_rows<D>(sm.plog, a.prev_log_f, W, H, seq, h, 0, min(acc, VWB));
-    IO bnext = vw_stage<IO>(sm.buf[0], a, seq, h, slot, acc, 0, min(W, VWB));
+    IO bnext = vw_stage<IO>(sm.buf[0], a, seq, h, slot, acc, rbase, 0, min(L, VWB));
     for (int c = tid; c < 3 * D; c += REC_THREADS) {
         const int ch = conv_channel<D>(c, h, H);
         for (int j = 0; j < K; ++j) sm.cw[c][j] = a.conv_w[(size_t)ch * K + j];
@@ -484,12 +497,13 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_verify_warp_kernel(const R
     IO* cs = static_cast<IO*>(a.conv_state);
     IO* lraw = static_cast<IO*>(a.log_raw);
     for (int blk = 0; blk < nblk; ++blk) {
-        const int t0 = blk * VWB, nr = min(VWB, W - t0);
+        const int t0 = blk * VWB, nr = min(VWB, L - t0);
         VwBuf<IO>& vb = sm.buf[blk & 1];
         if (tid < nr) vb.bv[tid] = Io<IO>::ld(&bnext);
         ptx::cp_async_wait_all();
         __syncthreads();  // the block is staged; the previous block (rows, epilogue) is done
-        if (blk + 1 < nblk) bnext = vw_stage<IO>(sm.buf[(blk + 1) & 1], a, seq, h, slot, acc, t0 + VWB, min(VWB, W - t0 - VWB));
+        if (blk + 1 < nblk)
+            bnext = vw_stage<IO>(sm.buf[(blk + 1) & 1], a, seq, h, slot, acc, rbase, t0 + VWB, min(VWB, L - t0 - VWB));
 
         if (CV && blk == 0 && acc > 0) {
             // the committed conv state: the history rows the window starts from
@@ -501,9 +515,9 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_verify_warp_kernel(const R
             }
         }
         // the raw q|k|v rows of the window into the log
-        for (int idx = tid; idx < nr * 3 * (D / EPP); idx += REC_THREADS) {
+        for (int idx = tid; !PF && idx < nr * 3 * (D / EPP); idx += REC_THREADS) {
             const int piece = idx % (D / EPP), seg = (idx / (D / EPP)) % 3, t = idx / (3 * (D / EPP));
-            *reinterpret_cast<int4*>(lraw + ((size_t)seq * W + t0 + t) * conv_dim + (size_t)seg * H * D + h * D +
+            *reinterpret_cast<int4*>(lraw + ((size_t)rbase + t0 + t) * conv_dim + (size_t)seg * H * D + h * D +
                                      piece * EPP) = *reinterpret_cast<const int4*>(&vb.rows[t][seg][piece * EPP]);
         }
         // ---- state-independent part of the block's rows: conv channels (q, k
@@ -531,9 +545,9 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_verify_warp_kernel(const R
         }
         __syncthreads();
         // decay and normalised key of each row into the log
-        for (int e = tid; e < nr * D; e += REC_THREADS) {
+        for (int e = tid; !PF && e < nr * D; e += REC_THREADS) {
             const int t = e / D, i = e % D;
-            float* lg = a.log_f + (((size_t)seq * W + t0 + t) * H + h) * (3 * D);
+            float* lg = a.log_f + (((size_t)rbase + t0 + t) * H + h) * (3 * D);
             lg[i] = sm.ap[t][vw_pad(i)];
             lg[D + i] = sm.kp[t][vw_pad(i)] * sm.rs[t][1];
         }
@@ -615,8 +629,10 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_verify_warp_kernel(const R
                 }
                 o01 = __fmul2_rn(o01, make_float2(rc.scale, rc.scale));
                 o23 = __fmul2_rn(o23, make_float2(rc.scale, rc.scale));
-                const size_t rh = ((size_t)seq * W + t0 + t) * H + h;
-                *reinterpret_cast<float4*>(a.log_f + rh * (3 * D) + 2 * D + c0) = make_float4(uc[0], uc[1], uc[2], uc[3]);
+                const size_t rh = ((size_t)rbase + t0 + t) * H + h;
+                if (!PF)
+                    *reinterpret_cast<float4*>(a.log_f + rh * (3 * D) + 2 * D + c0) =
+                        make_float4(uc[0], uc[1], uc[2], uc[3]);
                 if (has_g) {
                     *reinterpret_cast<float4*>(&sm.o[t][c0]) = make_float4(o01.x, o01.y, o23.x, o23.y);
                 } else {
@@ -646,8 +662,25 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_verify_warp_kernel(const R
                 const float r = rsqrtf(tot * (1.0f / D) + rc.norm_eps);
                 const float wn = rc.norm_w ? rc.norm_w[j] : 1.0f;
                 const float y = sm.o[t][j] * r * wn * sigmoidf_(ldv(&vb.rows[t][4][j]));
-                store_out(a.out, (((size_t)seq * W + t0 + t) * H + h) * D + j, y, a.out_bf16);
+                store_out(a.out, (((size_t)rbase + t0 + t) * H + h) * D + j, y, a.out_bf16);
             }
+        }
+    }
+
+    if (PF) {
+        // the final state, and the new conv state: the last K-1 raw rows of
+        // [old conv state; sequence], from the last staged block or its halo
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr)
+            st_stream4(Sg + (size_t)(r0 + rr) * D + c0, make_float4(s[rr][0], s[rr][1], s[rr][2], s[rr][3]));
+        const int tl = (nblk - 1) * VWB;
+        const VwBuf<IO>& vb = sm.buf[(nblk - 1) & 1];
+        for (int idx = tid; idx < 3 * (K - 1) * (D / EPP); idx += REC_THREADS) {
+            const int piece = idx % (D / EPP), seg = (idx / (D / EPP)) % 3, r = idx / (3 * (D / EPP));
+            const int x = L - (K - 1) + r - tl;  // row of the last block; < 0: its halo row x + 3
+            const IO* src = x >= 0 ? &vb.rows[x][seg][piece * EPP] : &vb.halo[x + 3][seg][piece * EPP];
+            *reinterpret_cast<int4*>(cs + ((size_t)slot * (K - 1) + r) * conv_dim + (size_t)seg * H * D + h * D +
+                                     piece * EPP) = *reinterpret_cast<const int4*>(src);
         }
     }
 }
@@ -909,6 +942,7 @@ template <int D, typename IO>
 static cudaError_t launch_rec_d(int mode, const RecArgs& a, int units, cudaStream_t st)
 {
     if constexpr (D == VWD) {
+        if (mode == REC_PREFILL) return launch_verify_warp<IO, REC_PREFILL>(a, units, st);
         if (mode == REC_VERIFY) return launch_verify_warp<IO, REC_VERIFY>(a, units, st);
         if (mode == REC_COMMIT_VERIFY) return launch_verify_warp<IO, REC_COMMIT_VERIFY>(a, units, st);
     }

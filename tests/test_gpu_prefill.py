@@ -38,6 +38,8 @@ VARLEN = [
     ([130, 0, 2, 1], 128, W.BF16, W.SAFE, 3, False, "random"),
     ([129, 64, 200], 128, W.BF16, W.SOFTPLUS, 4, True, "zero"),
     ([257, 3], 128, W.F32, W.SAFE, 2, True, "random"),
+    ([1, 0, 2, 9, 3], 128, W.BF16, W.SOFTPLUS, 4, True, "random"),
+    ([8, 16, 7, 24], 128, W.F32, W.SOFTPLUS, 3, False, "random"),
     ([0, 0], 64, W.F32, W.SAFE, 4, False, "random"),
 ]
 
@@ -55,6 +57,34 @@ CHUNK = [
     ([128, 200, 17], 2, False, "zero"),
     ([333], 3, True, "random"),
 ]
+
+
+@pytest.mark.parametrize("io,gate,K,og", [(W.BF16, W.SOFTPLUS, 4, True), (W.F32, W.SAFE, 3, False),
+                                           (W.BF16, W.SOFTPLUS, 2, False)])
+def test_row_path_prefill_is_decode_bits(cuda_lib, io, gate, K, og):
+    """dk = dv = 128 shapes the chunk kernel does not take run the delta rule
+    row by row: a prefilled sequence has the bits of the same rows decoded one
+    at a time (outputs, final state, conv state)."""
+    from tests.parity import gather_rows
+
+    T = 21
+    wl = W.make_workload("rowbits", 640 + K, [T], H=3, d=128, K=K, io_dtype=io,
+                         gate_mode=gate, lower_bound=-5.0, out_gate=og, init_state="random")
+    full = _prefill(cuda_lib, wl)
+    dec = DeviceCase(gather_rows(wl, [(0, 1)]))
+    outs = []
+    for r in range(T):
+        step = DeviceCase(gather_rows(wl, [(r, r + 1)]))
+        step.conv_state.copy_(dec.conv_state)
+        step.rec_state.copy_(dec.rec_state)
+        cuda_lib.check(step.decode())
+        outs.append(step.out[:1].clone())
+        dec = step
+    torch.cuda.synchronize()
+    assert int(dec.dev_status.item()) == 0
+    assert torch.equal(torch.cat(outs), full.out[:T])
+    assert torch.equal(dec.rec_state, full.rec_state)
+    assert torch.equal(dec.conv_state, full.conv_state)
 
 
 @pytest.mark.parametrize("lens,K,og,init", CHUNK)
