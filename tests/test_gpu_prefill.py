@@ -209,3 +209,36 @@ def test_long_prefill_sampled(cuda_lib, oracle_mod):
     wl = W.long_prefill_case()
     dc = _prefill(cuda_lib, wl)
     _check_sampled(oracle_mod, wl, dc, [(0, 0), (0, 13), (0, 31)])
+
+
+def _prefill_sweep_cases(n=16, seed=4242):
+    """Seeded shapes over both prefill paths: the tensor-core chunk kernel
+    (dk = dv = 128, bf16 rows, safe gate with lb >= -5) and the row kernels
+    (everything else), with empty, one-row, chunk-edge and ragged lengths."""
+    rng = np.random.default_rng(seed)
+    edge = [0, 1, 2, 3, 63, 64, 65, 127, 128, 129]
+    cases = []
+    for i in range(n):
+        chunk = i < 6  # the first six take the chunk kernel's shapes
+        d = 128 if chunk or i % 3 == 0 else int(rng.choice([32, 64]))
+        io = W.BF16 if chunk or i == n - 1 else [W.BF16, W.F32][i % 2]
+        gate = W.SAFE if chunk else [W.SOFTPLUS, W.SAFE][(i // 2) % 2]
+        lb = -5.0 if chunk else float(rng.choice([-5.0, -8.0, -1.5]))
+        N = int(rng.integers(1, 5))
+        lens = [int(rng.choice(edge)) if rng.random() < 0.5 else int(rng.integers(4, 300)) for _ in range(N)]
+        cases.append(dict(lens=lens, d=d, io=io, gate=gate, lb=lb, K=int(rng.integers(2, 5)),
+                          H=int(rng.integers(1, 4)), og=bool(rng.integers(0, 2)),
+                          init=["random", "zero"][int(rng.integers(0, 2))], seed=7000 + i))
+    return cases
+
+
+@pytest.mark.parametrize("case", _prefill_sweep_cases(),
+                         ids=lambda c: f"d{c['d']}{c['io']}g{c['gate']}k{c['K']}h{c['H']}n{len(c['lens'])}")
+def test_prefill_sweep(cuda_lib, oracle_mod, case):
+    """Seeded sweep of prefill shapes against the oracle: outputs, final
+    recurrent state and conv state (bit-equal: it holds raw rows)."""
+    c = case
+    wl = W.make_workload(f"psweep{c['seed']}", c["seed"], c["lens"], H=c["H"], d=c["d"], K=c["K"],
+                         io_dtype=c["io"], gate_mode=c["gate"], lower_bound=c["lb"], out_gate=c["og"],
+                         init_state=c["init"])
+    _check_all(_prefill(cuda_lib, wl), oracle_mod.forward(wl))
