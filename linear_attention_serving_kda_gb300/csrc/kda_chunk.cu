@@ -45,7 +45,9 @@
 // every factor stays in [e^-80, e^80] when each row's log-decay is >= -5 (the
 // safe gate with lower bound >= -5); the block of rows r in the second half
 // against columns s in the first half uses the second half's reference on
-// both sides.  Other gates run on the serial kernel.
+// both sides.  With other gates (softplus, lower bound < -5) a chunk ends
+// before the first row that would take a factor out of that range (chunk_cut),
+// so chunk boundaries follow the decays; the next chunk starts there.
 //
 // TMEM (512 columns): S^T [0,128); X^T [128,192), Y^T [192,256),
 // Ylo^T [256,320), D1 [320,416), D1c [416,512) until the first product is
@@ -118,6 +120,8 @@ struct Misc {
     uint64_t bbar;            // split chain: fourth-product operands
     uint32_t tmem;
     int err;
+    int ncut;                 // unbounded gates: first row that leaves the factored range
+    float ganc[2][D];         // unbounded gates: G at rows 0 and 32; then G at the chunk's last row
 };
 constexpr int SMEM_BYTES = SM_MISC + (int)sizeof(Misc);
 static_assert(RAW_END <= SM_B1H && RAW_END <= SM_PH, "raw staging overlaps B1 or the P tiles");
@@ -488,12 +492,64 @@ __device__ __forceinline__ ThreadConst thread_const(const ChunkArgs& a, int h, i
     return t;
 }
 
+// Unbounded gates: the number of rows this chunk takes, at most nvalid: the
+// longest prefix over which every key dim's running log-decay G stays within
+// 80 of the reference row of each 32-row half, so that every factor
+// e^{+-(G_r - G_m)} the chunk forms is finite (|G_r - G_m| < 88 would do).
+// With G held at row n - 1 beyond a prefix of n rows, the spans to check at
+// row j are G_0 - G_j for j <= 16, G_16 - G_j for j < 32, G_32 - G_j for
+// j <= 48 and G_48 - G_j after: each half's reference splits it into two
+// spans, of which row 16 (48) closes the first.  A single row always fits.
+// Rows past the cut get zero q, k, v and G held at the last row, as rows past
+// a segment's end do.  G is this thread's 16 rows (absolute within the chunk).
+__device__ __forceinline__ int chunk_cut(Misc& ms, int nvalid, float (&qv)[RPT], float (&kv)[RPT], float (&vv)[RPT],
+                                         float (&G)[RPT])
+{
+    const int tid = threadIdx.x, col = tid & (D - 1), qq = tid >> 7;
+    if (tid == 0) ms.ncut = C;
+    if ((qq & 1) == 0) ms.ganc[qq >> 1][col] = G[0];  // rows 0 and 32
+    __syncthreads();
+    int bad = C;
+#pragma unroll
+    for (int r = RPT - 1; r >= 0; --r) {
+        // the span's start: this quarter's first row, but for rows 16 and 48
+        // the first row of the quarter before
+        const float g0 = (r == 0 && (qq & 1)) ? ms.ganc[qq >> 1][col] : G[0];
+        if (g0 - G[r] > 80.0f) bad = RPT * qq + r;
+    }
+    bad = __reduce_min_sync(0xffffffffu, bad);
+    if ((tid & 31) == 0 && bad < C) atomicMin(&ms.ncut, bad);
+    __syncthreads();
+    const int n = min(nvalid, ms.ncut);
+    if (n < nvalid) {  // block-uniform
+#pragma unroll
+        for (int r = 0; r < RPT; ++r)
+            if (RPT * qq + r == n - 1) ms.ganc[0][col] = G[r];
+        __syncthreads();
+        const float gl = ms.ganc[0][col];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            if (RPT * qq + r >= n) {
+                qv[r] = 0.0f;
+                kv[r] = 0.0f;
+                vv[r] = 0.0f;
+                G[r] = gl;
+            }
+        }
+    }
+    return n;
+}
+
 // The state-independent prep of a chunk: conv + SiLU, the gate and the running
 // log-decay G of this thread's column and 16 rows, the q/k row norms applied.
 // Registers and the prep scratch of ms only (e^{G_C} is stored by chunk_rest).
-__device__ __forceinline__ void chunk_prep(unsigned char* sm, Misc& ms, const ChunkArgs& a, const ThreadConst& tc,
-                                           int nvalid, float (&qv)[RPT], float (&kv)[RPT], float (&vv)[RPT],
-                                           float (&G)[RPT])
+// Returns the number of rows the chunk takes: nvalid, or with UNB (gates
+// whose log-decays are not bounded by -5: softplus, or a lower bound below
+// -5) possibly fewer (chunk_cut).
+template <bool UNB>
+__device__ __forceinline__ int chunk_prep(unsigned char* sm, Misc& ms, const ChunkArgs& a, const ThreadConst& tc,
+                                          int nvalid, float (&qv)[RPT], float (&kv)[RPT], float (&vv)[RPT],
+                                          float (&G)[RPT])
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int col = tid & (D - 1);
@@ -518,6 +574,12 @@ __device__ __forceinline__ void chunk_prep(unsigned char* sm, Misc& ms, const Ch
         }
         const float2 dt2 = make_float2(dtc, dtc), ea2 = make_float2(ea, ea), lb2 = make_float2(a.lb, a.lb);
         const float2 one2 = make_float2(1.0f, 1.0f);
+        const bool sp = UNB && a.gate_mode != KDA_GATE_SAFE;
+        if (sp) {  // softplus decays first, into G (fewer values live than inside the conv loop)
+#pragma unroll
+            for (int r = 0; r < RPT; ++r)
+                G[r] = log_alpha(KDA_GATE_SOFTPLUS, 0.0f, ea, __bfloat162float(rawf[(r0 + r) * D + col]), dtc);
+        }
         float run = 0.0f;
 #pragma unroll
         for (int r = 0; r < RPT; r += 2) {
@@ -542,11 +604,15 @@ __device__ __forceinline__ void chunk_prep(unsigned char* sm, Misc& ms, const Ch
             const float2 sq = __fmul2_rn(aq, make_float2(__fdividef(1.0f, dq.x), __fdividef(1.0f, dq.y)));
             const float2 sk = __fmul2_rn(ak, make_float2(__fdividef(1.0f, dk.x), __fdividef(1.0f, dk.y)));
             const float2 sv = __fmul2_rn(av, make_float2(__fdividef(1.0f, dv.x), __fdividef(1.0f, dv.y)));
-            const float2 fz = __fmul2_rn(ea2, __fadd2_rn(make_float2(__bfloat162float(rawf[lr * D + col]),
-                                                                      __bfloat162float(rawf[(lr + 1) * D + col])),
-                                                          dt2));
-            const float2 gd = __fadd2_rn(one2, make_float2(__expf(-fz.x), __expf(-fz.y)));
-            const float2 la = __fmul2_rn(lb2, make_float2(__fdividef(1.0f, gd.x), __fdividef(1.0f, gd.y)));
+            float2 la;
+            if (!sp) {
+                const float f0 = __bfloat162float(rawf[lr * D + col]), f1 = __bfloat162float(rawf[(lr + 1) * D + col]);
+                const float2 fz = __fmul2_rn(ea2, __fadd2_rn(make_float2(f0, f1), dt2));
+                const float2 gd = __fadd2_rn(one2, make_float2(__expf(-fz.x), __expf(-fz.y)));
+                la = __fmul2_rn(lb2, make_float2(__fdividef(1.0f, gd.x), __fdividef(1.0f, gd.y)));
+            } else {
+                la = make_float2(G[r], G[r + 1]);
+            }
             const bool ok0 = lr < nvalid, ok1 = lr + 1 < nvalid;
             qv[r] = ok0 ? sq.x : 0.0f;
             kv[r] = ok0 ? sk.x : 0.0f;
@@ -578,11 +644,13 @@ __device__ __forceinline__ void chunk_prep(unsigned char* sm, Misc& ms, const Ch
         ms.gq[qq][col] = G[RPT - 1];
     }
     __syncthreads();
+    int n = nvalid;
     {
         float off = 0.0f;
         for (int q2 = 0; q2 < qq; ++q2) off += ms.gq[q2][col];
 #pragma unroll
         for (int r = 0; r < RPT; ++r) G[r] += off;
+        if (UNB) n = chunk_cut(ms, nvalid, qv, kv, vv, G);
         if (qq == 1) ms.gx[0][col] = G[0];          // row 16
         if (qq == 3) {
             ms.gx[1][col] = G[0];                   // row 48
@@ -601,6 +669,7 @@ __device__ __forceinline__ void chunk_prep(unsigned char* sm, Misc& ms, const Ch
         qv[r] *= ms.nrm[0][r0 + r];
         kv[r] *= ms.nrm[1][r0 + r];
     }
+    return n;
 }
 
 // The rest of the state-independent part of a chunk, from the prep's
@@ -887,7 +956,7 @@ __device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const C
                                             int nvalid, uint32_t tmem, uint32_t lane_base, uint32_t& ph)
 {
     float qv[RPT], kv[RPT], vv[RPT], G[RPT];
-    chunk_prep(sm, ms, a, tc, nvalid, qv, kv, vv, G);
+    chunk_prep<false>(sm, ms, a, tc, nvalid, qv, kv, vv, G);
     return chunk_rest(sm, ms, a, nvalid, tmem, lane_base, ph, qv, kv, vv, G);
 }
 
@@ -1021,16 +1090,19 @@ __device__ __forceinline__ void write_outputs_b(Misc& ms, const ChunkArgs& a, fl
     }
 }
 
-// a segment's first chunk: the rows before it are the carried conv state
-// (oldest first; zero where K - 1 < HALO)
-__device__ __forceinline__ void patch_halo(unsigned char* sm, const ChunkArgs& a, int slot, int h)
+// A chunk starting `off` < HALO rows into its segment: the halo rows before
+// the segment's first row are the carried conv state (oldest first; zero
+// where K - 1 < HALO); the others were staged with the chunk.
+__device__ __forceinline__ void patch_halo(unsigned char* sm, const ChunkArgs& a, int slot, int h, int off)
 {
     const int H = a.H, K = a.K, conv_dim = 3 * H * D;
     const __nv_bfloat16* cs = static_cast<const __nv_bfloat16*>(a.conv_state);
     __nv_bfloat16* rw = reinterpret_cast<__nv_bfloat16*>(sm + SM_RAW);
     for (int idx = threadIdx.x; idx < 3 * HALO * D; idx += NT) {
         const int tsel = idx / (HALO * D), sr = (idx / D) % HALO, cc = idx % D;
-        const int cr = (K - 1) - HALO + sr;
+        const int x = off - HALO + sr;  // the halo row's position in the segment
+        if (x >= 0) continue;
+        const int cr = (K - 1) + x;
         rw[tsel * RAWR * D + sr * D + cc] =
             cr >= 0 ? cs[((size_t)slot * (K - 1) + cr) * conv_dim + (size_t)tsel * H * D + h * D + cc]
                     : __float2bfloat16_rn(0.0f);
@@ -1052,6 +1124,7 @@ __device__ __forceinline__ bool wait_rows(Misc& ms, uint32_t& rph, int32_t* dev_
     return true;
 }
 
+template <bool UNB>
 __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, const __grid_constant__ RawMaps maps)
 {
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -1115,7 +1188,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
         ptx::tmem_st32(tmem + lane_base + TM_ST + 32 * qq, v);
     }
 
-    const int nchunks = (seg1 - seg0 + C - 1) / C;
+    // UNB (unbounded gates): chunks end where the decays leave the factored range
     // the new conv state: the sequence's last K-1 raw rows, from the staged rows
     // of the last chunk (nv valid rows)
     auto store_conv_state = [&](int nv) {
@@ -1131,30 +1204,36 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
     if (tid < C && seg0 + tid < seg1) bnext = __bfloat162float(bg[(size_t)(seg0 + tid) * H + h]);
     // A chunk's rows are staged as soon as the previous chunk's second product
     // has freed the staging region (two products and the outputs ahead of their use).
-    for (int ch = 0; ch < nchunks && !ms.err; ++ch) {
-        const int c0 = seg0 + ch * C;
+    for (int c0 = seg0; c0 < seg1 && !ms.err;) {
         const int nvalid = min(C, seg1 - c0);
         const int r0 = RPT * qq;
 
         if (tid < C) ms.beta[tid] = tid < nvalid ? sigmoidf_(bnext) : 0.0f;
         if (!wait_rows(ms, rph, a.dev_status)) break;
         rpending = false;
-        if (ch == 0) {
-            patch_halo(sm, a, slot, h);  // a segment's first chunk: the rows before it are the conv state
+        if (c0 - seg0 < HALO) {
+            // the rows before the segment are the conv state (only the first
+            // chunk with fixed chunks; a short first chunk's successor too)
+            patch_halo(sm, a, slot, h, c0 - seg0);
             __syncthreads();
         }
-        if (ch == nchunks - 1) store_conv_state(nvalid);
+        if (!UNB && c0 + nvalid == seg1) store_conv_state(nvalid);
+        int n;  // rows this chunk takes
         {
             float qv[RPT], kv[RPT], vv[RPT], G[RPT];
-            chunk_prep(sm, ms, a, tc, nvalid, qv, kv, vv, G);
-            if (!chunk_rest(sm, ms, a, nvalid, tmem, lane_base, ph, qv, kv, vv, G)) break;
+            n = chunk_prep<UNB>(sm, ms, a, tc, nvalid, qv, kv, vv, G);
+            if (UNB && c0 + n == seg1) {
+                store_conv_state(n);  // the staged rows are still intact: read before the operands overwrite them
+                __syncthreads();
+            }
+            if (!chunk_rest(sm, ms, a, n, tmem, lane_base, ph, qv, kv, vv, G)) break;
         }
 
         // the staging region is free: the next chunk's rows
-        if (ch + 1 < nchunks) {
-            if (tid == 0) stage_chunk(sm, maps, ms, c0 + C, h);
+        if (c0 + n < seg1) {
+            if (tid == 0) stage_chunk(sm, maps, ms, c0 + n, h);
             rpending = true;
-            if (tid < C && c0 + C + tid < seg1) bnext = __bfloat162float(bg[(size_t)(c0 + C + tid) * H + h]);
+            if (tid < C && c0 + n + tid < seg1) bnext = __bfloat162float(bg[(size_t)(c0 + n + tid) * H + h]);
         }
 
         // ---- -W tile from W^T as bf16 high and low parts (lane i = col, rows [16 qq, +16));
@@ -1178,17 +1257,18 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
         if (issuer(tid) >= 0)
             issue_fourth16<ISSUE_UNROLL>(sm, tmem, issuer(tid), FUSED_TILES, FUSED_TMEM, TM_OT, &ms.bar);
         uint32_t gp[RPT / 2];
-        load_gate_bits(gp, a, c0, r0, nvalid, h, col);  // while the product runs
+        load_gate_bits(gp, a, c0, r0, n, h, col);  // while the product runs
         if (!wait_mma(ms, ph, a.dev_status)) break;
 
         {
             float o[RPT];
             write_outputs_a(ms, a, tmem + lane_base + TM_OT + RPT * qq, o);
             __syncthreads();
-            write_outputs_b(ms, a, o, gp, c0, nvalid, h, nw);
+            write_outputs_b(ms, a, o, gp, c0, n, h, nw);
         }
         ptx::tc_fence_before();
         __syncthreads();
+        c0 += n;
     }
 
     // ---- final state S^T -> rec_state (S[i][j], lane j = col, key dims [32 qq, +32))
@@ -1318,7 +1398,7 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
         if (ms.err) break;
         if (!wait_rows(ms, rph, a.dev_status)) break;
         if (c == 0) {
-            patch_halo(sm, a, slot, h);
+            patch_halo(sm, a, slot, h, 0);
             __syncthreads();
         }
         if (!chunk_intra(sm, ms, a, tc, nvalid, tmem, lane_base, ph)) break;
@@ -1587,9 +1667,18 @@ __global__ void __launch_bounds__(NT, 1)
 
 }  // namespace chk
 
+// Per-row log decays >= -5 (the safe gate with lb >= -5): fixed 64-row
+// chunks.  Other gates cut a chunk where its decays leave the factored range
+// (the chunk boundaries then depend on the data, which the split path's
+// producers, working ahead of the chain, cannot know).
+static bool chunk_bounded(const kda_params* p)
+{
+    return p->gate_mode == KDA_GATE_SAFE && p->gate_lower_bound >= -5.0f;
+}
+
 bool chunk_split_wanted(const kda_params* p, int N, int T)
 {
-    return chunk_supported(p) && (long long)N * p->num_heads <= 64 && T >= 1024;
+    return chunk_supported(p) && chunk_bounded(p) && (long long)N * p->num_heads <= 64 && T >= 1024;
 }
 
 size_t chunk_split_bytes(int N, int H)
@@ -1601,10 +1690,8 @@ size_t chunk_split_bytes(int N, int H)
 
 bool chunk_supported(const kda_params* p)
 {
-    // dk = dv = 128, bf16 rows, and per-row log decay >= -5 (safe gate, lb >= -5),
-    // which keeps every factored decay inside fp32 range
-    return p->head_dim_k == 128 && p->head_dim_v == 128 && p->io_dtype == KDA_DTYPE_BF16 &&
-           p->gate_mode == KDA_GATE_SAFE && p->gate_lower_bound >= -5.0f;
+    // dk = dv = 128 and bf16 rows, either gate
+    return p->head_dim_k == 128 && p->head_dim_v == 128 && p->io_dtype == KDA_DTYPE_BF16;
 }
 
 namespace {
@@ -1644,12 +1731,17 @@ bool encode_rows(CUtensorMap* m, const void* base, int H, int T, int box_rows)
 cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
 {
     if (!io_bf16) return cudaErrorNotSupported;
+    // per-row log decays bounded by -5 (safe gate, lb >= -5): fixed 64-row chunks
+    const bool unb = !(a.gate_mode == KDA_GATE_SAFE && a.lb >= -5.0f);
     static bool attr_done[128];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 128 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(chk::kda_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(chk::kda_chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              chk::SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(chk::kda_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     chk::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
@@ -1660,7 +1752,7 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
             !encode_rows(&maps.v, a.v, a.H, a.T, chk::RAWR) || !encode_rows(&maps.f, a.f, a.H, a.T, chk::C))
             return cudaErrorInvalidValue;
     }
-    if (a.split_ws) {
+    if (a.split_ws && !unb) {
         // split path: one cooperative grid of one CTA per SM, chains first
         static bool split_attr[128];
         int sms = 0, per_sm = 0;
@@ -1690,7 +1782,8 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
         // too few SMs for producers beside the chains: the fused kernel below
     }
     if (a.schedule) chk::kda_chunk_schedule_kernel<<<1, 256, 0, st>>>(a.cu_seqlens, a.N, a.schedule);
-    chk::kda_chunk_kernel<<<a.N * a.H, chk::NT, chk::SMEM_BYTES, st>>>(a, maps);
+    if (unb) chk::kda_chunk_kernel<true><<<a.N * a.H, chk::NT, chk::SMEM_BYTES, st>>>(a, maps);
+    else chk::kda_chunk_kernel<false><<<a.N * a.H, chk::NT, chk::SMEM_BYTES, st>>>(a, maps);
     return cudaGetLastError();
 }
 

@@ -130,7 +130,13 @@ def test_split_workspace_size(lib):
     assert kda.kda_prefill_workspace_bytes(p, N, 1024) == sched + flags + nc * 8 * slot
     assert kda.kda_prefill_workspace_bytes(p, N, 1023) == 256          # short: fused path
     assert kda.kda_prefill_workspace_bytes(p, 17, 4096) == 256 * 1     # 68 chains: fused path
-    assert kda.kda_prefill_workspace_bytes(_params(gate_mode=kda.KDA_GATE_SOFTPLUS), N, 4096) == 0
+    assert kda.kda_prefill_workspace_bytes(_params(io_dtype=kda.KDA_DTYPE_F32, gate_mode=kda.KDA_GATE_SOFTPLUS),
+                                           N, 4096) == 0  # fp32 rows: the row path
+    # softplus (and safe gates below -5) chunk where the decays require: fused path only
+    assert kda.kda_prefill_workspace_bytes(_params(io_dtype=kda.KDA_DTYPE_BF16, gate_mode=kda.KDA_GATE_SOFTPLUS),
+                                           N, 4096) == 256
+    assert kda.kda_prefill_workspace_bytes(_params(io_dtype=kda.KDA_DTYPE_BF16, gate_lower_bound=-8.0),
+                                           N, 4096) == 256
 
 
 def test_status_strings(lib):

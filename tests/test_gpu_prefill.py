@@ -59,12 +59,12 @@ CHUNK = [
 ]
 
 
-@pytest.mark.parametrize("io,gate,K,og", [(W.BF16, W.SOFTPLUS, 4, True), (W.F32, W.SAFE, 3, False),
-                                           (W.BF16, W.SOFTPLUS, 2, False)])
+@pytest.mark.parametrize("io,gate,K,og", [(W.F32, W.SOFTPLUS, 4, True), (W.F32, W.SAFE, 3, False),
+                                           (W.F32, W.SOFTPLUS, 2, False)])
 def test_row_path_prefill_is_decode_bits(cuda_lib, io, gate, K, og):
-    """dk = dv = 128 shapes the chunk kernel does not take run the delta rule
-    row by row: a prefilled sequence has the bits of the same rows decoded one
-    at a time (outputs, final state, conv state)."""
+    """dk = dv = 128 shapes the chunk kernel does not take (fp32 rows) run the
+    delta rule row by row: a prefilled sequence has the bits of the same rows
+    decoded one at a time (outputs, final state, conv state)."""
     from tests.parity import gather_rows
 
     T = 21
@@ -241,4 +241,26 @@ def test_prefill_sweep(cuda_lib, oracle_mod, case):
     wl = W.make_workload(f"psweep{c['seed']}", c["seed"], c["lens"], H=c["H"], d=c["d"], K=c["K"],
                          io_dtype=c["io"], gate_mode=c["gate"], lower_bound=c["lb"], out_gate=c["og"],
                          init_state=c["init"])
+    _check_all(_prefill(cuda_lib, wl), oracle_mod.forward(wl))
+
+
+UNBOUNDED = [
+    # lens, gate, lower bound, A_log (all heads), K, out_gate -- bf16 rows, dk = dv = 128
+    ([200, 7, 130], W.SOFTPLUS, -5.0, 3.0, 4, True),    # ~-16 per row: chunks of a few rows
+    ([150, 64], W.SAFE, -12.0, 2.0, 3, False),          # safe gate below -5: cut near 13-16 rows
+    ([40, 3], W.SOFTPLUS, -5.0, 5.0, 2, True),          # ~-100 per row: one-row chunks
+    ([333, 1, 65], W.SOFTPLUS, -5.0, None, 4, False),   # A_log ~ U(-1, 1): mostly whole chunks
+]
+
+
+@pytest.mark.parametrize("lens,gate,lb,alog,K,og", UNBOUNDED)
+def test_chunk_path_unbounded_gates(cuda_lib, oracle_mod, lens, gate, lb, alog, K, og):
+    """Gates whose per-row log-decay is not bounded by -5 take the chunk
+    kernel with data-dependent chunk boundaries (a chunk ends before the first
+    row whose decay would take a factor out of range): against the oracle,
+    including decays strong enough for chunks of a single row."""
+    wl = W.make_workload("unb", 900 + sum(lens) + K, lens, H=2, d=128, K=K, io_dtype=W.BF16,
+                         gate_mode=gate, lower_bound=lb, out_gate=og, init_state="random")
+    if alog is not None:
+        wl.arrays["A_log"] = np.full_like(wl.arrays["A_log"], alog)
     _check_all(_prefill(cuda_lib, wl), oracle_mod.forward(wl))
