@@ -35,10 +35,12 @@
  *   - States are updated in place; verify never writes them.  The conv
  *     state and the recurrent state are the whole hand-off between calls: a
  *     prompt prefilled and then decoded (or verified and committed) row by
- *     row continues one recurrence.  On the chunked prefill path a prompt
- *     cut into calls at multiples of 64 rows gives the bits of one uncut
- *     call (TensorFold #850, Oct 15 comment: chunks start at a segment's
- *     first row).
+ *     row continues one recurrence.  On the chunked prefill path with the
+ *     safe gate and lb >= -5 a prompt cut into calls at multiples of 64 rows
+ *     gives the bits of one uncut call (TensorFold #850, Oct 15 comment:
+ *     chunks start at a segment's first row).  With a softplus gate or
+ *     lb < -5 chunk boundaries follow the decays, so a cut call agrees with
+ *     the uncut one to rounding, not bit for bit.
  *   - Under CUDA-graph capture a call keeps its pointers, sizes and params;
  *     the buffers' contents (rows, slot map, accepted counts) are read at
  *     each replay.  Make one call of each entry point on a device before
