@@ -500,10 +500,10 @@ __device__ __forceinline__ ThreadConst thread_const(const ChunkArgs& a, int h, i
 // row j are G_0 - G_j for j <= 16, G_16 - G_j for j < 32, G_32 - G_j for
 // j <= 48 and G_48 - G_j after: each half's reference splits it into two
 // spans, of which row 16 (48) closes the first.  A single row always fits.
-// Rows past the cut get zero q, k, v and G held at the last row, as rows past
+// Rows past the cut get G held at the last row here, and zero q, k (their
+// inverse norms) and beta from the caller, so they add nothing, as rows past
 // a segment's end do.  G is this thread's 16 rows (absolute within the chunk).
-__device__ __forceinline__ int chunk_cut(Misc& ms, int nvalid, float (&qv)[RPT], float (&kv)[RPT], float (&vv)[RPT],
-                                         float (&G)[RPT])
+__device__ __forceinline__ int chunk_cut(Misc& ms, int nvalid, float (&G)[RPT])
 {
     const int tid = threadIdx.x, col = tid & (D - 1), qq = tid >> 7;
     if (tid == 0) ms.ncut = C;
@@ -528,14 +528,8 @@ __device__ __forceinline__ int chunk_cut(Misc& ms, int nvalid, float (&qv)[RPT],
         __syncthreads();
         const float gl = ms.ganc[0][col];
 #pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-            if (RPT * qq + r >= n) {
-                qv[r] = 0.0f;
-                kv[r] = 0.0f;
-                vv[r] = 0.0f;
-                G[r] = gl;
-            }
-        }
+        for (int r = 0; r < RPT; ++r)
+            if (RPT * qq + r >= n) G[r] = gl;
     }
     return n;
 }
@@ -575,10 +569,14 @@ __device__ __forceinline__ int chunk_prep(unsigned char* sm, Misc& ms, const Chu
         const float2 dt2 = make_float2(dtc, dtc), ea2 = make_float2(ea, ea), lb2 = make_float2(a.lb, a.lb);
         const float2 one2 = make_float2(1.0f, 1.0f);
         const bool sp = UNB && a.gate_mode != KDA_GATE_SAFE;
-        if (sp) {  // softplus decays first, into G (fewer values live than inside the conv loop)
-#pragma unroll
+        // softplus decays first, into a scratch over the previous chunk's dead
+        // (K o e^{G_C - G})^T tiles: fewer values live than inside the conv loop
+        float* lsc = reinterpret_cast<float*>(sm + SM_KD);
+        if (sp) {
+#pragma unroll 4
             for (int r = 0; r < RPT; ++r)
-                G[r] = log_alpha(KDA_GATE_SOFTPLUS, 0.0f, ea, __bfloat162float(rawf[(r0 + r) * D + col]), dtc);
+                lsc[(r0 + r) * D + col] =
+                    log_alpha(KDA_GATE_SOFTPLUS, 0.0f, ea, __bfloat162float(rawf[(r0 + r) * D + col]), dtc);
         }
         float run = 0.0f;
 #pragma unroll
@@ -611,7 +609,7 @@ __device__ __forceinline__ int chunk_prep(unsigned char* sm, Misc& ms, const Chu
                 const float2 gd = __fadd2_rn(one2, make_float2(__expf(-fz.x), __expf(-fz.y)));
                 la = __fmul2_rn(lb2, make_float2(__fdividef(1.0f, gd.x), __fdividef(1.0f, gd.y)));
             } else {
-                la = make_float2(G[r], G[r + 1]);
+                la = make_float2(lsc[lr * D + col], lsc[(lr + 1) * D + col]);
             }
             const bool ok0 = lr < nvalid, ok1 = lr + 1 < nvalid;
             qv[r] = ok0 ? sq.x : 0.0f;
@@ -650,7 +648,7 @@ __device__ __forceinline__ int chunk_prep(unsigned char* sm, Misc& ms, const Chu
         for (int q2 = 0; q2 < qq; ++q2) off += ms.gq[q2][col];
 #pragma unroll
         for (int r = 0; r < RPT; ++r) G[r] += off;
-        if (UNB) n = chunk_cut(ms, nvalid, qv, kv, vv, G);
+        if (UNB) n = chunk_cut(ms, nvalid, G);
         if (qq == 1) ms.gx[0][col] = G[0];          // row 16
         if (qq == 3) {
             ms.gx[1][col] = G[0];                   // row 48
@@ -661,7 +659,9 @@ __device__ __forceinline__ int chunk_prep(unsigned char* sm, Misc& ms, const Chu
         const int qk = tid / C, r = tid % C;
         const float tot = ms.npart[qk][r >> 4][0][r & 15] + ms.npart[qk][r >> 4][1][r & 15] +
                           ms.npart[qk][r >> 4][2][r & 15] + ms.npart[qk][r >> 4][3][r & 15];
-        ms.nrm[qk][r] = rsqrtf(tot + a.l2_eps);
+        // rows past a cut: zero q and k (and, below, beta: no update from v)
+        ms.nrm[qk][r] = (!UNB || r < n) ? rsqrtf(tot + a.l2_eps) : 0.0f;
+        if (UNB && qk == 0 && r >= n) ms.beta[r] = 0.0f;
     }
     __syncthreads();
 #pragma unroll
