@@ -250,6 +250,7 @@ UNBOUNDED = [
     ([150, 64], W.SAFE, -12.0, 2.0, 3, False),          # safe gate below -5: cut near 13-16 rows
     ([40, 3], W.SOFTPLUS, -5.0, 5.0, 2, True),          # ~-100 per row: one-row chunks
     ([333, 1, 65], W.SOFTPLUS, -5.0, None, 4, False),   # A_log ~ U(-1, 1): mostly whole chunks
+    ([2048], W.SOFTPLUS, -5.0, 2.0, 4, True),           # hundreds of cut chunks in one chain
 ]
 
 
