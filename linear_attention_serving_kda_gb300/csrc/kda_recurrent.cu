@@ -1,11 +1,11 @@
 // kda_recurrent.cu -- row-recurrent KDA kernels for sm_103a: verify windows
-// (and commit fused into the next window), commit, and the serial prefill for
-// the shapes the chunk kernel does not take.  Rows follow kda_row.cuh, so they
-// carry decode's bits.  At dk = dv = 128 verify windows regroup the thread
-// tiles so that a row's sums stay inside a warp (kda_verify_warp_kernel) and
-// commit streams through shared-memory stages like decode
-// (kda_commit_stream_kernel); other widths run the register kernel, one CTA
-// per unit.
+// (and commit fused into the next window), commit, and the row-by-row prefill
+// for the shapes the chunk kernel does not take (fp32 rows, dk < 128).  Rows
+// follow kda_row.cuh, so they carry decode's bits.  At dk = dv = 128 verify
+// windows and that prefill regroup the thread tiles so that a row's sums stay
+// inside a warp (kda_verify_warp_kernel) and commit streams through
+// shared-memory stages like decode (kda_commit_stream_kernel); other widths
+// run the register kernel, one CTA per unit.
 #include "kda_row.cuh"
 
 namespace kda {
