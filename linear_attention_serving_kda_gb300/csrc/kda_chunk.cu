@@ -492,6 +492,24 @@ __device__ __forceinline__ ThreadConst thread_const(const ChunkArgs& a, int h, i
     return t;
 }
 
+// The chunk path's softplus log-decay, -ea * softplus(f + dt), with
+// softplus(x) = max(x, 0) + log1p(e^-|x|): log1p(y) for y = e^-|x| in (0, 1]
+// by the fast logarithm of 1 + y (absolute error ~4e-7) and, below 2^-7, by
+// y - y^2/2 + y^3/3 - y^4/4 (truncation below 3e-11).  The prep, the split
+// path's producers and its chunk-boundary pass all call this one function,
+// so their chunk boundaries agree.
+__device__ __forceinline__ float chunk_softplus_decay(float ea, float f, float dt)
+{
+    // explicit roundings: the same bits at every call site
+    const float x = __fadd_rn(f, dt);
+    const float y = __expf(-fabsf(x));
+    float p = __fmaf_rn(-0.25f, y, 0.33333334f);
+    p = __fmaf_rn(-y, p, 0.5f);
+    p = __fmaf_rn(-y, p, 1.0f);
+    const float l1p = y < 0.0078125f ? __fmul_rn(y, p) : __logf(__fadd_rn(1.0f, y));
+    return __fmul_rn(-ea, __fadd_rn(fmaxf(x, 0.0f), l1p));
+}
+
 // Unbounded gates: the number of rows this chunk takes, at most nvalid: the
 // longest prefix over which every key dim's running log-decay G stays within
 // 80 of the reference row of each 32-row half, so that every factor
@@ -537,10 +555,10 @@ __device__ __forceinline__ int chunk_cut(Misc& ms, int nvalid, float (&G)[RPT])
 // The state-independent prep of a chunk: conv + SiLU, the gate and the running
 // log-decay G of this thread's column and 16 rows, the q/k row norms applied.
 // Registers and the prep scratch of ms only (e^{G_C} is stored by chunk_rest).
-// Returns the number of rows the chunk takes: nvalid, or with UNB (gates
-// whose log-decays are not bounded by -5: softplus, or a lower bound below
-// -5) possibly fewer (chunk_cut).
-template <bool UNB>
+// UNB: either gate formula (the gates whose log-decays are not bounded by -5:
+// softplus, or a lower bound below -5).  Returns the number of rows the chunk
+// takes: nvalid, or with CUT possibly fewer (chunk_cut).
+template <bool UNB, bool CUT = UNB>
 __device__ __forceinline__ int chunk_prep(unsigned char* sm, Misc& ms, const ChunkArgs& a, const ThreadConst& tc,
                                           int nvalid, float (&qv)[RPT], float (&kv)[RPT], float (&vv)[RPT],
                                           float (&G)[RPT])
@@ -575,8 +593,7 @@ __device__ __forceinline__ int chunk_prep(unsigned char* sm, Misc& ms, const Chu
         if (sp) {
 #pragma unroll 4
             for (int r = 0; r < RPT; ++r)
-                lsc[(r0 + r) * D + col] =
-                    log_alpha(KDA_GATE_SOFTPLUS, 0.0f, ea, __bfloat162float(rawf[(r0 + r) * D + col]), dtc);
+                lsc[(r0 + r) * D + col] = chunk_softplus_decay(ea, __bfloat162float(rawf[(r0 + r) * D + col]), dtc);
         }
         float run = 0.0f;
 #pragma unroll
@@ -648,7 +665,7 @@ __device__ __forceinline__ int chunk_prep(unsigned char* sm, Misc& ms, const Chu
         for (int q2 = 0; q2 < qq; ++q2) off += ms.gq[q2][col];
 #pragma unroll
         for (int r = 0; r < RPT; ++r) G[r] += off;
-        if (UNB) n = chunk_cut(ms, nvalid, G);
+        if (CUT) n = chunk_cut(ms, nvalid, G);
         if (qq == 1) ms.gx[0][col] = G[0];          // row 16
         if (qq == 3) {
             ms.gx[1][col] = G[0];                   // row 48
@@ -660,8 +677,8 @@ __device__ __forceinline__ int chunk_prep(unsigned char* sm, Misc& ms, const Chu
         const float tot = ms.npart[qk][r >> 4][0][r & 15] + ms.npart[qk][r >> 4][1][r & 15] +
                           ms.npart[qk][r >> 4][2][r & 15] + ms.npart[qk][r >> 4][3][r & 15];
         // rows past a cut: zero q and k (and, below, beta: no update from v)
-        ms.nrm[qk][r] = (!UNB || r < n) ? rsqrtf(tot + a.l2_eps) : 0.0f;
-        if (UNB && qk == 0 && r >= n) ms.beta[r] = 0.0f;
+        ms.nrm[qk][r] = (!CUT || r < n) ? rsqrtf(tot + a.l2_eps) : 0.0f;
+        if (CUT && qk == 0 && r >= n) ms.beta[r] = 0.0f;
     }
     __syncthreads();
 #pragma unroll
@@ -952,11 +969,12 @@ __device__ __forceinline__ bool chunk_rest(unsigned char* sm, Misc& ms, const Ch
 // tensor memory holds W^T and U'^T, shared memory the T tile and the bf16
 // high/low P, Q o e^G and (K o e^{G_C - G})^T tiles, and ms.gamma holds
 // e^{G_C}.  False: a tensor-core wait ran out (ms.err set).
+template <bool UNB>
 __device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const ChunkArgs& a, const ThreadConst& tc,
                                             int nvalid, uint32_t tmem, uint32_t lane_base, uint32_t& ph)
 {
     float qv[RPT], kv[RPT], vv[RPT], G[RPT];
-    chunk_prep<false>(sm, ms, a, tc, nvalid, qv, kv, vv, G);
+    chunk_prep<UNB, false>(sm, ms, a, tc, nvalid, qv, kv, vv, G);
     return chunk_rest(sm, ms, a, nvalid, tmem, lane_base, ph, qv, kv, vv, G);
 }
 
@@ -1331,7 +1349,32 @@ struct SplitArgs {
     int* consumed;         // [NC]: chunks the chain has finished reading
     unsigned char* ring;   // [NC][SPLIT_RING][SLOT_BYTES]
     int NC;                // chains = N * H
+    // unbounded gates: chain u's chunks, bnd[u * bs] = count n, then the n
+    // chunk starts and the segment's end (kda_chunk_bounds_kernel); null:
+    // fixed 64-row chunks
+    const int* bnd;
+    int bs;
 };
+
+// chain u's number of chunks, and chunk c's first row and row count (UNB:
+// from the chunk lists)
+template <bool UNB>
+__device__ __forceinline__ int split_nchunks(const SplitArgs& sp, int u, int seg0, int seg1)
+{
+    return UNB ? sp.bnd[(size_t)u * sp.bs] : (seg1 - seg0 + C - 1) / C;
+}
+template <bool UNB>
+__device__ __forceinline__ void split_chunk(const SplitArgs& sp, int u, int c, int seg0, int seg1, int& c0, int& nv)
+{
+    if (UNB) {
+        const int* b = sp.bnd + (size_t)u * sp.bs + 1;
+        c0 = b[c];
+        nv = b[c + 1] - c0;
+    } else {
+        c0 = seg0 + c * C;
+        nv = min(C, seg1 - c0);
+    }
+}
 
 __device__ __forceinline__ unsigned char* slot_ptr(const SplitArgs& sp, int u, int c)
 {
@@ -1357,6 +1400,7 @@ __device__ __forceinline__ bool split_unit(const ChunkArgs& a, int u, int& slot,
     return seg1 > seg0;
 }
 
+template <bool UNB>
 __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, const RawMaps& maps,
                                const SplitArgs& sp, uint32_t tmem)
 {
@@ -1365,9 +1409,9 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
     const int H = a.H, NC = sp.NC;
     const int p = blockIdx.x - NC, NP = gridDim.x - NC;
     int maxc = 0;
-    for (int u = 0; u < NC; u += H) {
+    for (int u = 0; u < NC; u += (UNB ? 1 : H)) {  // fixed chunks: the same count for every head
         int slot, s0, s1;
-        if (split_unit(a, u, slot, s0, s1, false)) maxc = max(maxc, (s1 - s0 + C - 1) / C);
+        if (split_unit(a, u, slot, s0, s1, false)) maxc = max(maxc, split_nchunks<UNB>(sp, u, s0, s1));
     }
     uint32_t ph = 0, rph = 0;
     int cur_h = -1;
@@ -1377,9 +1421,9 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
         const int c = t / NC, u = t % NC, h = u % H;
         int slot, seg0, seg1;
         if (!split_unit(a, u, slot, seg0, seg1, false)) continue;
-        const int c0 = seg0 + c * C;
-        if (c0 >= seg1) continue;
-        const int nvalid = min(C, seg1 - c0);
+        if (c >= split_nchunks<UNB>(sp, u, seg0, seg1)) continue;
+        int c0, nvalid;
+        split_chunk<UNB>(sp, u, c, seg0, seg1, c0, nvalid);
         if (h != cur_h) {
             tc = thread_const(a, h, col);
             cur_h = h;
@@ -1397,11 +1441,11 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
         __syncthreads();
         if (ms.err) break;
         if (!wait_rows(ms, rph, a.dev_status)) break;
-        if (c == 0) {
-            patch_halo(sm, a, slot, h, 0);
+        if (c0 - seg0 < HALO) {
+            patch_halo(sm, a, slot, h, c0 - seg0);
             __syncthreads();
         }
-        if (!chunk_intra(sm, ms, a, tc, nvalid, tmem, lane_base, ph)) break;
+        if (!chunk_intra<UNB>(sm, ms, a, tc, nvalid, tmem, lane_base, ph)) break;
 
         // publish: the chain's operands as the bf16 high and low tiles
         // chunk_intra built (and -W from W^T), by bulk copies; U'^T and e^{G_C}
@@ -1447,13 +1491,14 @@ __device__ __forceinline__ void chain_fetch(unsigned char* sm, uint64_t* bar, co
         ptx::bulk_g2s(sm + off + o, src + off + o, min(32768u, bytes - o), bar);
 }
 
+template <bool UNB>
 __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, const SplitArgs& sp, uint32_t tmem,
                             int u, int slot, int seg0, int seg1)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lq = warp & 3, qq = tid >> 7, col = tid & (D - 1);
     const uint32_t lane_base = (uint32_t)(lq * 32) << 16;
     const int H = a.H, K = a.K, h = u % H, r0 = RPT * qq;
-    const int nchunks = (seg1 - seg0 + C - 1) / C;
+    const int nchunks = split_nchunks<UNB>(sp, u, seg0, seg1);
     const float nw = a.norm_w ? a.norm_w[col] : 1.0f;
     uint32_t ph = 0;
     bool pend_a = false, pend_b = false;
@@ -1512,13 +1557,14 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
     // output gate rows of a chunk, loaded one chunk ahead and unpacked after its products
     uint32_t gw[RPT / 2];
     auto load_gate = [&](int c) {
-        const int cc0 = seg0 + c * C;
-        load_gate_words(gw, a, cc0, r0, min(C, seg1 - cc0), h, col);
+        int cc0, cnv;
+        split_chunk<UNB>(sp, u, c, seg0, seg1, cc0, cnv);
+        load_gate_words(gw, a, cc0, r0, cnv, h, col);
     };
     load_gate(0);
     for (int c = 0; c < nchunks && !ms.err; ++c) {
-        const int c0 = seg0 + c * C;
-        const int nvalid = min(C, seg1 - c0);
+        int c0, nvalid;
+        split_chunk<UNB>(sp, u, c, seg0, seg1, c0, nvalid);
         const uint32_t c_ot = (c & 1) ? CT_OT1 : CT_OT0;
         ptx::tmem_st16(tmem + lane_base + CT_UT + RPT * qq, up);
         if (tid < D) ms.gamma[tid] = gam;
@@ -1633,6 +1679,7 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
     }
 }
 
+template <bool UNB>
 __global__ void __launch_bounds__(NT, 1)
     kda_chunk_split_kernel(const ChunkArgs a, const __grid_constant__ RawMaps maps, const SplitArgs sp)
 {
@@ -1658,27 +1705,79 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = ms.tmem;
-    if (chain) split_chain(sm, ms, a, sp, tmem, blockIdx.x, slot, seg0, seg1);
-    else split_producer(sm, ms, a, maps, sp, tmem);
+    if (chain) split_chain<UNB>(sm, ms, a, sp, tmem, blockIdx.x, slot, seg0, seg1);
+    else split_producer<UNB>(sm, ms, a, maps, sp, tmem);
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 0) ptx::tmem_dealloc(tmem, TM_COLS);
 }
 
-}  // namespace chk
-
-// Per-row log decays >= -5 (the safe gate with lb >= -5): fixed 64-row
-// chunks.  Other gates cut a chunk where its decays leave the factored range
-// (the chunk boundaries then depend on the data, which the split path's
-// producers, working ahead of the chain, cannot know).
-static bool chunk_bounded(const kda_params* p)
+// Unbounded gates on the split path: each chain's chunk boundaries, fixed
+// ahead of the producers by the fused kernel's own rule (chunk_cut) on the
+// same running log-decays -- the gate in the prep's arithmetic, each
+// quarter's sum in row order, then the quarter offsets -- so the chunks are
+// the fused kernel's.  One CTA per chain walks its chunks; chain u's list is
+// bnd[u * bs]: the count n, the n chunk starts, the segment's end.
+__global__ void __launch_bounds__(NT, 1) kda_chunk_bounds_kernel(const ChunkArgs a, int* bnd, int bs)
 {
-    return p->gate_mode == KDA_GATE_SAFE && p->gate_lower_bound >= -5.0f;
+    __shared__ Misc ms;
+    const int u = blockIdx.x, tid = threadIdx.x, col = tid & (D - 1), qq = tid >> 7, r0 = RPT * qq;
+    int* b = bnd + (size_t)u * bs;
+    int slot, seg0, seg1;
+    if (!split_unit(a, u, slot, seg0, seg1, false)) {
+        if (tid == 0) b[0] = 0;
+        return;
+    }
+    const int H = a.H, h = u % H;
+    const float ea = expf(a.A_log[h]), dtc = a.dt_bias[(size_t)h * D + col];
+    const __nv_bfloat16* fg = static_cast<const __nv_bfloat16*>(a.f);
+    int count = 0;
+    for (int c0 = seg0; c0 < seg1;) {
+        const int nvalid = min(C, seg1 - c0);
+        float G[RPT];
+        // all 16 rows' gates in flight at once (rows past the segment's end
+        // read its last row, unused)
+        __nv_bfloat16 fr[RPT];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) fr[r] = fg[((size_t)min(c0 + r0 + r, seg1 - 1) * H + h) * D + col];
+        float run = 0.0f;
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            float la = 0.0f;
+            if (r0 + r < nvalid) {
+                const float f = __bfloat162float(fr[r]);
+                if (a.gate_mode == KDA_GATE_SAFE) {  // the prep's lb * sigmoid(ea (f + dt)), operation by operation
+                    const float fz = __fmul_rn(ea, __fadd_rn(f, dtc));
+                    la = __fmul_rn(a.lb, __fdividef(1.0f, __fadd_rn(1.0f, __expf(-fz))));
+                } else {
+                    la = chunk_softplus_decay(ea, f, dtc);
+                }
+            }
+            run += la;
+            G[r] = run;
+        }
+        ms.gq[qq][col] = G[RPT - 1];
+        __syncthreads();
+        float off = 0.0f;
+        for (int q2 = 0; q2 < qq; ++q2) off += ms.gq[q2][col];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) G[r] += off;
+        const int n = chunk_cut(ms, nvalid, G);
+        if (tid == 0) b[1 + count] = c0;
+        ++count;
+        c0 += n;
+    }
+    if (tid == 0) {
+        b[1 + count] = seg1;
+        b[0] = count;
+    }
 }
+
+}  // namespace chk
 
 bool chunk_split_wanted(const kda_params* p, int N, int T)
 {
-    return chunk_supported(p) && chunk_bounded(p) && (long long)N * p->num_heads <= 64 && T >= 1024;
+    return chunk_supported(p) && (long long)N * p->num_heads <= 64 && T >= 1024;
 }
 
 size_t chunk_split_bytes(int N, int H)
@@ -1752,18 +1851,22 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
             !encode_rows(&maps.v, a.v, a.H, a.T, chk::RAWR) || !encode_rows(&maps.f, a.f, a.H, a.T, chk::C))
             return cudaErrorInvalidValue;
     }
-    if (a.split_ws && !unb) {
+    if (a.split_ws) {
         // split path: one cooperative grid of one CTA per SM, chains first
         static bool split_attr[128];
         int sms = 0, per_sm = 0;
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (dev >= 0 && dev < 128 && !split_attr[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(chk::kda_chunk_split_kernel,
+            cudaError_t e = cudaFuncSetAttribute(chk::kda_chunk_split_kernel<false>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, chk::SMEM_BYTES);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(chk::kda_chunk_split_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, chk::SMEM_BYTES);
             if (e != cudaSuccess) return e;
             split_attr[dev] = true;
         }
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chk::kda_chunk_split_kernel, chk::NT, chk::SMEM_BYTES);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chk::kda_chunk_split_kernel<false>, chk::NT,
+                                                      chk::SMEM_BYTES);
         const int nc = a.N * a.H;
         if (per_sm >= 1 && 2 * nc <= sms) {
             chk::SplitArgs sp;
@@ -1772,12 +1875,20 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
             sp.consumed = sp.ready + (size_t)nc * chk::SPLIT_RING;
             sp.ring = a.split_ws + flags;
             sp.NC = nc;
+            // unbounded gates: the chains' chunk lists after the ring
+            int* bnd = unb ? reinterpret_cast<int*>(a.split_ws + chunk_split_bytes(a.N, a.H)) : nullptr;
+            sp.bnd = bnd;
+            sp.bs = a.T + 2;
             cudaError_t e = cudaMemsetAsync(a.split_ws, 0, flags, st);
             if (e != cudaSuccess) return e;
+            if (unb) {
+                chk::kda_chunk_bounds_kernel<<<nc, chk::NT, 0, st>>>(a, bnd, sp.bs);
+                if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            }
             ChunkArgs aa = a;
             void* args[] = {&aa, &maps, &sp};
-            return cudaLaunchCooperativeKernel((const void*)chk::kda_chunk_split_kernel, dim3(sms), dim3(chk::NT),
-                                               args, chk::SMEM_BYTES, st);
+            const void* fn = unb ? (const void*)chk::kda_chunk_split_kernel<true> : (const void*)chk::kda_chunk_split_kernel<false>;
+            return cudaLaunchCooperativeKernel(fn, dim3(sms), dim3(chk::NT), args, chk::SMEM_BYTES, st);
         }
         // too few SMs for producers beside the chains: the fused kernel below
     }

@@ -133,10 +133,13 @@ def test_split_workspace_size(lib):
     assert kda.kda_prefill_workspace_bytes(_params(io_dtype=kda.KDA_DTYPE_F32, gate_mode=kda.KDA_GATE_SOFTPLUS),
                                            N, 4096) == 0  # fp32 rows: the row path
     # softplus (and safe gates below -5) chunk where the decays require: fused path only
-    assert kda.kda_prefill_workspace_bytes(_params(io_dtype=kda.KDA_DTYPE_BF16, gate_mode=kda.KDA_GATE_SOFTPLUS),
-                                           N, 4096) == 256
-    assert kda.kda_prefill_workspace_bytes(_params(io_dtype=kda.KDA_DTYPE_BF16, gate_lower_bound=-8.0),
-                                           N, 4096) == 256
+    # softplus (and safe gates below -5): the split path plus each chain's chunk
+    # list (a count, up to T chunk starts and the end: T + 2 int32), 1 KiB aligned
+    bnd = -(-(nc * (4096 + 2) * 4) // 1024) * 1024
+    for q in (_params(io_dtype=kda.KDA_DTYPE_BF16, gate_mode=kda.KDA_GATE_SOFTPLUS),
+              _params(io_dtype=kda.KDA_DTYPE_BF16, gate_lower_bound=-8.0)):
+        assert kda.kda_prefill_workspace_bytes(q, N, 4096) == sched + flags + nc * 8 * slot + bnd
+        assert kda.kda_prefill_workspace_bytes(q, N, 1000) == 256   # short: fused path, no list
 
 
 def test_status_strings(lib):

@@ -105,3 +105,28 @@ def test_split_slots(cuda_lib):
     t0, t1 = 900, 1400
     assert torch.all(torch.isnan(p.out[t0:t1]))
     assert torch.equal(p.out[:t0], f.out[:t0]) and torch.equal(p.out[t1:wl.T], f.out[t1:wl.T])
+
+
+UNBOUNDED = [
+    # lens, H, gate, lower bound, A_log (all heads or None), out_gate
+    ([1500, 0, 1100], 4, W.SOFTPLUS, -5.0, None, True),     # mostly whole chunks
+    ([1200, 3], 2, W.SOFTPLUS, -5.0, 3.0, False),           # chunks of a few rows, first chunks < 3 rows
+    ([1030], 4, W.SAFE, -12.0, 2.0, True),                  # safe gate below -5
+]
+
+
+@pytest.mark.parametrize("lens,H,gate,lb,alog,og", UNBOUNDED)
+def test_split_unbounded_gates(cuda_lib, oracle_mod, lens, H, gate, lb, alog, og):
+    """Gates with unbounded log-decay on the split path: a pass fixes each
+    chain's chunk boundaries by the fused kernel's rule on the same decays,
+    so split and fused agree bit for bit, and both match the oracle."""
+    wl = W.make_workload("split_u", 820 + sum(lens) + H, lens, H=H, d=128, K=4, io_dtype=W.BF16,
+                         gate_mode=gate, lower_bound=lb, out_gate=og, init_state="random")
+    if alog is not None:
+        wl.arrays["A_log"] = np.full_like(wl.arrays["A_log"], alog)
+    p, f = _both(wl, out_dtype=W.F32)
+    assert torch.equal(p.out[:wl.T], f.out[:wl.T])
+    assert torch.equal(p.rec_state, f.rec_state)
+    assert torch.equal(p.conv_state, f.conv_state)
+    units = [(s_, h) for s_ in range(wl.N) if lens[s_] > 0 for h in sorted({0, H - 1})]
+    _units_close(oracle_mod, wl, p, units, "split vs oracle")
