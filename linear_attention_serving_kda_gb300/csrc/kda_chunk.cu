@@ -1318,7 +1318,9 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
 // sides run the fused kernel's instructions on the same values (the producers
 // publish the bf16 tiles chunk_intra builds; the chain runs the fused kernel's
 // bf16 third and fourth products), so the results have the fused kernel's
-// bits.  All waits are bounded.
+// bits.  With unbounded gates the chunks are those of a chunk list fixed
+// beforehand by the fused kernel's rule (kda_chunk_bounds_kernel), so the
+// same holds.  All waits are bounded.
 
 constexpr int SPLIT_RING = 8;
 // Slot layout (bytes).  The chain's products run on bf16 operands split into a
