@@ -126,9 +126,10 @@ size_t prefill_workspace_bytes(const kda_params* p, int32_t N, int32_t T, bool a
     if (allow_split && chunk_split_wanted(p, N, T)) {
         size_t b = align1024(sched) + chunk_split_bytes(N, p->num_heads);
         // gates whose per-row log-decay is not bounded by -5: each chain's
-        // chunk list (a count, up to T chunk starts, the end) after the ring
+        // chunk list (a count, up to T chunk starts, the end, the first cut
+        // chunk) after the ring
         if (!(p->gate_mode == KDA_GATE_SAFE && p->gate_lower_bound >= -5.0f))
-            b += align1024((size_t)N * p->num_heads * ((size_t)T + 2) * sizeof(int32_t));
+            b += align1024((size_t)N * p->num_heads * ((size_t)T + 3) * sizeof(int32_t));
         return b;
     }
     return sched;

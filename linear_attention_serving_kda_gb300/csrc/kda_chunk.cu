@@ -1718,53 +1718,84 @@ __global__ void __launch_bounds__(NT, 1)
 // ahead of the producers by the fused kernel's own rule (chunk_cut) on the
 // same running log-decays -- the gate in the prep's arithmetic, each
 // quarter's sum in row order, then the quarter offsets -- so the chunks are
-// the fused kernel's.  One CTA per chain walks its chunks; chain u's list is
-// bnd[u * bs]: the count n, the n chunk starts, the segment's end.
+// the fused kernel's.  Chain u's list is bnd[u * bs]: the count n, the n
+// chunk starts, the segment's end; bnd[u * bs + bs - 1] is the first 64-row
+// chunk (from the segment's start) that gets cut.
+//
+// The rows of chunk [c0, c0 + nvalid) of (sequence seg, head h): returns the
+// rows it takes (all threads).
+__device__ __forceinline__ int bounds_chunk(Misc& ms, const ChunkArgs& a, int c0, int nvalid, int seg1, int h,
+                                            float ea, float dtc)
+{
+    const int tid = threadIdx.x, col = tid & (D - 1), qq = tid >> 7, r0 = RPT * qq, H = a.H;
+    const __nv_bfloat16* fg = static_cast<const __nv_bfloat16*>(a.f);
+    float G[RPT];
+    // all 16 rows' gates in flight at once (rows past the segment's end read
+    // its last row, unused)
+    __nv_bfloat16 fr[RPT];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) fr[r] = fg[((size_t)min(c0 + r0 + r, seg1 - 1) * H + h) * D + col];
+    float run = 0.0f;
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        float la = 0.0f;
+        if (r0 + r < nvalid) {
+            const float f = __bfloat162float(fr[r]);
+            if (a.gate_mode == KDA_GATE_SAFE) {  // the prep's lb * sigmoid(ea (f + dt)), operation by operation
+                const float fz = __fmul_rn(ea, __fadd_rn(f, dtc));
+                la = __fmul_rn(a.lb, __fdividef(1.0f, __fadd_rn(1.0f, __expf(-fz))));
+            } else {
+                la = chunk_softplus_decay(ea, f, dtc);
+            }
+        }
+        run += la;
+        G[r] = run;
+    }
+    ms.gq[qq][col] = G[RPT - 1];
+    __syncthreads();
+    float off = 0.0f;
+    for (int q2 = 0; q2 < qq; ++q2) off += ms.gq[q2][col];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) G[r] += off;
+    return chunk_cut(ms, nvalid, G);
+}
+
+// Every 64-row chunk from a segment's start, in parallel (block = chunk
+// blockIdx.x of chain blockIdx.y): the first one that gets cut, per chain.
+// Up to there the chain's chunks are these; the list's last entry starts
+// above any chunk index.
+__global__ void __launch_bounds__(NT) kda_chunk_cutscan_kernel(const ChunkArgs a, int* bnd, int bs)
+{
+    __shared__ Misc ms;
+    const int u = blockIdx.y, c = blockIdx.x, tid = threadIdx.x, col = tid & (D - 1);
+    int slot, seg0, seg1;
+    if (!split_unit(a, u, slot, seg0, seg1, false)) return;
+    const int c0 = seg0 + c * C;
+    if (c0 >= seg1) return;
+    const int h = u % a.H, nvalid = min(C, seg1 - c0);
+    const int n = bounds_chunk(ms, a, c0, nvalid, seg1, h, expf(a.A_log[h]), a.dt_bias[(size_t)h * D + col]);
+    if (tid == 0 && n < nvalid) atomicMin(bnd + (size_t)u * bs + bs - 1, c);
+}
+
+// The chunk lists: the 64-row chunks before each chain's first cut, then (one
+// CTA per chain) its chunks one after another from there.
 __global__ void __launch_bounds__(NT, 1) kda_chunk_bounds_kernel(const ChunkArgs a, int* bnd, int bs)
 {
     __shared__ Misc ms;
-    const int u = blockIdx.x, tid = threadIdx.x, col = tid & (D - 1), qq = tid >> 7, r0 = RPT * qq;
+    const int u = blockIdx.x, tid = threadIdx.x, col = tid & (D - 1);
     int* b = bnd + (size_t)u * bs;
     int slot, seg0, seg1;
     if (!split_unit(a, u, slot, seg0, seg1, false)) {
         if (tid == 0) b[0] = 0;
         return;
     }
-    const int H = a.H, h = u % H;
+    const int h = u % a.H;
+    const int nfix = min(b[bs - 1], (seg1 - seg0 + C - 1) / C);  // whole 64-row chunks before the first cut
+    for (int c = tid; c < nfix; c += NT) b[1 + c] = seg0 + c * C;
+    int count = nfix;
     const float ea = expf(a.A_log[h]), dtc = a.dt_bias[(size_t)h * D + col];
-    const __nv_bfloat16* fg = static_cast<const __nv_bfloat16*>(a.f);
-    int count = 0;
-    for (int c0 = seg0; c0 < seg1;) {
-        const int nvalid = min(C, seg1 - c0);
-        float G[RPT];
-        // all 16 rows' gates in flight at once (rows past the segment's end
-        // read its last row, unused)
-        __nv_bfloat16 fr[RPT];
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) fr[r] = fg[((size_t)min(c0 + r0 + r, seg1 - 1) * H + h) * D + col];
-        float run = 0.0f;
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-            float la = 0.0f;
-            if (r0 + r < nvalid) {
-                const float f = __bfloat162float(fr[r]);
-                if (a.gate_mode == KDA_GATE_SAFE) {  // the prep's lb * sigmoid(ea (f + dt)), operation by operation
-                    const float fz = __fmul_rn(ea, __fadd_rn(f, dtc));
-                    la = __fmul_rn(a.lb, __fdividef(1.0f, __fadd_rn(1.0f, __expf(-fz))));
-                } else {
-                    la = chunk_softplus_decay(ea, f, dtc);
-                }
-            }
-            run += la;
-            G[r] = run;
-        }
-        ms.gq[qq][col] = G[RPT - 1];
-        __syncthreads();
-        float off = 0.0f;
-        for (int q2 = 0; q2 < qq; ++q2) off += ms.gq[q2][col];
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) G[r] += off;
-        const int n = chunk_cut(ms, nvalid, G);
+    for (int c0 = seg0 + nfix * C; c0 < seg1;) {
+        const int n = bounds_chunk(ms, a, c0, min(C, seg1 - c0), seg1, h, ea, dtc);
         if (tid == 0) b[1 + count] = c0;
         ++count;
         c0 += n;
@@ -1880,10 +1911,14 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
             // unbounded gates: the chains' chunk lists after the ring
             int* bnd = unb ? reinterpret_cast<int*>(a.split_ws + chunk_split_bytes(a.N, a.H)) : nullptr;
             sp.bnd = bnd;
-            sp.bs = a.T + 2;
+            sp.bs = a.T + 3;
             cudaError_t e = cudaMemsetAsync(a.split_ws, 0, flags, st);
             if (e != cudaSuccess) return e;
             if (unb) {
+                // first cut per chain: "none" (0x7f7f7f7f) until the scan finds one
+                e = cudaMemsetAsync(bnd, 0x7f, (size_t)nc * sp.bs * sizeof(int), st);
+                if (e != cudaSuccess) return e;
+                chk::kda_chunk_cutscan_kernel<<<dim3((a.T + chk::C - 1) / chk::C, nc), chk::NT, 0, st>>>(a, bnd, sp.bs);
                 chk::kda_chunk_bounds_kernel<<<nc, chk::NT, 0, st>>>(a, bnd, sp.bs);
                 if ((e = cudaGetLastError()) != cudaSuccess) return e;
             }

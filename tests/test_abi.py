@@ -134,8 +134,9 @@ def test_split_workspace_size(lib):
                                            N, 4096) == 0  # fp32 rows: the row path
     # softplus (and safe gates below -5) chunk where the decays require: fused path only
     # softplus (and safe gates below -5): the split path plus each chain's chunk
-    # list (a count, up to T chunk starts and the end: T + 2 int32), 1 KiB aligned
-    bnd = -(-(nc * (4096 + 2) * 4) // 1024) * 1024
+    # list (a count, up to T chunk starts, the end, the first cut chunk: T + 3
+    # int32), 1 KiB aligned
+    bnd = -(-(nc * (4096 + 3) * 4) // 1024) * 1024
     for q in (_params(io_dtype=kda.KDA_DTYPE_BF16, gate_mode=kda.KDA_GATE_SOFTPLUS),
               _params(io_dtype=kda.KDA_DTYPE_BF16, gate_lower_bound=-8.0)):
         assert kda.kda_prefill_workspace_bytes(q, N, 4096) == sched + flags + nc * 8 * slot + bnd
