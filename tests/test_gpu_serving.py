@@ -109,6 +109,48 @@ def test_graph_verify_commit(cuda_lib):
         assert torch.equal(gr.conv_state, ea.conv_state)
 
 
+PREFILL_GRAPH = [
+    # lens, H, gate, A_log (all heads or None): fused / split path, bounded / unbounded gates
+    ([130, 70, 1], 2, W.SAFE, None),
+    ([200, 9], 2, W.SOFTPLUS, 3.0),
+    ([1100, 300], 2, W.SAFE, None),
+    ([1100, 300], 2, W.SOFTPLUS, 3.0),
+]
+
+
+@pytest.mark.parametrize("lens,H,gate,alog", PREFILL_GRAPH)
+def test_graph_prefill(cuda_lib, lens, H, gate, alog):
+    """A captured prefill (fused or split path; for unbounded gates with the
+    chunk-boundary kernels in the graph) replayed over new rows and reset
+    states gives the bits of eager calls."""
+    d = 128
+    wl = W.make_workload("gpre", 604, lens, H=H, d=d, K=4, io_dtype=W.BF16, gate_mode=gate,
+                         lower_bound=-5.0, out_gate=True, init_state="random")
+    if alog is not None:
+        wl.arrays["A_log"] = np.full_like(wl.arrays["A_log"], alog)
+    ea, gr = _pair(wl)
+    for dc in (ea, gr):  # first calls outside capture (one-time set-up, workspace)
+        K.check(dc.prefill())
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        K.check(gr.prefill())
+    torch.cuda.synchronize()
+    for step in range(2):
+        rows = make_rows(720 + step, lens, H, d, gate)
+        for dc in (ea, gr):  # new rows, initial states back in place (the graph holds the buffers)
+            _load_rows(dc, rows)
+            dc.conv_state.copy_(dc.conv_state0)
+            dc.rec_state.copy_(dc.rec_state0)
+        K.check(ea.prefill())
+        graph.replay()
+        torch.cuda.synchronize()
+        assert int(gr.dev_status.item()) == 0 and int(ea.dev_status.item()) == 0
+        assert torch.equal(gr.out[:wl.T], ea.out[:wl.T])
+        assert torch.equal(gr.rec_state, ea.rec_state)
+        assert torch.equal(gr.conv_state, ea.conv_state)
+
+
 def test_serving_loop_against_oracle(cuda_lib, oracle_mod):
     """Six decode steps with sequences paused and resumed (negative slots):
     every slot ends where the oracle puts its sequence after the rows it
