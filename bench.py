@@ -1,7 +1,7 @@
 """KDA layer throughput on GB300: tokens/s and fraction of the HBM roofline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|verify|prefill_varlen|prefill_long] [--no-legs]
+                    [--workload decode|verify|prefill_varlen|prefill_long|...] [--no-legs]
 
 One step is one pass of the layer's hot path over one batch of seeded
 synthetic input.  The headline workload is the decode step (64 sequences x
@@ -443,7 +443,8 @@ def main():
     ap.add_argument("--no-legs", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "verify", "prefill_varlen", "prefill_long", "prefill_small"])
+                    choices=["decode", "verify", "prefill_varlen", "prefill_long", "prefill_small",
+                             "prefill_varlen_softplus"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -550,6 +551,13 @@ def run_single_leg(kda, args, stream):
         fn = lambda: W.make_workload("prefill_small_n2x2048_h32_d128_bf16", 5, [2048, 2048], H=32, d=128,  # noqa: E731
                                      K=4, io_dtype=W.BF16, gate_mode=W.SAFE, lower_bound=-5.0,
                                      init_state="random")
+        return leg_prefill(kda, fn, args.steps, stream)
+    if args.workload == "prefill_varlen_softplus":
+        # the varlen case's lengths and rows with the softplus gate: the chunk
+        # kernel's data-dependent chunks
+        fn = lambda: W.make_workload("prefill_varlen_softplus_n8_h32_d128_bf16", 2, None, H=32, d=128,  # noqa: E731
+                                     K=4, io_dtype=W.BF16, gate_mode=W.SOFTPLUS, lower_bound=-5.0,
+                                     init_state="random", draw_lens=(8, 512, 8192))
         return leg_prefill(kda, fn, args.steps, stream)
     fn = W.varlen_prefill_case if args.workload == "prefill_varlen" else W.long_prefill_case
     return leg_prefill(kda, fn, args.steps, stream)
