@@ -157,6 +157,17 @@ def prefill_state_bytes(N, H, d=128, K=4, io=2):
 
 # --------------------------------------------------------------- workloads
 
+_WL_CACHE = {}
+
+
+def cached(wl_fn):
+    """The workload wl_fn() builds, drawn once per run (the full-size draws
+    take seconds)."""
+    if wl_fn not in _WL_CACHE:
+        _WL_CACHE[wl_fn] = wl_fn()
+    return _WL_CACHE[wl_fn]
+
+
 def make_sets(wl_fn, n_sets, out_dtype):
     from linear_attention_serving_kda_gb300.runtime import DeviceCase
 
@@ -227,7 +238,7 @@ def leg_prefill(kda, wl_fn, reps, stream):
     from linear_attention_serving_kda_gb300 import workloads as W
     from linear_attention_serving_kda_gb300.runtime import DeviceCase
 
-    wl = wl_fn()
+    wl = cached(wl_fn)
     dc = DeviceCase(wl, out_dtype=W.BF16)
     kda.check(dc.prefill(stream=stream))  # warm-up
     durs = []
@@ -239,15 +250,19 @@ def leg_prefill(kda, wl_fn, reps, stream):
     bpt = prefill_bytes_per_token_head(out=2, out_gate=wl.has_out_gate)
     alg = wl.T * wl.H * bpt + prefill_state_bytes(wl.N, wl.H)
     # algorithmic tensor work: 5 C d + 6 d^2 FLOPs per (row, head) (chunk C = 64;
-    # triangles at half), measured against the dense bf16 tensor peak (the
-    # kernels run tf32, whose nominal dense rate is half of bf16's)
+    # triangles at half), against the measured dense bf16 tensor peak (burst:
+    # the kernel is timed alone).  tf32_frac is a secondary figure: the same
+    # FLOPs against the tf32 rate (nominally half of bf16's) that the first
+    # two products run at.
     d = wl.dk
     flops = wl.T * wl.H * (5 * 64 * d + 6 * d * d)
     bf16_tflops = load_peaks()[1]
     tf = flops / (ms * 1e-3) / 1e12
     return {"workload": wl.name, "tokens": wl.T, "ms": ms, "tokens_per_s": wl.T / (ms * 1e-3),
             "alg_bytes": alg, "achieved_gbs": alg / (ms * 1e-3) / 1e9,
-            "alg_tflops": tf, "tf32_frac": tf / (bf16_tflops / 2.0)}
+            "alg_flops": flops, "alg_tflops": tf, "bf16_frac": tf / bf16_tflops,
+            "bf16_frac_of": f"measured bf16 dense burst peak {bf16_tflops} TFLOP/s",
+            "tf32_frac": tf / (bf16_tflops / 2.0)}
 
 
 def leg_verify(kda, reps, stream):
@@ -388,6 +403,91 @@ def e2e_decode(kda, steps, warmup, stream):
             "pipeline": "upload of step i+1 and download of step i overlap the decode of step i"}
 
 
+def _pack_rows(dc, names):
+    """Pack a DeviceCase's row tensors back to back (256-byte aligned pieces)
+    into one pinned host buffer and one device buffer, and rebind the case's
+    tensors to views of the device buffer, so that one host-to-device copy
+    brings in every input row of a call.  Returns (host, device, h2d bytes)."""
+    import torch
+
+    offs, off = {}, 0
+    for nm in names:
+        t = getattr(dc, nm)
+        offs[nm] = off
+        off += (t.numel() * t.element_size() + 255) // 256 * 256
+    host = torch.empty(off, dtype=torch.uint8).pin_memory()
+    dev = torch.empty(off, dtype=torch.uint8, device="cuda")
+    n_bytes = 0
+    for nm in names:
+        t = getattr(dc, nm)
+        n = t.numel() * t.element_size()
+        host[offs[nm]:offs[nm] + n].view(t.dtype).view(t.shape).copy_(t.cpu())
+        setattr(dc, nm, dev[offs[nm]:offs[nm] + n].view(t.dtype).view(t.shape))
+        n_bytes += n
+    return host, dev, n_bytes
+
+
+def e2e_leg(kda, dc, names, call, out_view, reps, stream):
+    """A leg's call end to end through the public API with host buffers: each
+    rep copies the call's input rows from pinned host memory (one packed
+    copy), runs `call()` on them and copies `out_view()` back to pinned host
+    memory, all on `stream` and inside the CUDA-event region.  States stay
+    resident (reset between reps, outside the region).  Median over reps."""
+    import torch
+
+    host, dev, h2d = _pack_rows(dc, names)
+    out_host = torch.empty(out_view().shape, dtype=out_view().dtype).pin_memory()
+    d2h = out_host.numel() * out_host.element_size()
+    durs = []
+    for r in range(reps + 1):
+        dc.reset_states()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            dev.copy_(host, non_blocking=True)
+            kda.check(call())
+            out_host.copy_(out_view(), non_blocking=True)
+            t1.record(stream)
+        torch.cuda.synchronize()
+        if r:  # the first rep warms up
+            durs.append(t0.elapsed_time(t1))
+    return statistics.median(durs), h2d, d2h
+
+
+def e2e_prefill(kda, wl_fn, reps, stream):
+    from linear_attention_serving_kda_gb300 import workloads as W
+    from linear_attention_serving_kda_gb300.runtime import DeviceCase
+
+    wl = cached(wl_fn)
+    dc = DeviceCase(wl, out_dtype=W.BF16)
+    names = ["q", "k", "v", "f", "b"] + (["g"] if wl.has_out_gate else [])
+    ms, h2d, d2h = e2e_leg(kda, dc, names, lambda: dc.prefill(stream=stream), lambda: dc.out[:wl.T], reps, stream)
+    return {"value": wl.T / (ms * 1e-3), "unit": "tokens/s", "ms": ms, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "path": "kda_prefill_varlen: rows host->device, prefill, outputs device->host"}
+
+
+def e2e_verify(kda, reps, stream):
+    from linear_attention_serving_kda_gb300 import workloads as W
+    from linear_attention_serving_kda_gb300.runtime import DeviceCase
+
+    wl = W.verify_case()
+    dc = DeviceCase(wl, out_dtype=W.BF16)
+    dc.alloc_log()
+    names = ["q", "k", "v", "f", "b", "accepted"] + (["g"] if wl.has_out_gate else [])
+
+    def call():
+        rc = dc.verify(stream=stream)
+        return rc if rc != 0 else dc.commit(stream=stream)
+
+    ms, h2d, d2h = e2e_leg(kda, dc, names, call, lambda: dc.out[:wl.N * wl.W], reps, stream)
+    acc = int(wl.arrays["accepted"].sum())
+    return {"value": wl.N * wl.W / (ms * 1e-3), "unit": "rows verified/s", "ms": ms,
+            "committed_tokens_per_s": acc / (ms * 1e-3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "window rows and accepted counts host->device, kda_verify_window + kda_commit, "
+                    "window outputs device->host"}
+
+
 # --------------------------------------------------------- CPU oracle legs
 
 def oracle_decode_rate(seconds=10.0):
@@ -410,6 +510,78 @@ def oracle_decode_rate(seconds=10.0):
         if el >= seconds:
             break
     return wl.N * steps / el, cores, steps, el
+
+
+def oracle_units_rate(wl, units, rows, threads):
+    """Row-heads per second of the oracle (as it stands) over the given
+    (sequence, head) units of a workload, each cut to its first `rows` rows
+    (pure data movement), run on `threads` threads."""
+    import oracle
+    from linear_attention_serving_kda_gb300 import workloads as W
+    from tests.parity import gather_rows
+
+    oracle.build()
+    subs = []
+    for s, h in units:
+        sub = W.head_slice(wl, s, h)
+        if rows is not None and sub.T > rows:
+            sub = gather_rows(sub, [(0, rows)])
+        subs.append(sub)
+    work = sum(sb.T for sb in subs)
+    from concurrent.futures import ThreadPoolExecutor
+
+    t0 = time.perf_counter()
+    if threads <= 1:
+        for sb in subs:
+            oracle.forward(sb, threads=1)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda sb: oracle.forward(sb, threads=1), subs))
+    el = time.perf_counter() - t0
+    return work / el, work, el
+
+
+def oracle_leg_baseline(wl, rows, per_thread_units=1):
+    """The oracle on a bounded sample of a leg's own workload: one
+    (sequence, head) unit per host core (cut to `rows` rows) on all cores,
+    and one unit on one thread.  tokens/s = row-heads/s / H."""
+    cores = os.cpu_count() or 1
+    n = cores * per_thread_units
+    units = [(i % wl.N, (i // wl.N) % wl.H) for i in range(n)]
+    rate_mt, work_mt, el_mt = oracle_units_rate(wl, units, rows, cores)
+    rate_1, work_1, el_1 = oracle_units_rate(wl, units[:1], 2048 if rows is None else min(rows, 2048), 1)
+    return {"value": rate_mt / wl.H, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "value_1thread": rate_1 / wl.H,
+            "sample": f"{len(units)} (sequence, head) units of {wl.name}, "
+                      f"{'whole' if rows is None else f'each its first {rows} rows'} "
+                      f"({work_mt} row-heads in {el_mt:.1f} s on {cores} threads; 1 thread: {work_1} row-heads "
+                      f"in {el_1:.1f} s); tokens/s = row-heads/s / {wl.H} heads"}
+
+
+def oracle_verify_baseline(seconds_hint=None):
+    """The oracle on the verify workload: the window rows of every (sequence,
+    head) unit (the verify step) on all cores, and on one thread over the
+    first unit's window repeated."""
+    import oracle
+    from linear_attention_serving_kda_gb300 import workloads as W
+
+    oracle.build()
+    wl = W.verify_case()
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.forward(wl, threads=cores)
+    el = time.perf_counter() - t0
+    rows = wl.N * wl.W
+    sub = W.head_slice(wl, 0, 0)
+    t1 = time.perf_counter()
+    reps = 8
+    for _ in range(reps):
+        oracle.forward(sub, threads=1)
+    el1 = time.perf_counter() - t1
+    return {"value": rows / el, "unit": "rows verified/s", "cores": cores, "kind": "oracle",
+            "value_1thread": reps * wl.W / el1 / wl.H,
+            "sample": f"the whole verify window ({wl.N} x {wl.W} rows x {wl.H} heads) in {el:.2f} s on {cores} "
+                      f"threads; 1 thread: one (sequence, head) window x {reps} in {el1:.2f} s, scaled by 1/{wl.H}"}
 
 
 def measured_traffic():
@@ -504,6 +676,9 @@ def main():
         legs["verify_commit"] = leg_verify(kda, 10, stream)
         for k in ("prefill_varlen", "prefill_long"):
             legs[k]["hbm_frac"] = legs[k]["achieved_gbs"] / hbm_gbs
+        legs["prefill_varlen"]["e2e"] = e2e_prefill(kda, W.varlen_prefill_case, 3, stream)
+        legs["prefill_long"]["e2e"] = e2e_prefill(kda, W.long_prefill_case, 3, stream)
+        legs["verify_commit"]["e2e"] = e2e_verify(kda, 10, stream)
     e2e = e2e_decode(kda, args.steps, args.warmup, stream)
     e2e["value"] *= world
     clocks = sampler.stop() if sampler else None
@@ -513,6 +688,13 @@ def main():
         rate, cores, n, el = oracle_decode_rate(args.cpu_seconds)
         cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"full decode step (64 seq x 32 heads) repeated {n}x with carried state, {el:.1f} s"}
+
+    if rank == 0 and world == 1 and legs and args.cpu_seconds > 0:
+        from linear_attention_serving_kda_gb300 import workloads as W
+
+        legs["prefill_varlen"]["cpu_baseline"] = oracle_leg_baseline(cached(W.varlen_prefill_case), None, 2)
+        legs["prefill_long"]["cpu_baseline"] = oracle_leg_baseline(cached(W.long_prefill_case), 8192, 2)
+        legs["verify_commit"]["cpu_baseline"] = oracle_verify_baseline()
 
     traffic = measured_traffic()
 

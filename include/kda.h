@@ -149,7 +149,9 @@ KDA_API size_t kda_prefill_workspace_bytes(const kda_params* p, int32_t N, int32
  *   - Returns KDA_ERR_WORKSPACE, before any launch, when N needs more scratch
  *     than the array holds.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     (cudaGetSymbolAddress), and so does the first call after the device's
+ *     context changed (cudaDeviceReset, a new primary context); make those
+ *     calls before any stream capture.
  *   - All calls share the array.  Calls whose kernels could run at the same
  *     time on one GPU (unordered streams) race on it: order them.
  */

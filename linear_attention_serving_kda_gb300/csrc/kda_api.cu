@@ -53,20 +53,22 @@ int check_ptrs(std::initializer_list<const void*> ps)
 
 int check_opt(const void* x) { return (x && !aligned16(x)) ? KDA_ERR_INVALID_ARGUMENT : KDA_OK; }
 
-// The library is built for sm_103a only; remember the answer per device.
+// The library is built for sm_103a only; remember the answer per device
+// (the set-up object records only a successful check; -1 marks another GPU).
 int check_device()
 {
-    static signed char ok[128];  // 0 unknown, 1 yes, -1 no
+    static PerDeviceOnce once;
+    static std::atomic<signed char> ok[kMaxDevices];  // 0 unknown, 1 yes, -1 no
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return KDA_ERR_DEVICE;
-    if (ok[dev] == 0) {
+    cudaError_t e = once.run([&](int d) {
         int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-            return KDA_ERR_DEVICE;
-        ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
-    }
-    return ok[dev] == 1 ? KDA_OK : KDA_ERR_DEVICE;
+        cudaError_t r = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d);
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d);
+        if (r == cudaSuccess) ok[d].store((major == 10 && minor == 3) ? 1 : -1, std::memory_order_relaxed);
+        return r;
+    });
+    if (e != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_DEVICE;
+    return ok[dev].load(std::memory_order_relaxed) == 1 ? KDA_OK : KDA_ERR_DEVICE;
 }
 
 void fill_common(RecArgs& a, const kda_params* p)

@@ -1865,18 +1865,18 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
     if (!io_bf16) return cudaErrorNotSupported;
     // per-row log decays bounded by -5 (safe gate, lb >= -5): fixed 64-row chunks
     const bool unb = !(a.gate_mode == KDA_GATE_SAFE && a.lb >= -5.0f);
-    static bool attr_done[128];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 128 && !attr_done[dev]) {
+    static PerDeviceOnce attr;
+    cudaError_t ae = attr.run([](int) {
         cudaError_t e = cudaFuncSetAttribute(chk::kda_chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              chk::SMEM_BYTES);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(chk::kda_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      chk::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
+        return e;
+    });
+    if (ae != cudaSuccess) return ae;
+    int dev = 0;
+    cudaGetDevice(&dev);
     chk::RawMaps maps;
     memset(&maps, 0, sizeof(maps));
     if (a.T > 0) {  // with no rows every unit returns before its first copy
@@ -1886,18 +1886,18 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
     }
     if (a.split_ws) {
         // split path: one cooperative grid of one CTA per SM, chains first
-        static bool split_attr[128];
+        static PerDeviceOnce split_attr;
         int sms = 0, per_sm = 0;
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (dev >= 0 && dev < 128 && !split_attr[dev]) {
+        cudaError_t se = split_attr.run([](int) {
             cudaError_t e = cudaFuncSetAttribute(chk::kda_chunk_split_kernel<false>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, chk::SMEM_BYTES);
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(chk::kda_chunk_split_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, chk::SMEM_BYTES);
-            if (e != cudaSuccess) return e;
-            split_attr[dev] = true;
-        }
+            return e;
+        });
+        if (se != cudaSuccess) return se;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chk::kda_chunk_split_kernel<false>, chk::NT,
                                                       chk::SMEM_BYTES);
         const int nc = a.N * a.H;

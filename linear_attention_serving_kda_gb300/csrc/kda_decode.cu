@@ -211,15 +211,12 @@ static_assert(sizeof(DecSmem<float>) <= 232448, "decode stage buffers exceed sha
 
 template <typename IO> static cudaError_t launch_decode_stream(const RecArgs& a, int units, cudaStream_t st)
 {
-    static bool attr_done[128];
-    int dev = 0;
-    cudaGetDevice(&dev);
+    static PerDeviceOnce smem_attr;
     const int smem = (int)sizeof(DecSmem<IO>);
-    if (dev >= 0 && dev < 128 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kda_decode_stream_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
+    cudaError_t e = smem_attr.run([&](int) {
+        return cudaFuncSetAttribute(kda_decode_stream_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
+    if (e != cudaSuccess) return e;
     // Streaming CTAs: about 27/32 of the SMs (128 of the 152 on GB300).  Measured:
     // more concurrent state streams lower the total HBM rate (B = 256 decode:
     // 6.24 TB/s with 128 CTAs, 5.86 TB/s with 152), while below ~112 CTAs the

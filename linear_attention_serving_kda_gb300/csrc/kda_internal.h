@@ -4,9 +4,35 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/kda.h"
 
 namespace kda {
+
+// One-time host set-up per device (kernel attributes, capability checks) that
+// several host threads may reach at once.  fn(dev) runs with the device
+// current, under this object's mutex, until it has succeeded once on that
+// device; afterwards callers only read an atomic flag.
+constexpr int kMaxDevices = 128;
+struct PerDeviceOnce {
+    std::atomic<bool> done[kMaxDevices] = {};
+    std::mutex m;
+    template <class F> cudaError_t run(F&& fn)
+    {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+        if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+        std::lock_guard<std::mutex> lock(m);
+        if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+        e = fn(dev);
+        if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+        return e;
+    }
+};
 
 // REC_COMMIT_VERIFY: replay the accepted rows of the previous window's log,
 // store the committed states, then verify the new window on them.

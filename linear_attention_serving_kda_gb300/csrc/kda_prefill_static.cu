@@ -13,6 +13,9 @@
 // so nothing has to be cleared between calls.  Two calls whose kernels run at
 // the same time on one GPU (different streams, no ordering between them)
 // would race on the array and must not be issued.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "kda_internal.h"
@@ -28,21 +31,55 @@ constexpr size_t kStaticWorkspaceBytes = 256 * 1024;
 // the device address that cudaGetSymbolAddress returns for it.
 static __device__ __align__(256) unsigned char g_prefill_scratch[kStaticWorkspaceBytes];
 
-std::mutex g_setup_mutex;
-void* g_scratch_addr[128];  // per device ordinal, filled on first use
+// The unique ID of the calling thread's current CUDA context (0: none, or the
+// driver entry points are unavailable).  IDs are never reused, so a context
+// destroyed and created again (after cudaDeviceReset, say) has a new one.
+unsigned long long current_context_id()
+{
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr && get_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
+}
 
-// Device address of the scratch on the current device (set up once per device).
+struct ScratchEntry {
+    unsigned long long ctx_id;  // context the address was looked up in
+    void* ptr;
+};
+std::mutex g_setup_mutex;
+ScratchEntry g_scratch[kda::kMaxDevices];  // per device ordinal
+
+// Device address of the scratch on the current device.  Looked up on the first
+// call in a context and again whenever the context has changed (a device
+// reset reloads the library's device code, which may move the array).
 int scratch_address(void** out)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return KDA_ERR_DEVICE;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kda::kMaxDevices) return KDA_ERR_DEVICE;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
+    ScratchEntry& e = g_scratch[dev];
+    const unsigned long long id = current_context_id();
+    if (e.ptr == nullptr || id == 0 || id != e.ctx_id) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_prefill_scratch) != cudaSuccess || ptr == nullptr) return KDA_ERR_DEVICE;
-        g_scratch_addr[dev] = ptr;
+        e.ptr = ptr;
+        e.ctx_id = current_context_id();  // the lookup made the primary context current if none was
     }
-    *out = g_scratch_addr[dev];
+    *out = e.ptr;
     return KDA_OK;
 }
 

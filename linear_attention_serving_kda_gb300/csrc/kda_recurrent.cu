@@ -907,16 +907,12 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) kda_commit_stream_kernel(const
 // The window modes stage rows in dynamic shared memory (VerSmem).
 template <int D, typename IO, int MODE> static cudaError_t launch_window(const RecArgs& a, int units, cudaStream_t st)
 {
-    static bool attr_done[128];
-    int dev = 0;
-    cudaGetDevice(&dev);
+    static PerDeviceOnce smem_attr;
     const int smem = (int)sizeof(VerSmem<D, IO>);
-    if (dev >= 0 && dev < 128 && !attr_done[dev]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kda_recurrent_kernel<D, IO, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
+    cudaError_t e = smem_attr.run([&](int) {
+        return cudaFuncSetAttribute(kda_recurrent_kernel<D, IO, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
+    if (e != cudaSuccess) return e;
     kda_recurrent_kernel<D, IO, MODE><<<dim3(units), dim3(REC_THREADS), smem, st>>>(a);
     return cudaGetLastError();
 }
@@ -924,16 +920,12 @@ template <int D, typename IO, int MODE> static cudaError_t launch_window(const R
 // Verify windows at dk = dv = 128: the warp-local kernel (dynamic shared memory VwSmem).
 template <typename IO, int MODE> static cudaError_t launch_verify_warp(const RecArgs& a, int units, cudaStream_t st)
 {
-    static bool attr_done[128];
-    int dev = 0;
-    cudaGetDevice(&dev);
+    static PerDeviceOnce smem_attr;
     const int smem = (int)sizeof(VwSmem<IO>);
-    if (dev >= 0 && dev < 128 && !attr_done[dev]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kda_verify_warp_kernel<IO, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
+    cudaError_t e = smem_attr.run([&](int) {
+        return cudaFuncSetAttribute(kda_verify_warp_kernel<IO, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
+    if (e != cudaSuccess) return e;
     kda_verify_warp_kernel<IO, MODE><<<dim3(units), dim3(REC_THREADS), smem, st>>>(a);
     return cudaGetLastError();
 }
@@ -973,15 +965,12 @@ static_assert(sizeof(CmtSmem<float>) <= 232448, "commit stage buffers exceed sha
 
 template <typename IO> static cudaError_t launch_commit_stream(const CommitArgs& a, int units, cudaStream_t st)
 {
-    static bool attr_done[128];
-    int dev = 0;
-    cudaGetDevice(&dev);
+    static PerDeviceOnce smem_attr;
     const int smem = (int)sizeof(CmtSmem<IO>);
-    if (dev >= 0 && dev < 128 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kda_commit_stream_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
+    cudaError_t e = smem_attr.run([&](int) {
+        return cudaFuncSetAttribute(kda_commit_stream_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
+    if (e != cudaSuccess) return e;
     // as many streaming CTAs as the decode kernel (27/32 of the SMs)
     const int cap = sm_count() * 27 / 32 > 0 ? sm_count() * 27 / 32 : 1;
     cudaLaunchConfig_t cfg = {};

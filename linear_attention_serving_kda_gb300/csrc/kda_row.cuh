@@ -319,18 +319,20 @@ template <int D> __device__ __forceinline__ float row_update(const RowSmem<D>& s
 constexpr int DEC_D = 128;
 constexpr int DEC_THREADS = REC_THREADS + 32;
 
+// SM count of the current device, remembered per device (an atomic: several
+// host threads may ask at once; each stores the same value)
 static inline int sm_count()
 {
-    static int n[128];
+    static std::atomic<int> n[kMaxDevices];
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 128) return 148;
-    if (n[dev] == 0) {
-        int c = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    int c = n[dev].load(std::memory_order_relaxed);
+    if (c == 0) {
         cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
-        n[dev] = c > 0 ? c : 148;
+        c = c > 0 ? c : 148;
+        n[dev].store(c, std::memory_order_relaxed);
     }
-    return n[dev];
+    return c;
 }
 
 }  // namespace kda

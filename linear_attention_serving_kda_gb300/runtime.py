@@ -3,13 +3,48 @@
 A thin convenience over the binding: torch allocates device memory, the
 binding passes pointers to the CUDA library.  Used by the tests, the
 benchmark and the smoke check.
+
+Every buffer the library writes (outputs, conv and recurrent states, the
+verify log, the prefill workspace) sits inside a larger allocation between
+two guard regions of GUARD_BYTES filled with the byte SENTINEL; a write past
+either end shows up as a changed guard byte (``DeviceCase.guards_intact``).
 """
 from __future__ import annotations
+
+import weakref
 
 import torch
 
 from . import kda as K
 from . import workloads as W
+
+
+GUARD_BYTES = 4096
+SENTINEL = 0xA5
+
+# every live DeviceCase, so a test harness can check all guards after a test
+LIVE = weakref.WeakSet()
+
+
+class Guarded:
+    """A device tensor of `shape` and `dtype` with GUARD_BYTES of SENTINEL
+    bytes before and after it (the tensor starts 4 KiB into the allocation,
+    so it keeps the allocation's alignment)."""
+
+    def __init__(self, shape, dtype, device):
+        n = 1
+        for x in shape:
+            n *= int(x)
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        self.nbytes = nbytes
+        self.raw = torch.full((2 * GUARD_BYTES + (nbytes + 15) // 16 * 16,), SENTINEL, dtype=torch.uint8,
+                              device=device)
+        self.tensor = self.raw[GUARD_BYTES:GUARD_BYTES + nbytes].view(dtype).view(tuple(shape))
+
+    def intact(self) -> bool:
+        head = self.raw[:GUARD_BYTES]
+        tail = self.raw[GUARD_BYTES + self.nbytes:]
+        return bool((head == SENTINEL).all().item()) and bool((tail == SENTINEL).all().item())
 
 
 def io_code(dtype: str) -> int:
@@ -51,9 +86,22 @@ class DeviceCase:
         self.cu_seqlens = torch.from_numpy(wl.cu_seqlens).to(self.device)
         self.accepted = t("accepted") if "accepted" in wl.arrays else None
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self._guards = []
+        self.conv_state = self._guarded(self.conv_state0.shape, self.conv_state0.dtype)
+        self.rec_state = self._guarded(self.rec_state0.shape, self.rec_state0.dtype)
         self.reset_states()
         odt = torch.bfloat16 if out_dtype == W.BF16 else torch.float32
-        self.out = torch.empty((max(wl.T, 1), wl.H, wl.dv), dtype=odt, device=self.device)
+        self.out = self._guarded((max(wl.T, 1), wl.H, wl.dv), odt)
+        LIVE.add(self)
+
+    def _guarded(self, shape, dtype):
+        g = Guarded(shape, dtype, self.device)
+        self._guards.append(g)
+        return g.tensor
+
+    def guards_intact(self) -> bool:
+        """True when no guard byte around any library-written buffer changed."""
+        return all(g.intact() for g in self._guards)
 
     def params(self) -> K.Params:
         wl = self.wl
@@ -65,8 +113,8 @@ class DeviceCase:
                         num_slots=self.num_slots)
 
     def reset_states(self):
-        self.conv_state = self.conv_state0.clone()
-        self.rec_state = self.rec_state0.clone()
+        self.conv_state.copy_(self.conv_state0)
+        self.rec_state.copy_(self.rec_state0)
 
     # -------------------------------------------------------- entry points
     def prefill(self, stream=None) -> int:
@@ -74,7 +122,7 @@ class DeviceCase:
         p = self.params()
         need = K.kda_prefill_workspace_bytes(p, wl.N, wl.T)
         if need and (getattr(self, "workspace", None) is None or self.workspace.numel() < need):
-            self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+            self.workspace = self._guarded((need,), torch.uint8)
         ws = self.workspace if need else None
         return K.kda_prefill_varlen(p, self.cu_seqlens, wl.N, wl.T, self.q, self.k, self.v, self.f,
                                     self.b, self.g, self.slots, self.conv_state, self.rec_state,
@@ -88,7 +136,7 @@ class DeviceCase:
         q, k, v, f, b = self.q[sl], self.k[sl], self.v[sl], self.f[sl], self.b[sl]
         g = None if self.g is None else self.g[sl]
         B = q.shape[0]
-        out = self.out[:B] if rows is None else torch.empty_like(self.out[:B])
+        out = self.out[:B] if rows is None else self._guarded(self.out[:B].shape, self.out.dtype)
         rc = K.kda_decode(self.params(), B, q.contiguous(), k.contiguous(), v.contiguous(), f.contiguous(),
                           b.contiguous(), None if g is None else g.contiguous(), self.slots,
                           self.conv_state, self.rec_state, out, self.dev_status, stream)
@@ -98,7 +146,7 @@ class DeviceCase:
     def alloc_log(self):
         wl = self.wl
         n = K.kda_verify_log_bytes(self.params(), wl.N, wl.W)
-        self.log = torch.empty(max(n, 16), dtype=torch.uint8, device=self.device)
+        self.log = self._guarded((max(n, 16),), torch.uint8)
         return self.log
 
     def verify(self, stream=None) -> int:

@@ -34,6 +34,25 @@ def cuda_lib():
     return kda
 
 
+@pytest.fixture(autouse=True)
+def _guard_regions(request):
+    """After every GPU test: no guard region around a buffer the library
+    wrote (outputs, states, verify logs, workspaces of every DeviceCase the
+    test made) has changed -- the out-of-bounds check that stands in for a
+    memory sanitizer."""
+    yield
+    if request.node.get_closest_marker("gpu") is None:
+        return
+    import torch
+
+    from linear_attention_serving_kda_gb300 import runtime
+
+    torch.cuda.synchronize()
+    bad = [dc.wl.name for dc in list(runtime.LIVE) if not dc.guards_intact()]
+    runtime.LIVE.clear()
+    assert not bad, f"guard bytes changed around a library buffer of: {bad}"
+
+
 def pytest_terminal_summary(terminalreporter):
     try:
         from tests.parity import RECORD

@@ -147,3 +147,59 @@ def test_status_strings(lib):
     for rc in range(7):
         assert kda.status_string(rc).startswith("KDA_")
     assert kda.status_string(99) == "KDA_ERR_UNKNOWN"
+
+
+def test_guard_regions_catch_writes_past_either_end():
+    """The guard regions the GPU tests put around every library-written
+    buffer: untouched after in-bounds writes, changed by a write one byte
+    before the buffer or one element past its end (checked here on host
+    memory; the GPU tests use the same class on device memory)."""
+    import torch
+
+    from linear_attention_serving_kda_gb300.runtime import GUARD_BYTES, Guarded
+
+    g = Guarded((3, 5), torch.float32, "cpu")
+    g.tensor.fill_(1.0)
+    assert g.intact()
+    g.raw[GUARD_BYTES - 1] = 0
+    assert not g.intact()
+    g = Guarded((7,), torch.bfloat16, "cpu")
+    g.tensor.fill_(2.0)
+    assert g.intact()
+    g.raw[GUARD_BYTES + 14] = 0  # the first byte after the 7 bf16 values
+    assert not g.intact()
+
+
+def test_no_unsynchronised_per_device_statics():
+    """Per-device host set-up (kernel attributes, capability checks, SM
+    counts, the built-in scratch address) is safe to reach from several host
+    threads at once: it goes through the PerDeviceOnce helper, atomics or a
+    mutex, never a plain static array."""
+    import glob
+    import re
+
+    csrc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "linear_attention_serving_kda_gb300", "csrc")
+    plain = re.compile(r"^\s*static\s+(bool|int|signed char|char|void\*)\s+\w+\[")
+    for path in glob.glob(os.path.join(csrc, "*.c*")) + glob.glob(os.path.join(csrc, "*.h")):
+        with open(path) as fh:
+            for i, line in enumerate(fh, 1):
+                assert not plain.match(line), f"{os.path.basename(path)}:{i}: plain per-device static: {line.strip()}"
+
+
+def test_size_queries_from_many_threads(lib):
+    """Size queries and status names called from several host threads at once
+    give the answers of one thread."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    p = _params()
+
+    def q(_):
+        return (kda.kda_prefill_workspace_bytes(p, 8, 32768), kda.kda_prefill_workspace_bytes(p, 1, 32768),
+                kda.kda_verify_log_bytes(p, 32, 8), lib.kda_status_string(3))
+
+    want = q(None)
+    assert want[0] > 0 and want[1] > 0
+    with ThreadPoolExecutor(max_workers=16) as ex:
+        got = list(ex.map(q, range(256)))
+    assert all(g == want for g in got)

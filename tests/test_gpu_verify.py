@@ -64,7 +64,8 @@ def test_verify_commit_full_size(cuda_lib, oracle_mod):
     """32 sequences x 8 draft rows, H=32, dk=dv=128, bf16, accepted ~U{0..8}."""
     wl = W.verify_case()
     acc = wl.arrays["accepted"]
-    assert (acc == 0).any() or (acc == wl.W).any() or True
+    # the seeded counts reach both edges: a sequence that keeps nothing and one that keeps the whole window
+    assert acc.min() == 0 and acc.max() == wl.W and np.all((acc >= 0) & (acc <= wl.W))
     _check_window(cuda_lib, oracle_mod, wl)
 
 
