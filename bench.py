@@ -3,6 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload decode|verify|prefill_varlen|prefill_long|...] [--no-legs]
 
+With --gpus N > 1 outside torchrun the script relaunches itself under
+torch.distributed.run with N processes (one per GPU).
+
 One step is one pass of the layer's hot path over one batch of seeded
 synthetic input.  The headline workload is the decode step (64 sequences x
 1 row, 32 heads, dk = dv = 128, bf16 rows, fp32 state, softplus gate, gated
@@ -574,7 +577,7 @@ def oracle_verify_baseline(seconds_hint=None):
     rows = wl.N * wl.W
     sub = W.head_slice(wl, 0, 0)
     t1 = time.perf_counter()
-    reps = 8
+    reps = 64
     for _ in range(reps):
         oracle.forward(sub, threads=1)
     el1 = time.perf_counter() - t1
@@ -620,9 +623,22 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU: run this same command under torchrun
+        import socket
+
+        with socket.socket() as so:
+            so.bind(("127.0.0.1", 0))
+            port = so.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+        sys.exit(subprocess.call(cmd))
+
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus and rank == 0:
+        print(f"bench.py: --gpus {args.gpus} but {world} ranks were launched; measuring {world}", file=sys.stderr)
 
     if args.impl == "reference":
         if rank != 0:

@@ -165,6 +165,26 @@ KDA_API int kda_prefill_varlen_static_ws(const kda_params* p, const int32_t* cu_
 KDA_API size_t kda_prefill_static_workspace_capacity(void);
 
 /*
+ * Test hook for the bounded on-chip waits (no counterpart on the source
+ * pages).  Same arguments as kda_prefill_varlen for a long-prompt shape that
+ * takes the split (producer / chain) path -- bf16 rows, dk = dv = 128, the safe
+ * gate with lb >= -5, N * H <= 64, T >= 1024 -- plus a poll limit.  Launches
+ * only the chain CTAs, without the producers that publish their operands, and
+ * limits every flag wait to `poll_limit` polls (about a microsecond each):
+ * each chain's first wait runs out, the chain sets KDA_DEV_TIMEOUT in
+ * *dev_status and returns with nothing in flight, leaving the states and the
+ * context as they were.  Returns KDA_ERR_INVALID_ARGUMENT for any other shape
+ * or a zero limit.  The failure is made on the host (the producers are not
+ * launched); nothing faults or traps.
+ */
+KDA_API int kda_debug_split_chains_only(const kda_params* p, const int32_t* cu_seqlens, int32_t N, int32_t T,
+                                        const void* q, const void* k, const void* v, const void* gate,
+                                        const void* beta, const void* out_gate, const int32_t* slots,
+                                        void* conv_state, float* rec_state, void* out, void* workspace,
+                                        size_t ws_bytes, int32_t* dev_status, uint32_t poll_limit,
+                                        cudaStream_t stream);
+
+/*
  * Decode: one row per sequence, B sequences (row b belongs to sequence b).
  * Updates the conv and recurrent states in place and writes out [B][H][dv]
  * (TensorFold #850, Oct 15 comment: decode rows).

@@ -159,7 +159,7 @@ int kda::prefill_varlen_impl(const kda_params* p, const int32_t* cu_seqlens, int
                              const void* q, const void* k, const void* v, const void* gate, const void* beta,
                              const void* out_gate, const int32_t* slots, void* conv_state, float* rec_state,
                              void* out, void* workspace, size_t ws_bytes, int32_t* dev_status,
-                             cudaStream_t stream, bool allow_split)
+                             cudaStream_t stream, bool allow_split, uint32_t dbg_chains_only_polls)
 {
     int rc = check_params(p);
     if (rc != KDA_OK) return rc;
@@ -200,6 +200,7 @@ int kda::prefill_varlen_impl(const kda_params* p, const int32_t* cu_seqlens, int
         c.schedule = static_cast<int32_t*>(workspace);
         if (allow_split && chunk_split_wanted(p, N, T))
             c.split_ws = static_cast<unsigned char*>(workspace) + align1024(align256((size_t)(N + 1) * sizeof(int32_t)));
+        c.dbg_chains_only_polls = dbg_chains_only_polls;
         return launch_chunk(p->io_dtype == KDA_DTYPE_BF16, c, stream) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
     }
     RecArgs a;
@@ -229,6 +230,19 @@ KDA_API int kda_prefill_varlen(const kda_params* p, const int32_t* cu_seqlens, i
 {
     return prefill_varlen_impl(p, cu_seqlens, N, T, q, k, v, gate, beta, out_gate, slots, conv_state, rec_state,
                                out, workspace, ws_bytes, dev_status, stream, true);
+}
+
+KDA_API int kda_debug_split_chains_only(const kda_params* p, const int32_t* cu_seqlens, int32_t N, int32_t T,
+                                        const void* q, const void* k, const void* v, const void* gate,
+                                        const void* beta, const void* out_gate, const int32_t* slots,
+                                        void* conv_state, float* rec_state, void* out, void* workspace,
+                                        size_t ws_bytes, int32_t* dev_status, uint32_t poll_limit,
+                                        cudaStream_t stream)
+{
+    if (!chunk_supported(p) || !chunk_split_wanted(p, N, T) || poll_limit == 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!(p->gate_mode == KDA_GATE_SAFE && p->gate_lower_bound >= -5.0f)) return KDA_ERR_INVALID_ARGUMENT;
+    return prefill_varlen_impl(p, cu_seqlens, N, T, q, k, v, gate, beta, out_gate, slots, conv_state, rec_state,
+                               out, workspace, ws_bytes, dev_status, stream, true, poll_limit);
 }
 
 KDA_API int kda_decode(const kda_params* p, int32_t B, const void* q, const void* k,

@@ -1356,6 +1356,7 @@ struct SplitArgs {
     // fixed 64-row chunks
     const int* bnd;
     int bs;
+    uint32_t flag_polls;   // limit of every flag wait (polls with back-off)
 };
 
 // chain u's number of chunks, and chunk c's first row and row count (UNB:
@@ -1432,7 +1433,7 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
         }
         if (tid == 0) {
             // the slot is free once the chain has read chunk c - SPLIT_RING
-            if (c >= SPLIT_RING && !ptx::wait_flag_ge(&sp.consumed[u], c - SPLIT_RING + 1)) {
+            if (c >= SPLIT_RING && !ptx::wait_flag_ge(&sp.consumed[u], c - SPLIT_RING + 1, sp.flag_polls)) {
                 ms.err = 1;
                 flag_status(a.dev_status, KDA_DEV_TIMEOUT);
             } else {
@@ -1518,7 +1519,7 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
     // after that acquire.  Thread 128 issues no products, so it can wait while
     // the issuers are busy.
     auto acquire_by = [&](int c, int who) {
-        if (tid == who && !ptx::wait_flag_ge(&sp.ready[u * SPLIT_RING + c % SPLIT_RING], c + 1)) {
+        if (tid == who && !ptx::wait_flag_ge(&sp.ready[u * SPLIT_RING + c % SPLIT_RING], c + 1, sp.flag_polls)) {
             ms.err = 1;
             flag_status(a.dev_status, KDA_DEV_TIMEOUT);
         }
@@ -1912,6 +1913,7 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
             int* bnd = unb ? reinterpret_cast<int*>(a.split_ws + chunk_split_bytes(a.N, a.H)) : nullptr;
             sp.bnd = bnd;
             sp.bs = a.T + 3;
+            sp.flag_polls = a.dbg_chains_only_polls ? a.dbg_chains_only_polls : (1u << 25);
             cudaError_t e = cudaMemsetAsync(a.split_ws, 0, flags, st);
             if (e != cudaSuccess) return e;
             if (unb) {
@@ -1925,7 +1927,9 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
             ChunkArgs aa = a;
             void* args[] = {&aa, &maps, &sp};
             const void* fn = unb ? (const void*)chk::kda_chunk_split_kernel<true> : (const void*)chk::kda_chunk_split_kernel<false>;
-            return cudaLaunchCooperativeKernel(fn, dim3(sms), dim3(chk::NT), args, chk::SMEM_BYTES, st);
+            // test hook: the chains alone, so that their first flag wait runs out
+            const int grid = a.dbg_chains_only_polls ? nc : sms;
+            return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(chk::NT), args, chk::SMEM_BYTES, st);
         }
         // too few SMs for producers beside the chains: the fused kernel below
     }

@@ -100,6 +100,10 @@ struct ChunkArgs {
     int32_t* dev_status;
     int32_t* schedule;  // workspace: sequence order, longest first
     unsigned char* split_ws;  // workspace of the split (producer / chain) path, or null: fused kernel
+    // Test hook (kda_debug_split_chains_only): launch the split path's chain
+    // CTAs without producers, their flag waits limited to this many polls
+    // (0: the normal grid and limit).
+    uint32_t dbg_chains_only_polls;
 };
 
 cudaError_t launch_recurrent(int mode, int io_bf16, const RecArgs& a, int units, cudaStream_t st);
@@ -119,7 +123,8 @@ size_t chunk_split_bytes(int N, int H);  // flags + ring, 1 KiB aligned parts
 int prefill_varlen_impl(const kda_params* p, const int32_t* cu_seqlens, int32_t N, int32_t T, const void* q,
                         const void* k, const void* v, const void* gate, const void* beta, const void* out_gate,
                         const int32_t* slots, void* conv_state, float* rec_state, void* out, void* workspace,
-                        size_t ws_bytes, int32_t* dev_status, cudaStream_t stream, bool allow_split);
+                        size_t ws_bytes, int32_t* dev_status, cudaStream_t stream, bool allow_split,
+                        uint32_t dbg_chains_only_polls = 0);
 size_t prefill_workspace_bytes(const kda_params* p, int32_t N, int32_t T, bool allow_split);
 cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st);
 

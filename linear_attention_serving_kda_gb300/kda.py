@@ -54,6 +54,9 @@ _SIG = {
     "kda_prefill_varlen_static_ws": (ctypes.c_int, [ctypes.POINTER(kda_params), _VP, _I32, _I32, _VP, _VP, _VP,
                                                     _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "kda_prefill_static_workspace_capacity": (ctypes.c_size_t, []),
+    "kda_debug_split_chains_only": (ctypes.c_int, [ctypes.POINTER(kda_params), _VP, _I32, _I32, _VP, _VP, _VP,
+                                                   _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t,
+                                                   _VP, ctypes.c_uint32, _VP]),
     "kda_decode": (ctypes.c_int, [ctypes.POINTER(kda_params), _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   _VP, _VP, _VP, _VP, _VP]),
     "kda_verify_window": (ctypes.c_int, [ctypes.POINTER(kda_params), _I32, _I32, _VP, _VP, _VP, _VP, _VP,
@@ -177,6 +180,17 @@ def kda_prefill_varlen_static_ws(params: Params, cu_seqlens, N: int, T: int, q, 
         ctypes.byref(params.c_struct()), _ptr(cu_seqlens), N, T, _ptr(q), _ptr(k), _ptr(v), _ptr(gate),
         _ptr(beta), _ptr(out_gate), _ptr(slots), _ptr(conv_state), _ptr(rec_state), _ptr(out),
         _ptr(dev_status), _stream(stream))
+
+
+def kda_debug_split_chains_only(params: Params, cu_seqlens, N: int, T: int, q, k, v, gate, beta, out_gate,
+                                slots, conv_state, rec_state, out, workspace, ws_bytes: int, dev_status,
+                                poll_limit: int, stream=None) -> int:
+    """Test hook: the split path's chains without producers, flag waits
+    limited to poll_limit polls (they run out and report KDA_DEV_TIMEOUT)."""
+    return load().kda_debug_split_chains_only(
+        ctypes.byref(params.c_struct()), _ptr(cu_seqlens), N, T, _ptr(q), _ptr(k), _ptr(v), _ptr(gate),
+        _ptr(beta), _ptr(out_gate), _ptr(slots), _ptr(conv_state), _ptr(rec_state), _ptr(out),
+        _ptr(workspace), ws_bytes, _ptr(dev_status), poll_limit, _stream(stream))
 
 
 def kda_prefill_static_workspace_capacity() -> int:

@@ -130,3 +130,32 @@ def test_split_unbounded_gates(cuda_lib, oracle_mod, lens, H, gate, lb, alog, og
     assert torch.equal(p.conv_state, f.conv_state)
     units = [(s_, h) for s_ in range(wl.N) if lens[s_] > 0 for h in sorted({0, H - 1})]
     _units_close(oracle_mod, wl, p, units, "split vs oracle")
+
+
+def test_chain_flag_wait_runs_out_and_reports(cuda_lib):
+    """A bounded wait that runs out: the split path's chains launched without
+    the producers that would publish their operands (a host-side fault: the
+    flag is never set), each flag wait limited to 1024 polls.  Every chain
+    gives up, reports KDA_DEV_TIMEOUT and returns with nothing in flight: the
+    states are untouched and the same context then runs the normal call with
+    the fused kernel's bits."""
+    wl = W.make_workload("tmo", 818, [2048], H=4, d=128, K=4, io_dtype=W.BF16, gate_mode=W.SAFE,
+                         lower_bound=-5.0, out_gate=True, init_state="random")
+    dc = DeviceCase(wl, out_dtype=W.BF16)
+    p = dc.params()
+    need = K.kda_prefill_workspace_bytes(p, wl.N, wl.T)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    rs0, cs0 = dc.rec_state.clone(), dc.conv_state.clone()
+    rc = K.kda_debug_split_chains_only(p, dc.cu_seqlens, wl.N, wl.T, dc.q, dc.k, dc.v, dc.f, dc.b, dc.g, None,
+                                       dc.conv_state, dc.rec_state, dc.out, ws, need, dc.dev_status, 1024)
+    assert rc == K.KDA_OK
+    torch.cuda.synchronize()
+    assert int(dc.dev_status.item()) & K.KDA_DEV_TIMEOUT
+    assert torch.equal(dc.rec_state, rs0) and torch.equal(dc.conv_state, cs0)
+    # other shapes are refused before any launch
+    assert K.kda_debug_split_chains_only(p, dc.cu_seqlens, wl.N, wl.T, dc.q, dc.k, dc.v, dc.f, dc.b, dc.g, None,
+                                         dc.conv_state, dc.rec_state, dc.out, ws, need, dc.dev_status,
+                                         0) == K.KDA_ERR_INVALID_ARGUMENT
+    # the context is still usable: the normal call gives the fused kernel's bits
+    pp, ff = _both(wl)
+    assert torch.equal(pp.out[:wl.T], ff.out[:wl.T]) and torch.equal(pp.rec_state, ff.rec_state)

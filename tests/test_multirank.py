@@ -1,10 +1,14 @@
-"""The benchmark's multi-rank host logic on CPU: two gloo ranks on 127.0.0.1.
+"""Multi-rank host logic on CPU: two gloo ranks on 127.0.0.1.
 
 Each rank runs its own batch (weak scaling); the only collective is the
 max-over-ranks of the timed region, and the whole-job value counts every
-rank's tokens against that slowest time."""
+rank's tokens against that slowest time.  A varlen batch splits into
+per-rank shards of whole sequences whose results, gathered, are those of one
+unsharded run."""
 import os
 import socket
+
+import numpy as np
 
 import pytest
 import torch.distributed as dist
@@ -52,3 +56,65 @@ def test_single_rank_needs_no_collective():
 
     assert bench.max_over_ranks(3.5, None) == 3.5
     assert bench.weak_scaling_value(64, 1, 10, 2.0) == pytest.approx(64 * 10 / 2e-3)
+
+
+def test_partition_balances_rows_and_covers_every_sequence():
+    from linear_attention_serving_kda_gb300 import shard
+
+    lens = np.array([6945, 2521, 1351, 2804, 3690, 6766, 3978, 1218, 0, 5])
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    for world in (1, 2, 3, 4, 8, 16):
+        parts = shard.partition_sequences(cu, world)
+        assert len(parts) == world
+        flat = sorted(s for p in parts for s in p)
+        assert flat == list(range(len(lens)))          # every sequence exactly once
+        loads = [int(lens[p].sum()) if p else 0 for p in parts]
+        # greedy longest-first: no rank exceeds the best possible by more than the longest sequence
+        assert max(loads) <= max(lens.sum() / world, lens.max()) + lens.max()
+        assert parts == shard.partition_sequences(cu, world)  # deterministic
+    with pytest.raises(ValueError):
+        shard.partition_sequences([0, 5, 3], 2)
+
+
+def _shard_worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import oracle
+    from linear_attention_serving_kda_gb300 import shard, workloads as W
+
+    wl = W.make_workload("dp", 41, [37, 130, 5, 64, 0, 71], H=2, d=32, K=4, io_dtype=W.BF16, gate_mode=W.SAFE,
+                         lower_bound=-5.0, out_gate=True, init_state="random")
+    seqs = shard.partition_sequences(wl.cu_seqlens, world)[rank]
+    mine = oracle.forward(shard.shard_workload(wl, seqs), threads=1)
+    got = [None] * world
+    dist.all_gather_object(got, (seqs, mine))
+    if rank == 0:
+        full = oracle.forward(wl, threads=1)
+        ok = True
+        for sq, res in got:
+            sub_cu = np.concatenate([[0], np.cumsum([wl.cu_seqlens[s + 1] - wl.cu_seqlens[s] for s in sq])]).astype(int)
+            for j, s in enumerate(sq):
+                a0, a1 = wl.cu_seqlens[s], wl.cu_seqlens[s + 1]
+                ok &= np.array_equal(res["out"][sub_cu[j]:sub_cu[j + 1]], full["out"][a0:a1])
+                ok &= np.array_equal(res["rec_state"][j], full["rec_state"][s])
+                ok &= np.array_equal(res["conv_state"][j], full["conv_state"][s])
+        out.put(bool(ok) and sorted(s for sq, _ in got for s in sq) == list(range(wl.N)))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_shard_sequences_bit_for_bit():
+    """Two gloo ranks each run the oracle on their partition of a varlen
+    batch; the gathered outputs and final states equal one unsharded run bit
+    for bit (the units are independent: replicas need no data exchange)."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    ok = q.get(timeout=180)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert ok
