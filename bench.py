@@ -268,6 +268,36 @@ def leg_prefill(kda, wl_fn, reps, stream):
             "tf32_frac": tf / (bf16_tflops / 2.0)}
 
 
+def leg_prefill_scan(kda, wl_fn, segments, reps, stream):
+    """The same prefill through kda_prefill_scan (the affine state scan over
+    `segments` pieces per sequence): time per call and tokens/s."""
+    import torch
+
+    from linear_attention_serving_kda_gb300 import workloads as W
+    from linear_attention_serving_kda_gb300.runtime import DeviceCase
+
+    wl = cached(wl_fn)
+    dc = DeviceCase(wl, out_dtype=W.BF16)
+    p = dc.params()
+    need = kda.kda_prefill_scan_workspace_bytes(p, wl.N, wl.T, segments)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+
+    def call(i):
+        kda.check(kda.kda_prefill_scan(p, dc.cu_seqlens, wl.N, wl.T, dc.q, dc.k, dc.v, dc.f, dc.b, dc.g, None,
+                                       dc.conv_state, dc.rec_state, dc.out, ws, need, segments, dc.dev_status,
+                                       stream))
+
+    call(0)  # warm-up
+    durs = []
+    for _ in range(reps):
+        dc.reset_states()
+        torch.cuda.synchronize()
+        durs += time_steps(call, 1, stream)[0]
+    ms = statistics.median(durs)
+    return {"workload": wl.name, "segments": segments, "tokens": wl.T, "ms": ms,
+            "tokens_per_s": wl.T / (ms * 1e-3), "workspace_bytes": need}
+
+
 def leg_verify(kda, reps, stream):
     import torch
 
@@ -619,7 +649,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "verify", "prefill_varlen", "prefill_long", "prefill_small",
-                             "prefill_varlen_softplus"])
+                             "prefill_varlen_softplus", "prefill_long_scan"])
+    ap.add_argument("--segments", type=int, default=4, help="pieces per sequence for prefill_long_scan")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -690,6 +721,7 @@ def main():
         legs["prefill_varlen"] = leg_prefill(kda, W.varlen_prefill_case, 3, stream)
         legs["prefill_long"] = leg_prefill(kda, W.long_prefill_case, 3, stream)
         legs["verify_commit"] = leg_verify(kda, 10, stream)
+        legs["prefill_long_scan"] = leg_prefill_scan(kda, W.long_prefill_case, 4, 3, stream)
         for k in ("prefill_varlen", "prefill_long"):
             legs[k]["hbm_frac"] = legs[k]["achieved_gbs"] / hbm_gbs
         legs["prefill_varlen"]["e2e"] = e2e_prefill(kda, W.varlen_prefill_case, 3, stream)
@@ -744,6 +776,8 @@ def run_single_leg(kda, args, stream):
 
     if args.workload == "verify":
         return leg_verify(kda, args.steps, stream)
+    if args.workload == "prefill_long_scan":
+        return leg_prefill_scan(kda, W.long_prefill_case, args.segments, args.steps, stream)
     if args.workload == "prefill_small":
         # a profiling-sized prefill: 2 sequences x 2048 rows, 32 heads, same dtypes and gate
         fn = lambda: W.make_workload("prefill_small_n2x2048_h32_d128_bf16", 5, [2048, 2048], H=32, d=128,  # noqa: E731

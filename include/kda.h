@@ -165,6 +165,39 @@ KDA_API int kda_prefill_varlen_static_ws(const kda_params* p, const int32_t* cu_
 KDA_API size_t kda_prefill_static_workspace_capacity(void);
 
 /*
+ * Chunk-parallel prefill by an affine state scan: the context-parallel form
+ * of kda_prefill_varlen (same arguments and results, same supported shape as
+ * its tensor-core path: bf16 rows, dk = dv = 128), for long sequences.  The
+ * delta rule is linear in the state, so over any run of rows
+ *     S_out = M S_in + N   and   o_r = obar_r + psi_r S_in,
+ * with (N, obar) what the rows give from a zero state and (M, psi) what they
+ * give from the identity with zero values.  Each sequence is cut into
+ * `segments` pieces of whole 64-row chunks (TensorFold #850, Oct 15 comment:
+ * chunks from a segment's first row); all pieces run at once (zero-state and
+ * transfer runs, one launch of the chunk kernel); a scan S_{p+1} = M_p S_p +
+ * N_p gives each piece's start state; a fix-up adds psi_r S_p to the outputs
+ * and applies the gated RMSNorm.  On several GPUs each would take its own
+ * pieces and only the states of the scan would travel; here the pieces share
+ * one GPU.
+ *   - Results agree with kda_prefill_varlen and the serial recurrence to
+ *     rounding, not bit for bit (another summation order); prompt-cut bit
+ *     identity does not hold across the two entry points.
+ *   - workspace: kda_prefill_scan_workspace_bytes(p, N, T, segments) bytes,
+ *     16-byte aligned (about 1 KiB per row-head: raw outputs and corrections
+ *     in fp32, plus two states per piece and head).
+ *   - segments in [1, KDA_SCAN_MAX_SEGMENTS]; other shapes of p give
+ *     KDA_ERR_UNSUPPORTED_GEOMETRY, before any launch.
+ */
+#define KDA_SCAN_MAX_SEGMENTS 64
+KDA_API int kda_prefill_scan(const kda_params* p, const int32_t* cu_seqlens, int32_t N, int32_t T, const void* q,
+                             const void* k, const void* v, const void* gate, const void* beta, const void* out_gate,
+                             const int32_t* slots, void* conv_state, float* rec_state, void* out, void* workspace,
+                             size_t ws_bytes, int32_t segments, int32_t* dev_status, cudaStream_t stream);
+
+/* Workspace bytes of kda_prefill_scan (0 for an unsupported shape). */
+KDA_API size_t kda_prefill_scan_workspace_bytes(const kda_params* p, int32_t N, int32_t T, int32_t segments);
+
+/*
  * Test hook for the bounded on-chip waits (no counterpart on the source
  * pages).  Same arguments as kda_prefill_varlen for a long-prompt shape that
  * takes the split (producer / chain) path -- bf16 rows, dk = dv = 128, the safe

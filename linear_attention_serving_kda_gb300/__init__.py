@@ -9,7 +9,8 @@ from .kda import (  # noqa: F401
     KDA_DTYPE_F32, KDA_ERR_DEVICE, KDA_ERR_INVALID_ARGUMENT, KDA_ERR_INVALID_BOUND,
     KDA_ERR_LAUNCH, KDA_ERR_UNSUPPORTED_GEOMETRY, KDA_ERR_WORKSPACE, KDA_GATE_SAFE,
     KDA_GATE_SOFTPLUS, KDA_OK, KdaError, Params, Prepared, check, kda_commit, kda_commit_verify, kda_decode,
-    kda_prefill_static_workspace_capacity, kda_prefill_varlen, kda_prefill_varlen_static_ws,
+    kda_prefill_scan, kda_prefill_scan_workspace_bytes, kda_prefill_static_workspace_capacity,
+    kda_prefill_varlen, kda_prefill_varlen_static_ws,
     kda_prefill_workspace_bytes, kda_verify_log_bytes, kda_verify_window,
     load, status_string,
 )

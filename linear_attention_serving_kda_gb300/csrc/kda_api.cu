@@ -174,6 +174,36 @@ int kda::prefill_varlen_impl(const kda_params* p, const int32_t* cu_seqlens, int
 
     if (chunk_supported(p)) {
         ChunkArgs c;
+        fill_chunk(c, p, cu_seqlens, N, T, q, k, v, gate, beta, out_gate, slots, conv_state, rec_state, out,
+                   dev_status);
+        c.schedule = static_cast<int32_t*>(workspace);
+        if (allow_split && chunk_split_wanted(p, N, T))
+            c.split_ws = static_cast<unsigned char*>(workspace) + align1024(align256((size_t)(N + 1) * sizeof(int32_t)));
+        c.dbg_chains_only_polls = dbg_chains_only_polls;
+        return launch_chunk(p->io_dtype == KDA_DTYPE_BF16, c, stream) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+    }
+    RecArgs a;
+    fill_common(a, p);
+    a.N = N;
+    a.W = 1;
+    a.T = T;
+    a.cu_seqlens = cu_seqlens;
+    a.q = q; a.k = k; a.v = v; a.f = gate; a.b = beta; a.g = out_gate;
+    a.slots = slots;
+    a.conv_state = conv_state;
+    a.rec_state = rec_state;
+    a.out = out;
+    a.dev_status = dev_status;
+    return launch_recurrent(REC_PREFILL, p->io_dtype == KDA_DTYPE_BF16, a, N * p->num_heads, stream) == cudaSuccess
+               ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+void kda::fill_chunk(ChunkArgs& c, const kda_params* p, const int32_t* cu_seqlens, int32_t N, int32_t T,
+                     const void* q, const void* k, const void* v, const void* gate, const void* beta,
+                     const void* out_gate, const int32_t* slots, void* conv_state, float* rec_state, void* out,
+                     int32_t* dev_status)
+{
+    {
         std::memset(&c, 0, sizeof(c));
         c.H = p->num_heads;
         c.K = p->conv_kernel;
@@ -197,26 +227,7 @@ int kda::prefill_varlen_impl(const kda_params* p, const int32_t* cu_seqlens, int
         c.rec_state = rec_state;
         c.out = out;
         c.dev_status = dev_status;
-        c.schedule = static_cast<int32_t*>(workspace);
-        if (allow_split && chunk_split_wanted(p, N, T))
-            c.split_ws = static_cast<unsigned char*>(workspace) + align1024(align256((size_t)(N + 1) * sizeof(int32_t)));
-        c.dbg_chains_only_polls = dbg_chains_only_polls;
-        return launch_chunk(p->io_dtype == KDA_DTYPE_BF16, c, stream) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
     }
-    RecArgs a;
-    fill_common(a, p);
-    a.N = N;
-    a.W = 1;
-    a.T = T;
-    a.cu_seqlens = cu_seqlens;
-    a.q = q; a.k = k; a.v = v; a.f = gate; a.b = beta; a.g = out_gate;
-    a.slots = slots;
-    a.conv_state = conv_state;
-    a.rec_state = rec_state;
-    a.out = out;
-    a.dev_status = dev_status;
-    return launch_recurrent(REC_PREFILL, p->io_dtype == KDA_DTYPE_BF16, a, N * p->num_heads, stream) == cudaSuccess
-               ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
 extern "C" {
@@ -230,6 +241,35 @@ KDA_API int kda_prefill_varlen(const kda_params* p, const int32_t* cu_seqlens, i
 {
     return prefill_varlen_impl(p, cu_seqlens, N, T, q, k, v, gate, beta, out_gate, slots, conv_state, rec_state,
                                out, workspace, ws_bytes, dev_status, stream, true);
+}
+
+KDA_API size_t kda_prefill_scan_workspace_bytes(const kda_params* p, int32_t N, int32_t T, int32_t segments)
+{
+    if (check_params(p) != KDA_OK || N < 0 || T < 0 || segments < 1 || segments > KDA_SCAN_MAX_SEGMENTS) return 0;
+    if (!chunk_supported(p)) return 0;
+    return prefill_scan_workspace_bytes(p, N, T, segments);
+}
+
+KDA_API int kda_prefill_scan(const kda_params* p, const int32_t* cu_seqlens, int32_t N, int32_t T, const void* q,
+                             const void* k, const void* v, const void* gate, const void* beta, const void* out_gate,
+                             const int32_t* slots, void* conv_state, float* rec_state, void* out, void* workspace,
+                             size_t ws_bytes, int32_t segments, int32_t* dev_status, cudaStream_t stream)
+{
+    int rc = check_params(p);
+    if (rc != KDA_OK) return rc;
+    if (N < 0 || T < 0 || segments < 1 || segments > KDA_SCAN_MAX_SEGMENTS) return KDA_ERR_INVALID_ARGUMENT;
+    if (!chunk_supported(p)) return KDA_ERR_UNSUPPORTED_GEOMETRY;
+    if (N == 0) return KDA_OK;
+    if ((rc = check_ptrs({cu_seqlens, conv_state, rec_state})) != KDA_OK) return rc;
+    if (T > 0 && (rc = check_ptrs({q, k, v, gate, beta, out})) != KDA_OK) return rc;
+    if ((rc = check_opt(out_gate)) != KDA_OK || (rc = check_opt(slots)) != KDA_OK) return rc;
+    const size_t need = prefill_scan_workspace_bytes(p, N, T, segments);
+    if (!workspace || ws_bytes < need || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
+    if ((rc = check_device()) != KDA_OK) return rc;
+    ChunkArgs c;
+    fill_chunk(c, p, cu_seqlens, N, T, q, k, v, gate, beta, out_gate, slots, conv_state, rec_state, out, dev_status);
+    return launch_prefill_scan(p, c, segments, static_cast<unsigned char*>(workspace), stream) == cudaSuccess
+               ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
 KDA_API int kda_debug_split_chains_only(const kda_params* p, const int32_t* cu_seqlens, int32_t N, int32_t T,

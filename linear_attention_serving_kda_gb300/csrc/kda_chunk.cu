@@ -214,13 +214,18 @@ __device__ __forceinline__ bool wait_mma(Misc& ms, uint32_t& ph, int32_t* dev_st
     return ms.err == 0;
 }
 
-__global__ void kda_chunk_schedule_kernel(const int32_t* cu, int N, int32_t* order)
+// rows of unit sequence s (a transfer run, s >= nsplit > 0, covers sequence s - nsplit)
+__device__ __forceinline__ int unit_rows_seq(int s, int nsplit) { return (nsplit > 0 && s >= nsplit) ? s - nsplit : s; }
+
+__global__ void kda_chunk_schedule_kernel(const int32_t* cu, int N, int nsplit, int32_t* order)
 {
     for (int s = threadIdx.x; s < N; s += blockDim.x) {
-        const int ls = cu[s + 1] - cu[s];
+        const int rs = unit_rows_seq(s, nsplit);
+        const int ls = cu[rs + 1] - cu[rs];
         int rank = 0;
         for (int t = 0; t < N; ++t) {
-            const int lt = cu[t + 1] - cu[t];
+            const int rt = unit_rows_seq(t, nsplit);
+            const int lt = cu[rt + 1] - cu[rt];
             rank += (lt > ls) || (lt == ls && t < s);
         }
         order[rank] = s;
@@ -561,7 +566,7 @@ __device__ __forceinline__ int chunk_cut(Misc& ms, int nvalid, float (&G)[RPT])
 template <bool UNB, bool CUT = UNB>
 __device__ __forceinline__ int chunk_prep(unsigned char* sm, Misc& ms, const ChunkArgs& a, const ThreadConst& tc,
                                           int nvalid, float (&qv)[RPT], float (&kv)[RPT], float (&vv)[RPT],
-                                          float (&G)[RPT])
+                                          float (&G)[RPT], bool zero_v = false)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int col = tid & (D - 1);
@@ -631,10 +636,10 @@ __device__ __forceinline__ int chunk_prep(unsigned char* sm, Misc& ms, const Chu
             const bool ok0 = lr < nvalid, ok1 = lr + 1 < nvalid;
             qv[r] = ok0 ? sq.x : 0.0f;
             kv[r] = ok0 ? sk.x : 0.0f;
-            vv[r] = ok0 ? sv.x : 0.0f;
+            vv[r] = (ok0 && !zero_v) ? sv.x : 0.0f;  // a transfer run: zero values, so U' = 0
             qv[r + 1] = ok1 ? sq.y : 0.0f;
             kv[r + 1] = ok1 ? sk.y : 0.0f;
-            vv[r + 1] = ok1 ? sv.y : 0.0f;
+            vv[r + 1] = (ok1 && !zero_v) ? sv.y : 0.0f;
             run += ok0 ? la.x : 0.0f;
             G[r] = run;
             run += ok1 ? la.y : 0.0f;
@@ -1061,7 +1066,8 @@ __device__ __forceinline__ void write_outputs_a(Misc& ms, const ChunkArgs& a, ui
 }
 
 __device__ __forceinline__ void write_outputs_b(Misc& ms, const ChunkArgs& a, float (&o)[RPT],
-                                                const uint32_t (&gp)[RPT / 2], int c0, int nvalid, int h, float nw)
+                                                const uint32_t (&gp)[RPT / 2], int c0, int nvalid, int h, float nw,
+                                                void* outp)
 {
     const int tid = threadIdx.x, lane = tid & 31, qq = tid >> 7, col = tid & (D - 1);
     const int r0 = RPT * qq, H = a.H;
@@ -1090,7 +1096,7 @@ __device__ __forceinline__ void write_outputs_b(Misc& ms, const ChunkArgs& a, fl
         // 4-byte (c, c+1) pairs, after one exchange per row
         const bool odd = lane & 1;
         const int cpair = col & ~1;
-        __nv_bfloat162* ou = static_cast<__nv_bfloat162*>(a.out);
+        __nv_bfloat162* ou = static_cast<__nv_bfloat162*>(outp);
 #pragma unroll
         for (int x = 0; x < RPT / 2; ++x) {
             const float send = odd ? o[x] : o[RPT / 2 + x];
@@ -1101,7 +1107,7 @@ __device__ __forceinline__ void write_outputs_b(Misc& ms, const ChunkArgs& a, fl
         }
     } else {
         const size_t ob = ((size_t)(c0 + r0) * H + h) * D + col;
-        float* ou = static_cast<float*>(a.out);
+        float* ou = static_cast<float*>(outp);
 #pragma unroll
         for (int x = 0; x < RPT; ++x)
             if (r0 + x < nvalid) ou[ob + (size_t)x * H * D] = o[x];
@@ -1142,7 +1148,9 @@ __device__ __forceinline__ bool wait_rows(Misc& ms, uint32_t& rph, int32_t* dev_
     return true;
 }
 
-template <bool UNB>
+// SCAN: the instantiation for kda_prefill_scan, whose units past a.nsplit are
+// transfer runs (zero values, outputs to a.out2); the others never test it.
+template <bool UNB, bool SCAN = false>
 __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, const __grid_constant__ RawMaps maps)
 {
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -1153,11 +1161,13 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
     const int lq = warp & 3;        // TMEM lane quarter of this warp (lanes 32 lq ..)
     const int H = a.H, K = a.K;
     const int conv_dim = 3 * H * D;
-    const int seq = a.schedule ? a.schedule[blockIdx.x / H] : blockIdx.x / H;
+    const int useq = a.schedule ? a.schedule[blockIdx.x / H] : blockIdx.x / H;  // the unit's sequence index
     const int h = blockIdx.x % H;
+    const bool xfer = SCAN && a.nsplit > 0 && useq >= a.nsplit;  // a transfer run of the state scan
+    const int seq = xfer ? useq - a.nsplit : useq;      // whose rows it reads
 
     // ---- unit checks (before any tensor-memory allocation)
-    const int slot = a.slots ? a.slots[seq] : seq;
+    const int slot = a.slots ? a.slots[useq] : useq;
     if (slot < 0) return;
     if (slot >= a.num_slots) {
         if (tid == 0) flag_status(a.dev_status, KDA_DEV_BAD_SLOT);
@@ -1239,7 +1249,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
         int n;  // rows this chunk takes
         {
             float qv[RPT], kv[RPT], vv[RPT], G[RPT];
-            n = chunk_prep<UNB>(sm, ms, a, tc, nvalid, qv, kv, vv, G);
+            n = chunk_prep<UNB>(sm, ms, a, tc, nvalid, qv, kv, vv, G, xfer);
             if (UNB && c0 + n == seg1) {
                 store_conv_state(n);  // the staged rows are still intact: read before the operands overwrite them
                 __syncthreads();
@@ -1282,7 +1292,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
             float o[RPT];
             write_outputs_a(ms, a, tmem + lane_base + TM_OT + RPT * qq, o);
             __syncthreads();
-            write_outputs_b(ms, a, o, gp, c0, n, h, nw);
+            write_outputs_b(ms, a, o, gp, c0, n, h, nw, xfer ? a.out2 : a.out);
         }
         ptx::tc_fence_before();
         __syncthreads();
@@ -1625,7 +1635,7 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         // while the fourth product runs: the rest of the previous chunk's outputs
         // (warp-local), then chunk c's output gate
         if (have_prev) {
-            write_outputs_b(ms, a, o, gp, prev_c0, prev_nvalid, h, nw);
+            write_outputs_b(ms, a, o, gp, prev_c0, prev_nvalid, h, nw, a.out);
             have_prev = false;
         }
         gate_bits_from_words(gp, gw, col);
@@ -1648,7 +1658,7 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         float o[RPT];
         write_outputs_a(ms, a, tmem + lane_base + c_ot + RPT * qq, o);
         __syncthreads();
-        write_outputs_b(ms, a, o, gp, prev_c0, prev_nvalid, h, nw);
+        write_outputs_b(ms, a, o, gp, prev_c0, prev_nvalid, h, nw, a.out);
     }
     if (tid == 0 && mma_pending) (void)ptx::mbar_wait(&ms.bar, ph);  // after a failed wait: let the products end
 
@@ -1868,11 +1878,12 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
     const bool unb = !(a.gate_mode == KDA_GATE_SAFE && a.lb >= -5.0f);
     static PerDeviceOnce attr;
     cudaError_t ae = attr.run([](int) {
-        cudaError_t e = cudaFuncSetAttribute(chk::kda_chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             chk::SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(chk::kda_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     chk::SMEM_BYTES);
+        const void* fns[4] = {(const void*)chk::kda_chunk_kernel<false>, (const void*)chk::kda_chunk_kernel<true>,
+                              (const void*)chk::kda_chunk_kernel<false, true>,
+                              (const void*)chk::kda_chunk_kernel<true, true>};
+        cudaError_t e = cudaSuccess;
+        for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+            e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, chk::SMEM_BYTES);
         return e;
     });
     if (ae != cudaSuccess) return ae;
@@ -1933,9 +1944,16 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
         }
         // too few SMs for producers beside the chains: the fused kernel below
     }
-    if (a.schedule) chk::kda_chunk_schedule_kernel<<<1, 256, 0, st>>>(a.cu_seqlens, a.N, a.schedule);
-    if (unb) chk::kda_chunk_kernel<true><<<a.N * a.H, chk::NT, chk::SMEM_BYTES, st>>>(a, maps);
-    else chk::kda_chunk_kernel<false><<<a.N * a.H, chk::NT, chk::SMEM_BYTES, st>>>(a, maps);
+    if (a.schedule) chk::kda_chunk_schedule_kernel<<<1, 256, 0, st>>>(a.cu_seqlens, a.N, a.nsplit, a.schedule);
+    const dim3 grid(a.N * a.H);
+    if (a.nsplit > 0) {  // kda_prefill_scan's zero-state and transfer runs
+        if (unb) chk::kda_chunk_kernel<true, true><<<grid, chk::NT, chk::SMEM_BYTES, st>>>(a, maps);
+        else chk::kda_chunk_kernel<false, true><<<grid, chk::NT, chk::SMEM_BYTES, st>>>(a, maps);
+    } else if (unb) {
+        chk::kda_chunk_kernel<true><<<grid, chk::NT, chk::SMEM_BYTES, st>>>(a, maps);
+    } else {
+        chk::kda_chunk_kernel<false><<<grid, chk::NT, chk::SMEM_BYTES, st>>>(a, maps);
+    }
     return cudaGetLastError();
 }
 

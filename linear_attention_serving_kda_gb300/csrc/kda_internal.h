@@ -104,6 +104,12 @@ struct ChunkArgs {
     // CTAs without producers, their flag waits limited to this many polls
     // (0: the normal grid and limit).
     uint32_t dbg_chains_only_polls;
+    // Affine state scan (kda_prefill_scan): when nsplit > 0, units of
+    // sequence index s >= nsplit are transfer runs over the rows of sequence
+    // s - nsplit -- values v forced to zero, outputs to out2 -- while slots
+    // stay indexed by s itself.  0: every unit is an ordinary sequence.
+    int nsplit;
+    void* out2;
 };
 
 cudaError_t launch_recurrent(int mode, int io_bf16, const RecArgs& a, int units, cudaStream_t st);
@@ -126,6 +132,14 @@ int prefill_varlen_impl(const kda_params* p, const int32_t* cu_seqlens, int32_t 
                         size_t ws_bytes, int32_t* dev_status, cudaStream_t stream, bool allow_split,
                         uint32_t dbg_chains_only_polls = 0);
 size_t prefill_workspace_bytes(const kda_params* p, int32_t N, int32_t T, bool allow_split);
+// ChunkArgs of a prefill call (every other field zero)
+void fill_chunk(ChunkArgs& c, const kda_params* p, const int32_t* cu_seqlens, int32_t N, int32_t T, const void* q,
+                const void* k, const void* v, const void* gate, const void* beta, const void* out_gate,
+                const int32_t* slots, void* conv_state, float* rec_state, void* out, int32_t* dev_status);
 cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st);
+// Affine state scan over P segments per sequence (kda_scan.cu): a0 holds the
+// call's arguments as for the fused chunk kernel; ws its workspace.
+size_t prefill_scan_workspace_bytes(const kda_params* p, int N, int T, int P);
+cudaError_t launch_prefill_scan(const kda_params* p, const ChunkArgs& a0, int P, unsigned char* ws, cudaStream_t st);
 
 }  // namespace kda

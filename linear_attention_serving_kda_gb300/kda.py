@@ -54,6 +54,9 @@ _SIG = {
     "kda_prefill_varlen_static_ws": (ctypes.c_int, [ctypes.POINTER(kda_params), _VP, _I32, _I32, _VP, _VP, _VP,
                                                     _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "kda_prefill_static_workspace_capacity": (ctypes.c_size_t, []),
+    "kda_prefill_scan": (ctypes.c_int, [ctypes.POINTER(kda_params), _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP,
+                                        _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _I32, _VP, _VP]),
+    "kda_prefill_scan_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(kda_params), _I32, _I32, _I32]),
     "kda_debug_split_chains_only": (ctypes.c_int, [ctypes.POINTER(kda_params), _VP, _I32, _I32, _VP, _VP, _VP,
                                                    _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t,
                                                    _VP, ctypes.c_uint32, _VP]),
@@ -180,6 +183,19 @@ def kda_prefill_varlen_static_ws(params: Params, cu_seqlens, N: int, T: int, q, 
         ctypes.byref(params.c_struct()), _ptr(cu_seqlens), N, T, _ptr(q), _ptr(k), _ptr(v), _ptr(gate),
         _ptr(beta), _ptr(out_gate), _ptr(slots), _ptr(conv_state), _ptr(rec_state), _ptr(out),
         _ptr(dev_status), _stream(stream))
+
+
+def kda_prefill_scan(params: Params, cu_seqlens, N: int, T: int, q, k, v, gate, beta, out_gate, slots,
+                     conv_state, rec_state, out, workspace, ws_bytes: int, segments: int, dev_status=None,
+                     stream=None) -> int:
+    return load().kda_prefill_scan(
+        ctypes.byref(params.c_struct()), _ptr(cu_seqlens), N, T, _ptr(q), _ptr(k), _ptr(v), _ptr(gate),
+        _ptr(beta), _ptr(out_gate), _ptr(slots), _ptr(conv_state), _ptr(rec_state), _ptr(out),
+        _ptr(workspace), ws_bytes, segments, _ptr(dev_status), _stream(stream))
+
+
+def kda_prefill_scan_workspace_bytes(params: Params, N: int, T: int, segments: int) -> int:
+    return load().kda_prefill_scan_workspace_bytes(ctypes.byref(params.c_struct()), N, T, segments)
 
 
 def kda_debug_split_chains_only(params: Params, cu_seqlens, N: int, T: int, q, k, v, gate, beta, out_gate,

@@ -397,3 +397,31 @@ def test_epilogue_composes(oracle_mod):
         for h in range(2):
             y = oracle_mod.gated_rmsnorm(raw["out"][t, h], wl.arrays["g"][t, h], wl.arrays["norm_w"], wl.norm_eps)
             assert np.allclose(gated["out"][t, h], y, rtol=1e-14, atol=1e-15)
+
+
+def test_state_transfer_decomposition(oracle_mod):
+    """What the affine state scan relies on, pinned on the oracle alone: the
+    rows of a segment map any start state S linearly, S_out = M S + N and
+    o = obar + psi S, where (N, obar) come from S = 0 and (M, psi) from the
+    identity with the values v set to zero; outputs before the gated norm."""
+    from linear_attention_serving_kda_gb300 import workloads as W
+
+    wl = W.make_workload("xfer", 77, [23], H=1, d=8, K=3, io_dtype=W.F32, gate_mode=W.SOFTPLUS,
+                         lower_bound=-5.0, out_gate=False, init_state="random")
+    S = wl.arrays["rec_state"][0, 0].astype(np.float64)
+    full = oracle_mod.forward(wl)
+    zero = dict(wl.arrays)
+    zero["rec_state"] = np.zeros_like(wl.arrays["rec_state"])
+    r0 = oracle_mod.forward(wl, arrays=zero)
+    ident = dict(zero)
+    ident["rec_state"] = np.eye(8)[None, None].astype(np.float64)
+    ident["v"] = np.zeros_like(wl.arrays["v"])
+    # v = 0 must not change the conv taps of the other channels: v's own
+    # channels see zero rows, and its carried history is zeroed too
+    cs = wl.arrays["conv_state"].copy()
+    cs[:, :, 2 * 8:] = 0.0
+    ident["conv_state"] = cs
+    rm = oracle_mod.forward(wl, arrays=ident)
+    M, N = rm["rec_state"][0, 0], r0["rec_state"][0, 0]
+    np.testing.assert_allclose(full["rec_state"][0, 0], M @ S + N, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(full["out"][:, 0], r0["out"][:, 0] + rm["out"][:, 0] @ S, rtol=0, atol=1e-12)
