@@ -35,6 +35,14 @@ def cuda_lib():
 
 
 @pytest.fixture(autouse=True)
+def _name_parity_records(request):
+    from tests import parity
+
+    parity.CURRENT[0] = request.node.name
+    yield
+
+
+@pytest.fixture(autouse=True)
 def _guard_regions(request):
     """After every GPU test: no guard region around a buffer the library
     wrote (outputs, states, verify logs, workspaces of every DeviceCase the
@@ -61,4 +69,4 @@ def pytest_terminal_summary(terminalreporter):
     if RECORD:
         terminalreporter.write_line("parity record (what, rel L2, max-abs/RMS):")
         for what, e, m in RECORD:
-            terminalreporter.write_line(f"  {what:40s} {e:.3e} {m:.3e}")
+            terminalreporter.write_line(f"  {what:70s} {e:.3e} {m:.3e}")

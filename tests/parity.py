@@ -15,6 +15,8 @@ BF16_SLACK_RMS = 1e-3
 
 # (what, rel L2, max-abs / RMS) of every comparison, printed at the end of the run
 RECORD = []
+# the running test's name (set by a fixture), prefixed to each record
+CURRENT = [""]
 
 
 def to_np(t):
@@ -40,7 +42,7 @@ def assert_close(x, ref, what="", rel=REL_L2, maxabs_rms=MAX_ABS_RMS):
     e = rel_l2(x, ref)
     rms = np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
     m = np.max(np.abs(x - ref)) if ref.size else 0.0
-    RECORD.append((what, e, m / max(rms, 1e-30)))
+    RECORD.append((f"{CURRENT[0]}: {what}", e, m / max(rms, 1e-30)))
     assert e <= rel, f"{what}: rel L2 {e:.3e} > {rel:.1e}"
     assert m <= maxabs_rms * max(rms, 1e-30), f"{what}: max abs {m:.3e} > {maxabs_rms:.0e} * RMS {rms:.3e}"
     return e, m / max(rms, 1e-30)
@@ -57,7 +59,7 @@ def assert_bf16_within_one_ulp(x_bf16, ref):
     ulp = np.exp2(np.floor(np.log2(mag)) - 7)
     rms = np.sqrt(np.mean(ref * ref))
     bad = np.abs(x - r) > ulp + BF16_SLACK_RMS * rms
-    RECORD.append(("bf16 out: max |x - RNE(ref)| / ulp", float(np.max(np.abs(x - r) / ulp)), 0.0))
+    RECORD.append((f"{CURRENT[0]}: bf16 out: max |x - RNE(ref)| / ulp", float(np.max(np.abs(x - r) / ulp)), 0.0))
     assert not bad.any(), f"{bad.sum()} bf16 outputs more than one ulp (+1e-3 RMS) from RNE(oracle)"
 
 
