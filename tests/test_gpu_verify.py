@@ -148,7 +148,7 @@ def test_commit_verify_equals_separate_calls(cuda_lib, d, io, gate, alias):
     K.check(sep.verify())
     # one call
     _load_rows(fus, win2)
-    log2 = fus.log if alias else torch.empty_like(fus.log)
+    log2 = fus.log if alias else fus._guarded(fus.log.shape, torch.uint8)  # sentinel-filled like the others
     K.check(_commit_verify(fus, acc, fus.log, log2))
     torch.cuda.synchronize()
     assert int(sep.dev_status.item()) == 0 and int(fus.dev_status.item()) == 0
@@ -177,7 +177,7 @@ def test_commit_verify_long_windows(cuda_lib, Wn, alias):
     _load_rows(sep, win2)
     K.check(sep.verify())
     _load_rows(fus, win2)
-    log2 = fus.log if alias else torch.empty_like(fus.log)
+    log2 = fus.log if alias else fus._guarded(fus.log.shape, torch.uint8)  # sentinel-filled like the others
     K.check(_commit_verify(fus, acc, fus.log, log2))
     torch.cuda.synchronize()
     assert int(sep.dev_status.item()) == 0 and int(fus.dev_status.item()) == 0
@@ -205,7 +205,7 @@ def test_commit_verify_bad_accepted(cuda_lib):
     good = torch.tensor([2, 0, 1], dtype=torch.int32, device="cuda")
     _load_rows(fus, win2)
     fus.out.fill_(float("nan"))
-    log2 = torch.empty_like(fus.log)
+    log2 = fus._guarded(fus.log.shape, torch.uint8)
     K.check(_commit_verify(fus, bad, fus.log, log2))
     K.check(sep.commit(accepted=good))
     _load_rows(sep, win2)
@@ -251,7 +251,7 @@ def test_verify_slot_map_negative_and_bad(cuda_lib):
         assert torch.equal(dc.rec_state[sl], ref.rec_state[sl])
         assert torch.equal(dc.conv_state[sl], ref.conv_state[sl])
     dc.out.fill_(float("nan"))
-    log2r, log2d = torch.empty_like(ref.log), torch.empty_like(dc.log)
+    log2r, log2d = ref._guarded(ref.log.shape, torch.uint8), dc._guarded(dc.log.shape, torch.uint8)
     K.check(_commit_verify(ref, acc, ref.log, log2r))
     K.check(_commit_verify(dc, acc, dc.log, log2d))
     torch.cuda.synchronize()
