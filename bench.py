@@ -649,7 +649,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "verify", "prefill_varlen", "prefill_long", "prefill_small",
-                             "prefill_varlen_softplus", "prefill_long_scan"])
+                             "prefill_varlen_softplus", "prefill_long_scan", "prefill_scan_small"])
     ap.add_argument("--segments", type=int, default=4, help="pieces per sequence for prefill_long_scan")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -778,6 +778,10 @@ def run_single_leg(kda, args, stream):
         return leg_verify(kda, args.steps, stream)
     if args.workload == "prefill_long_scan":
         return leg_prefill_scan(kda, W.long_prefill_case, args.segments, args.steps, stream)
+    if args.workload == "prefill_scan_small":
+        # a profiling-sized prompt for the scan path: 1 sequence x 8192 rows, the long prompt's dtypes and gate
+        fn = lambda: W.long_prefill_case(8192)  # noqa: E731
+        return leg_prefill_scan(kda, fn, args.segments, args.steps, stream)
     if args.workload == "prefill_small":
         # a profiling-sized prefill: 2 sequences x 2048 rows, 32 heads, same dtypes and gate
         fn = lambda: W.make_workload("prefill_small_n2x2048_h32_d128_bf16", 5, [2048, 2048], H=32, d=128,  # noqa: E731
