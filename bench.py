@@ -160,6 +160,25 @@ def prefill_state_bytes(N, H, d=128, K=4, io=2):
 
 # --------------------------------------------------------------- workloads
 
+class nvtx_range:
+    """An NVTX range around a leg of the benchmark (shows in nsys/ncu
+    timelines; a no-op without a profiler)."""
+
+    def __init__(self, name):
+        self.name = name
+
+    def __enter__(self):
+        import torch
+
+        torch.cuda.nvtx.range_push(self.name)
+
+    def __exit__(self, *exc):
+        import torch
+
+        torch.cuda.nvtx.range_pop()
+        return False
+
+
 _WL_CACHE = {}
 
 
@@ -707,8 +726,10 @@ def main():
             print(json.dumps(res))
         return
 
-    wl, sets, step, per_set = bench_decode(kda, args.steps, args.warmup, stream)
-    total_ms, durs, wall = run_timed(step, args.steps, stream, dist)
+    with nvtx_range("decode warm-up"):
+        wl, sets, step, per_set = bench_decode(kda, args.steps, args.warmup, stream)
+    with nvtx_range("decode timed"):
+        total_ms, durs, wall = run_timed(step, args.steps, stream, dist)
     ms = total_ms / args.steps
     value = weak_scaling_value(wl.N, world, args.steps, total_ms)
     kernel_ms = statistics.mean(durs)
@@ -718,16 +739,22 @@ def main():
     if not args.no_legs:
         from linear_attention_serving_kda_gb300 import workloads as W
 
-        legs["prefill_varlen"] = leg_prefill(kda, W.varlen_prefill_case, 3, stream)
-        legs["prefill_long"] = leg_prefill(kda, W.long_prefill_case, 3, stream)
-        legs["verify_commit"] = leg_verify(kda, 10, stream)
-        legs["prefill_long_scan"] = leg_prefill_scan(kda, W.long_prefill_case, 4, 3, stream)
+        with nvtx_range("leg prefill_varlen"):
+            legs["prefill_varlen"] = leg_prefill(kda, W.varlen_prefill_case, 3, stream)
+        with nvtx_range("leg prefill_long"):
+            legs["prefill_long"] = leg_prefill(kda, W.long_prefill_case, 3, stream)
+        with nvtx_range("leg verify_commit"):
+            legs["verify_commit"] = leg_verify(kda, 10, stream)
+        with nvtx_range("leg prefill_long_scan"):
+            legs["prefill_long_scan"] = leg_prefill_scan(kda, W.long_prefill_case, 4, 3, stream)
         for k in ("prefill_varlen", "prefill_long"):
             legs[k]["hbm_frac"] = legs[k]["achieved_gbs"] / hbm_gbs
-        legs["prefill_varlen"]["e2e"] = e2e_prefill(kda, W.varlen_prefill_case, 3, stream)
-        legs["prefill_long"]["e2e"] = e2e_prefill(kda, W.long_prefill_case, 3, stream)
-        legs["verify_commit"]["e2e"] = e2e_verify(kda, 10, stream)
-    e2e = e2e_decode(kda, args.steps, args.warmup, stream)
+        with nvtx_range("legs end to end"):
+            legs["prefill_varlen"]["e2e"] = e2e_prefill(kda, W.varlen_prefill_case, 3, stream)
+            legs["prefill_long"]["e2e"] = e2e_prefill(kda, W.long_prefill_case, 3, stream)
+            legs["verify_commit"]["e2e"] = e2e_verify(kda, 10, stream)
+    with nvtx_range("decode end to end"):
+        e2e = e2e_decode(kda, args.steps, args.warmup, stream)
     e2e["value"] *= world
     clocks = sampler.stop() if sampler else None
 
