@@ -248,3 +248,27 @@ def test_chunk_path_unbounded_gates(cuda_lib, oracle_mod, lens, gate, lb, alog, 
     if alog is not None:
         wl.arrays["A_log"] = np.full_like(wl.arrays["A_log"], alog)
     _check_all(_prefill(cuda_lib, wl), oracle_mod.forward(wl))
+
+
+@pytest.mark.slow
+def test_varlen_full_size_softplus(cuda_lib, oracle_mod):
+    """The varlen workload's lengths and rows (29 273 rows, H=32, bf16) with the
+    softplus gate: the chunk kernel with data-dependent chunk boundaries,
+    every unit against the oracle (whole tensors)."""
+    wl = W.make_workload("prefill_varlen_softplus_n8_h32_d128_bf16", 2, None, H=32, d=128, K=4, io_dtype=W.BF16,
+                         gate_mode=W.SOFTPLUS, lower_bound=-5.0, init_state="random", draw_lens=(8, 512, 8192))
+    dc = _prefill(cuda_lib, wl)
+    _check_all(dc, oracle_mod.forward(wl))
+
+
+@pytest.mark.slow
+def test_long_prefill_full_size_softplus(cuda_lib, oracle_mod):
+    """A 32 768-row prompt, H=32, bf16, gated RMSNorm, softplus gate: the split
+    path with each chain's chunk list fixed by the boundary pass, all heads
+    against the oracle (whole tensors)."""
+    wl = W.make_workload("prefill_long_softplus_t32768_h32_d128_bf16", 4, [32768], H=32, d=128, K=4,
+                         io_dtype=W.BF16, gate_mode=W.SOFTPLUS, lower_bound=-5.0, out_gate=True,
+                         init_state="zero")
+    dc = _prefill(cuda_lib, wl)
+    assert cuda_lib.kda_prefill_workspace_bytes(dc.params(), wl.N, wl.T) > 2**25  # the split path's ring
+    _check_all(dc, oracle_mod.forward(wl))
