@@ -203,3 +203,29 @@ def test_size_queries_from_many_threads(lib):
     with ThreadPoolExecutor(max_workers=16) as ex:
         got = list(ex.map(q, range(256)))
     assert all(g == want for g in got)
+
+
+def test_plain_c_consumer(lib, tmp_path):
+    """include/kda.h compiles as C11 and a C program linked against the
+    library calls its host-side entry points (no GPU needed)."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    cuda_inc = None
+    for cand in ("/usr/local/cuda/include", os.path.join(os.path.dirname(os.path.dirname(shutil.which("nvcc") or "/x/x")), "include")):
+        if os.path.exists(os.path.join(cand, "cuda_runtime_api.h")):
+            cuda_inc = cand
+            break
+    if cuda_inc is None:
+        pytest.skip("CUDA headers not found")
+    src = os.path.join(ROOT, "tests", "c_consumer", "kda_c_consumer.c")
+    exe = str(tmp_path / "kda_c_consumer")
+    libdir = os.path.dirname(kbuild.LIB)
+    subprocess.check_call([gcc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+                           src, "-o", exe, "-L", libdir, "-lkda", f"-Wl,-rpath,{libdir}"])
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "FAIL" not in r.stdout and r.stdout.count("ok") >= 10
