@@ -206,10 +206,20 @@ __global__ void __launch_bounds__(256, 1)
     }
 }
 
-// The fix-up (one block per (64-row output tile, head)): o = obar (+ psi S_p
-// for segments p >= 1), then the optional sigmoid-gated RMSNorm, stored in the
-// output type.  Thread (row group g = tid / 32, lane) owns rows [8 g, +8) and
-// columns [4 lane, +4).
+// The fix-up: o = obar (+ psi S_p for segments p >= 1), then the optional
+// sigmoid-gated RMSNorm, stored in the output type.  Grid (tiles, H): one
+// CTA per 64-row output tile and head (any CTA past the last tile returns).
+// Thread (row group
+// gq = tid / 32, lane) owns rows [8 gq, +8) and columns [4 lane, +4); each
+// output sums obar and the 128 terms psi_ri S_ij in key order i.  The psi
+// tile is stored transposed (key dim major) with its 8-row groups permuted by
+// the key dim (an XOR of the row index's upper bits), so the 8 rows a thread
+// needs for one key dim are 32 contiguous bytes and the transposing stores
+// spread over the banks.
+constexpr int FX_PT = 68;  // row pitch (floats) of the transposed psi tile
+
+__device__ __forceinline__ int fx_row(int r, int i) { return r ^ (8 * ((i >> 2) & 7)); }
+
 __global__ void __launch_bounds__(256, 2)
     kda_scan_fixup_kernel(int N, int P, int H, const int32_t* pcu, const int32_t* pslots, const int32_t* tiles,
                           const float* obar, const float* psi, const float* wrec, const void* g, const float* norm_w,
@@ -217,74 +227,94 @@ __global__ void __launch_bounds__(256, 2)
 {
     extern __shared__ __align__(16) float scn_smem[];
     float* Ss = scn_smem;          // [D][D] segment start state
-    float* Ps = scn_smem + D * D;  // [C][D] psi rows
+    float* Pt = scn_smem + D * D;  // [D][FX_PT] psi tile, transposed and row-permuted
     const int NP = N * P;
-    const int t = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int h = blockIdx.y, tid = threadIdx.x;
     const int ntiles = tiles[NP];
-    if (t >= ntiles) return;
-    int lo = 0, hi = NP - 1;  // the pseudo-sequence j with tiles[j] <= t < tiles[j + 1]
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (tiles[mid] <= t) lo = mid;
-        else hi = mid - 1;
-    }
-    const int j = lo, p = j % P;
-    if (pslots[j] < 0) return;
-    const int r0 = pcu[j] + (t - tiles[j]) * C;
-    const int nrows = min(C, seg_end(pcu, j) - r0);
-    if (nrows <= 0) return;
     const int gq = tid >> 5, lane = tid & 31, c0 = 4 * lane;
-    float acc[8][4];
-#pragma unroll
-    for (int a = 0; a < 8; ++a) {
-        const int r = 8 * gq + a;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < nrows) x = *reinterpret_cast<const float4*>(obar + ((size_t)(r0 + r) * H + h) * D + c0);
-        acc[a][0] = x.x; acc[a][1] = x.y; acc[a][2] = x.z; acc[a][3] = x.w;
-    }
-    if (p > 0) {
-        const float* St = wrec + ((size_t)j * H + h) * D * D;  // segment p's start state
-        for (int e = tid * 4; e < D * D; e += 256 * 4)
-            *reinterpret_cast<float4*>(Ss + e) = *reinterpret_cast<const float4*>(St + e);
-        for (int e = tid * 4; e < C * D; e += 256 * 4) {
-            const int r = e / D;
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < nrows) x = *reinterpret_cast<const float4*>(psi + ((size_t)(r0 + r) * H + h) * D + (e % D));
-            *reinterpret_cast<float4*>(Ps + e) = x;
+    int loaded = -1;  // pseudo-sequence whose start state is in Ss
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        int lo = 0, hi = NP - 1;  // the pseudo-sequence j with tiles[j] <= t < tiles[j + 1]
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (tiles[mid] <= t) lo = mid;
+            else hi = mid - 1;
         }
-        __syncthreads();
-        for (int kk = 0; kk < D; ++kk) {
-            const float4 sv = *reinterpret_cast<const float4*>(Ss + kk * D + c0);
+        const int j = lo, p = j % P;
+        if (pslots[j] < 0) continue;  // block-uniform
+        const int r0 = pcu[j] + (t - tiles[j]) * C;
+        const int nrows = min(C, seg_end(pcu, j) - r0);
+        if (nrows <= 0) continue;
+        float2 acc[4][4];  // (rows 8 gq + 2 a, + 1) x column c0 + b
 #pragma unroll
-            for (int a = 0; a < 8; ++a) {
-                const float pv = Ps[(8 * gq + a) * D + kk];
-                acc[a][0] = __fmaf_rn(pv, sv.x, acc[a][0]);
-                acc[a][1] = __fmaf_rn(pv, sv.y, acc[a][1]);
-                acc[a][2] = __fmaf_rn(pv, sv.z, acc[a][2]);
-                acc[a][3] = __fmaf_rn(pv, sv.w, acc[a][3]);
+        for (int a = 0; a < 4; ++a) {
+            float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+            const int ra = 8 * gq + 2 * a;
+            if (ra < nrows) x0 = *reinterpret_cast<const float4*>(obar + ((size_t)(r0 + ra) * H + h) * D + c0);
+            if (ra + 1 < nrows) x1 = *reinterpret_cast<const float4*>(obar + ((size_t)(r0 + ra + 1) * H + h) * D + c0);
+            acc[a][0] = make_float2(x0.x, x1.x);
+            acc[a][1] = make_float2(x0.y, x1.y);
+            acc[a][2] = make_float2(x0.z, x1.z);
+            acc[a][3] = make_float2(x0.w, x1.w);
+        }
+        if (p > 0) {
+            __syncthreads();  // the previous tile's reads of Ss and Pt are done
+            if (loaded != j) {
+                const float* St = wrec + ((size_t)j * H + h) * D * D;  // segment p's start state
+                for (int e = tid * 4; e < D * D; e += 256 * 4)
+                    *reinterpret_cast<float4*>(Ss + e) = *reinterpret_cast<const float4*>(St + e);
+                loaded = j;
+            }
+            for (int e = tid * 4; e < C * D; e += 256 * 4) {
+                const int r = e / D, i = e % D;
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (r < nrows) x = *reinterpret_cast<const float4*>(psi + ((size_t)(r0 + r) * H + h) * D + i);
+                const int rr = fx_row(r, i);  // i .. i + 3 share (i >> 2)
+                Pt[(i + 0) * FX_PT + rr] = x.x;
+                Pt[(i + 1) * FX_PT + rr] = x.y;
+                Pt[(i + 2) * FX_PT + rr] = x.z;
+                Pt[(i + 3) * FX_PT + rr] = x.w;
+            }
+            __syncthreads();
+#pragma unroll 4
+            for (int i = 0; i < D; ++i) {
+                const float* pc = Pt + i * FX_PT + fx_row(8 * gq, i);  // rows 8 gq .. + 7 of key dim i
+                const float4 p0 = *reinterpret_cast<const float4*>(pc);
+                const float4 p1 = *reinterpret_cast<const float4*>(pc + 4);
+                const float4 sv = *reinterpret_cast<const float4*>(Ss + i * D + c0);
+                const float2 pr[4] = {make_float2(p0.x, p0.y), make_float2(p0.z, p0.w), make_float2(p1.x, p1.y),
+                                      make_float2(p1.z, p1.w)};
+                const float2 s2[4] = {make_float2(sv.x, sv.x), make_float2(sv.y, sv.y), make_float2(sv.z, sv.z),
+                                      make_float2(sv.w, sv.w)};
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[a][b] = __ffma2_rn(pr[a], s2[b], acc[a][b]);
             }
         }
-    }
 #pragma unroll
-    for (int a = 0; a < 8; ++a) {
-        const int r = 8 * gq + a;
-        float y[4] = {acc[a][0], acc[a][1], acc[a][2], acc[a][3]};
-        if (has_g) {
-            const float ss = warp_sum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]);
-            const float rn = rsqrtf(ss * (1.0f / D) + norm_eps);
-            if (r < nrows) {
-                const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(g) + ((size_t)(r0 + r) * H + h) * D + c0;
+        for (int a = 0; a < 8; ++a) {
+            const int r = 8 * gq + a;
+            float y[4];
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const float w = norm_w ? norm_w[c0 + b] : 1.0f;
-                    y[b] = y[b] * rn * w * sigmoidf_(__bfloat162float(gb[b]));
+            for (int b = 0; b < 4; ++b) y[b] = (a & 1) ? acc[a >> 1][b].y : acc[a >> 1][b].x;
+            if (has_g) {
+                const float ss = warp_sum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]);
+                const float rn = rsqrtf(ss * (1.0f / D) + norm_eps);
+                if (r < nrows) {
+                    const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(g) + ((size_t)(r0 + r) * H + h) * D + c0;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const float w = norm_w ? norm_w[c0 + b] : 1.0f;
+                        y[b] = y[b] * rn * w * sigmoidf_(__bfloat162float(gb[b]));
+                    }
                 }
             }
-        }
-        if (r < nrows) {
-            const size_t o = ((size_t)(r0 + r) * H + h) * D + c0;
+            if (r < nrows) {
+                const size_t o = ((size_t)(r0 + r) * H + h) * D + c0;
 #pragma unroll
-            for (int b = 0; b < 4; ++b) store_out(out, o + b, y[b], out_bf16);
+                for (int b = 0; b < 4; ++b) store_out(out, o + b, y[b], out_bf16);
+            }
         }
     }
 }
@@ -365,7 +395,7 @@ cudaError_t launch_prefill_scan(const kda_params* p, const ChunkArgs& a0, int P,
     if ((e = launch_chunk(1, c, st)) != cudaSuccess) return e;
 
     static PerDeviceOnce attr;
-    const int smem_scan = 2 * D * D * 4, smem_fix = (D * D + C * D) * 4;
+    const int smem_scan = 2 * D * D * 4, smem_fix = (D * D + D * FX_PT) * 4;
     e = attr.run([&](int) {
         cudaError_t r = cudaFuncSetAttribute(kda_scan_states_kernel<__nv_bfloat16>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem_scan);
@@ -376,10 +406,11 @@ cudaError_t launch_prefill_scan(const kda_params* p, const ChunkArgs& a0, int P,
     if (e != cudaSuccess) return e;
     kda_scan_states_kernel<__nv_bfloat16><<<dim3(N, H), 256, smem_scan, st>>>(
         a0.slots, N, P, H, K, pslots, wrec, wconv, a0.rec_state, static_cast<__nv_bfloat16*>(a0.conv_state));
+    // one CTA per (64-row tile, head): many tiles in flight hide the loads
     const int max_tiles = (T + C - 1) / C + NP;
     kda_scan_fixup_kernel<<<dim3(max_tiles, H), 256, smem_fix, st>>>(N, P, H, pcu, pslots, tiles, obar, psi, wrec,
-                                                                     a0.g, a0.norm_w, a0.norm_eps, a0.g != nullptr,
-                                                                     a0.out, a0.out_bf16);
+                                                                    a0.g, a0.norm_w, a0.norm_eps, a0.g != nullptr,
+                                                                    a0.out, a0.out_bf16);
     return cudaGetLastError();
 }
 
