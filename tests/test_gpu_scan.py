@@ -104,3 +104,36 @@ def test_scan_long_prefill_full_size(cuda_lib, oracle_mod):
     wl = W.long_prefill_case()
     dc = _scan(DeviceCase(wl), 4)
     _check(dc, oracle_mod.forward(wl))
+
+
+def test_scan_flags_bad_inputs_without_faulting(cuda_lib, oracle_mod):
+    """An out-of-range slot and a non-monotone cu_seqlens are flagged in the
+    status word and their sequences skipped (no output rows, no state
+    written); the other sequences still match the oracle."""
+    wl = W.make_workload("scanbad2", 1400, [200, 90, 150], H=2, d=128, K=4, io_dtype=W.BF16, gate_mode=W.SAFE,
+                         lower_bound=-5.0, out_gate=False, init_state="random")
+    ref = oracle_mod.forward(wl)
+    dc = DeviceCase(wl, num_slots=3, slots=[0, 7, 2])  # sequence 1's slot is out of range
+    rs0 = dc.rec_state.clone()
+    dc.out.fill_(float("nan"))
+    p = dc.params()
+    need = K.kda_prefill_scan_workspace_bytes(p, wl.N, wl.T, 2)
+    ws = dc._guarded((need,), torch.uint8)
+    K.check(K.kda_prefill_scan(p, dc.cu_seqlens, wl.N, wl.T, dc.q, dc.k, dc.v, dc.f, dc.b, None, dc.slots,
+                               dc.conv_state, dc.rec_state, dc.out, ws, need, 2, dc.dev_status))
+    torch.cuda.synchronize()
+    assert int(dc.dev_status.item()) & K.KDA_DEV_BAD_SLOT
+    out = to_np(dc.out)
+    assert np.all(np.isnan(out[200:290]))
+    assert torch.equal(dc.rec_state[1], rs0[1])  # no sequence's slot
+    assert_close(out[:200], ref["out"][:200], "scan out s0")
+    assert_close(out[290:], ref["out"][290:], "scan out s2")
+    assert_close(to_np(dc.rec_state[0]), ref["rec_state"][0], "scan state s0")
+    assert_close(to_np(dc.rec_state[2]), ref["rec_state"][2], "scan state s2")
+    # a non-monotone cu_seqlens: flagged, no fault
+    dc2 = DeviceCase(wl)
+    dc2.cu_seqlens.copy_(torch.tensor([0, 210, 190, 440], dtype=torch.int32))
+    K.check(K.kda_prefill_scan(p, dc2.cu_seqlens, wl.N, wl.T, dc2.q, dc2.k, dc2.v, dc2.f, dc2.b, None, None,
+                               dc2.conv_state, dc2.rec_state, dc2.out, ws, need, 2, dc2.dev_status))
+    torch.cuda.synchronize()
+    assert int(dc2.dev_status.item()) & K.KDA_DEV_BAD_SEQLENS
