@@ -519,6 +519,79 @@ def e2e_prefill(kda, wl_fn, reps, stream):
             "d2h_bytes_per_step": d2h, "path": "kda_prefill_varlen: rows host->device, prefill, outputs device->host"}
 
 
+def e2e_prefill_pipelined(kda, wl_fn, pieces, reps, stream):
+    """The same prefill end to end as a serving loop would overlap it: the
+    batch is cut into `pieces` -- whole-sequence groups (balanced by rows) for
+    a varlen batch, consecutive 64-row-aligned cuts of the prompt (state
+    carried from one cut to the next) for a single sequence -- each piece's
+    rows are uploaded from pinned host memory on a copy stream, each piece is
+    prefilled as soon as its rows are on the device (groups on streams of
+    their own, cuts in order on one stream), and each piece's outputs are
+    copied back as soon as it is done.  The CUDA-event region spans the first
+    upload to the last download; states stay resident and are reset outside it.
+    A prompt cut at multiples of 64 rows gives the uncut call's bits (bounded
+    gates), so the cuts change only the schedule."""
+    import torch
+
+    from linear_attention_serving_kda_gb300 import shard
+    from linear_attention_serving_kda_gb300 import workloads as W
+    from linear_attention_serving_kda_gb300.runtime import DeviceCase
+
+    wl = cached(wl_fn)
+    names = ["q", "k", "v", "f", "b"] + (["g"] if wl.has_out_gate else [])
+    if wl.N > 1:
+        groups = [g for g in shard.partition_sequences(wl.cu_seqlens, pieces) if g]
+        subs = [shard.shard_workload(wl, g) for g in groups]
+        chained = False
+    else:
+        subs = [shard.cut_prompt(wl, a, b) for a, b in shard.prompt_cuts(wl.T, pieces)]
+        chained = True
+    cases = [DeviceCase(sw, out_dtype=W.BF16) for sw in subs]
+    if chained:  # the cuts carry one sequence's states
+        for dc in cases[1:]:
+            dc.conv_state, dc.rec_state = cases[0].conv_state, cases[0].rec_state
+    packs = [_pack_rows(dc, names) for dc in cases]
+    outs = [torch.empty(dc.out[:dc.wl.T].shape, dtype=dc.out.dtype).pin_memory() for dc in cases]
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    comp = [stream] if chained else [torch.cuda.Stream() for _ in cases]
+    for dc in cases:  # workspaces allocated outside the timed region
+        dc.prefill(stream=stream)
+    torch.cuda.synchronize()
+    durs = []
+    for r in range(reps + 1):
+        for dc in cases[:1] if chained else cases:  # the cuts share the first case's states
+            dc.reset_states()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(up)
+        done = []
+        for i, (dc, (host, dev, _)) in enumerate(zip(cases, packs)):
+            ev_up, ev_done = torch.cuda.Event(), torch.cuda.Event()
+            with torch.cuda.stream(up):
+                dev.copy_(host, non_blocking=True)
+                ev_up.record(up)
+            cs = comp[0] if chained else comp[i]
+            cs.wait_event(ev_up)
+            kda.check(dc.prefill(stream=cs))
+            ev_done.record(cs)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_done)
+                outs[i].copy_(dc.out[:dc.wl.T], non_blocking=True)
+            done.append(ev_done)
+        t1.record(down)
+        torch.cuda.synchronize()
+        if r:
+            durs.append(t0.elapsed_time(t1))
+    ms = statistics.median(durs)
+    h2d = sum(p[2] for p in packs)
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    return {"value": wl.T / (ms * 1e-3), "unit": "tokens/s", "ms": ms, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "pieces": len(cases),
+            "path": ("kda_prefill_varlen per group of whole sequences" if not chained else
+                     "kda_prefill_varlen per 64-row-aligned cut, state carried") +
+                    ": each piece's upload, call and download overlapped with the others'"}
+
+
 def e2e_verify(kda, reps, stream):
     from linear_attention_serving_kda_gb300 import workloads as W
     from linear_attention_serving_kda_gb300.runtime import DeviceCase
@@ -569,15 +642,14 @@ def oracle_units_rate(wl, units, rows, threads):
     (sequence, head) units of a workload, each cut to its first `rows` rows
     (pure data movement), run on `threads` threads."""
     import oracle
-    from linear_attention_serving_kda_gb300 import workloads as W
-    from tests.parity import gather_rows
+    from linear_attention_serving_kda_gb300 import shard, workloads as W
 
     oracle.build()
     subs = []
     for s, h in units:
         sub = W.head_slice(wl, s, h)
         if rows is not None and sub.T > rows:
-            sub = gather_rows(sub, [(0, rows)])
+            sub = shard.cut_prompt(sub, 0, rows)
         subs.append(sub)
     work = sum(sb.T for sb in subs)
     from concurrent.futures import ThreadPoolExecutor
@@ -668,8 +740,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "verify", "prefill_varlen", "prefill_long", "prefill_small",
-                             "prefill_varlen_softplus", "prefill_long_scan", "prefill_scan_small"])
-    ap.add_argument("--segments", type=int, default=4, help="pieces per sequence for prefill_long_scan")
+                             "prefill_varlen_softplus", "prefill_long_scan", "prefill_scan_small",
+                             "e2e_prefill_varlen", "e2e_prefill_long"])
+    ap.add_argument("--segments", type=int, default=4,
+                    help="segments of the prompt for prefill_long_scan; pieces for the e2e_prefill_* workloads")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -753,6 +827,9 @@ def main():
             legs["prefill_varlen"]["e2e"] = e2e_prefill(kda, W.varlen_prefill_case, 3, stream)
             legs["prefill_long"]["e2e"] = e2e_prefill(kda, W.long_prefill_case, 3, stream)
             legs["verify_commit"]["e2e"] = e2e_verify(kda, 10, stream)
+            legs["prefill_varlen"]["e2e_pipelined"] = e2e_prefill_pipelined(kda, W.varlen_prefill_case, 8, 3,
+                                                                            stream)
+            legs["prefill_long"]["e2e_pipelined"] = e2e_prefill_pipelined(kda, W.long_prefill_case, 16, 3, stream)
     with nvtx_range("decode end to end"):
         e2e = e2e_decode(kda, args.steps, args.warmup, stream)
     e2e["value"] *= world
@@ -805,6 +882,10 @@ def run_single_leg(kda, args, stream):
         return leg_verify(kda, args.steps, stream)
     if args.workload == "prefill_long_scan":
         return leg_prefill_scan(kda, W.long_prefill_case, args.segments, args.steps, stream)
+    if args.workload in ("e2e_prefill_varlen", "e2e_prefill_long"):
+        fn = W.varlen_prefill_case if args.workload == "e2e_prefill_varlen" else W.long_prefill_case
+        return {"serial": e2e_prefill(kda, fn, args.steps, stream),
+                "pipelined": e2e_prefill_pipelined(kda, fn, args.segments, args.steps, stream)}
     if args.workload == "prefill_scan_small":
         # a profiling-sized prompt for the scan path: 1 sequence x 8192 rows, the long prompt's dtypes and gate
         fn = lambda: W.long_prefill_case(8192)  # noqa: E731

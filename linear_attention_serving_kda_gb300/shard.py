@@ -56,3 +56,29 @@ def shard_workload(wl, seqs):
         else:
             sub.arrays[nm] = a
     return sub
+
+
+def cut_prompt(wl, start: int, stop: int):
+    """Rows [start, stop) of a one-sequence workload as a one-sequence
+    workload of its own (same parameters and initial states).  Run in order
+    with the states carried from one cut to the next, cuts at multiples of
+    the 64-row chunk give the uncut prompt's result.  Pure data movement."""
+    from . import workloads as W
+
+    if wl.N != 1 or not 0 <= start <= stop <= wl.T:
+        raise ValueError("cut_prompt wants one sequence and 0 <= start <= stop <= T")
+    sub = W.Workload(**{**wl.__dict__, "arrays": {}})
+    sub.name = f"{wl.name}[{start}:{stop}]"
+    sub.cu_seqlens = np.array([0, stop - start], dtype=np.int32)
+    for nm, a in wl.arrays.items():
+        sub.arrays[nm] = np.ascontiguousarray(a[start:stop]) if nm in ("q", "k", "v", "f", "b", "g") else a
+    return sub
+
+
+def prompt_cuts(T: int, pieces: int, chunk: int = 64):
+    """`pieces` (or fewer) consecutive (start, stop) row ranges covering
+    [0, T), every boundary a multiple of `chunk`."""
+    if pieces < 1:
+        raise ValueError("pieces must be >= 1")
+    step = max((T // pieces + chunk - 1) // chunk * chunk, chunk)
+    return [(a, min(a + step, T)) for a in range(0, T, step)]

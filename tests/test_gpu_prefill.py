@@ -134,6 +134,28 @@ def test_prompt_cut_bits(cuda_lib):
     assert torch.equal(db.conv_state, full.conv_state)
 
 
+@pytest.mark.parametrize("T,pieces", [(2304, 3), (3072, 2), (1000, 4)])
+def test_prompt_cuts_in_order_share_states(cuda_lib, T, pieces):
+    """A prompt cut by ``shard.prompt_cuts`` and run in order on one stream,
+    every cut bound to the same state tensors, gives the uncut call's bits --
+    whichever path (split or fused) the whole prompt and each cut take."""
+    from linear_attention_serving_kda_gb300 import shard
+
+    wl = W.make_workload("cuts", 314 + T, [T], H=2, d=128, K=4, io_dtype=W.BF16,
+                         gate_mode=W.SAFE, lower_bound=-5.0, out_gate=True, init_state="random")
+    full = _prefill(cuda_lib, wl, out_dtype=W.BF16)
+    cuts = shard.prompt_cuts(T, pieces)
+    cases = [DeviceCase(shard.cut_prompt(wl, a, b), out_dtype=W.BF16) for a, b in cuts]
+    for dc in cases[1:]:
+        dc.conv_state, dc.rec_state = cases[0].conv_state, cases[0].rec_state
+    for dc in cases:
+        cuda_lib.check(dc.prefill())
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([dc.out[:dc.wl.T] for dc in cases]), full.out[:T])
+    assert torch.equal(cases[0].rec_state, full.rec_state)
+    assert torch.equal(cases[0].conv_state, full.conv_state)
+
+
 def test_slots_and_bad_seqlens(cuda_lib, oracle_mod):
     wl = W.make_workload("pslot", 313, [70, 5, 33], H=2, d=64, K=4, io_dtype=W.F32,
                          gate_mode=W.SAFE, lower_bound=-5.0, init_state="random")

@@ -76,6 +76,43 @@ def test_partition_balances_rows_and_covers_every_sequence():
         shard.partition_sequences([0, 5, 3], 2)
 
 
+def test_prompt_cuts_cover_the_prompt_on_chunk_boundaries():
+    from linear_attention_serving_kda_gb300 import shard
+
+    for T in (0, 1, 63, 64, 65, 1000, 32768):
+        for pieces in (1, 2, 3, 4, 7, 8):
+            cuts = shard.prompt_cuts(T, pieces)
+            assert len(cuts) <= pieces and (T > 0) == bool(cuts)
+            assert [a for a, _ in cuts] == ([0] if T else []) + [b for _, b in cuts[:-1]]   # consecutive
+            assert (cuts[-1][1] if cuts else 0) == T                                        # cover [0, T)
+            assert all(a % 64 == 0 and a < b for a, b in cuts)
+    with pytest.raises(ValueError):
+        shard.prompt_cuts(10, 0)
+
+
+def test_oracle_over_cuts_with_carried_states_is_the_uncut_run():
+    """The oracle's serial recurrence run cut by cut, each cut starting from
+    the previous cut's fp64 states, gives the uncut run bit for bit: the cuts
+    move data only."""
+    import oracle
+    from linear_attention_serving_kda_gb300 import shard, workloads as W
+
+    wl = W.make_workload("cuts", 43, [300], H=2, d=32, K=4, io_dtype=W.BF16, gate_mode=W.SAFE,
+                         lower_bound=-5.0, out_gate=True, init_state="random")
+    full = oracle.forward(wl, threads=1)
+    outs, conv, rec = [], None, None
+    for a, b in shard.prompt_cuts(wl.T, 3):
+        sub = shard.cut_prompt(wl, a, b)
+        arrays = dict(sub.arrays) if conv is None else dict(sub.arrays, conv_state=conv, rec_state=rec)
+        res = oracle.forward(sub, threads=1, arrays=arrays)
+        outs.append(res["out"])
+        conv, rec = res["conv_state"], res["rec_state"]
+    assert np.array_equal(np.concatenate(outs), full["out"])
+    assert np.array_equal(rec, full["rec_state"]) and np.array_equal(conv, full["conv_state"])
+    with pytest.raises(ValueError):
+        shard.cut_prompt(W.make_workload("two", 1, [5, 6], H=1, d=16, K=4), 0, 3)
+
+
 def _shard_worker(rank, world, port, out):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
     dist.init_process_group("gloo", rank=rank, world_size=world)
