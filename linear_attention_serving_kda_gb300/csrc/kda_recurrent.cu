@@ -367,31 +367,45 @@ __device__ __forceinline__ IO vw_stage(VwBuf<IO>& vb, const RecArgs& a, int seq,
 // channel `it` (q | k | v) of this thread: the register kernel's row_conv
 // expressions -- acc = fma(w_j, x_{t-K+1+j}, acc) over j = 0..K-1 from 0,
 // SiLU, and for q and k the warp's sum of squares over its 32 consecutive
-// channels -- with the raw values in a sliding window of registers.
+// channels.  All VWB rows of the block are computed at once (rows past nr
+// read whatever the buffer holds and are never stored), so the rows' loads,
+// exponentials and shuffle reductions overlap instead of running one row at
+// a time; every stored value has the one-row-at-a-time bits.
 template <int KK, typename IO>
 __device__ __forceinline__ void vw_conv_channel(VwSmem<IO>& sm, const VwBuf<IO>& vb, int it, int nr, int lane)
 {
     constexpr int D = VWD;
     const int seg = it / D, ch = it % D;
-    float w[KK], xs[KK];
+    float w[KK], xs[KK - 1 + VWB];  // raw rows -(KK-1) .. VWB-1 of the block
 #pragma unroll
     for (int j = 0; j < KK; ++j) w[j] = sm.cw[it][j];
 #pragma unroll
-    for (int j = 1; j < KK; ++j) xs[j] = ldv(&vb.halo[3 - KK + j][seg][ch]);  // rows j - KK .. -1
-    for (int t = 0; t < nr; ++t) {
+    for (int j = 0; j + 1 < KK; ++j) xs[j] = ldv(&vb.halo[4 - KK + j][seg][ch]);
 #pragma unroll
-        for (int j = 0; j + 1 < KK; ++j) xs[j] = xs[j + 1];
-        xs[KK - 1] = ldv(&vb.rows[t][seg][ch]);
+    for (int t = 0; t < VWB; ++t) xs[KK - 1 + t] = ldv(&vb.rows[t][seg][ch]);
+    float x[VWB];
+#pragma unroll
+    for (int t = 0; t < VWB; ++t) {
         float accv = 0.0f;
 #pragma unroll
-        for (int j = 0; j < KK; ++j) accv = __fmaf_rn(w[j], xs[j], accv);
-        const float x = siluf_(accv);
-        if (seg == 2) {
-            sm.vp[t][ch] = x;
-        } else {  // warp-uniform: a warp holds 32 consecutive q or k channels
-            (seg == 0 ? sm.qp : sm.kp)[t][vw_pad(ch)] = x;
-            const float ss = warp_sum(x * x);
-            if (lane == 0) sm.nrm[t][it >> 5] = ss;
+        for (int j = 0; j < KK; ++j) accv = __fmaf_rn(w[j], xs[t + j], accv);
+        x[t] = siluf_(accv);
+    }
+    if (seg == 2) {
+#pragma unroll
+        for (int t = 0; t < VWB; ++t)
+            if (t < nr) sm.vp[t][ch] = x[t];
+    } else {  // warp-uniform: a warp holds 32 consecutive q or k channels
+        float(*dst)[VWP] = seg == 0 ? sm.qp : sm.kp;
+        float ss[VWB];
+#pragma unroll
+        for (int t = 0; t < VWB; ++t) ss[t] = warp_sum(x[t] * x[t]);
+#pragma unroll
+        for (int t = 0; t < VWB; ++t) {
+            if (t < nr) {
+                dst[t][vw_pad(ch)] = x[t];
+                if (lane == 0) sm.nrm[t][it >> 5] = ss[t];
+            }
         }
     }
 }
@@ -528,8 +542,12 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_verify_warp_kernel(const R
         } else {
             const int i = tid - D;
             const float dti = sm.dtb[i];
-            for (int t = 0; t < nr; ++t)
-                sm.ap[t][vw_pad(i)] = __expf(log_alpha(rc.gate_mode, rc.lb, rc.ea, ldv(&vb.rows[t][3][i]), dti));
+            float al[VWB];  // all rows of the block at once, as in the conv
+#pragma unroll
+            for (int t = 0; t < VWB; ++t) al[t] = __expf(log_alpha(rc.gate_mode, rc.lb, rc.ea, ldv(&vb.rows[t][3][i]), dti));
+#pragma unroll
+            for (int t = 0; t < VWB; ++t)
+                if (t < nr) sm.ap[t][vw_pad(i)] = al[t];
         }
         __syncthreads();
         if (tid < nr) {  // the register kernel's norms and beta of row tid
