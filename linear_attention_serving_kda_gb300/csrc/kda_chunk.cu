@@ -507,7 +507,7 @@ __device__ __forceinline__ float chunk_softplus_decay(float ea, float f, float d
 {
     // explicit roundings: the same bits at every call site
     const float x = __fadd_rn(f, dt);
-    const float y = __expf(-fabsf(x));
+    const float y = exp_sfu(-fabsf(x));
     float p = __fmaf_rn(-0.25f, y, 0.33333334f);
     p = __fmaf_rn(-y, p, 0.5f);
     p = __fmaf_rn(-y, p, 1.0f);
@@ -618,18 +618,18 @@ __device__ __forceinline__ int chunk_prep(unsigned char* sm, Misc& ms, const Chu
                 av = __ffma2_rn(make_float2(wv[j], wv[j]), make_float2(xv[j], xv[j + 1]), av);
             }
             // SiLU: x / (1 + e^-x); the gate: lb * sigmoid(ea (f + dt))
-            const float2 dq = __fadd2_rn(one2, make_float2(__expf(-aq.x), __expf(-aq.y)));
-            const float2 dk = __fadd2_rn(one2, make_float2(__expf(-ak.x), __expf(-ak.y)));
-            const float2 dv = __fadd2_rn(one2, make_float2(__expf(-av.x), __expf(-av.y)));
-            const float2 sq = __fmul2_rn(aq, make_float2(__fdividef(1.0f, dq.x), __fdividef(1.0f, dq.y)));
-            const float2 sk = __fmul2_rn(ak, make_float2(__fdividef(1.0f, dk.x), __fdividef(1.0f, dk.y)));
-            const float2 sv = __fmul2_rn(av, make_float2(__fdividef(1.0f, dv.x), __fdividef(1.0f, dv.y)));
+            const float2 dq = __fadd2_rn(one2, make_float2(exp_sfu(-aq.x), exp_sfu(-aq.y)));
+            const float2 dk = __fadd2_rn(one2, make_float2(exp_sfu(-ak.x), exp_sfu(-ak.y)));
+            const float2 dv = __fadd2_rn(one2, make_float2(exp_sfu(-av.x), exp_sfu(-av.y)));
+            const float2 sq = __fmul2_rn(aq, make_float2(rcp_sfu(dq.x), rcp_sfu(dq.y)));
+            const float2 sk = __fmul2_rn(ak, make_float2(rcp_sfu(dk.x), rcp_sfu(dk.y)));
+            const float2 sv = __fmul2_rn(av, make_float2(rcp_sfu(dv.x), rcp_sfu(dv.y)));
             float2 la;
             if (!sp) {
                 const float f0 = __bfloat162float(rawf[lr * D + col]), f1 = __bfloat162float(rawf[(lr + 1) * D + col]);
                 const float2 fz = __fmul2_rn(ea2, __fadd2_rn(make_float2(f0, f1), dt2));
-                const float2 gd = __fadd2_rn(one2, make_float2(__expf(-fz.x), __expf(-fz.y)));
-                la = __fmul2_rn(lb2, make_float2(__fdividef(1.0f, gd.x), __fdividef(1.0f, gd.y)));
+                const float2 gd = __fadd2_rn(one2, make_float2(exp_sfu(-fz.x), exp_sfu(-fz.y)));
+                la = __fmul2_rn(lb2, make_float2(rcp_sfu(gd.x), rcp_sfu(gd.y)));
             } else {
                 la = make_float2(lsc[lr * D + col], lsc[(lr + 1) * D + col]);
             }
@@ -708,7 +708,7 @@ __device__ __forceinline__ bool chunk_rest(unsigned char* sm, Misc& ms, const Ch
     const int lq = warp & 3;
     const int r0 = RPT * qq;
     (void)lq;
-    if (qq == 3) ms.gamma[col] = __expf(G[RPT - 1]);  // e^{G_C}; read after later block barriers
+    if (qq == 3) ms.gamma[col] = exp_sfu(G[RPT - 1]);  // e^{G_C}; read after later block barriers
     // ---- operands of the first and second products; q^ e^G and k^ e^{G_C - G}
     // are formed here too and kept in registers until their tiles are free
     const float Gm = ms.gx[half][col];   // reference row 16 (first half) or 48 (second half)
@@ -722,8 +722,8 @@ __device__ __forceinline__ bool chunk_rest(unsigned char* sm, Misc& ms, const Ch
         // of per-half code paths
         const float Gx = half == 0 ? Gm1 : Gm;
         const int xrow = half == 0 ? 64 : 0;
-        const float eGm = __expf(Gm);          // first half: e^{G_16} >= e^{-85}
-        const float cGC = __expf(GC - Gm);     // second half: e^{G_63 - G_48} >= e^{-75}
+        const float eGm = exp_sfu(Gm);          // first half: e^{G_16} >= e^{-85}
+        const float cGC = exp_sfu(GC - Gm);     // second half: e^{G_63 - G_48} >= e^{-75}
         float xt[RPT], yt[RPT], yl[RPT];
         // two rows at a time in packed f32x2 arithmetic; the exponentials, TF32
         // roundings and the stores (one address per element) stay per element
@@ -737,8 +737,8 @@ __device__ __forceinline__ bool chunk_rest(unsigned char* sm, Misc& ms, const Ch
         for (int r = 0; r < RPT; r += 2) {
             const int rr = r0 + r;
             const float2 dg = __fadd2_rn(make_float2(G[r], G[r + 1]), mGm2);  // G - Gm
-            const float2 e = make_float2(__expf(dg.x), __expf(dg.y));
-            const float2 ie = make_float2(__expf(-dg.x), __expf(-dg.y));
+            const float2 e = make_float2(exp_sfu(dg.x), exp_sfu(dg.y));
+            const float2 ie = make_float2(exp_sfu(-dg.x), exp_sfu(-dg.y));
             const float2 k2 = make_float2(kv[r], kv[r + 1]), q2 = make_float2(qv[r], qv[r + 1]);
             const float2 ke = __fmul2_rn(k2, e), qe2 = __fmul2_rn(q2, e), kie = __fmul2_rn(k2, ie);
             const float2 qel = lo2(qe2), kiel = lo2(kie);
@@ -761,12 +761,12 @@ __device__ __forceinline__ bool chunk_rest(unsigned char* sm, Misc& ms, const Ch
             // the second.  (half is uniform over a warp: one side runs.)
             float2 cross, eG, edec;
             if (half == 0) {
-                cross = make_float2(__expf(Gx - G[r]), __expf(Gx - G[r + 1]));
+                cross = make_float2(exp_sfu(Gx - G[r]), exp_sfu(Gx - G[r + 1]));
                 eG = __fmul2_rn(e, eGm2);
-                edec = make_float2(__expf(GC - G[r]), __expf(GC - G[r + 1]));
+                edec = make_float2(exp_sfu(GC - G[r]), exp_sfu(GC - G[r + 1]));
             } else {
                 cross = ie;
-                eG = make_float2(__expf(G[r]), __expf(G[r + 1]));
+                eG = make_float2(exp_sfu(G[r]), exp_sfu(G[r + 1]));
                 edec = __fmul2_rn(ie, cGC2);
             }
             const float2 kc = __fmul2_rn(k2, cross), kcl = lo2(kc);
@@ -1754,7 +1754,7 @@ __device__ __forceinline__ int bounds_chunk(Misc& ms, const ChunkArgs& a, int c0
             const float f = __bfloat162float(fr[r]);
             if (a.gate_mode == KDA_GATE_SAFE) {  // the prep's lb * sigmoid(ea (f + dt)), operation by operation
                 const float fz = __fmul_rn(ea, __fadd_rn(f, dtc));
-                la = __fmul_rn(a.lb, __fdividef(1.0f, __fadd_rn(1.0f, __expf(-fz))));
+                la = __fmul_rn(a.lb, rcp_sfu(__fadd_rn(1.0f, exp_sfu(-fz))));
             } else {
                 la = chunk_softplus_decay(ea, f, dtc);
             }

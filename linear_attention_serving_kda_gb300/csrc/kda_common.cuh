@@ -40,13 +40,30 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float x, int ou
 // The same expressions are used by decode, verify and commit so that a
 // verified row has the bits of the serially decoded one.
 
-__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+// e^x as 2^(x log2 e) on the special-function unit (PTX ex2.approx.ftz: a
+// few ulp; inputs below about -87 give 0, the subnormal results flushed), and
+// 1/x by rcp.approx.ftz: one multiply and one SFU instruction each, with no
+// range handling around them.
+__device__ __forceinline__ float exp_sfu(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(__fmul_rn(x, 1.44269504088896341f)));
+    return y;
+}
+__device__ __forceinline__ float rcp_sfu(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
-__device__ __forceinline__ float siluf_(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float sigmoidf_(float x) { return rcp_sfu(__fadd_rn(1.0f, exp_sfu(-x))); }
+
+__device__ __forceinline__ float siluf_(float x) { return __fmul_rn(x, rcp_sfu(__fadd_rn(1.0f, exp_sfu(-x)))); }
 
 // softplus(x) = log(1 + e^x); above 20 the correction e^-x is below fp32
 // resolution of x.
-__device__ __forceinline__ float softplusf_(float x) { return x > 20.0f ? x : log1pf(__expf(x)); }
+__device__ __forceinline__ float softplusf_(float x) { return x > 20.0f ? x : log1pf(exp_sfu(x)); }
 
 // Per-key-dim log decay.  ea = exp(A_log_h).
 __device__ __forceinline__ float log_alpha(int gate_mode, float lb, float ea, float f, float dt)

@@ -544,7 +544,7 @@ __global__ void __launch_bounds__(REC_THREADS, 2) kda_verify_warp_kernel(const R
             const float dti = sm.dtb[i];
             float al[VWB];  // all rows of the block at once, as in the conv
 #pragma unroll
-            for (int t = 0; t < VWB; ++t) al[t] = __expf(log_alpha(rc.gate_mode, rc.lb, rc.ea, ldv(&vb.rows[t][3][i]), dti));
+            for (int t = 0; t < VWB; ++t) al[t] = exp_sfu(log_alpha(rc.gate_mode, rc.lb, rc.ea, ldv(&vb.rows[t][3][i]), dti));
 #pragma unroll
             for (int t = 0; t < VWB; ++t)
                 if (t < nr) sm.ap[t][vw_pad(i)] = al[t];

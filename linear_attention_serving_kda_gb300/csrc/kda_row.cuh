@@ -156,7 +156,7 @@ __device__ __forceinline__ void row_conv(RowSmem<D>& sm, int K, const RowConst& 
             }
         } else {
             const int i = it - 3 * D;
-            sm.alpha[i] = __expf(log_alpha(rc.gate_mode, rc.lb, rc.ea, fr(i), sm.dtb[i]));
+            sm.alpha[i] = exp_sfu(log_alpha(rc.gate_mode, rc.lb, rc.ea, fr(i), sm.dtb[i]));
         }
     }
     row_sync();
