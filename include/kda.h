@@ -218,6 +218,25 @@ KDA_API int kda_debug_split_chains_only(const kda_params* p, const int32_t* cu_s
                                         cudaStream_t stream);
 
 /*
+ * Test hook for the device activations every kernel shares (no counterpart
+ * on the source pages; the pages name the functions, not their arithmetic):
+ * y[i] = f(x[i]) for i < n, with f by `which`:
+ *   KDA_ACT_EXP     e^x (on the special-function unit's base-2 exponential)
+ *   KDA_ACT_RCP     1/x
+ *   KDA_ACT_SIGMOID 1/(1 + e^-x)   (beta, the safe gate, the output gate)
+ *   KDA_ACT_SILU    x/(1 + e^-x)   (after the causal conv)
+ * x and y are device arrays of n floats (n >= 0; they may alias), 16-byte
+ * aligned.  Returns KDA_ERR_INVALID_ARGUMENT for an unknown `which`, n < 0,
+ * or (n > 0) a null or misaligned pointer, all before any launch;
+ * KDA_ERR_LAUNCH if the launch fails.
+ */
+#define KDA_ACT_EXP 0
+#define KDA_ACT_RCP 1
+#define KDA_ACT_SIGMOID 2
+#define KDA_ACT_SILU 3
+KDA_API int kda_debug_activations(int32_t which, const float* x, float* y, int32_t n, cudaStream_t stream);
+
+/*
  * Decode: one row per sequence, B sequences (row b belongs to sequence b).
  * Updates the conv and recurrent states in place and writes out [B][H][dv]
  * (TensorFold #850, Oct 15 comment: decode rows).

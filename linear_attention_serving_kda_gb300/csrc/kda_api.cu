@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstring>
 
+#include "kda_common.cuh"
 #include "kda_internal.h"
 
 namespace {
@@ -283,6 +284,30 @@ KDA_API int kda_debug_split_chains_only(const kda_params* p, const int32_t* cu_s
     if (!(p->gate_mode == KDA_GATE_SAFE && p->gate_lower_bound >= -5.0f)) return KDA_ERR_INVALID_ARGUMENT;
     return prefill_varlen_impl(p, cu_seqlens, N, T, q, k, v, gate, beta, out_gate, slots, conv_state, rec_state,
                                out, workspace, ws_bytes, dev_status, stream, true, poll_limit);
+}
+
+namespace {
+__global__ void activations_kernel(int which, const float* x, float* y, int n)
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const float v = x[i];
+        y[i] = which == KDA_ACT_EXP ? kda::exp_sfu(v)
+             : which == KDA_ACT_RCP ? kda::rcp_sfu(v)
+             : which == KDA_ACT_SIGMOID ? kda::sigmoidf_(v)
+             : kda::siluf_(v);
+    }
+}
+}  // namespace
+
+KDA_API int kda_debug_activations(int32_t which, const float* x, float* y, int32_t n, cudaStream_t stream)
+{
+    if (which < KDA_ACT_EXP || which > KDA_ACT_SILU || n < 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (n == 0) return KDA_OK;
+    int rc = check_ptrs({x, y});
+    if (rc != KDA_OK) return rc;
+    if ((rc = check_device()) != KDA_OK) return rc;
+    activations_kernel<<<(n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024, 256, 0, stream>>>(which, x, y, n);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
 KDA_API int kda_decode(const kda_params* p, int32_t B, const void* q, const void* k,

@@ -26,6 +26,10 @@ KDA_DEV_BAD_SEQLENS = 1
 KDA_DEV_BAD_SLOT = 2
 KDA_DEV_BAD_ACCEPTED = 4
 KDA_DEV_TIMEOUT = 8
+KDA_ACT_EXP = 0
+KDA_ACT_RCP = 1
+KDA_ACT_SIGMOID = 2
+KDA_ACT_SILU = 3
 KDA_DTYPE_F32 = 0
 KDA_DTYPE_BF16 = 1
 KDA_GATE_SOFTPLUS = 0
@@ -60,6 +64,7 @@ _SIG = {
     "kda_debug_split_chains_only": (ctypes.c_int, [ctypes.POINTER(kda_params), _VP, _I32, _I32, _VP, _VP, _VP,
                                                    _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t,
                                                    _VP, ctypes.c_uint32, _VP]),
+    "kda_debug_activations": (ctypes.c_int, [_I32, _VP, _VP, _I32, _VP]),
     "kda_decode": (ctypes.c_int, [ctypes.POINTER(kda_params), _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                   _VP, _VP, _VP, _VP, _VP]),
     "kda_verify_window": (ctypes.c_int, [ctypes.POINTER(kda_params), _I32, _I32, _VP, _VP, _VP, _VP, _VP,
@@ -207,6 +212,12 @@ def kda_debug_split_chains_only(params: Params, cu_seqlens, N: int, T: int, q, k
         ctypes.byref(params.c_struct()), _ptr(cu_seqlens), N, T, _ptr(q), _ptr(k), _ptr(v), _ptr(gate),
         _ptr(beta), _ptr(out_gate), _ptr(slots), _ptr(conv_state), _ptr(rec_state), _ptr(out),
         _ptr(workspace), ws_bytes, _ptr(dev_status), poll_limit, _stream(stream))
+
+
+def kda_debug_activations(which: int, x, y, n: int, stream=None) -> int:
+    """Test hook: y[i] = f(x[i]) with the kernels' shared activation f
+    (KDA_ACT_EXP, KDA_ACT_RCP, KDA_ACT_SIGMOID, KDA_ACT_SILU)."""
+    return load().kda_debug_activations(which, _ptr(x), _ptr(y), n, _stream(stream))
 
 
 def kda_prefill_static_workspace_capacity() -> int:

@@ -73,11 +73,13 @@ def test_params_rejected_before_launch(lib, kw, rc):
 
 
 def test_bound_checked_only_in_safe_mode(lib):
-    # a positive bound is irrelevant to the softplus gate: validation passes and
-    # the call only fails later at the device check (no GPU here)
+    # a positive bound is irrelevant to the softplus gate: the parameters pass
+    # validation and the call fails only at the pointer check that follows
+    # (a null q row pointer) -- before any launch, so the placeholder
+    # addresses are never handed to a kernel, with or without a GPU
     p = _params(gate_mode=kda.KDA_GATE_SOFTPLUS, gate_lower_bound=3.0)
-    assert _decode(p) in (kda.KDA_ERR_DEVICE, kda.KDA_OK, kda.KDA_ERR_LAUNCH)
-    assert _decode(_params(gate_lower_bound=3.0)) == kda.KDA_ERR_INVALID_BOUND
+    assert _decode(p, q=None) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert _decode(_params(gate_lower_bound=3.0), q=None) == kda.KDA_ERR_INVALID_BOUND
 
 
 def test_pointer_checks(lib):
@@ -101,6 +103,12 @@ def test_pointer_checks(lib):
         assert kda.kda_commit_verify(p, 2, 4, *args.values(), None, 0) == kda.KDA_ERR_INVALID_ARGUMENT, over
     assert kda.kda_commit_verify(p, 0, 4, *([None] * 13), None, 0) == kda.KDA_OK  # empty batch: no-op
     assert kda.kda_commit_verify(p, -1, 4, *cv.values(), None, 0) == kda.KDA_ERR_INVALID_ARGUMENT
+    # activation hook: unknown function, negative size, null or misaligned arrays; empty is a no-op
+    assert kda.kda_debug_activations(4, FAKE, FAKE, 8, 0) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert kda.kda_debug_activations(kda.KDA_ACT_EXP, FAKE, FAKE, -1, 0) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert kda.kda_debug_activations(kda.KDA_ACT_SILU, None, FAKE, 8, 0) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert kda.kda_debug_activations(kda.KDA_ACT_SILU, FAKE, FAKE + 4, 8, 0) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert kda.kda_debug_activations(kda.KDA_ACT_RCP, None, None, 0, 0) == kda.KDA_OK
 
 
 def test_sizes(lib):
