@@ -195,7 +195,7 @@ def make_sets(wl_fn, n_sets, out_dtype):
 
     sets = []
     wl = wl_fn()
-    for i in range(n_sets):
+    for _ in range(n_sets):
         sets.append(DeviceCase(wl, out_dtype=out_dtype))
     return wl, sets
 
@@ -564,7 +564,6 @@ def e2e_prefill_pipelined(kda, wl_fn, pieces, reps, stream):
         torch.cuda.synchronize()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(up)
-        done = []
         for i, (dc, (host, dev, _)) in enumerate(zip(cases, packs)):
             ev_up, ev_done = torch.cuda.Event(), torch.cuda.Event()
             with torch.cuda.stream(up):
@@ -577,7 +576,6 @@ def e2e_prefill_pipelined(kda, wl_fn, pieces, reps, stream):
             with torch.cuda.stream(down):
                 down.wait_event(ev_done)
                 outs[i].copy_(dc.out[:dc.wl.T], non_blocking=True)
-            done.append(ev_done)
         t1.record(down)
         torch.cuda.synchronize()
         if r:
@@ -789,7 +787,7 @@ def main():
         dist.barrier()
     kda.load()
     stream = torch.cuda.current_stream()  # every launch and every event goes on this stream
-    hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = load_peaks()
+    hbm_gbs, _, _, peak_src = load_peaks()
     sampler = ClockSampler(local_rank).start() if rank == 0 else None
 
     if args.workload != "decode":
@@ -803,7 +801,7 @@ def main():
     with nvtx_range("decode warm-up"):
         wl, sets, step, per_set = bench_decode(kda, args.steps, args.warmup, stream)
     with nvtx_range("decode timed"):
-        total_ms, durs, wall = run_timed(step, args.steps, stream, dist)
+        total_ms, durs, _ = run_timed(step, args.steps, stream, dist)
     ms = total_ms / args.steps
     value = weak_scaling_value(wl.N, world, args.steps, total_ms)
     kernel_ms = statistics.mean(durs)

@@ -131,7 +131,6 @@ class DeviceCase:
     def decode(self, rows=None, stream=None) -> int:
         """One decode row per sequence; rows selects the row tensors'
         slice (default: the workload's own B rows)."""
-        wl = self.wl
         sl = slice(None) if rows is None else rows
         q, k, v, f, b = self.q[sl], self.k[sl], self.v[sl], self.f[sl], self.b[sl]
         g = None if self.g is None else self.g[sl]
