@@ -635,6 +635,25 @@ def oracle_decode_rate(seconds=10.0):
     return wl.N * steps / el, cores, steps, el
 
 
+def oracle_decode_rate_1thread(seconds=1.0):
+    """The oracle on one thread: all heads of one sequence's decode row,
+    repeated for about `seconds`; tokens/s = rows (all heads) per second."""
+    import oracle
+    from linear_attention_serving_kda_gb300 import shard, workloads as W
+
+    oracle.build()
+    one = shard.shard_workload(W.decode_case(), [0])  # sequence 0: its row, states and the parameters
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.forward(one, threads=1)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return n / el, n, el
+
+
 def oracle_units_rate(wl, units, rows, threads):
     """Row-heads per second of the oracle (as it stands) over the given
     (sequence, head) units of a workload, each cut to its first `rows` rows
@@ -836,8 +855,10 @@ def main():
     cpu = None
     if rank == 0 and world == 1:
         rate, cores, n, el = oracle_decode_rate(args.cpu_seconds)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"full decode step (64 seq x 32 heads) repeated {n}x with carried state, {el:.1f} s"}
+        rate1, n1, el1 = oracle_decode_rate_1thread(max(0.1, args.cpu_seconds / 10))
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "value_1thread": rate1,
+               "sample": f"full decode step (64 seq x 32 heads) repeated {n}x with carried state, {el:.1f} s; "
+                         f"1 thread: one sequence's row through all 32 heads x {n1} in {el1:.2f} s"}
 
     if rank == 0 and world == 1 and legs and args.cpu_seconds > 0:
         from linear_attention_serving_kda_gb300 import workloads as W
