@@ -841,12 +841,12 @@ def main():
         for k in ("prefill_varlen", "prefill_long"):
             legs[k]["hbm_frac"] = legs[k]["achieved_gbs"] / hbm_gbs
         with nvtx_range("legs end to end"):
-            legs["prefill_varlen"]["e2e"] = e2e_prefill(kda, W.varlen_prefill_case, 3, stream)
-            legs["prefill_long"]["e2e"] = e2e_prefill(kda, W.long_prefill_case, 3, stream)
+            legs["prefill_varlen"]["e2e"] = e2e_prefill(kda, W.varlen_prefill_case, 5, stream)
+            legs["prefill_long"]["e2e"] = e2e_prefill(kda, W.long_prefill_case, 5, stream)
             legs["verify_commit"]["e2e"] = e2e_verify(kda, 10, stream)
-            legs["prefill_varlen"]["e2e_pipelined"] = e2e_prefill_pipelined(kda, W.varlen_prefill_case, 8, 3,
+            legs["prefill_varlen"]["e2e_pipelined"] = e2e_prefill_pipelined(kda, W.varlen_prefill_case, 8, 5,
                                                                             stream)
-            legs["prefill_long"]["e2e_pipelined"] = e2e_prefill_pipelined(kda, W.long_prefill_case, 16, 3, stream)
+            legs["prefill_long"]["e2e_pipelined"] = e2e_prefill_pipelined(kda, W.long_prefill_case, 16, 5, stream)
     with nvtx_range("decode end to end"):
         e2e = e2e_decode(kda, args.steps, args.warmup, stream)
     e2e["value"] *= world
