@@ -1250,6 +1250,8 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
         {
             float qv[RPT], kv[RPT], vv[RPT], G[RPT];
             n = chunk_prep<UNB>(sm, ms, a, tc, nvalid, qv, kv, vv, G, xfer);
+            // the next chunk's beta logits: loaded now, used a chunk later
+            if (tid < C && c0 + n + tid < seg1) bnext = __bfloat162float(bg[(size_t)(c0 + n + tid) * H + h]);
             if (UNB && c0 + n == seg1) {
                 store_conv_state(n);  // the staged rows are still intact: read before the operands overwrite them
                 __syncthreads();
@@ -1261,7 +1263,6 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
         if (c0 + n < seg1) {
             if (tid == 0) stage_chunk(sm, maps, ms, c0 + n, h);
             rpending = true;
-            if (tid < C && c0 + n + tid < seg1) bnext = __bfloat162float(bg[(size_t)(c0 + n + tid) * H + h]);
         }
 
         // ---- -W tile from W^T as bf16 high and low parts (lane i = col, rows [16 qq, +16));
