@@ -133,6 +133,8 @@ size_t prefill_workspace_bytes(const kda_params* p, int32_t N, int32_t T, bool a
         // chunk) after the ring
         if (!(p->gate_mode == KDA_GATE_SAFE && p->gate_lower_bound >= -5.0f))
             b += align1024((size_t)N * p->num_heads * ((size_t)T + 3) * sizeof(int32_t));
+        // the chains' outputs before the epilogue: fp32 [T][H][dv]
+        b += align1024((size_t)T * p->num_heads * p->head_dim_v * sizeof(float));
         return b;
     }
     return sched;

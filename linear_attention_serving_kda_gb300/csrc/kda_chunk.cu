@@ -279,6 +279,11 @@ struct Bf16Tmem {
 // columns (S^T pairs over the dead Y^T / Ylo^T, U^T pairs after U^T)
 constexpr uint32_t TM_SH = 192, TM_SL16 = 256, TM_UH = 448, TM_UL16 = 480;
 constexpr Bf16Tiles FUSED_TILES{SM_KDL, SM_KDL + 16384, SM_QE, SM_QE + 16384, SM_PH, SM_PH + 8192, SM_KD, SM_KD + 16384};
+// the split path's producers publish these tiles while the next task's rows
+// are staged below them
+static_assert(RAW_END <= FUSED_TILES.ph && RAW_END <= FUSED_TILES.qeh && RAW_END <= FUSED_TILES.kdh &&
+                  RAW_END <= FUSED_TILES.nwh,
+              "published tiles overlap the raw-row staging region");
 constexpr Bf16Tmem FUSED_TMEM{TM_ST, TM_SH, TM_SL16, TM_UT, TM_UH, TM_UL16};
 static_assert(SM_KDL % 1024 == 0 && SM_QE % 1024 == 0 && SM_PH % 1024 == 0 && SM_KD % 1024 == 0,
               "bf16 tiles need 1 KiB-aligned bases");
@@ -1041,10 +1046,17 @@ __device__ __forceinline__ void gate_bits_from_words(uint32_t (&gp)[RPT / 2], co
 // then syncs the block.  Part B needs no block barrier: lanes 0..15 of every
 // warp form the inverse RMS of the quarter's 16 rows from the four partials
 // (the same sum in the same order in every warp) and the warp reads them back.
+__device__ __forceinline__ void outputs_a_regs(Misc& ms, const ChunkArgs& a, float (&o)[RPT]);
 __device__ __forceinline__ void write_outputs_a(Misc& ms, const ChunkArgs& a, uint32_t t_ot, float (&o)[RPT])
 {
-    const int tid = threadIdx.x, lane = tid & 31, lq = (tid >> 5) & 3, qq = tid >> 7;
     ptx::tmem_ld16(t_ot, o);
+    outputs_a_regs(ms, a, o);
+}
+
+// part A on this thread's 16 rows of O already in registers
+__device__ __forceinline__ void outputs_a_regs(Misc& ms, const ChunkArgs& a, float (&o)[RPT])
+{
+    const int tid = threadIdx.x, lane = tid & 31, lq = (tid >> 5) & 3, qq = tid >> 7;
     const float2 sc2 = make_float2(a.scale, a.scale);
 #pragma unroll
     for (int x = 0; x < RPT; x += 2) {
@@ -1368,6 +1380,7 @@ struct SplitArgs {
     const int* bnd;
     int bs;
     uint32_t flag_polls;   // limit of every flag wait (polls with back-off)
+    float* raw_o;          // [T][H][D]: the chains' outputs before scale, norm and gate
 };
 
 // chain u's number of chunks, and chunk c's first row and row count (UNB:
@@ -1431,6 +1444,23 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
     int cur_h = -1;
     ThreadConst tc;
     const __nv_bfloat16* bg = static_cast<const __nv_bfloat16*>(a.b);
+    // The bulk copies that publish a task run on while the next task's rows
+    // are staged and its prep runs (the staging region and the prep's
+    // scratch lie below the published tiles); thread 0 completes them and
+    // releases the slot's flag before the operand build overwrites the tiles
+    // -- or at once, if the next task's slot is still taken (its chain may be
+    // waiting for this very publication).
+    int pend = -1;  // thread 0: the ready-flag index of a publication in flight, -1 none
+    int pend_v = 0;
+    auto complete_pending = [&]() {
+        if (pend >= 0) {
+            ptx::bulk_wait_all();
+            ptx::fence_proxy_async_global();
+            __threadfence();
+            ptx::st_release_gpu(&sp.ready[pend], pend_v);
+            pend = -1;
+        }
+    };
     for (int t = p; t < maxc * NC && !ms.err; t += NP) {
         const int c = t / NC, u = t % NC, h = u % H;
         int slot, seg0, seg1;
@@ -1444,12 +1474,14 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
         }
         if (tid == 0) {
             // the slot is free once the chain has read chunk c - SPLIT_RING
-            if (c >= SPLIT_RING && !ptx::wait_flag_ge(&sp.consumed[u], c - SPLIT_RING + 1, sp.flag_polls)) {
-                ms.err = 1;
-                flag_status(a.dev_status, KDA_DEV_TIMEOUT);
-            } else {
-                stage_chunk(sm, maps, ms, c0, h);
+            if (c >= SPLIT_RING && ptx::ld_acquire_gpu(&sp.consumed[u]) < c - SPLIT_RING + 1) {
+                complete_pending();
+                if (!ptx::wait_flag_ge(&sp.consumed[u], c - SPLIT_RING + 1, sp.flag_polls)) {
+                    ms.err = 1;
+                    flag_status(a.dev_status, KDA_DEV_TIMEOUT);
+                }
             }
+            if (!ms.err) stage_chunk(sm, maps, ms, c0, h);
         }
         if (tid < C) ms.beta[tid] = tid < nvalid ? sigmoidf_(__bfloat162float(bg[(size_t)(c0 + tid) * H + h])) : 0.0f;
         __syncthreads();
@@ -1459,7 +1491,15 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
             patch_halo(sm, a, slot, h, c0 - seg0);
             __syncthreads();
         }
-        if (!chunk_intra<UNB>(sm, ms, a, tc, nvalid, tmem, lane_base, ph)) break;
+        float qv[RPT], kv[RPT], vv[RPT], G[RPT];
+        if (UNB) {  // the softplus prep writes a scratch over a published tile: the copies must have read it
+            if (tid == 0) complete_pending();
+            __syncthreads();
+        }
+        chunk_prep<UNB, false>(sm, ms, a, tc, nvalid, qv, kv, vv, G);
+        if (tid == 0) complete_pending();
+        __syncthreads();  // the published tiles are read: the operand build may overwrite them
+        if (!chunk_rest(sm, ms, a, nvalid, tmem, lane_base, ph, qv, kv, vv, G)) break;
 
         // publish: the chain's operands as the bf16 high and low tiles
         // chunk_intra built (and -W from W^T), by bulk copies; U'^T and e^{G_C}
@@ -1484,15 +1524,14 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
             ptx::bulk_s2g(dst + SL_PH, sm + FUSED_TILES.ph, 16384);    // P high, low
             ptx::bulk_s2g(dst + SL_KDH, sm + FUSED_TILES.kdh, 32768);  // (K o e^{G_C - G})^T high, low
             ptx::bulk_commit();
-            ptx::bulk_wait_all();
-            ptx::fence_proxy_async_global();
-            __threadfence();
-            ptx::st_release_gpu(&sp.ready[u * SPLIT_RING + c % SPLIT_RING], c + 1);
+            pend = u * SPLIT_RING + c % SPLIT_RING;  // completed and released during the next task
+            pend_v = c + 1;
         }
         ptx::tc_fence_before();
         __syncthreads();
         ptx::tc_fence_after();
     }
+    if (tid == 0) complete_pending();  // the last publication (or one cut short by an error)
     (void)rph;
 }
 
@@ -1513,7 +1552,6 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
     const uint32_t lane_base = (uint32_t)(lq * 32) << 16;
     const int H = a.H, K = a.K, h = u % H, r0 = RPT * qq;
     const int nchunks = split_nchunks<UNB>(sp, u, seg0, seg1);
-    const float nw = a.norm_w ? a.norm_w[col] : 1.0f;
     uint32_t ph = 0;
     bool pend_a = false, pend_b = false;
 
@@ -1548,11 +1586,19 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         if (tid < D) gam = reinterpret_cast<const float*>(src + SL_GAM)[tid];
     };
 
-    // The outputs of chunk c are formed while the products of chunk c + 1 run
-    // (O^T alternates between two TMEM column blocks): O^T is read and the norm
-    // partials formed while the third product runs, the norm and the stores
-    // while the fourth runs, whose issuers have half the MMAs.  Chunk c + 1's
-    // slot is acquired and its U'^T loaded during the third product too.
+    // The outputs of chunk c leave while the third product of chunk c + 1 runs
+    // (O^T alternates between two TMEM column blocks), as they come from the
+    // products: scale, gated norm and the final stores are the epilogue
+    // kernel's, off the chain.  Chunk c + 1's slot is acquired and its U'^T
+    // loaded during the third product too.
+    auto store_raw = [&](uint32_t t_ot, int cc0, int cnv) {
+        float o[RPT];
+        ptx::tmem_ld16(t_ot, o);
+        float* dst = sp.raw_o + ((size_t)(cc0 + r0) * H + h) * D + col;
+#pragma unroll
+        for (int x = 0; x < RPT; ++x)
+            if (r0 + x < cnv) dst[(size_t)x * H * D] = o[x];
+    };
     bool mma_pending = false;
     acquire_by(0, 0);
     __syncthreads();
@@ -1565,17 +1611,8 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         pend_a = pend_b = true;
         load_ut(0);
     }
-    uint32_t gp[RPT / 2];   // output gate of the chunk whose outputs are pending (bf16 bits, 2 per register)
     int prev_c0 = 0, prev_nvalid = 0;
     bool have_prev = false;
-    // output gate rows of a chunk, loaded one chunk ahead and unpacked after its products
-    uint32_t gw[RPT / 2];
-    auto load_gate = [&](int c) {
-        int cc0, cnv;
-        split_chunk<UNB>(sp, u, c, seg0, seg1, cc0, cnv);
-        load_gate_words(gw, a, cc0, r0, cnv, h, col);
-    };
-    load_gate(0);
     for (int c = 0; c < nchunks && !ms.err; ++c) {
         int c0, nvalid;
         split_chunk<UNB>(sp, u, c, seg0, seg1, c0, nvalid);
@@ -1600,8 +1637,10 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
         // while the third product runs: the previous chunk's O^T and norm
         // partials (the barrier of the wait below orders them before part B),
         // chunk c + 1's slot and U'^T
-        float o[RPT];
-        if (have_prev) write_outputs_a(ms, a, tmem + lane_base + (c_ot ^ (CT_OT0 ^ CT_OT1)) + RPT * qq, o);
+        if (have_prev) {
+            store_raw(tmem + lane_base + (c_ot ^ (CT_OT0 ^ CT_OT1)) + RPT * qq, prev_c0, prev_nvalid);
+            have_prev = false;
+        }
         if (c + 1 < nchunks) acquire_by(c + 1, 128);
         __syncthreads();
         if (ms.err) break;
@@ -1633,14 +1672,6 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
             issue_fourth16<CHAIN_UNROLL>(sm, tmem, issuer(tid), CHAIN_TILES, CHAIN_TMEM, c_ot, &ms.bar);
         }
         mma_pending = true;
-        // while the fourth product runs: the rest of the previous chunk's outputs
-        // (warp-local), then chunk c's output gate
-        if (have_prev) {
-            write_outputs_b(ms, a, o, gp, prev_c0, prev_nvalid, h, nw, a.out);
-            have_prev = false;
-        }
-        gate_bits_from_words(gp, gw, col);
-        if (c + 1 < nchunks) load_gate(c + 1);
         // chunk c's slot is read (both tile copies have landed, U'^T and e^{G_C}
         // are in registers): hand it back (a thread that issues no products)
         if (tid == 128) ptx::st_release_gpu(&sp.consumed[u], c + 1);
@@ -1656,10 +1687,7 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
     }
     if (have_prev && !ms.err) {
         const uint32_t c_ot = ((nchunks - 1) & 1) ? CT_OT1 : CT_OT0;
-        float o[RPT];
-        write_outputs_a(ms, a, tmem + lane_base + c_ot + RPT * qq, o);
-        __syncthreads();
-        write_outputs_b(ms, a, o, gp, prev_c0, prev_nvalid, h, nw, a.out);
+        store_raw(tmem + lane_base + c_ot + RPT * qq, prev_c0, prev_nvalid);
     }
     if (tid == 0 && mma_pending) (void)ptx::mbar_wait(&ms.bar, ph);  // after a failed wait: let the products end
 
@@ -1690,6 +1718,37 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
                             : cs[((size_t)slot * (K - 1) + sr + K - 1) * conv_dim + ch];
             }
         }
+    }
+}
+
+// The split path's output epilogue, after the split kernel: chunk c of
+// chain blockIdx.y for c = blockIdx.x, + gridDim.x, ...; the fused kernel's
+// output steps (scale, the gated RMSNorm with its per-warp partial sums in the
+// same order, the stores) on the chains' raw outputs, with the same thread
+// layout, so the results carry the fused kernel's bits.
+template <bool UNB>
+__global__ void __launch_bounds__(NT) kda_split_outputs_kernel(const ChunkArgs a, const SplitArgs sp)
+{
+    __shared__ Misc ms;
+    const int u = blockIdx.y, tid = threadIdx.x, qq = tid >> 7, col = tid & (D - 1), r0 = RPT * qq;
+    int slot, seg0, seg1;
+    if (!split_unit(a, u, slot, seg0, seg1, false)) return;
+    const int H = a.H, h = u % H;
+    const int nch = split_nchunks<UNB>(sp, u, seg0, seg1);
+    const float nw = a.norm_w ? a.norm_w[col] : 1.0f;
+    for (int c = blockIdx.x; c < nch; c += gridDim.x) {
+        int c0, nvalid;
+        split_chunk<UNB>(sp, u, c, seg0, seg1, c0, nvalid);
+        float o[RPT];
+        const float* src = sp.raw_o + ((size_t)(c0 + r0) * H + h) * D + col;
+#pragma unroll
+        for (int x = 0; x < RPT; ++x) o[x] = r0 + x < nvalid ? src[(size_t)x * H * D] : 0.0f;
+        uint32_t gp[RPT / 2];
+        load_gate_bits(gp, a, c0, r0, nvalid, h, col);
+        outputs_a_regs(ms, a, o);
+        __syncthreads();
+        write_outputs_b(ms, a, o, gp, c0, nvalid, h, nw, a.out);
+        __syncthreads();  // the norm partials are reused by the next chunk
     }
 }
 
@@ -1926,6 +1985,9 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
             sp.bnd = bnd;
             sp.bs = a.T + 3;
             sp.flag_polls = a.dbg_chains_only_polls ? a.dbg_chains_only_polls : (1u << 25);
+            sp.raw_o = reinterpret_cast<float*>(
+                a.split_ws + chunk_split_bytes(a.N, a.H) +
+                (unb ? (((size_t)nc * sp.bs * sizeof(int) + 1023) & ~size_t(1023)) : 0));
             cudaError_t e = cudaMemsetAsync(a.split_ws, 0, flags, st);
             if (e != cudaSuccess) return e;
             if (unb) {
@@ -1941,7 +2003,14 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
             const void* fn = unb ? (const void*)chk::kda_chunk_split_kernel<true> : (const void*)chk::kda_chunk_split_kernel<false>;
             // test hook: the chains alone, so that their first flag wait runs out
             const int grid = a.dbg_chains_only_polls ? nc : sms;
-            return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(chk::NT), args, chk::SMEM_BYTES, st);
+            e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(chk::NT), args, chk::SMEM_BYTES, st);
+            if (e != cudaSuccess || a.dbg_chains_only_polls) return e;
+            // the output epilogue: about four CTAs per SM over the chains' chunks
+            int gx = (4 * sms) / nc > 1 ? (4 * sms) / nc : 1;
+            if (!unb && gx > (a.T + chk::C - 1) / chk::C) gx = (a.T + chk::C - 1) / chk::C;
+            if (unb) chk::kda_split_outputs_kernel<true><<<dim3(gx, nc), chk::NT, 0, st>>>(a, sp);
+            else chk::kda_split_outputs_kernel<false><<<dim3(gx, nc), chk::NT, 0, st>>>(a, sp);
+            return cudaGetLastError();
         }
         // too few SMs for producers beside the chains: the fused kernel below
     }

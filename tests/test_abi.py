@@ -126,7 +126,8 @@ def test_split_workspace_size(lib):
     the schedule, then one release flag per ring slot plus one consumed
     counter per chain, then 8 slots of 147968 bytes per chain (each slot: the
     chain's operand tiles of a chunk as bf16 high and low parts, then U'^T and
-    e^{G_C} in fp32)."""
+    e^{G_C} in fp32), and last the chains' raw outputs for the epilogue
+    (fp32 [T][H][128], 1 KiB aligned)."""
     p = _params(io_dtype=kda.KDA_DTYPE_BF16)  # H = 4
     N, nc = 2, 8
     sched = 1024                      # 3 int32 rounded to 256, then to 1 KiB
@@ -135,7 +136,8 @@ def test_split_workspace_size(lib):
     # 2 bytes each; U'^T (128 x 64 fp32); e^{G_C} (128 fp32)
     slot = 2 * 2 * (64 * 128 + 64 * 128 + 64 * 64 + 128 * 64) + 128 * 64 * 4 + 128 * 4
     assert slot == 147968
-    assert kda.kda_prefill_workspace_bytes(p, N, 1024) == sched + flags + nc * 8 * slot
+    raw = lambda T: -(-(T * 4 * 128 * 4) // 1024) * 1024  # noqa: E731
+    assert kda.kda_prefill_workspace_bytes(p, N, 1024) == sched + flags + nc * 8 * slot + raw(1024)
     assert kda.kda_prefill_workspace_bytes(p, N, 1023) == 256          # short: fused path
     assert kda.kda_prefill_workspace_bytes(p, 17, 4096) == 256 * 1     # 68 chains: fused path
     assert kda.kda_prefill_workspace_bytes(_params(io_dtype=kda.KDA_DTYPE_F32, gate_mode=kda.KDA_GATE_SOFTPLUS),
@@ -147,7 +149,7 @@ def test_split_workspace_size(lib):
     bnd = -(-(nc * (4096 + 3) * 4) // 1024) * 1024
     for q in (_params(io_dtype=kda.KDA_DTYPE_BF16, gate_mode=kda.KDA_GATE_SOFTPLUS),
               _params(io_dtype=kda.KDA_DTYPE_BF16, gate_lower_bound=-8.0)):
-        assert kda.kda_prefill_workspace_bytes(q, N, 4096) == sched + flags + nc * 8 * slot + bnd
+        assert kda.kda_prefill_workspace_bytes(q, N, 4096) == sched + flags + nc * 8 * slot + bnd + raw(4096)
         assert kda.kda_prefill_workspace_bytes(q, N, 1000) == 256   # short: fused path, no list
 
 
