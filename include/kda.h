@@ -133,7 +133,10 @@ KDA_API int kda_prefill_varlen(const kda_params* p, const int32_t* cu_seqlens, i
                                void* out, void* workspace, size_t ws_bytes,
                                int32_t* dev_status, cudaStream_t stream);
 
-/* Scratch bytes kda_prefill_varlen needs for N sequences and T rows. */
+/* Scratch bytes kda_prefill_varlen needs for N sequences and T rows: a few
+ * bytes per sequence; for few long sequences (N * H <= 64, T >= 1024, the
+ * producer / chain path) also the operand ring and T * H * dv fp32 values
+ * for the chains' outputs before their gated norm. */
 KDA_API size_t kda_prefill_workspace_bytes(const kda_params* p, int32_t N, int32_t T);
 
 /*
