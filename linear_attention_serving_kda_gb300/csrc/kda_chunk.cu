@@ -1455,8 +1455,7 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
     auto complete_pending = [&]() {
         if (pend >= 0) {
             ptx::bulk_wait_all();
-            ptx::fence_proxy_async_global();
-            __threadfence();
+            ptx::fence_proxy_async_global();  // the bulk writes before the flag (release at gpu scope)
             ptx::st_release_gpu(&sp.ready[pend], pend_v);
             pend = -1;
         }
@@ -1514,8 +1513,9 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
             for (int j = 0; j < RPT / 4; ++j) ut[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
             if (tid < D) reinterpret_cast<float*>(dst + SL_GAM)[tid] = ms.gamma[tid];
         }
+        // no per-thread fence for these stores: the barrier orders them before
+        // thread 0's fence and release of the flag (the grid-barrier pattern)
         ptx::fence_proxy_async_smem();
-        __threadfence();
         ptx::tc_fence_before();
         __syncthreads();
         if (tid == 0) {
