@@ -1727,7 +1727,7 @@ __device__ void split_chain(unsigned char* sm, Misc& ms, const ChunkArgs& a, con
 // same order, the stores) on the chains' raw outputs, with the same thread
 // layout, so the results carry the fused kernel's bits.
 template <bool UNB>
-__global__ void __launch_bounds__(NT) kda_split_outputs_kernel(const ChunkArgs a, const SplitArgs sp)
+__global__ void __launch_bounds__(NT, 2) kda_split_outputs_kernel(const ChunkArgs a, const SplitArgs sp)
 {
     __shared__ Misc ms;
     const int u = blockIdx.y, tid = threadIdx.x, qq = tid >> 7, col = tid & (D - 1), r0 = RPT * qq;
@@ -1739,12 +1739,25 @@ __global__ void __launch_bounds__(NT) kda_split_outputs_kernel(const ChunkArgs a
     for (int c = blockIdx.x; c < nch; c += gridDim.x) {
         int c0, nvalid;
         split_chunk<UNB>(sp, u, c, seg0, seg1, c0, nvalid);
+        // every load in flight at once: rows past the chunk's end read its last
+        // row (in bounds) and are then zeroed
         float o[RPT];
-        const float* src = sp.raw_o + ((size_t)(c0 + r0) * H + h) * D + col;
+        uint32_t gb16[RPT];
+        const unsigned short* gbs = static_cast<const unsigned short*>(a.g);
 #pragma unroll
-        for (int x = 0; x < RPT; ++x) o[x] = r0 + x < nvalid ? src[(size_t)x * H * D] : 0.0f;
+        for (int x = 0; x < RPT; ++x) {
+            const int r = min(r0 + x, nvalid - 1);
+            o[x] = sp.raw_o[((size_t)(c0 + r) * H + h) * D + col];
+            gb16[x] = gbs ? gbs[((size_t)(c0 + r) * H + h) * D + col] : 0u;
+        }
         uint32_t gp[RPT / 2];
-        load_gate_bits(gp, a, c0, r0, nvalid, h, col);
+#pragma unroll
+        for (int x = 0; x < RPT; ++x) {
+            const bool ok = r0 + x < nvalid;
+            o[x] = ok ? o[x] : 0.0f;
+            if ((x & 1) == 0) gp[x >> 1] = 0u;
+            gp[x >> 1] |= (ok ? gb16[x] : 0u) << (16 * (x & 1));
+        }
         outputs_a_regs(ms, a, o);
         __syncthreads();
         write_outputs_b(ms, a, o, gp, c0, nvalid, h, nw, a.out);
