@@ -1330,8 +1330,9 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
 // ------------------------------------------------------------------------
 // Split prefill for few (sequence, head) chains (long prompts): one persistent
 // cooperative grid, one CTA per SM.  CTA b < NC runs chain b: only the
-// state-dependent products (third and fourth) and the outputs, chunk after
-// chunk.  The other CTAs are producers: they take (chain, chunk) tasks in
+// state-dependent products (third and fourth), chunk after chunk, leaving the
+// raw outputs to kda_split_outputs_kernel (after the grid: the fused kernel's
+// output steps).  The other CTAs are producers: they take (chain, chunk) tasks in
 // chunk-major order, run the state-independent part of the chunk
 // (chunk_intra, the fused kernel's steps) and publish its operands -- -W,
 // Q o e^G, P and (K o e^{G_C - G})^T as bf16 high and low tiles, U'^T and
@@ -2018,7 +2019,7 @@ cudaError_t launch_chunk(int io_bf16, const ChunkArgs& a, cudaStream_t st)
             const int grid = a.dbg_chains_only_polls ? nc : sms;
             e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(chk::NT), args, chk::SMEM_BYTES, st);
             if (e != cudaSuccess || a.dbg_chains_only_polls) return e;
-            // the output epilogue: about four CTAs per SM over the chains' chunks
+            // the output epilogue: four CTAs per SM's worth of CTAs over the chains' chunks (two resident)
             int gx = (4 * sms) / nc > 1 ? (4 * sms) / nc : 1;
             if (!unb && gx > (a.T + chk::C - 1) / chk::C) gx = (a.T + chk::C - 1) / chk::C;
             if (unb) chk::kda_split_outputs_kernel<true><<<dim3(gx, nc), chk::NT, 0, st>>>(a, sp);
