@@ -75,6 +75,19 @@ def test_split_has_fused_bits_and_oracle_parity(cuda_lib, oracle_mod, lens, H, o
     _units_close(oracle_mod, wl, p, units, "split vs oracle")
 
 
+@pytest.mark.parametrize("og", [True, False])
+def test_split_bf16_outputs_have_fused_bits(cuda_lib, og):
+    """bf16 outputs (the serving case) through the split path's output
+    epilogue: the same bits as the fused kernel's output steps, with a short
+    last chunk in every sequence."""
+    lens, H = [1031, 90, 1700], 4
+    wl = W.make_workload("split_b", 812 + int(og), lens, H=H, d=128, K=4, io_dtype=W.BF16, gate_mode=W.SAFE,
+                         lower_bound=-5.0, out_gate=og, init_state="random")
+    p, f = _both(wl, out_dtype=W.BF16)
+    assert torch.equal(p.out[:wl.T], f.out[:wl.T])
+    assert torch.equal(p.rec_state, f.rec_state)
+
+
 def test_split_against_oracle(cuda_lib, oracle_mod):
     """Every (sequence, head) of a small split-path case against the oracle."""
     lens, H = [1100, 200, 77], 2
