@@ -102,8 +102,6 @@ constexpr int SM_PL = 84992;                   // P low tile
 constexpr int SM_QE = 101376;                  // Q o e^G tile 64 x 128
 constexpr int SM_KD = 134144;                  // (K o e^{G_C - G})^T tile 128 x 64
 constexpr int SM_KDL = 166912;                 // low part of the KD tile
-constexpr int SM_QEL = 0;                      // low part of the QE tile (after the solve)
-constexpr int SM_NW = 33792;                   // -W tile 64 x 128 (after the second product)
 constexpr int SM_MISC = 199680;
 struct Misc {
     float beta[C];
@@ -121,6 +119,8 @@ struct Misc {
     uint32_t tmem;
     int err;
     int ncut;                 // unbounded gates: first row that leaves the factored range
+    int staged_t;             // split producers: the task whose rows are staged ahead (-1: none)
+    int rows_pending;         // split producers: a row staging in flight, not yet waited for
     float ganc[2][D];         // unbounded gates: G at rows 0 and 32; then G at the chunk's last row
 };
 constexpr int SMEM_BYTES = SM_MISC + (int)sizeof(Misc);
@@ -131,8 +131,6 @@ static_assert(SM_PTMP >= SM_AKK + 64 * 65 * 4 && SM_TS >= SM_PTMP + 64 * 65 * 4 
               "scratch overlap");
 static_assert(SM_PH >= SM_T + 16384 && SM_PL >= SM_PH + 16384 && SM_QE >= SM_PL + 16384 &&
               SM_KD >= SM_QE + 32768 && SM_KDL >= SM_KD + 32768 && SM_KDL + 32768 <= SM_MISC, "tile overlap");
-static_assert(SM_QEL + 32768 <= SM_TS && SM_NW >= SM_QEL + 32768 && SM_NW + 32768 <= SM_PH,
-              "late tiles overlap");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(offsetof(Misc, gamma) % 16 == 0 && SM_MISC % 16 == 0, "e^{G_C} is read as float4");
 static_assert(offsetof(Misc, rms) % 8 == 0, "row inverse norms are read as float2");
@@ -1461,6 +1459,14 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
             pend = -1;
         }
     };
+    // A task's rows are staged as soon as the previous task's second product
+    // has freed the staging region when that task is t + NP (the common case:
+    // no skipped unit between them); the bookkeeping lives in shared memory.
+    if (tid == 0) {
+        ms.staged_t = -1;
+        ms.rows_pending = 0;
+    }
+    __syncthreads();
     for (int t = p; t < maxc * NC && !ms.err; t += NP) {
         const int c = t / NC, u = t % NC, h = u % H;
         int slot, seg0, seg1;
@@ -1481,12 +1487,16 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
                     flag_status(a.dev_status, KDA_DEV_TIMEOUT);
                 }
             }
-            if (!ms.err) stage_chunk(sm, maps, ms, c0, h);
+            if (!ms.err && ms.staged_t != t) {
+                stage_chunk(sm, maps, ms, c0, h);
+                ms.rows_pending = 1;
+            }
         }
         if (tid < C) ms.beta[tid] = tid < nvalid ? sigmoidf_(__bfloat162float(bg[(size_t)(c0 + tid) * H + h])) : 0.0f;
         __syncthreads();
         if (ms.err) break;
         if (!wait_rows(ms, rph, a.dev_status)) break;
+        if (tid == 0) ms.rows_pending = 0;
         if (c0 - seg0 < HALO) {
             patch_halo(sm, a, slot, h, c0 - seg0);
             __syncthreads();
@@ -1500,6 +1510,17 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
         if (tid == 0) complete_pending();
         __syncthreads();  // the published tiles are read: the operand build may overwrite them
         if (!chunk_rest(sm, ms, a, nvalid, tmem, lane_base, ph, qv, kv, vv, G)) break;
+        if (tid == 0) {  // the staging region is free: the next task's rows, if it is t + NP
+            const int tn = t + NP, cn = tn / NC, un = tn % NC;
+            int sln, sn0, sn1, cn0, nvn;
+            if (tn < maxc * NC && split_unit(a, un, sln, sn0, sn1, false) &&
+                cn < split_nchunks<UNB>(sp, un, sn0, sn1)) {
+                split_chunk<UNB>(sp, un, cn, sn0, sn1, cn0, nvn);
+                stage_chunk(sm, maps, ms, cn0, un % H);
+                ms.staged_t = tn;
+                ms.rows_pending = 1;
+            }
+        }
 
         // publish: the chain's operands as the bf16 high and low tiles
         // chunk_intra built (and -W from W^T), by bulk copies; U'^T and e^{G_C}
@@ -1532,8 +1553,11 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
         __syncthreads();
         ptx::tc_fence_after();
     }
-    if (tid == 0) complete_pending();  // the last publication (or one cut short by an error)
-    (void)rph;
+    if (tid == 0) {
+        complete_pending();  // the last publication (or one cut short by an error)
+        // rows staged for a task that did not run (after an error) land before the CTA ends
+        if (ms.rows_pending) (void)ptx::mbar_wait(&ms.rbar, rph);
+    }
 }
 
 // bulk-copy one half of a published slot into the chain's tiles
