@@ -121,6 +121,8 @@ struct Misc {
     int ncut;                 // unbounded gates: first row that leaves the factored range
     int staged_t;             // split producers: the task whose rows are staged ahead (-1: none)
     int rows_pending;         // split producers: a row staging in flight, not yet waited for
+    int next_ok;              // split producers: the staged task's slot is known to be free
+    float beta_next[C];       // split producers: the staged task's beta
     float ganc[2][D];         // unbounded gates: G at rows 0 and 32; then G at the chunk's last row
 };
 constexpr int SMEM_BYTES = SM_MISC + (int)sizeof(Misc);
@@ -700,9 +702,16 @@ __device__ __forceinline__ int chunk_prep(unsigned char* sm, Misc& ms, const Chu
 // The rest of the state-independent part of a chunk, from the prep's
 // results: e^{G_C}, the operands, the first product, A and P, the solve for T
 // and the second product (see chunk_intra).
+struct NoHook {
+    __device__ __forceinline__ void operator()() const {}
+};
+
+// hook(): run by every thread while the first product runs (the split
+// producers' look-ahead for their next task; nothing in the fused kernel)
+template <typename Hook = NoHook>
 __device__ __forceinline__ bool chunk_rest(unsigned char* sm, Misc& ms, const ChunkArgs& a, int nvalid, uint32_t tmem,
                                            uint32_t lane_base, uint32_t& ph, float (&qv)[RPT], float (&kv)[RPT],
-                                           float (&vv)[RPT], float (&G)[RPT])
+                                           float (&vv)[RPT], float (&G)[RPT], const Hook& hook = Hook())
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int col = tid & (D - 1);
@@ -804,6 +813,7 @@ __device__ __forceinline__ bool chunk_rest(unsigned char* sm, Misc& ms, const Ch
 
     // ---- first product: D1 = [K~; Q~hi](B1hi + B1lo)^T, D1c = [Q~lo; K~] B1hi^T
     if (issuer(tid) >= 0) issue_first<ISSUE_UNROLL>(sm, tmem, issuer(tid), &ms.bar);
+    hook();
     if (!wait_mma(ms, ph, a.dev_status)) return false;
 
     // ---- A (D1 lanes 0..63) and the D1c part of P.  D1 column of (row r,
@@ -1465,6 +1475,7 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
     if (tid == 0) {
         ms.staged_t = -1;
         ms.rows_pending = 0;
+        ms.next_ok = 0;
     }
     __syncthreads();
     for (int t = p; t < maxc * NC && !ms.err; t += NP) {
@@ -1478,21 +1489,26 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
             tc = thread_const(a, h, col);
             cur_h = h;
         }
+        const bool staged = ms.staged_t == t;
         if (tid == 0) {
-            // the slot is free once the chain has read chunk c - SPLIT_RING
-            if (c >= SPLIT_RING && ptx::ld_acquire_gpu(&sp.consumed[u]) < c - SPLIT_RING + 1) {
+            // the slot is free once the chain has read chunk c - SPLIT_RING (for a
+            // staged task, checked while the previous task's first product ran)
+            if (c >= SPLIT_RING && !(staged && ms.next_ok) &&
+                ptx::ld_acquire_gpu(&sp.consumed[u]) < c - SPLIT_RING + 1) {
                 complete_pending();
                 if (!ptx::wait_flag_ge(&sp.consumed[u], c - SPLIT_RING + 1, sp.flag_polls)) {
                     ms.err = 1;
                     flag_status(a.dev_status, KDA_DEV_TIMEOUT);
                 }
             }
-            if (!ms.err && ms.staged_t != t) {
+            if (!ms.err && !staged) {
                 stage_chunk(sm, maps, ms, c0, h);
                 ms.rows_pending = 1;
             }
         }
-        if (tid < C) ms.beta[tid] = tid < nvalid ? sigmoidf_(__bfloat162float(bg[(size_t)(c0 + tid) * H + h])) : 0.0f;
+        if (tid < C)
+            ms.beta[tid] = staged ? ms.beta_next[tid]
+                                  : (tid < nvalid ? sigmoidf_(__bfloat162float(bg[(size_t)(c0 + tid) * H + h])) : 0.0f);
         __syncthreads();
         if (ms.err) break;
         if (!wait_rows(ms, rph, a.dev_status)) break;
@@ -1507,9 +1523,29 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
             __syncthreads();
         }
         chunk_prep<UNB, false>(sm, ms, a, tc, nvalid, qv, kv, vv, G);
-        if (tid == 0) complete_pending();
+        if (tid == 0 && pend >= 0) ptx::bulk_wait_read_all();  // released while the first product runs
         __syncthreads();  // the published tiles are read: the operand build may overwrite them
-        if (!chunk_rest(sm, ms, a, nvalid, tmem, lane_base, ph, qv, kv, vv, G)) break;
+        // while the first product runs: the pending publication released, and
+        // the next task's (t + NP) slot checked and beta loaded
+        auto lookahead = [&]() {
+            if (tid == 0) complete_pending();
+            if (tid == 128 || (tid >= 256 && tid < 256 + C)) {
+                const int tn = t + NP, cn = tn / NC, un = tn % NC;
+                int sln, sn0, sn1, cn0, nvn;
+                if (tn < maxc * NC && split_unit(a, un, sln, sn0, sn1, false) &&
+                    cn < split_nchunks<UNB>(sp, un, sn0, sn1)) {
+                    split_chunk<UNB>(sp, un, cn, sn0, sn1, cn0, nvn);
+                    if (tid == 128) {
+                        ms.next_ok = cn < SPLIT_RING || ptx::ld_acquire_gpu(&sp.consumed[un]) >= cn - SPLIT_RING + 1;
+                    } else {
+                        const int r = tid - 256;
+                        ms.beta_next[r] =
+                            r < nvn ? sigmoidf_(__bfloat162float(bg[(size_t)(cn0 + r) * H + un % H])) : 0.0f;
+                    }
+                }
+            }
+        };
+        if (!chunk_rest(sm, ms, a, nvalid, tmem, lane_base, ph, qv, kv, vv, G, lookahead)) break;
         if (tid == 0) {  // the staging region is free: the next task's rows, if it is t + NP
             const int tn = t + NP, cn = tn / NC, un = tn % NC;
             int sln, sn0, sn1, cn0, nvn;
