@@ -1455,10 +1455,11 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
     const __nv_bfloat16* bg = static_cast<const __nv_bfloat16*>(a.b);
     // The bulk copies that publish a task run on while the next task's rows
     // are staged and its prep runs (the staging region and the prep's
-    // scratch lie below the published tiles); thread 0 completes them and
-    // releases the slot's flag before the operand build overwrites the tiles
-    // -- or at once, if the next task's slot is still taken (its chain may be
-    // waiting for this very publication).
+    // scratch lie below the published tiles).  Thread 0 waits for their
+    // reads before the operand build overwrites the tiles and completes them
+    // and releases the slot's flag while the first product runs -- or at
+    // once, if the next task's slot is still taken (its chain may be waiting
+    // for this very publication).
     int pend = -1;  // thread 0: the ready-flag index of a publication in flight, -1 none
     int pend_v = 0;
     auto complete_pending = [&]() {
