@@ -162,21 +162,7 @@ __device__ __forceinline__ void st_raw(unsigned char* sm, uint32_t off, float x)
 // store the TF32 value nearest to x (an operand used unsplit)
 __device__ __forceinline__ void st_hi(unsigned char* sm, uint32_t off, float x) { st_raw(sm, off, tf32r(x)); }
 
-// Low part of a split operand.  The tensor core reads an fp32 operand with its
-// low 13 mantissa bits dropped, so x itself serves as the high part and the
-// remainder x - trunc(x) (exact in fp32) as the low part; the low part is read
-// truncated too, which leaves x = hi + lo to within 2^-20 |x|.
-__device__ __forceinline__ float tf32_lo(float x)
-{
-    return x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-}
 
-// store x as a split operand: high part (x) and low part into two tiles
-__device__ __forceinline__ void st_split(unsigned char* sm, uint32_t off_hi, uint32_t off_lo, float x)
-{
-    st_raw(sm, off_hi, x);
-    st_raw(sm, off_lo, tf32_lo(x));
-}
 
 // Warp transpose-reduction of 16 values per lane: lane l returns the sum over
 // all 32 lanes of v[l & 15].  16 shuffles.
@@ -701,7 +687,11 @@ __device__ __forceinline__ int chunk_prep(unsigned char* sm, Misc& ms, const Chu
 
 // The rest of the state-independent part of a chunk, from the prep's
 // results: e^{G_C}, the operands, the first product, A and P, the solve for T
-// and the second product (see chunk_intra).
+// and the second product (after chunk_prep: together the state-independent
+// part of a chunk).  On return (true) the tensor memory holds W^T and U'^T,
+// shared memory the T tile and the bf16 high/low P, Q o e^G and
+// (K o e^{G_C - G})^T tiles, and ms.gamma holds e^{G_C}.  False: a
+// tensor-core wait ran out (ms.err set).
 struct NoHook {
     __device__ __forceinline__ void operator()() const {}
 };
@@ -741,7 +731,7 @@ __device__ __forceinline__ bool chunk_rest(unsigned char* sm, Misc& ms, const Ch
         // roundings and the stores (one address per element) stay per element
         const float2 eGm2 = make_float2(eGm, eGm), cGC2 = make_float2(cGC, cGC);
         const float2 mGm2 = make_float2(-Gm, -Gm);
-        auto lo2 = [](float2 x) {  // tf32_lo of both lanes: x - trunc(x)
+        auto lo2 = [](float2 x) {  // low parts of both lanes: x - trunc(x), exact in fp32
             return __fadd2_rn(x, make_float2(-__uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u),
                                              -__uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u)));
         };
@@ -980,21 +970,6 @@ __device__ __forceinline__ bool chunk_rest(unsigned char* sm, Misc& ms, const Ch
     return true;
 }
 
-// The state-independent part of one chunk (all 512 threads): from the staged
-// raw rows (q, k, v with the HALO rows before the chunk, gate f) and beta in
-// shared memory, compute conv + SiLU, the gates and G, the first product (A
-// and P), the solve for T and the second product.  On return (true) the
-// tensor memory holds W^T and U'^T, shared memory the T tile and the bf16
-// high/low P, Q o e^G and (K o e^{G_C - G})^T tiles, and ms.gamma holds
-// e^{G_C}.  False: a tensor-core wait ran out (ms.err set).
-template <bool UNB>
-__device__ __forceinline__ bool chunk_intra(unsigned char* sm, Misc& ms, const ChunkArgs& a, const ThreadConst& tc,
-                                            int nvalid, uint32_t tmem, uint32_t lane_base, uint32_t& ph)
-{
-    float qv[RPT], kv[RPT], vv[RPT], G[RPT];
-    chunk_prep<UNB, false>(sm, ms, a, tc, nvalid, qv, kv, vv, G);
-    return chunk_rest(sm, ms, a, nvalid, tmem, lane_base, ph, qv, kv, vv, G);
-}
 
 // ---- inter-chunk steps shared by the fused kernel and the chain role of the
 // split kernel; `t*` arguments are TMEM addresses (this warp's lane quarter
@@ -1017,36 +992,7 @@ __device__ __forceinline__ void load_gate_bits(uint32_t (&gp)[RPT / 2], const Ch
     }
 }
 
-// The output gate of a chunk as 4-byte (c, c+1) bf16 pairs of this thread's
-// column pair: rows [r0, r0+8) on even lanes, [r0+8, r0+16) on odd lanes
-// (half the load instructions of per-element loads).
-__device__ __forceinline__ void load_gate_words(uint32_t (&w)[RPT / 2], const ChunkArgs& a, int c0, int r0,
-                                                int nvalid, int h, int col)
-{
-    const int rb = r0 + ((col & 1) ? RPT / 2 : 0);
-    const uint32_t* gb = static_cast<const uint32_t*>(a.g);
-#pragma unroll
-    for (int x = 0; x < RPT / 2; ++x)
-        w[x] = (gb != nullptr && rb + x < nvalid) ? gb[(((size_t)(c0 + rb + x) * a.H + h) * D + (col & ~1)) >> 1] : 0u;
-}
 
-// This thread's column of the gate words above, after one lane exchange per
-// row pair: gp[k] holds rows r0 + 2k (low half) and r0 + 2k + 1 (high half).
-__device__ __forceinline__ void gate_bits_from_words(uint32_t (&gp)[RPT / 2], const uint32_t (&w)[RPT / 2], int col)
-{
-    const bool odd = col & 1;
-    uint32_t v[RPT];
-#pragma unroll
-    for (int x = 0; x < RPT / 2; ++x) {
-        const uint32_t other = __shfl_xor_sync(0xffffffffu, w[x], 1);
-        // even lanes: own word for rows [r0, r0+8), the partner's for [r0+8, r0+16); low halves
-        // odd lanes: the partner's word for rows [r0, r0+8), own for [r0+8, r0+16); high halves
-        v[x] = odd ? (other >> 16) : (w[x] & 0xFFFFu);
-        v[RPT / 2 + x] = odd ? (w[x] >> 16) : (other & 0xFFFFu);
-    }
-#pragma unroll
-    for (int k = 0; k < RPT / 2; ++k) gp[k] = v[2 * k] | (v[2 * k + 1] << 16);
-}
 
 // Outputs of this thread's 16 rows (lane j = col), optional gated RMSNorm, in
 // two parts.  Part A (all threads) reads O^T, applies the scale and, when
@@ -1342,13 +1288,13 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_kernel(const ChunkArgs a, con
 // raw outputs to kda_split_outputs_kernel (after the grid: the fused kernel's
 // output steps).  The other CTAs are producers: they take (chain, chunk) tasks in
 // chunk-major order, run the state-independent part of the chunk
-// (chunk_intra, the fused kernel's steps) and publish its operands -- -W,
+// (chunk_prep and chunk_rest, the fused kernel's steps) and publish its operands -- -W,
 // Q o e^G, P and (K o e^{G_C - G})^T as bf16 high and low tiles, U'^T and
 // e^{G_C} in fp32 -- in a ring of SPLIT_RING slots per chain, with a release
 // flag.  The chain waits for the flag, bulk-copies the tiles and returns the
 // slot (a consumed counter the producer waits on before reusing it).  Both
 // sides run the fused kernel's instructions on the same values (the producers
-// publish the bf16 tiles chunk_intra builds; the chain runs the fused kernel's
+// publish the bf16 tiles chunk_rest builds; the chain runs the fused kernel's
 // bf16 third and fourth products), so the results have the fused kernel's
 // bits.  With unbounded gates the chunks are those of a chunk list fixed
 // beforehand by the fused kernel's rule (kda_chunk_bounds_kernel), so the
@@ -1560,7 +1506,7 @@ __device__ void split_producer(unsigned char* sm, Misc& ms, const ChunkArgs& a, 
         }
 
         // publish: the chain's operands as the bf16 high and low tiles
-        // chunk_intra built (and -W from W^T), by bulk copies; U'^T and e^{G_C}
+        // chunk_rest built (and -W from W^T), by bulk copies; U'^T and e^{G_C}
         // in fp32 by plain stores
         unsigned char* dst = slot_ptr(sp, u, c);
         store_neg_w16(sm, FUSED_TILES, tmem + lane_base + TM_WT + RPT * qq, qq, col);
